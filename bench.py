@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of masked second-order HLA on one GB300 (or N replicas).
+
+Headline: forward tokens/s (B*H*T per second) on the long-context workload
+B=1 H=16 T=65536 d=dv=128, bf16 inputs, fp32 outputs, through hla2_forward.
+A "step" is one hla2_forward over that batch: segment summaries, exclusive
+scan, segment outputs.  Inputs (1.3 GB read + written per step) exceed the
+129 MB L2, so no flush is needed between steps.
+
+Also reported on the same line:
+  roofline      dominant kernel (segment outputs) against measured HBM peak;
+  e2e           the same metric through the public API with pinned host
+                buffers, host->device inputs and device->host outputs timed;
+  decode        hla2_step tokens/s on n=4096 heads, d=dv=128 (fp32 state),
+                with its own HBM roofline;
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample.
+`--impl reference` times the oracle alone as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload
+(independent heads, no collective on the data path); value = all ranks'
+tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "masked HLA-2 fwd tokens/s (B·H·T/s) at 1 GB300; % tensor/HBM roofline"
+UNIT = "tokens/s"
+FWD_WORKLOAD = 3          # B1 H16 T65536 d=dv=128 bf16
+BYTES_PER_TOKEN_FWD = None  # set from the workload: 2*(2d+dv) + 4*dv
+# ncu DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU seconds for the oracle sample")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        fd, self.path = tempfile.mkstemp(prefix="hla2_clocks_", suffix=".csv")
+        os.close(fd)
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100", *sel]
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # nvidia-smi samples every 100 ms; keep those taken while the timed work ran
+        n = len(rows)
+        span = max(1e-6, time.time() - self.t0)
+        idx = [i for i in range(n) if t_begin - self.t0 <= (i + 0.5) * span / n <= t_end - self.t0 + 0.1]
+        sel = [rows[i] for i in idx] or rows
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in sel if num(r[1]) is not None]
+        mx = [num(r[2]) for r in sel if num(r[2]) is not None]
+        pw = [num(r[3]) for r in sel if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in sel:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(sel), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- oracle leg --
+def oracle_sample(w, seconds: float):
+    """Time the fp64 oracle on all heads of the workload, first T_s tokens,
+    T_s sized for about `seconds` of CPU time.  Returns (tokens/s, cores, sample)."""
+    import oracle
+    from higher_order_linear_gb300 import workloads as W
+    cores = os.cpu_count() or 1
+    threads = min(cores, w.BH)
+    oracle.build()
+
+    def run(T):
+        q, k, v = W.make_inputs(w, T=T)
+        Q, K, V = (x.double().numpy() for x in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.serial(Q, K, V, normalized=w.normalized, nthreads=threads)
+        return time.perf_counter() - t0
+
+    T_cal = min(w.T, 512)
+    t_cal = run(T_cal)
+    T_s = int(min(w.T, max(T_cal, T_cal * seconds / max(t_cal, 1e-6))))
+    t = run(T_s) if T_s != T_cal else t_cal
+    return w.BH * T_s / t, threads, f"all {w.BH} heads x first {T_s} of {w.T} tokens (same recipe), {t:.1f} s"
+
+
+# ----------------------------------------------------------------- config --
+def fwd_config(w, plan_segments=None):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "input_dtype": w.dtype,
+            "output_dtype": "fp32", "normalized": w.normalized, "segments_per_head": plan_segments,
+            "l2": "inputs exceed L2 (1.34 GB moved per step vs 129 MB L2); no flush",
+            "parallelism": "replicas (heads independent, no collective)"}
+
+
+def segments_per_head(BH, T):
+    # mirrors the library's segment plan (two waves of 152 SMs, 128-token chunks)
+    nchunk = (T + 127) // 128
+    return min(max(1, (304 + BH - 1) // BH), nchunk)
+
+
+def reference_arm(args):
+    from higher_order_linear_gb300 import workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.WORKLOADS[FWD_WORKLOAD]
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    threads = min(cores, w.BH)
+    # each step: all heads, first T_s tokens, sized for ~2 s of CPU work
+    T_cal = 256
+    q, k, v = W.make_inputs(w, T=T_cal)
+    t0 = time.perf_counter()
+    oracle.serial(q.double().numpy(), k.double().numpy(), v.double().numpy(), nthreads=threads)
+    t_cal = time.perf_counter() - t0
+    T_s = int(min(w.T, max(T_cal, T_cal * 2.0 / max(t_cal, 1e-6))))
+    q, k, v = W.make_inputs(w, T=T_s)
+    Q, K, V = (x.double().numpy() for x in (q, k, v))
+    for _ in range(args.warmup):
+        oracle.serial(Q, K, V, nthreads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.serial(Q, K, V, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = w.BH * T_s * args.steps / tot
+    sample = f"each step: all {w.BH} heads x first {T_s} of {w.T} tokens (same recipe), fp64 serial recurrence"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": fwd_config(w, segments_per_head(w.BH, w.T)),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours --
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+    import torch.distributed as dist
+    from higher_order_linear_gb300 import build as hbuild, hla2, workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        raise SystemExit(f"WORLD_SIZE={world} but --gpus {args.gpus}")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    hbuild.build()
+    L = hla2.lib()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peaks = load_peaks()
+    w = W.WORKLOADS[FWD_WORKLOAD]
+    tokens = w.BH * w.T
+    bytes_per_token = 2 * (2 * w.d + w.dv) + 4 * w.dv  # read Q,K,V bf16 once, write O fp32 once
+    q, k, v = W.make_inputs_on(w, dev, seed=w.seed + 1000 * rank)
+    O = torch.empty(w.B, w.H, w.T, w.dv, device=dev, dtype=torch.float32)
+    need = hla2.hla2_forward_workspace(w.B, w.H, w.T, w.d, w.dv, hla2.HLA2_DTYPE_BF16)
+    ws = torch.empty(need, device=dev, dtype=torch.uint8)
+    path = "tcgen05" if L.hla2_forward_path(w.d, w.dv, hla2.HLA2_DTYPE_BF16, 0, 0) == 1 else "cuda-core"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        hla2.hla2_forward(q, k, v, O, workspace=ws)
+    barrier()
+    hla2.hla2_profile_read()
+    hla2.hla2_profile_enable(True)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        hla2.hla2_forward(q, k, v, O, workspace=ws)
+    e1.record(stream)
+    barrier()
+    t_end = time.time()
+    hla2.hla2_profile_enable(False)
+    phase_ms, nfwd, launches = hla2.hla2_profile_read()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    ms_step_max = max_over_ranks(ms_step)
+    status = hla2.hla2_device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status}: {hla2.hla2_last_error_detail()}")
+    value = world * tokens / (ms_step_max / 1e3)
+
+    # dominant kernel: segment outputs (phase 2)
+    out_ms = phase_ms[2] / max(nfwd, 1)
+    achieved = bytes_per_token * tokens / (out_ms / 1e3) / 1e9
+    traffic = NCU_TRAFFIC.get(path)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": f"segment outputs ({path})", "ms_per_launch": out_ms,
+                "phase_ms_per_step": {"summaries": phase_ms[0] / max(nfwd, 1), "scan": phase_ms[1] / max(nfwd, 1),
+                                      "outputs": out_ms},
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)" if peaks["source"] == "measured"
+                else "fallback 6.8 TB/s",
+                "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+                "tensor_frac_of_bf16_burst": (237568 * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]}
+
+    # ---- e2e through the public API with pinned host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hO = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+        n_e2e = max(2, min(args.steps, 10))
+        dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for _ in range(2):
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
+            hla2.hla2_forward(dq, dk, dvv, O, workspace=ws)
+            hO.copy_(O, non_blocking=True)
+        barrier()
+        e2 = torch.cuda.Event(enable_timing=True); e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(n_e2e):
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
+            hla2.hla2_forward(dq, dk, dvv, O, workspace=ws)
+            hO.copy_(O, non_blocking=True)
+        e3.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(e2.elapsed_time(e3) / n_e2e)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        d2h = hO.numel() * hO.element_size()
+        e2e = {"value": world * tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e}
+        del dq, dk, dvv, hq, hk, hv, hO
+
+    # ---- decode: hla2_step on n=4096 heads, d=dv=128 ----
+    decode = None
+    if not args.no_decode:
+        wd = W.DECODE
+        R = W.state_floats(wd.d, wd.dv)
+        state = torch.zeros(wd.n, R, device=dev)
+        toks = list(W.decode_tokens(wd, device=dev, seed=wd.seed + 1000 * rank))
+        for t in range(wd.prefill):
+            hla2.hla2_step(state, *toks[t])
+        barrier()
+        o = torch.empty(wd.n, wd.dv, device=dev)
+        e4 = torch.cuda.Event(enable_timing=True); e5 = torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        for t in range(wd.prefill, wd.prefill + wd.steps):
+            hla2.hla2_step(state, *toks[t], o=o)
+        e5.record(stream)
+        barrier()
+        ms_dec = max_over_ranks(e4.elapsed_time(e5) / wd.steps)
+        bytes_head = 8 * R + 4 * (2 * wd.d + 2 * wd.dv)
+        ach = wd.n * bytes_head / (ms_dec / 1e3) / 1e9
+        decode = {"metric": "hla2_step tokens/s (heads*steps/s)", "workload": wd.name,
+                  "value": world * wd.n / (ms_dec / 1e3), "unit": "tokens/s", "ms_per_step": ms_dec,
+                  "steps": wd.steps, "prefill": wd.prefill,
+                  "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC.get("step"),
+                               "bytes_per_head_step": bytes_head}}
+        del toks, state
+    clk = clocks.stop(t_begin, t_end)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, cores, sample = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
+                "config": fwd_config(w, segments_per_head(w.BH, w.T)), "path": path,
+                "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+                "cpu_baseline": cpu, "decode": decode}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

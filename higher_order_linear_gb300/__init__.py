@@ -1,0 +1,16 @@
+"""Masked second-order Higher-order Linear Attention (HLA) for NVIDIA GB300.
+
+The computation lives in ``libhla2.so`` (CUDA, sm_103a), whose C ABI is
+declared in ``include/hla2.h``; ``hla2`` is the thin Python binding.
+"""
+from .hla2 import (  # noqa: F401
+    HLA2Error,
+    hla2_chunk_summaries,
+    hla2_device_status,
+    hla2_forward,
+    hla2_forward_workspace,
+    hla2_last_error_detail,
+    hla2_scan,
+    hla2_step,
+    record_len,
+)

@@ -1,0 +1,396 @@
+// hla2_api.cu -- the C ABI of libhla2 (declared in include/hla2.h).
+//
+// Host code only: argument checks, the segment plan, workspace carving and
+// the launch sequence.  Every step of the computation runs in the CUDA
+// kernels of this library; there is no host or CPU fallback.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/hla2.h"
+#include "hla2_internal.h"
+
+namespace hla2 {
+
+// Device-side error word (one per device that loads the library).
+__device__ int g_status_word;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(HLA2_ERR_LAUNCH, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+// Segments per head for the forward: enough CTAs to fill two waves of the
+// GB300's 152 SMs, never more than the head's 128-token chunks.
+constexpr int kGranule = 128;
+constexpr int kTargetCtas = 2 * 152;
+
+SegPlan forward_plan(int BH, int T) {
+    SegPlan p;
+    p.granule = kGranule;
+    p.nchunk = (T + kGranule - 1) / kGranule;
+    int want = (kTargetCtas + BH - 1) / BH;
+    if (want < 1) want = 1;
+    p.nseg = want < p.nchunk ? want : p.nchunk;
+    if (p.nseg > 65535) p.nseg = 65535;
+    return p;
+}
+
+struct FwdWorkspace {
+    float* summ;    // [BH][nseg][R]
+    float* prefix;  // [BH][nseg][R]
+    float* tot;     // [BH][R]
+    size_t bytes;
+};
+
+FwdWorkspace carve(void* base, int BH, SegPlan p, int d, int dv) {
+    const size_t R = record_len(d, dv);
+    const size_t seg_floats = (size_t)BH * p.nseg * R;
+    auto up = [](size_t n) { return (n + 63) & ~size_t(63); };  // 256-byte granules
+    FwdWorkspace w;
+    char* c = static_cast<char*>(base);
+    w.summ = reinterpret_cast<float*>(c);
+    w.prefix = reinterpret_cast<float*>(c + up(seg_floats) * 4);
+    w.tot = reinterpret_cast<float*>(c + 2 * up(seg_floats) * 4);
+    w.bytes = (2 * up(seg_floats) + up((size_t)BH * R)) * 4;
+    return w;
+}
+
+int check_common(const void* Q, const void* K, const void* V, int B, int H, int T, int d, int dv, int dtype) {
+    if (!Q || !K || !V) return fail(HLA2_ERR_INVALID, "null input pointer");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return fail(HLA2_ERR_INVALID, "input pointer not 16-byte aligned");
+    if (B <= 0 || H <= 0 || T <= 0 || d <= 0 || dv <= 0)
+        return fail(HLA2_ERR_INVALID, "sizes must be positive (B=%d H=%d T=%d d=%d dv=%d)", B, H, T, d, dv);
+    if (dtype != HLA2_DTYPE_F32 && dtype != HLA2_DTYPE_BF16) return fail(HLA2_ERR_UNSUPPORTED, "unknown dtype %d", dtype);
+    if (d > 128 || dv > 128) return fail(HLA2_ERR_UNSUPPORTED, "d=%d dv=%d: this build supports d, dv <= 128", d, dv);
+    const long long BH = (long long)B * H;
+    if (BH > 65535) return fail(HLA2_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", BH);
+    if (BH * T * (long long)(d > dv ? d : dv) > (1LL << 40)) return fail(HLA2_ERR_UNSUPPORTED, "problem too large");
+    return HLA2_OK;
+}
+
+}  // namespace
+
+// ---- instrumentation: launch counter and per-phase events ----
+namespace {
+std::atomic<long long> g_launches{0};
+std::atomic<int> g_profile_on{0};
+std::mutex g_prof_mu;
+struct PhaseEvents {
+    cudaEvent_t ev[4];
+};
+std::vector<PhaseEvents> g_prof_pending;  // recorded, not yet read
+std::vector<PhaseEvents> g_prof_pool;     // reusable
+
+bool prof_begin(PhaseEvents& pe) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_pool.empty()) {
+        pe = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return true;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventCreate(&pe.ev[i]) != cudaSuccess) return false;
+    return true;
+}
+void prof_commit(const PhaseEvents& pe) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_pending.push_back(pe);
+}
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int* device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<int*>(p);
+    }
+    return g_status_addr[dev];
+}
+
+// Runs the P-form scan over the segment summaries in ws (see hla2_scan.cu),
+// leaving every segment's exclusive prefix in ws.prefix and, when wanted,
+// the inclusive totals in ws.tot.
+static int forward_scan(const FwdWorkspace& ws, int BH, SegPlan plan, int d, int dv, bool want_extra,
+                        bool want_tot, cudaStream_t s) {
+    const RecOff ro = summary_offsets(d, dv);
+    const size_t R = ro.R;
+    cudaError_t e;
+    // 1. exclusive sums of S | C | m
+    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, R, 0, ro.X, want_tot ? ws.tot : nullptr, R, s);
+    if (e != cudaSuccess) return cuda_fail(e, "scan: prefix sums of S, C, m");
+    // 2. X_r = P_r + S_<r C_r  (and p_r + S_<r m_r)
+    CrossArgs a{};
+    a.A = ws.prefix + ro.S; a.sA = (long long)R;
+    a.B = ws.summ + ro.C;   a.sB = (long long)R;
+    a.bx = want_extra ? ws.summ + ro.m : nullptr; a.sbx = (long long)R;
+    a.base = ws.summ + ro.X; a.sbase = (long long)R;
+    a.basex = ws.summ + ro.x; a.sbasex = (long long)R;
+    a.out = ws.prefix + ro.X; a.sout = (long long)R;
+    a.outx = want_extra ? ws.prefix + ro.x : nullptr; a.soutx = (long long)R;
+    a.alpha = 1.f; a.d = d; a.dv = dv;
+    for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
+        CrossArgs c = a;
+        const long long nb = (long long)BH * plan.nseg - b0;
+        c.nb = (int)(nb < 65535 ? nb : 65535);
+        c.A += b0 * R; c.B += b0 * R; if (c.bx) c.bx += b0 * R;
+        c.base += b0 * R; c.basex += b0 * R; c.out += b0 * R; if (c.outx) c.outx += b0 * R;
+        e = launch_cross(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "scan: cross terms");
+    }
+    // 3. exclusive sums of the corrected part P | p (in place)
+    const size_t xlen = want_extra ? R - ro.X : (size_t)d * dv;
+    e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, R, ro.X, xlen, want_tot ? ws.tot + ro.X : nullptr, R, s);
+    if (e != cudaSuccess) return cuda_fail(e, "scan: prefix sums of P");
+    return HLA2_OK;
+}
+
+}  // namespace hla2
+
+using namespace hla2;
+
+extern "C" {
+
+size_t hla2_forward_workspace(int B, int H, int T, int d, int dv, int dtype) {
+    if (B <= 0 || H <= 0 || T <= 0 || d <= 0 || dv <= 0 || d > 128 || dv > 128) return 0;
+    if (dtype != HLA2_DTYPE_F32 && dtype != HLA2_DTYPE_BF16) return 0;
+    if ((long long)B * H > 65535) return 0;
+    const int BH = B * H;
+    SegPlan p = forward_plan(BH, T);
+    return carve(nullptr, BH, p, d, dv).bytes;
+}
+
+int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, int H, int T, int d, int dv,
+                 int normalized, int dtype, void* workspace, size_t ws_bytes, float* state_out,
+                 hla2_stream_t stream) {
+    int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);
+    if (rc) return rc;
+    if (!O) return fail(HLA2_ERR_INVALID, "null output pointer");
+    if (!aligned16(O) || (state_out && !aligned16(state_out))) return fail(HLA2_ERR_INVALID, "output pointer not 16-byte aligned");
+    const size_t need = hla2_forward_workspace(B, H, T, d, dv, dtype);
+    if (!workspace || ws_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : (size_t)0, need);
+    if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const SegPlan plan = forward_plan(BH, T);
+    const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
+    const bool want_extra = normalized || state_out;  // p (and m) needed
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool use_tc = !state_out && tc_supported(d, dv, dtype, normalized, dev);
+    int* status = device_status_word();
+    if (!status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    cudaError_t e;
+    PhaseEvents pe;
+    const bool prof = g_profile_on.load() && prof_begin(pe);
+    if (prof) cudaEventRecord(pe.ev[0], s);
+
+    // segment summaries
+    if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, plan, status, s);
+    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
+    if (prof) cudaEventRecord(pe.ev[1], s);
+    // exclusive scan of the summaries
+    rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, s);
+    if (rc) return rc;
+    if (prof) cudaEventRecord(pe.ev[2], s);
+    // outputs
+    if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, plan, status, s);
+    else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "segment outputs");
+    if (prof) {
+        cudaEventRecord(pe.ev[3], s);
+        prof_commit(pe);
+    }
+
+    if (state_out) {
+        // final state in decode order S|C|G|m|h: G = S C - P, h = S m - p
+        const RecOff so = summary_offsets(d, dv);
+        const RecOff dof = decode_offsets(d, dv);
+        const long long R = (long long)so.R;
+        e = launch_copy_strided(ws.tot + so.S, R, state_out + dof.S, R, (size_t)d * d + (size_t)d * dv, BH, s);
+        if (e == cudaSuccess) e = launch_copy_strided(ws.tot + so.m, R, state_out + dof.m, R, (size_t)d, BH, s);
+        if (e != cudaSuccess) return cuda_fail(e, "state_out copy");
+        CrossArgs a{};
+        a.A = ws.tot + so.S; a.sA = R;
+        a.B = ws.tot + so.C; a.sB = R;
+        a.bx = ws.tot + so.m; a.sbx = R;
+        a.base = ws.tot + so.X; a.sbase = R;
+        a.basex = ws.tot + so.x; a.sbasex = R;
+        a.out = state_out + dof.X; a.sout = R;
+        a.outx = state_out + dof.x; a.soutx = R;
+        a.alpha = -1.f; a.d = d; a.dv = dv; a.nb = BH;
+        e = launch_cross(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "state_out G");
+    }
+    return HLA2_OK;
+}
+
+int hla2_step(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,
+              int normalized, hla2_stream_t stream) {
+    if (!state || !q || !k || !v || !o) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    auto pow2_4_128 = [](int x) { return x >= 4 && x <= 128 && (x & (x - 1)) == 0; };
+    if (!pow2_4_128(d) || !pow2_4_128(dv))
+        return fail(HLA2_ERR_UNSUPPORTED, "hla2_step needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
+    if (n > 2147483647 / 2) return fail(HLA2_ERR_UNSUPPORTED, "n too large");
+    cudaError_t e = launch_step(state, q, k, v, o, n, d, dv, normalized, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_step");
+    return HLA2_OK;
+}
+
+int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* summ, int B, int H, int T, int d,
+                         int dv, int L, int dtype, hla2_stream_t stream) {
+    int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);
+    if (rc) return rc;
+    if (!summ) return fail(HLA2_ERR_INVALID, "null summary pointer");
+    if (!aligned16(summ)) return fail(HLA2_ERR_INVALID, "summary pointer not 16-byte aligned");
+    if (L <= 0) return fail(HLA2_ERR_INVALID, "chunk length must be positive (L=%d)", L);
+    SegPlan p;
+    p.granule = L;
+    p.nchunk = (T + L - 1) / L;
+    p.nseg = p.nchunk;  // one chunk per segment
+    if (p.nseg > 65535) return fail(HLA2_ERR_UNSUPPORTED, "%d chunks per head exceeds 65535", p.nseg);
+    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, p,
+                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_chunk_summaries");
+    return HLA2_OK;
+}
+
+int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int dv, hla2_stream_t stream) {
+    if (!summ || !prefix) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(summ) || !aligned16(prefix)) return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || dv <= 0)
+        return fail(HLA2_ERR_INVALID, "sizes must be positive (B=%d H=%d N=%d d=%d dv=%d)", B, H, N, d, dv);
+    if (d > 128 || dv > 128) return fail(HLA2_ERR_UNSUPPORTED, "d, dv must be <= 128");
+    if ((long long)B * H > 65535) return fail(HLA2_ERR_UNSUPPORTED, "B*H exceeds 65535");
+    const RecOff ro = summary_offsets(d, dv);
+    const size_t R = ro.R;
+    const long long BH = (long long)B * H;
+    const long long total = BH * N * (long long)R;
+    if (summ < prefix + total && prefix < summ + total) return fail(HLA2_ERR_INVALID, "summ and prefix overlap");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // 1. exclusive sums of S | C | m
+    cudaError_t e = launch_exscan(summ, prefix, (int)BH, N, R, 0, ro.X, nullptr, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_scan: prefix sums");
+    // 2. Y_r = G_r + S_r C_<r, y_r = h_r + S_r m_<r
+    CrossArgs a{};
+    a.A = summ + ro.S; a.sA = (long long)R;
+    a.B = prefix + ro.C; a.sB = (long long)R;
+    a.bx = prefix + ro.m; a.sbx = (long long)R;
+    a.base = summ + ro.X; a.sbase = (long long)R;
+    a.basex = summ + ro.x; a.sbasex = (long long)R;
+    a.out = prefix + ro.X; a.sout = (long long)R;
+    a.outx = prefix + ro.x; a.soutx = (long long)R;
+    a.alpha = 1.f; a.d = d; a.dv = dv;
+    for (long long b0 = 0; b0 < BH * N; b0 += 65535) {
+        CrossArgs c = a;
+        const long long nb = BH * N - b0;
+        c.nb = (int)(nb < 65535 ? nb : 65535);
+        c.A += b0 * R; c.B += b0 * R; c.bx += b0 * R;
+        c.base += b0 * R; c.basex += b0 * R; c.out += b0 * R; c.outx += b0 * R;
+        e = launch_cross(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "hla2_scan: cross terms");
+    }
+    // 3. exclusive sums of G | h (in place)
+    e = launch_exscan(prefix, prefix, (int)BH, N, R, ro.X, R - ro.X, nullptr, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_scan: prefix sums of G");
+    return HLA2_OK;
+}
+
+int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return (!with_state_out && tc_supported(d, dv, dtype, normalized, dev)) ? 1 : 0;
+}
+
+int hla2_profile_enable(int on) {
+    g_profile_on.store(on ? 1 : 0);
+    return HLA2_OK;
+}
+
+int hla2_profile_read(float* ms_out, int n, int* forwards, long long* launches) {
+    std::vector<PhaseEvents> pend;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        pend.swap(g_prof_pending);
+    }
+    float acc[3] = {0.f, 0.f, 0.f};
+    int rc = HLA2_OK;
+    for (auto& pe : pend) {
+        if (cudaEventSynchronize(pe.ev[3]) != cudaSuccess) rc = fail(HLA2_ERR_LAUNCH, "profile event sync failed");
+        for (int i = 0; i < 3; ++i) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, pe.ev[i], pe.ev[i + 1]) == cudaSuccess) acc[i] += ms;
+        }
+    }
+    for (int i = 0; i < n && i < 3; ++i) ms_out[i] = acc[i];
+    if (forwards) *forwards = (int)pend.size();
+    if (launches) *launches = g_launches.exchange(0);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& pe : pend) g_prof_pool.push_back(pe);
+    return rc;
+}
+
+int hla2_last_error_detail(char* buf, size_t n) {
+    const std::string& m = t_last_error;
+    if (buf && n) {
+        size_t c = m.size() < n - 1 ? m.size() : n - 1;
+        memcpy(buf, m.data(), c);
+        buf[c] = '\0';
+    }
+    return (int)m.size();
+}
+
+int hla2_device_status(hla2_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_device_status: stream synchronize");
+    int* w = device_status_word();
+    if (!w) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    int v = 0;
+    e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_device_status: read");
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "hla2_device_status: clear");
+        return fail(HLA2_ERR_DEVICE, "device reported error %d (%s)", v,
+                    v == kDevWaitTimeout ? "bounded wait ran out" : v == kDevBounds ? "bounds check failed"
+                                                                           : v == kDevTmemAlloc ? "tensor memory allocation"
+                                                                                                : "unknown");
+    }
+    return HLA2_OK;
+}
+
+}  // extern "C"

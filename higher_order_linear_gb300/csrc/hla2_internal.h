@@ -1,0 +1,114 @@
+// hla2_internal.h -- launch wrappers shared between the CUDA translation
+// units of libhla2.  Host-only declarations; no torch types anywhere.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace hla2 {
+
+// Device-side error codes written into the library's status word.
+enum DeviceError : int {
+    kDevOk = 0,
+    kDevWaitTimeout = 1,   // a bounded mbarrier wait ran out
+    kDevBounds = 2,        // an index check failed; the access was skipped
+    kDevTmemAlloc = 3,     // tensor-memory allocation returned an unexpected address
+};
+
+// Address of this device's status word (looked up once per device).
+int* device_status_word();
+
+// Counts kernel launches issued by the library (for instrumentation).
+void note_launches(int n);
+
+// Length (in floats) of one summary / decode-state record:
+// d*d + 2*d*dv + 2*d.
+__host__ __device__ inline size_t record_len(int d, int dv) {
+    return (size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d;
+}
+// Offsets inside a summary record S | C | m | X | x (X = G or P, x = h or p).
+struct RecOff {
+    size_t S, C, m, X, x, R;
+};
+__host__ __device__ inline RecOff summary_offsets(int d, int dv) {
+    RecOff o;
+    o.S = 0;
+    o.C = (size_t)d * d;
+    o.m = o.C + (size_t)d * dv;
+    o.X = o.m + d;
+    o.x = o.X + (size_t)d * dv;
+    o.R = o.x + d;
+    return o;
+}
+// Offsets inside a decode-state record S | C | G | m | h.
+__host__ __device__ inline RecOff decode_offsets(int d, int dv) {
+    RecOff o;
+    o.S = 0;
+    o.C = (size_t)d * d;
+    o.X = o.C + (size_t)d * dv;  // G
+    o.m = o.X + (size_t)d * dv;
+    o.x = o.m + d;               // h
+    o.R = o.x + d;
+    return o;
+}
+
+// Segment partition: a head's ceil(T/granule) chunks are split into nseg
+// contiguous runs; segment s owns chunks [s*nc/nseg, (s+1)*nc/nseg).
+struct SegPlan {
+    int granule;  // tokens per chunk
+    int nchunk;   // chunks per head
+    int nseg;     // segments per head
+};
+
+// ---- decode step (hla2_decode.cu) ----
+cudaError_t launch_step(float* state, const float* q, const float* k, const float* v, float* o,
+                        int n, int d, int dv, int normalized, cudaStream_t s);
+
+// ---- segment walks on CUDA cores (hla2_walk.cu) ----
+// mode 0: P-form segment summary  S|C|m|P|p from zero state.
+// mode 1: outputs, starting from the prefix record S|.|.|P|p of the segment.
+// mode 2: G-form summary S|C|m|G|h from zero state (chunk summaries).
+cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, int dtype,
+                        float* O, const float* prefix, float* summ,
+                        int BH, int T, int d, int dv, int normalized, SegPlan plan,
+                        cudaStream_t s);
+
+// ---- scans (hla2_scan.cu) ----
+// Exclusive running sum along the record axis for the element range
+// [off, off+len) of every record: out[b][n][i] = sum_{r<n} in[b][r][i].
+// in may equal out.  If total != nullptr, total[b*total_stride + i] receives
+// the inclusive sum (element i relative to off).
+cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
+                          float* total, size_t total_stride, cudaStream_t s);
+
+// Batched out = alpha*base + A * [B | bx] for nb matrices:
+//   A d x d (row stride d), B d x dv (row stride dv), bx a d-vector taken as
+//   column dv; base/out split the same way (main d x dv + extra vector).
+//   Element strides between consecutive batch items are given per operand.
+struct CrossArgs {
+    const float* A;  long long sA;
+    const float* B;  long long sB;
+    const float* bx; long long sbx;
+    const float* base;  long long sbase;
+    const float* basex; long long sbasex;
+    float* out;  long long sout;
+    float* outx; long long soutx;
+    float alpha;
+    int d, dv, nb;
+};
+cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s);
+
+// Copy `len` floats from each of nb records (strided) to another layout.
+cudaError_t launch_copy_strided(const float* src, long long s_src, float* dst, long long s_dst,
+                                size_t len, int nb, cudaStream_t s);
+
+// ---- tensor-core segment walks (hla2_tc.cu) ----
+bool tc_supported(int d, int dv, int dtype, int normalized, int device);
+cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V,
+                           float* O, const float* prefix, float* summ,
+                           int BH, int T, int d, int dv, SegPlan plan, int* status,
+                           cudaStream_t s);
+
+}  // namespace hla2

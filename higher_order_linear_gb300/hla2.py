@@ -1,0 +1,210 @@
+"""Thin Python binding of libhla2 (the C ABI in include/hla2.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU, checks type/shape/contiguity, and passes raw device pointers,
+sizes and the current CUDA stream to the C entry point of the same name.  All
+computation happens in the library's CUDA kernels.  If ``libhla2.so`` is
+missing or cannot be loaded, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhla2.so")
+
+HLA2_OK = 0
+HLA2_ERR_INVALID = -1
+HLA2_ERR_UNSUPPORTED = -2
+HLA2_ERR_WORKSPACE = -3
+HLA2_ERR_LAUNCH = -4
+HLA2_ERR_DEVICE = -5
+HLA2_DTYPE_F32 = 0
+HLA2_DTYPE_BF16 = 1
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class HLA2Error(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        super().__init__(f"{where} failed with status {code}: {detail}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libhla2.so (built in-tree by ``higher_order_linear_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libhla2.so not built ({LIB_PATH}); run higher_order_linear_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.hla2_forward_workspace.argtypes = [i, i, i, i, i, i]
+            L.hla2_forward_workspace.restype = sz
+            L.hla2_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
+            L.hla2_forward.restype = i
+            L.hla2_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+            L.hla2_step.restype = i
+            L.hla2_chunk_summaries.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+            L.hla2_chunk_summaries.restype = i
+            L.hla2_scan.argtypes = [vp, vp, i, i, i, i, i, vp]
+            L.hla2_scan.restype = i
+            L.hla2_last_error_detail.argtypes = [ctypes.c_char_p, sz]
+            L.hla2_last_error_detail.restype = i
+            L.hla2_device_status.argtypes = [vp]
+            L.hla2_device_status.restype = i
+            L.hla2_profile_enable.argtypes = [i]
+            L.hla2_profile_enable.restype = i
+            L.hla2_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), i, ctypes.POINTER(i),
+                                            ctypes.POINTER(ctypes.c_longlong)]
+            L.hla2_profile_read.restype = i
+            L.hla2_forward_path.argtypes = [i, i, i, i, i]
+            L.hla2_forward_path.restype = i
+            _lib = L
+        return _lib
+
+
+def hla2_last_error_detail() -> str:
+    buf = ctypes.create_string_buffer(512)
+    lib().hla2_last_error_detail(buf, 512)
+    return buf.value.decode(errors="replace")
+
+
+def _check(code: int, where: str) -> None:
+    if code != HLA2_OK:
+        raise HLA2Error(code, where, hla2_last_error_detail())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return HLA2_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return HLA2_DTYPE_BF16
+    raise ValueError(f"unsupported input dtype {t.dtype}")
+
+
+def hla2_forward_workspace(B: int, H: int, T: int, d: int, dv: int, dtype: int) -> int:
+    return int(lib().hla2_forward_workspace(B, H, T, d, dv, dtype))
+
+
+def record_len(d: int, dv: int) -> int:
+    return d * d + 2 * d * dv + 2 * d
+
+
+def hla2_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                 normalized: bool = False, workspace: torch.Tensor | None = None,
+                 state_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Masked second-order HLA forward.  Q, K [B,H,T,d], V [B,H,T,dv] (fp32 or
+    bf16, same dtype) -> O [B,H,T,dv] fp32.  ``state_out`` [B*H, record] fp32
+    receives the final decode state if given."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    code = _dtype_code(Q)
+    if O is None:
+        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
+    elif O.shape != (B, H, T, dv):
+        raise ValueError("O has the wrong shape")
+    need = hla2_forward_workspace(B, H, T, d, dv, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
+    sptr = None
+    if state_out is not None:
+        if state_out.numel() != B * H * record_len(d, dv):
+            raise ValueError("state_out must hold B*H records")
+        sptr = _dev(state_out, "state_out", torch.float32)
+    rc = lib().hla2_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                            B, H, T, d, dv, int(bool(normalized)), code,
+                            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                            sptr, _stream(stream))
+    _check(rc, "hla2_forward")
+    return O
+
+
+def hla2_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+              o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """One decode step for n heads.  state [n, record] fp32 (updated in place),
+    q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
+    n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * record_len(d, dv):
+        raise ValueError("shape mismatch for hla2_step")
+    if o is None:
+        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
+    rc = lib().hla2_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
+                         _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
+                         n, d, dv, int(bool(normalized)), _stream(stream))
+    _check(rc, "hla2_step")
+    return o
+
+
+def hla2_chunk_summaries(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, L: int,
+                         summ: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """[B,H,N,record] fp32 chunk summaries S|C|m|G|h, N = ceil(T/L)."""
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    N = (T + L - 1) // L
+    if summ is None:
+        summ = torch.empty((B, H, N, record_len(d, dv)), device=Q.device, dtype=torch.float32)
+    rc = lib().hla2_chunk_summaries(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(summ, "summ", torch.float32),
+                                    B, H, T, d, dv, int(L), _dtype_code(Q), _stream(stream))
+    _check(rc, "hla2_chunk_summaries")
+    return summ
+
+
+def hla2_scan(summ: torch.Tensor, d: int, dv: int, prefix: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exclusive scan of [B,H,N,record] summaries with the semidirect combine."""
+    B, H, N, R = summ.shape
+    if R != record_len(d, dv):
+        raise ValueError("record length does not match d, dv")
+    if prefix is None:
+        prefix = torch.empty_like(summ)
+    rc = lib().hla2_scan(_dev(summ, "summ", torch.float32), _dev(prefix, "prefix", torch.float32),
+                         B, H, N, d, dv, _stream(stream))
+    _check(rc, "hla2_scan")
+    return prefix
+
+
+def hla2_device_status(stream=None) -> int:
+    return int(lib().hla2_device_status(_stream(stream)))
+
+
+def hla2_profile_enable(on: bool = True) -> None:
+    _check(lib().hla2_profile_enable(int(bool(on))), "hla2_profile_enable")
+
+
+def hla2_profile_read():
+    """(phase_ms[3], profiled forwards, kernels launched) since the last read;
+    phases are segment summaries, scan, segment outputs."""
+    ms = (ctypes.c_float * 3)()
+    nf = ctypes.c_int(0)
+    nl = ctypes.c_longlong(0)
+    _check(lib().hla2_profile_read(ms, 3, ctypes.byref(nf), ctypes.byref(nl)), "hla2_profile_read")
+    return [float(x) for x in ms], int(nf.value), int(nl.value)

@@ -100,21 +100,54 @@ def make_inputs(w: Workload, B: int | None = None, H: int | None = None, T: int 
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
 
 
-def make_decode_inputs(w: DecodeWorkload = DECODE, n: int | None = None, prefill: int | None = None,
-                       steps: int | None = None, seed: int | None = None):
-    """Prefill tokens [prefill, n, d|dv] then step tokens [steps, n, d|dv], fp32,
-    drawn in that order (prefill q,k,v then step q,k,v)."""
+def decode_tokens(w: DecodeWorkload = DECODE, n: int | None = None, count: int | None = None,
+                  seed: int | None = None, device: str | torch.device = "cpu"):
+    """Yields the decode stream token by token: for t = 0, 1, ... (prefill
+    tokens first, then step tokens) the fp32 tensors q_t, k_t [n, d] and
+    v_t [n, dv], drawn in that order from one generator.  ``device`` chooses
+    where the generator runs (a CUDA generator gives a different stream with
+    the same distribution; the parity tests use the CPU stream)."""
     n = w.n if n is None else n
-    prefill = w.prefill if prefill is None else prefill
-    steps = w.steps if steps is None else steps
-    gen = torch.Generator().manual_seed(w.seed if seed is None else seed)
-    pq = _draw(gen, (prefill, n, w.d), "normal", w.d)
-    pk = _draw(gen, (prefill, n, w.d), "normal", w.d)
-    pv = _draw(gen, (prefill, n, w.dv), "normal", w.d)
-    sq = _draw(gen, (steps, n, w.d), "normal", w.d)
-    sk = _draw(gen, (steps, n, w.d), "normal", w.d)
-    sv = _draw(gen, (steps, n, w.dv), "normal", w.d)
-    return (pq, pk, pv), (sq, sk, sv)
+    count = (w.prefill + w.steps) if count is None else count
+    dist = "uniform" if w.normalized else "normal"
+    gen = torch.Generator(device=device).manual_seed(w.seed if seed is None else seed)
+    for _ in range(count):
+        if device == "cpu":
+            q = _draw(gen, (n, w.d), dist, w.d)
+            k = _draw(gen, (n, w.d), dist, w.d)
+            v = _draw(gen, (n, w.dv), "normal", w.d)
+        else:
+            q = _draw_on(gen, (n, w.d), dist, w.d, device)
+            k = _draw_on(gen, (n, w.d), dist, w.d, device)
+            v = _draw_on(gen, (n, w.dv), "normal", w.d, device)
+        yield q, k, v
+
+
+def _draw_on(gen, shape, dist, d, device):
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32, device=device) / math.sqrt(d)
+    return torch.randn(shape, generator=gen, dtype=torch.float32, device=device) / math.sqrt(d)
+
+
+def make_inputs_on(w: Workload, device, seed: int | None = None):
+    """Same recipe as make_inputs, drawn by a generator on ``device`` (for
+    timing runs whose inputs are too large to draw on the host quickly)."""
+    gen = torch.Generator(device=device).manual_seed(w.seed if seed is None else seed)
+    shp = (w.B, w.H, w.T)
+
+    def draw(dim, dist):
+        if dist == "uniform":
+            x = torch.rand((*shp, dim), generator=gen, dtype=torch.float32, device=device) / math.sqrt(w.d)
+        elif dist == "unit":
+            x = torch.randn((*shp, dim), generator=gen, dtype=torch.float32, device=device)
+        else:
+            x = torch.randn((*shp, dim), generator=gen, dtype=torch.float32, device=device) / math.sqrt(w.d)
+        return x.to(w.torch_dtype)
+
+    q = draw(w.d, w.qk_dist)
+    k = draw(w.d, w.qk_dist)
+    v = draw(w.dv, w.v_dist)
+    return q, k, v
 
 
 def state_floats(d: int, dv: int) -> int:

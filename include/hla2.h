@@ -1,0 +1,185 @@
+/*
+ * hla2.h -- C ABI of libhla2: masked second-order Higher-order Linear
+ * Attention (HLA) on NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: the technical summary pages of "Higher-order Linear
+ * Attention" (arXiv 2510.27258), Japanese and French editions (gist.science),
+ * cited below as [HLA §1] ("Second-order HLA"), [HLA §4] ("Parallel training
+ * via associative scans") and [HLA R] ("Results and claims").
+ *
+ * Per head, with tokens t = 0..T-1, q_t, k_t in R^d and v_t in R^dv:
+ *   S_t = sum_{i<=t} k_i k_i^T      C_t = sum_{i<=t} q_i v_i^T     m_t = sum_{i<=t} q_i
+ *   G_t = G_{t-1} + k_t k_t^T C_{t-1}          h_t = h_{t-1} + k_t k_t^T m_{t-1}
+ *   o_t = q_t^T (S_t C_t - G_t) = sum_{i<=j<=t} (q_t.k_i)(k_i.q_j) v_j        [HLA §1]
+ *   ratio-normalised: o_t / (q_t^T (S_t m_t - h_t))                            [HLA §1]
+ * (The pages name G_t and h_t without printing their update; the update above
+ * is the reading that makes o_t the causal sum, and it is what this library
+ * computes.)
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers, owned by the caller.  The
+ *    library never allocates, frees or keeps them past the call.
+ *  - Tensors are dense, row-major, with no padding:
+ *      Q, K: [B][H][T][d]     V: [B][H][T][dv]     O: [B][H][T][dv] (fp32)
+ *    and every pointer must be 16-byte aligned.
+ *  - `dtype` gives the element type of Q, K, V: HLA2_DTYPE_F32 (float) or
+ *    HLA2_DTYPE_BF16 (bfloat16).  All arithmetic accumulates in fp32.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising, except
+ *    hla2_device_status.
+ *  - Return value: HLA2_OK (0) or a negative HLA2_ERR_* code; a one-line
+ *    reason is kept per host thread for hla2_last_error_detail.
+ *  - T need not be a multiple of any chunk length: the ragged tail behaves as
+ *    if padded with zero tokens, which leaves every output unchanged.
+ *  - Supported sizes: 1 <= d, dv <= 128 and B*H <= 65535 for the forward,
+ *    summary and scan calls; d, dv powers of two in [4, 128] for hla2_step.
+ */
+#ifndef HLA2_H
+#define HLA2_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define HLA2_API __attribute__((visibility("default")))
+#else
+#define HLA2_API
+#endif
+
+/* ABI-compatible with cudaStream_t without including CUDA headers. */
+typedef struct CUstream_st* hla2_stream_t;
+
+enum {
+    HLA2_OK = 0,
+    HLA2_ERR_INVALID = -1,     /* null pointer, misaligned pointer, non-positive size */
+    HLA2_ERR_UNSUPPORTED = -2, /* size or type outside what this build supports */
+    HLA2_ERR_WORKSPACE = -3,   /* workspace pointer null or smaller than required */
+    HLA2_ERR_LAUNCH = -4,      /* a CUDA call or kernel launch failed */
+    HLA2_ERR_DEVICE = -5       /* a kernel reported a device-side error (timeout, bounds) */
+};
+
+enum { HLA2_DTYPE_F32 = 0, HLA2_DTYPE_BF16 = 1 };
+
+/*
+ * Bytes of device workspace hla2_forward needs for this problem (valid for
+ * either value of `normalized`).  Returns 0 for sizes hla2_forward rejects.
+ */
+HLA2_API size_t hla2_forward_workspace(int B, int H, int T, int d, int dv, int dtype);
+
+/*
+ * Masked second-order HLA forward, chunk-parallel [HLA §4]: the sequence of
+ * each head is cut into segments; every segment's summary is computed in
+ * parallel, an exclusive scan with the semidirect-product combine gives each
+ * segment its prefix state, and every segment then walks its chunks from that
+ * prefix, emitting o_t.  The result equals the serial recurrence [HLA §1]
+ * up to fp32 rounding [HLA §4].
+ *
+ *   Q, K, V   inputs as above (dtype), read only.
+ *   O         [B][H][T][dv] fp32 output, fully overwritten.
+ *   normalized  0: o_t as above; 1: ratio-normalised o_t (plain IEEE division,
+ *             a zero denominator gives inf/NaN).
+ *   workspace device scratch of at least hla2_forward_workspace(...) bytes,
+ *             16-byte aligned; contents need not be initialised and are
+ *             garbage afterwards.
+ *   state_out optional (NULL to skip): receives each head's final state after
+ *             token T-1 in the hla2_step layout, [B*H][d*d + 2*d*dv + 2*d]
+ *             fp32, so that decoding can continue with hla2_step.
+ * Errors: HLA2_ERR_INVALID (nulls, sizes <= 0, misalignment),
+ *         HLA2_ERR_UNSUPPORTED (d or dv > 128, unknown dtype),
+ *         HLA2_ERR_WORKSPACE, HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_forward(const void* Q, const void* K, const void* V, float* O,
+                 int B, int H, int T, int d, int dv, int normalized, int dtype,
+                 void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * One streaming decode step for n independent heads [HLA §1, online update;
+ * HLA R: O(d^2 + d dv) per token, independent of the prefix length].
+ *   state  [n][d*d + 2*d*dv + 2*d] fp32, per head S (d x d) | C (d x dv) |
+ *          G (d x dv) | m (d) | h (d), row-major; read and updated in place.
+ *   q, k   [n][d] fp32;  v [n][dv] fp32;  o [n][dv] fp32 output.
+ *   The token is absorbed first (G += k k^T C, h += k k^T m, then S, C, m
+ *   grow), then o = q^T (S C - G) is emitted (divided by q^T (S m - h) when
+ *   normalized).  A zero state is the empty prefix.
+ * Errors: HLA2_ERR_INVALID, HLA2_ERR_UNSUPPORTED (d or dv not a power of two
+ *         in [4, 128]), HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_step(float* state, const float* q, const float* k, const float* v, float* o,
+              int n, int d, int dv, int normalized, hla2_stream_t stream);
+
+/*
+ * Summary of every chunk of L consecutive tokens [HLA §4, segment summaries]:
+ * the state the recurrence of [HLA §1] reaches from zero on that chunk alone.
+ *   summ  [B][H][N][d*d + 2*d*dv + 2*d] fp32, N = ceil(T/L), record
+ *         S (d x d) | C (d x dv) | m (d) | G (d x dv) | h (d).
+ *         The last chunk may be shorter than L.
+ * Errors: HLA2_ERR_INVALID, HLA2_ERR_UNSUPPORTED, HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* summ,
+                         int B, int H, int T, int d, int dv, int L, int dtype,
+                         hla2_stream_t stream);
+
+/*
+ * Exclusive scan over N summaries per head with the semidirect-product
+ * combine of [HLA §4] (A earlier, B later):
+ *   S = S_A + S_B, C = C_A + C_B, m = m_A + m_B,
+ *   G = G_A + G_B + S_B C_A,  h = h_A + h_B + S_B m_A.
+ * prefix[n] = summ[0] o ... o summ[n-1], prefix[0] = zero (the identity).
+ *   summ, prefix  [B][H][N][record] as for hla2_chunk_summaries; must not
+ *                 overlap.
+ * Because S, C and m combine by plain addition, the scan is evaluated as an
+ * exclusive sum of (S, C, m), one product S_r C_<r (and S_r m_<r) per record,
+ * and an exclusive sum of G_r + S_r C_<r: the same value as any bracketing of
+ * the combine, up to fp32 rounding.
+ * Errors: HLA2_ERR_INVALID, HLA2_ERR_UNSUPPORTED, HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int dv,
+              hla2_stream_t stream);
+
+/*
+ * Copies the calling host thread's last error reason (NUL-terminated,
+ * truncated to n bytes) into buf.  Returns the length of the full message.
+ */
+HLA2_API int hla2_last_error_detail(char* buf, size_t n);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device-side
+ * error word (set by a kernel whose bounded wait ran out or whose bounds
+ * check failed; such a kernel skips the offending access and returns).
+ * Returns HLA2_OK, HLA2_ERR_DEVICE (word was set) or HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_device_status(hla2_stream_t stream);
+
+/*
+ * Instrumentation (no counterpart on the pages).  While enabled, every
+ * hla2_forward records CUDA events on its stream around its three phases:
+ * [0] segment summaries, [1] exclusive scan, [2] segment outputs.
+ * The library also counts every kernel it launches, enabled or not.
+ */
+HLA2_API int hla2_profile_enable(int on);
+
+/*
+ * Which implementation hla2_forward picks for these arguments on the current
+ * device: 1 = tensor-core segment walks (tcgen05, bf16 operands, fp32
+ * accumulation), 0 = CUDA-core segment walks (fp32 arithmetic).  Both are
+ * CUDA kernels of this library.
+ */
+HLA2_API int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_out);
+
+/*
+ * Waits for the events recorded since the previous read, writes the summed
+ * phase durations in milliseconds to ms_out[0..min(n,3)-1], the number of
+ * profiled forwards to *forwards (if not NULL) and the number of kernels the
+ * library launched since the previous read to *launches (if not NULL), then
+ * clears both records.  Returns HLA2_OK or HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_profile_read(float* ms_out, int n, int* forwards, long long* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLA2_H */

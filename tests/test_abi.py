@@ -1,0 +1,94 @@
+"""The C-ABI library: builds, loads, exports every symbol include/hla2.h
+declares, and rejects bad arguments on the host (no GPU work is issued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from higher_order_linear_gb300 import build as hbuild
+from higher_order_linear_gb300 import hla2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hla2.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    hbuild.build()
+    return hla2.lib()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"HLA2_API\s+[\w\s\*]+?\b(hla2_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for want in ("hla2_forward", "hla2_forward_workspace", "hla2_step", "hla2_chunk_summaries", "hla2_scan",
+                 "hla2_last_error_detail", "hla2_device_status"):
+        assert want in syms
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_workspace_query(L):
+    R = lambda d, dv: d * d + 2 * d * dv + 2 * d
+    # one head, T=64: one segment -> summary + prefix + total records (256-byte rounded)
+    ws = hla2.hla2_forward_workspace(1, 1, 64, 16, 16, 0)
+    up = lambda n: (n + 63) // 64 * 64
+    assert ws == 4 * (2 * up(R(16, 16)) + up(R(16, 16)))
+    big = hla2.hla2_forward_workspace(1, 16, 65536, 128, 128, 1)
+    assert big > 0 and big % 256 == 0
+    assert hla2.hla2_forward_workspace(1, 1, 64, 200, 16, 0) == 0   # unsupported d
+    assert hla2.hla2_forward_workspace(1, 1, 0, 16, 16, 0) == 0     # empty
+    assert hla2.hla2_forward_workspace(1, 1, 64, 16, 16, 7) == 0    # bad dtype
+
+
+def _fake(addr=4096):
+    return ctypes.c_void_p(addr)
+
+
+def test_forward_rejects_bad_arguments(L):
+    p = _fake()
+    ws = hla2.hla2_forward_workspace(1, 1, 64, 16, 16, 0)
+    assert L.hla2_forward(None, p, p, p, 1, 1, 64, 16, 16, 0, 0, p, ws, None, None) == hla2.HLA2_ERR_INVALID
+    assert "null" in hla2.hla2_last_error_detail()
+    assert L.hla2_forward(_fake(4097), p, p, p, 1, 1, 64, 16, 16, 0, 0, p, ws, None, None) == hla2.HLA2_ERR_INVALID
+    assert "aligned" in hla2.hla2_last_error_detail()
+    assert L.hla2_forward(p, p, p, p, 1, 1, 0, 16, 16, 0, 0, p, ws, None, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_forward(p, p, p, p, 1, 1, 64, 129, 16, 0, 0, p, ws, None, None) == hla2.HLA2_ERR_UNSUPPORTED
+    assert L.hla2_forward(p, p, p, p, 1, 1, 64, 16, 16, 0, 3, p, ws, None, None) == hla2.HLA2_ERR_UNSUPPORTED
+    assert L.hla2_forward(p, p, p, p, 1, 1, 64, 16, 16, 0, 0, p, ws - 1, None, None) == hla2.HLA2_ERR_WORKSPACE
+    assert L.hla2_forward(p, p, p, p, 1, 1, 64, 16, 16, 0, 0, None, ws, None, None) == hla2.HLA2_ERR_WORKSPACE
+    assert L.hla2_forward(p, p, p, p, 300, 300, 64, 16, 16, 0, 0, p, 1 << 40, None, None) == hla2.HLA2_ERR_UNSUPPORTED
+
+
+def test_step_rejects_bad_arguments(L):
+    p = _fake()
+    assert L.hla2_step(None, p, p, p, p, 4, 16, 16, 0, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_step(p, p, p, p, p, 0, 16, 16, 0, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_step(p, p, p, p, p, 4, 12, 16, 0, None) == hla2.HLA2_ERR_UNSUPPORTED
+    assert L.hla2_step(p, p, p, p, p, 4, 16, 256, 0, None) == hla2.HLA2_ERR_UNSUPPORTED
+    assert L.hla2_step(p, _fake(4100), p, p, p, 4, 16, 16, 0, None) == hla2.HLA2_ERR_INVALID
+
+
+def test_summaries_and_scan_reject_bad_arguments(L):
+    p = _fake()
+    assert L.hla2_chunk_summaries(p, p, p, p, 1, 1, 64, 16, 16, 0, 0, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_chunk_summaries(p, p, p, None, 1, 1, 64, 16, 16, 16, 0, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_scan(p, p, 1, 1, 4, 16, 16, None) == hla2.HLA2_ERR_INVALID  # overlap
+    assert L.hla2_scan(p, _fake(1 << 30), 1, 1, 0, 16, 16, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_scan(p, _fake(1 << 30), 1, 1, 4, 130, 16, None) == hla2.HLA2_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(hla2, "_lib", None)
+    monkeypatch.setattr(hla2, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        hla2.lib()

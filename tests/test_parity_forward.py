@@ -1,0 +1,175 @@
+"""GPU forward (hla2_forward through the C ABI) against the fp64 oracle.
+
+Inputs are the seeded workloads; sizes span several 128-token chunks,
+several segments and ragged tails.  Full-size workloads are compared on
+every head where the oracle finishes in seconds, otherwise on sampled heads
+(all of their tokens).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from higher_order_linear_gb300 import hla2, workloads as W
+from tests._parity import (TOL_FP32_WALK, TOL_NORMALIZED, TOL_TC_BF16, f64, forward_tolerance, oracle_forward,
+                           relerr, NTHREADS)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run_gpu(q, k, v, normalized=False, state_out=None):
+    out = hla2.hla2_forward(q.to(DEV), k.to(DEV), v.to(DEV), normalized=normalized, state_out=state_out)
+    torch.cuda.synchronize()
+    assert hla2.hla2_device_status() == 0
+    return out
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from higher_order_linear_gb300 import build
+    build.build()
+
+
+# ------------------------------------------------------ seeded workloads ----
+def test_workload0_fp32_d16():
+    w = W.WORKLOADS[0]
+    q, k, v = W.make_inputs(w)
+    ref = oracle_forward(q, k, v)
+    got = run_gpu(q, k, v)
+    assert relerr(f64(got), ref) < TOL_FP32_WALK
+
+
+def test_workload1_full():
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w)
+    ref = oracle_forward(q, k, v)
+    got = run_gpu(q, k, v)
+    assert relerr(f64(got), ref) < TOL_TC_BF16
+
+
+def test_workload2_normalized_full():
+    w = W.WORKLOADS[2]
+    q, k, v = W.make_inputs(w)
+    ref = oracle_forward(q, k, v, normalized=True)
+    got = run_gpu(q, k, v, normalized=True)
+    assert relerr(f64(got), ref) < TOL_NORMALIZED
+
+
+def test_workload3_full_size_sampled_heads():
+    """B1 H16 T65536 d=dv=128: all heads run on the GPU in the benchmark's
+    launch configuration; three heads are checked token by token."""
+    w = W.WORKLOADS[3]
+    q, k, v = W.make_inputs(w)
+    got = run_gpu(q, k, v)
+    heads = [0, 7, 15]
+    ref = oracle.serial(f64(q[:, heads]), f64(k[:, heads]), f64(v[:, heads]), nthreads=3)
+    assert relerr(f64(got[:, heads]), ref) < TOL_TC_BF16
+    assert torch.isfinite(got).all()
+
+
+def test_workload3_recipe_short_all_heads():
+    w = W.WORKLOADS[3]
+    q, k, v = W.make_inputs(w, T=3000)
+    got = run_gpu(q, k, v)
+    assert relerr(f64(got), oracle_forward(q, k, v)) < TOL_TC_BF16
+
+
+# ------------------------------------------------------------ edge cases ----
+@pytest.mark.parametrize("B,H,T,d,dv,dtype,norm", [
+    (1, 1, 1, 16, 16, torch.float32, False),      # single token
+    (1, 2, 127, 64, 64, torch.bfloat16, False),   # one ragged chunk
+    (2, 1, 129, 64, 64, torch.bfloat16, False),   # chunk + 1
+    (1, 3, 1000, 128, 128, torch.bfloat16, False),
+    (1, 1, 700, 128, 64, torch.bfloat16, False),  # d != dv
+    (1, 2, 300, 5, 3, torch.float32, False),      # odd sizes
+    (1, 1, 50, 1, 1, torch.float32, False),       # scalar case
+    (3, 1, 513, 64, 64, torch.bfloat16, True),    # normalised, ragged
+    (1, 1, 257, 128, 128, torch.float32, True),
+    (1, 40, 200, 32, 32, torch.float32, False),   # many heads, short
+])
+def test_edge_shapes(B, H, T, d, dv, dtype, norm):
+    g = torch.Generator().manual_seed(B * 1000 + H * 100 + T + d)
+    if norm:
+        q = torch.rand(B, H, T, d, generator=g) / d ** 0.5
+        k = torch.rand(B, H, T, d, generator=g) / d ** 0.5
+        v = torch.randn(B, H, T, dv, generator=g)
+    else:
+        q = torch.randn(B, H, T, d, generator=g) / d ** 0.5
+        k = torch.randn(B, H, T, d, generator=g) / d ** 0.5
+        v = torch.randn(B, H, T, dv, generator=g) / d ** 0.5
+    q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
+    got = run_gpu(q, k, v, normalized=norm)
+    ref = oracle_forward(q, k, v, normalized=norm)
+    assert relerr(f64(got), ref) < forward_tolerance(dtype, d, dv, norm)
+
+
+def test_zero_inputs_give_zero():
+    q = torch.zeros(1, 2, 300, 64, dtype=torch.bfloat16)
+    got = run_gpu(q, q, torch.zeros(1, 2, 300, 64, dtype=torch.bfloat16))
+    assert (got == 0).all()
+
+
+# ------------------------------------------------------------ invariants ----
+def test_causality_bit_exact_on_gpu():
+    """Perturbing tokens after t leaves every output at or before t unchanged."""
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w, B=1, H=4, T=1500)
+    base = run_gpu(q, k, v)
+    for cut in (0, 200, 777, 1280):
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
+        q2[..., cut + 1:, :] = -q2[..., cut + 1:, :] * 2
+        k2[..., cut + 1:, :] = k2[..., cut + 1:, :].flip(-1)
+        v2[..., cut + 1:, :] += 1
+        out = run_gpu(q2, k2, v2)
+        assert torch.equal(out[..., :cut + 1, :], base[..., :cut + 1, :]), cut
+
+
+def test_deterministic():
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w, B=1, H=4, T=1100)
+    a = run_gpu(q, k, v)
+    b = run_gpu(q, k, v)
+    assert torch.equal(a, b)
+
+
+def test_zero_padding_within_tolerance():
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w, B=1, H=2, T=900)
+    pad = lambda x: torch.cat([x, torch.zeros(*x.shape[:2], 300, x.shape[-1], dtype=x.dtype)], dim=2)
+    a = run_gpu(q, k, v)
+    b = run_gpu(pad(q), pad(k), pad(v))[..., :900, :]
+    assert relerr(f64(b), f64(a)) < 1e-3
+
+
+# -------------------------------------------------- prefill -> decode -----
+@pytest.mark.parametrize("dtype,norm", [(torch.float32, False), (torch.bfloat16, False), (torch.float32, True)])
+def test_state_out_then_step_continues(dtype, norm):
+    """forward(T) hands its final state to hla2_step; stepping the next tokens
+    reproduces the oracle's outputs for the whole sequence."""
+    B, H, T, extra, d, dv = 1, 3, 400, 20, 32, 32
+    g = torch.Generator().manual_seed(77)
+    if norm:
+        q = torch.rand(B, H, T + extra, d, generator=g) / d ** 0.5
+        k = torch.rand(B, H, T + extra, d, generator=g) / d ** 0.5
+    else:
+        q = torch.randn(B, H, T + extra, d, generator=g) / d ** 0.5
+        k = torch.randn(B, H, T + extra, d, generator=g) / d ** 0.5
+    v = torch.randn(B, H, T + extra, dv, generator=g) / d ** 0.5
+    q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
+    ref = oracle_forward(q, k, v, normalized=norm)
+    state = torch.empty(B * H, hla2.record_len(d, dv), device=DEV)
+    out = run_gpu(q[..., :T, :], k[..., :T, :], v[..., :T, :], normalized=norm, state_out=state)
+    assert relerr(f64(out), ref[..., :T, :]) < TOL_FP32_WALK
+    # the handed-over state equals the oracle's whole-prefix summary
+    summ = oracle.chunk_summaries(f64(q[..., :T, :]), f64(k[..., :T, :]), f64(v[..., :T, :]), L=T)[:, :, 0]
+    expect = oracle.summary_to_decode_state(summ, d, dv).reshape(B * H, -1)
+    assert relerr(f64(state), expect) < 1e-5
+    outs = []
+    for t in range(T, T + extra):
+        qt = q[..., t, :].reshape(B * H, d).float().to(DEV)
+        kt = k[..., t, :].reshape(B * H, d).float().to(DEV)
+        vt = v[..., t, :].reshape(B * H, dv).float().to(DEV)
+        outs.append(hla2.hla2_step(state, qt, kt, vt, normalized=norm))
+    got = torch.stack(outs, dim=1).reshape(B, H, extra, dv)
+    assert relerr(f64(got), ref[..., T:, :]) < 1e-4
