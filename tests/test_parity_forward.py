@@ -31,6 +31,30 @@ def _built():
     build.build()
 
 
+def test_tensor_core_path_selected():
+    """bf16 d = dv in {64, 128} (unnormalised) runs on the tcgen05 walks; the
+    other cases run on the CUDA-core walks.  Both are this library's kernels."""
+    L = hla2.lib()
+    assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
+    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
+    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 0) == 0
+    assert L.hla2_forward_path(16, 16, hla2.HLA2_DTYPE_F32, 0, 0) == 0
+    assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 1) == 0
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 383, 2000, 5000])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_walk_lengths(T, d):
+    """Chunk boundaries, ragged tails and multi-segment heads on the tcgen05 walks."""
+    g = torch.Generator().manual_seed(T * 7 + d)
+    B, H = 1, 3
+    q = (torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    k = (torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    v = (torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    got = run_gpu(q, k, v)
+    assert relerr(f64(got), oracle_forward(q, k, v)) < TOL_TC_BF16
+
+
 # ------------------------------------------------------ seeded workloads ----
 def test_workload0_fp32_d16():
     w = W.WORKLOADS[0]
