@@ -34,7 +34,7 @@ namespace hla2 {
 namespace {
 
 constexpr int kL = 128;          // tokens per chunk (MMA M)
-constexpr int kThreadsTC = 128;  // four warps: one per 32-lane quarter of TMEM
+constexpr int kThreadsTC = 256;  // eight warps: two per 32-lane quarter of TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -164,7 +164,7 @@ struct Tile {
 
 // Write 32 fp32 values (columns col0..col0+31 of row r) to a bf16 tile,
 // optionally zeroing columns > r (causal mask).
-__device__ __forceinline__ void put_row32(const Tile& t, int r, int col0, const uint32_t (&v)[32], bool mask) {
+__device__ __forceinline__ void put_row32(const Tile& t, int r, int col0, const uint32_t* v, bool mask) {
     const int b = col0 >> 6;
     const int c0 = (col0 & 63) >> 3;  // 0 or 4
 #pragma unroll
@@ -182,6 +182,48 @@ __device__ __forceinline__ void put_row32(const Tile& t, int r, int col0, const 
         }
         st_shared_v4(t.chunk(r, b, c0 + q), w[0], w[1], w[2], w[3]);
     }
+}
+
+// Same, splitting each masked value x into hi = bf16(x) (written to the tile)
+// and lo = bf16(x - hi), returned as 16 packed bf16 pairs.
+__device__ __forceinline__ void put_row32_split(const Tile& t, int r, int col0, const uint32_t* v, bool mask,
+                                                uint32_t* lo) {
+    const int b = col0 >> 6;
+    const int c0 = (col0 & 63) >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int j = q * 8 + h * 2;
+            float x0 = __uint_as_float(v[j]), x1 = __uint_as_float(v[j + 1]);
+            if (mask) {
+                if (col0 + j > r) x0 = 0.f;
+                if (col0 + j + 1 > r) x1 = 0.f;
+            }
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+            w[h] = *reinterpret_cast<const uint32_t*>(&hv);
+            lo[q * 4 + h] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
+        }
+        st_shared_v4(t.chunk(r, b, c0 + q), w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Load NC (32 or 64) consecutive TMEM columns of this thread's lane, one wait.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    if (NC == 64) tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    tmem_ld_wait();
+}
+
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
 }
 
 // ------------------------------------------------------------- kernel ----
@@ -207,6 +249,8 @@ struct Layout {
     static constexpr uint32_t kBytes = S + kSt + kPad;
 };
 
+// Eight warps: warp w drains TMEM lanes 32*(w%4).. (its lane quarter) and the
+// w/4-th half of each region's columns.  Thread 0 issues TMA and MMAs.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -219,12 +263,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int row = tid;  // TMEM lane / tile row owned by this thread
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + (tid & 31);  // TMEM lane / tile row owned by this thread
     const int seg = blockIdx.x;
     const int head = blockIdx.y;
     const int c_begin = (int)((long long)seg * p.nchunk / p.nseg);
     const int c_end = (int)((long long)(seg + 1) * p.nchunk / p.nseg);
+    const bool state_rows = (D == 128) || quarter < D / 32;  // warp holds rows < D
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
@@ -252,11 +298,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const uint32_t tmem = tmem_slot;
     // tensor-memory regions (column offsets)
     const uint32_t tA_ = tmem + 0;           // A, then W, then O (mode 1); A then X (mode 0)
-    const uint32_t tX_ = tmem + 128;         // X (mode 1)
+    const uint32_t tX_ = tmem + 128;         // X, then packed bf16 W_lo (mode 1)
     const uint32_t tS_ = tmem + (MODE == 1 ? 256 : 128);
     const uint32_t tP_ = tmem + (MODE == 1 ? 256 + D : 128 + D);
     const uint32_t tC_ = tmem + 128 + 2 * D;  // mode 0 only
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // this warp's column window in a 128-wide and in a D-wide region
+    const int c128 = half * 64;
+    const int cD = half * (D / 2);
 
     uint32_t ph_load = 0, ph_mma = 0;
     constexpr uint32_t kTileBytes = kL * D * 2;
@@ -279,31 +328,49 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) tma_load_3d(t.base + b * t.block_bytes(), map, b * 64, chunk * kL, head, bar);
     };
+    // drain this warp's share of a 128-wide fp32 region into a bf16 tile
+    auto drain128 = [&](uint32_t treg, const Tile& t, bool mask) {
+        uint32_t r[64];
+        tmem_ld_cols<64>(treg + lane_off + c128, r);
+        put_row32(t, row, c128, r, mask);
+        put_row32(t, row, c128 + 32, r + 32, mask);
+    };
+    // drain this warp's share of a D-wide fp32 region into a bf16 tile
+    auto drainD = [&](uint32_t treg, const Tile& t) {
+        uint32_t r[64];
+        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        put_row32(t, row, cD, r, false);
+        if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
+    };
 
     // ---- initial state ----
-    if (MODE == 1) {
+    if (MODE == 1 && state_rows) {
         // S0, P0 from the segment's exclusive prefix: fp32 into TMEM, bf16 into smem
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
-        const float* S0 = pre;                       // S at offset 0
+        const float* S0 = pre;                          // S at offset 0
         const float* P0 = pre + 2 * (size_t)D * D + D;  // P after S, C, m
-        if (row < D) {
 #pragma unroll 1
-            for (int cb = 0; cb < D / 32; ++cb) {
-                uint32_t r[32];
+        for (int cb = cD; cb < cD + D / 2; cb += 32) {
+            uint32_t r[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(S0[(size_t)row * D + cb * 32 + j]);
-                tmem_st32(tS_ + lane_off + cb * 32, r);
-                put_row32(tS, row, cb * 32, r, false);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(P0[(size_t)row * D + cb * 32 + j]);
-                tmem_st32(tP_ + lane_off + cb * 32, r);
-                put_row32(tP, row, cb * 32, r, false);
+            for (int j = 0; j < 32; j += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(S0 + (size_t)row * D + cb + j);
+                r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
+                r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
             }
-        } else if (D < 128) {
-            // lanes >= D of warps that hold no state rows still take part in tcgen05.st
+            tmem_st32(tS_ + lane_off + cb, r);
+            put_row32(tS, row, cb, r, false);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(P0 + (size_t)row * D + cb + j);
+                r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
+                r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
+            }
+            tmem_st32(tP_ + lane_off + cb, r);
+            put_row32(tP, row, cb, r, false);
         }
-        if (D == 128 || warp < D / 32) tmem_st_wait();
+        tmem_st_wait();
     }
     fence_proxy_async();
     tc_fence_before();
@@ -349,30 +416,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         tc_fence_after();
         // drain 1: A -> sA (masked); mode 1 also X -> sX and S -> sS
         if (!abort_flag) {
-#pragma unroll 1
-            for (int cb = 0; cb < kL / 32; ++cb) {
-                uint32_t r[32];
-                tmem_ld32(tA_ + lane_off + cb * 32, r);
-                tmem_ld_wait();
-                put_row32(tA, row, cb * 32, r, true);
-            }
+            drain128(tA_, tA, true);
             if (MODE == 1) {
-#pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tX_ + lane_off + cb * 32, r);
-                    tmem_ld_wait();
-                    put_row32(tX, row, cb * 32, r, false);
-                }
-                if (D == 128 || warp < D / 32) {
-#pragma unroll 1
-                    for (int cb = 0; cb < D / 32; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(tS_ + lane_off + cb * 32, r);
-                        tmem_ld_wait();
-                        if (row < D) put_row32(tS, row, cb * 32, r, false);
-                    }
-                }
+                drainD(tX_, tX);
+                if (state_rows) drainD(tS_, tS);
             }
         }
         fence_proxy_async();
@@ -404,39 +451,23 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         // drain 2
         if (!abort_flag) {
             if (MODE == 1) {
-                // W -> sA (masked), X -> sX
-#pragma unroll 1
-                for (int cb = 0; cb < kL / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tA_ + lane_off + cb * 32, r);
-                    tmem_ld_wait();
-                    put_row32(tA, row, cb * 32, r, true);
+                // X -> sX; W -> hi in sA (masked), lo packed into the X region of TMEM
+                drainD(tX_, tX);
+                uint32_t lo[32];
+                {
+                    uint32_t r[64];
+                    tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                    put_row32_split(tA, row, c128, r, true, lo);
+                    put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
                 }
-#pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tX_ + lane_off + cb * 32, r);
-                    tmem_ld_wait();
-                    put_row32(tX, row, cb * 32, r, false);
-                }
+                // both warps of this lane quarter have read X before it is overwritten
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+                tmem_st32(tX_ + lane_off + half * 32, lo);
+                tmem_st_wait();
             } else {
                 // X -> sX ; S -> sS (S_local for the next chunk)
-#pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tA_ + lane_off + cb * 32, r);
-                    tmem_ld_wait();
-                    put_row32(tX, row, cb * 32, r, false);
-                }
-                if (has_next && (D == 128 || warp < D / 32)) {
-#pragma unroll 1
-                    for (int cb = 0; cb < D / 32; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(tS_ + lane_off + cb * 32, r);
-                        tmem_ld_wait();
-                        if (row < D) put_row32(tS, row, cb * 32, r, false);
-                    }
-                }
+                drainD(tA_, tX);
+                if (has_next && state_rows) drainD(tS_, tS);
             }
         }
         fence_proxy_async();
@@ -450,9 +481,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             tc_fence_after();
             if (!abort_flag) {
                 if (MODE == 1) {
-                    // O = Q P0 + W V
+                    // O = Q P0 + W_hi V + W_lo V
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + ks * 8, tV.mnmaj(ks), iKM, 1);
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                 } else {
@@ -473,26 +505,20 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         if (MODE == 1 && !abort_flag) {
             // drain 3: O -> fp32 staging in sA|sX (TMA store boxes of 32 columns);
             // P -> sP (P0 of the next chunk)
-#pragma unroll 1
-            for (int cb = 0; cb < D / 32; ++cb) {
-                uint32_t r[32];
-                tmem_ld32(tA_ + lane_off + cb * 32, r);
-                tmem_ld_wait();
-                const uint32_t box = tA.base + (uint32_t)cb * 16384u + (uint32_t)row * 128u;
+            {
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(box + (uint32_t)((q ^ (row & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
-                                 r[4 * q + 3]);
-            }
-            if (has_next && (D == 128 || warp < D / 32)) {
-#pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tP_ + lane_off + cb * 32, r);
-                    tmem_ld_wait();
-                    if (row < D) put_row32(tP, row, cb * 32, r, false);
+                for (int g = 0; g < D / 64; ++g) {
+                    const int cb = (cD >> 5) + g;
+                    const uint32_t box = tA.base + (uint32_t)cb * 16384u + (uint32_t)row * 128u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(box + (uint32_t)((q ^ (row & 7)) << 4), r[32 * g + 4 * q], r[32 * g + 4 * q + 1],
+                                     r[32 * g + 4 * q + 2], r[32 * g + 4 * q + 3]);
                 }
             }
+            if (has_next && state_rows) drainD(tP_, tP);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -513,36 +539,20 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     }
 
     // ---- segment summary out (mode 0): S | C | m | P | p records, fp32 ----
-    if (MODE == 0 && !abort_flag && (D == 128 || warp < D / 32)) {
+    if (MODE == 0 && !abort_flag && state_rows) {
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
-        float* oS = out;
-        float* oC = out + (size_t)D * D;
-        float* oP = out + 2 * (size_t)D * D + D;
-#pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t r[32];
-            tmem_ld32(tS_ + lane_off + cb * 32, r);
-            tmem_ld_wait();
-            if (row < D)
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(oS + (size_t)row * D + cb * 32 + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
-            tmem_ld32(tC_ + lane_off + cb * 32, r);
-            tmem_ld_wait();
-            if (row < D)
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(oC + (size_t)row * D + cb * 32 + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
-            tmem_ld32(tP_ + lane_off + cb * 32, r);
-            tmem_ld_wait();
-            if (row < D)
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(oP + (size_t)row * D + cb * 32 + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
+        float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // S, C, P
+        const uint32_t src[3] = {tS_, tC_, tP_};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            uint32_t r[64];
+            tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
+#pragma unroll
+            for (int j = 0; j < D / 2; j += 4)
+                *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
+                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                __uint_as_float(r[j + 3]));
         }
     }
     if (MODE == 1 && tid == 0) tma_store_wait_all();
