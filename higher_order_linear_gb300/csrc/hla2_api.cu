@@ -124,6 +124,16 @@ void prof_commit(const PhaseEvents& pe) {
 
 void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int set_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
 int* device_status_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

@@ -23,6 +23,9 @@ int* device_status_word();
 // Counts kernel launches issued by the library (for instrumentation).
 void note_launches(int n);
 
+// Records a formatted reason for hla2_last_error_detail and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 // Length (in floats) of one summary / decode-state record:
 // d*d + 2*d*dv + 2*d.
 __host__ __device__ inline size_t record_len(int d, int dv) {

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.hla2_profile_read.restype = i
             L.hla2_forward_path.argtypes = [i, i, i, i, i]
             L.hla2_forward_path.restype = i
+            L.hla2_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+            L.hla2_forward_noalloc.restype = i
             _lib = L
         return _lib
 
@@ -145,6 +147,24 @@ def hla2_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Ten
                             _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                             sptr, _stream(stream))
     _check(rc, "hla2_forward")
+    return O
+
+
+def hla2_forward_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                         normalized: bool = False, stream=None) -> torch.Tensor:
+    """hla2_forward for callers that cannot allocate device scratch: the
+    library uses its own fixed 64 MiB device array instead of a workspace
+    (larger problems raise).  Only O is allocated here, and only when the
+    caller passes none."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    if O is None:
+        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
+    rc = lib().hla2_forward_noalloc(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                                    B, H, T, d, dv, int(bool(normalized)), _dtype_code(Q), _stream(stream))
+    _check(rc, "hla2_forward_noalloc")
     return O
 
 

@@ -96,6 +96,30 @@ HLA2_API int hla2_forward(const void* Q, const void* K, const void* V, float* O,
                  void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
 
 /*
+ * hla2_forward without a caller workspace.  The pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory where
+ * they run the forward (a host framework that owns a fixed device arena and
+ * bans cudaMalloc from its callbacks, a runtime that hands its plugins only
+ * input and output buffers, a loop where allocation is forbidden after
+ * start-up).  It computes exactly what hla2_forward computes with
+ * state_out = NULL, taking its scratch from a fixed 64 MiB array that the
+ * library defines as a static device object: every GPU that loads the
+ * library holds that array until the process exits.
+ *  - Problems whose hla2_forward_workspace(...) exceeds 64 MiB are rejected
+ *    with HLA2_ERR_UNSUPPORTED and a message saying so; nothing runs.
+ *  - The first call made on a device (with it current) looks up the array's
+ *    device address; make that first call before any stream capture.
+ *  - All calls share the array and it keeps the previous call's contents
+ *    (nothing in it needs to start at zero).  Calls whose GPU work overlaps,
+ *    e.g. on two streams, race on it: the caller must serialise them.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ * Other arguments and errors as for hla2_forward.
+ */
+HLA2_API int hla2_forward_noalloc(const void* Q, const void* K, const void* V, float* O,
+                                  int B, int H, int T, int d, int dv, int normalized, int dtype,
+                                  hla2_stream_t stream);
+
+/*
  * One streaming decode step for n independent heads [HLA §1, online update;
  * HLA R: O(d^2 + d dv) per token, independent of the prefix length].
  *   state  [n][d*d + 2*d*dv + 2*d] fp32, per head S (d x d) | C (d x dv) |
