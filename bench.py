@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU seconds for the oracle sample")
+    p.add_argument("--no-forward", action="store_true", help="skip the forward (profiling the decode step alone)")
+    p.add_argument("--T", type=int, default=None, help="override T (profiling a smaller case; not a bench line)")
+    p.add_argument("--H", type=int, default=None, help="override H (profiling a smaller case; not a bench line)")
     return p.parse_args()
 
 
@@ -254,6 +257,9 @@ def main():
 
     peaks = load_peaks()
     w = W.WORKLOADS[FWD_WORKLOAD]
+    if args.T or args.H:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.T or w.T, H=args.H or w.H, name=w.name + f"-override-H{args.H or w.H}-T{args.T or w.T}")
     tokens = w.BH * w.T
     bytes_per_token = 2 * (2 * w.d + w.dv) + 4 * w.dv  # read Q,K,V bf16 once, write O fp32 once
     q, k, v = W.make_inputs_on(w, dev, seed=w.seed + 1000 * rank)
@@ -264,7 +270,8 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
-    for _ in range(args.warmup):
+    fwd_steps = 0 if args.no_forward else args.steps
+    for _ in range(0 if args.no_forward else args.warmup):
         hla2.hla2_forward(q, k, v, O, workspace=ws)
     barrier()
     hla2.hla2_profile_read()
@@ -273,23 +280,23 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_begin = time.time()
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(fwd_steps):
         hla2.hla2_forward(q, k, v, O, workspace=ws)
     e1.record(stream)
     barrier()
     t_end = time.time()
     hla2.hla2_profile_enable(False)
     phase_ms, nfwd, launches = hla2.hla2_profile_read()
-    ms_step = e0.elapsed_time(e1) / args.steps
+    ms_step = e0.elapsed_time(e1) / max(fwd_steps, 1)
     ms_step_max = max_over_ranks(ms_step)
     status = hla2.hla2_device_status()
     if status != 0:
         raise SystemExit(f"device status {status}: {hla2.hla2_last_error_detail()}")
-    value = world * tokens / (ms_step_max / 1e3)
+    value = world * tokens / (ms_step_max / 1e3) if fwd_steps else 0.0
 
     # dominant kernel: segment outputs (phase 2)
     out_ms = phase_ms[2] / max(nfwd, 1)
-    achieved = bytes_per_token * tokens / (out_ms / 1e3) / 1e9
+    achieved = bytes_per_token * tokens / (out_ms / 1e3) / 1e9 if out_ms > 0 else 0.0
     traffic = NCU_TRAFFIC.get(path)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
@@ -298,12 +305,13 @@ def main():
                                       "outputs": out_ms},
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)" if peaks["source"] == "measured"
                 else "fallback 6.8 TB/s",
-                "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
-                "tensor_frac_of_bf16_burst": (237568 * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]}
+                "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"] if fwd_steps else 0.0,
+                "tensor_frac_of_bf16_burst": (237568 * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
+                if fwd_steps else 0.0}
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.no_forward:
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         hO = torch.empty(O.shape, dtype=torch.float32).pin_memory()
         n_e2e = max(2, min(args.steps, 10))

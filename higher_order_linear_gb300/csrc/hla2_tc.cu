@@ -257,7 +257,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
     using LY = Layout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    __shared__ __align__(8) unsigned long long bars[4];  // Q, K, V loads; MMA completion
+    __shared__ __align__(8) unsigned long long bars[5];  // Q, K, V loads; MMA completion; Q released
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -277,6 +277,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
     const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
     const uint32_t bQ = smem_u32(&bars[0]), bK = smem_u32(&bars[1]), bV = smem_u32(&bars[2]), bM = smem_u32(&bars[3]);
+    const uint32_t bR = smem_u32(&bars[4]);
 
     if (tid == 0) {
         abort_flag = 0;
@@ -284,6 +285,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         mbar_init(bK, 1);
         mbar_init(bV, 1);
         mbar_init(bM, 1);
+        mbar_init(bR, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -307,7 +309,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const int c128 = half * 64;
     const int cD = half * (D / 2);
 
-    uint32_t ph_load = 0, ph_mma = 0;
+    uint32_t ph_load = 0, ph_mma = 0, ph_rel = 0;
     constexpr uint32_t kTileBytes = kL * D * 2;
     auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
         if (abort_flag) return false;
@@ -476,25 +478,35 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 
         // ================= phase 3 =================
         if (tid == 0 && !abort_flag) {
-            if (has_next && MODE == 1) issue_load(bK, &mK, tK, c + 1);  // sK is free
+            if (has_next) issue_load(bK, &mK, tK, c + 1);  // sK was last read in phase 2
             wait_bar(bV, ph_load);
             tc_fence_after();
             if (!abort_flag) {
+                // the products that read Q go first, with their own commit, so
+                // that the next chunk's Q can load while the rest runs
                 if (MODE == 1) {
-                    // O = Q P0 + W_hi V + W_lo V
+                    // O = Q P0 (+ W_hi V + W_lo V below)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
+                } else {
+                    // C += Q^T V
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (!first || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(bR);
+                if (MODE == 1) {
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + ks * 8, tV.mnmaj(ks), iKM, 1);
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                 } else {
-                    // P += X^T V ; C += Q^T V
+                    // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (!first || ks > 0) ? 1u : 0u);
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (!first || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(bM);
+                const bool q_free = wait_bar(bR, ph_rel);
+                ph_rel ^= 1;
+                if (has_next && q_free) issue_load(bQ, &mQ, tQ, c + 1);
             }
         }
         ph_load ^= 1;
@@ -502,6 +514,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         wait_bar(bM, ph_mma);
         ph_mma ^= 1;
         tc_fence_after();
+        if (tid == 0 && has_next && !abort_flag) issue_load(bV, &mV, tV, c + 1);  // sV is free
         if (MODE == 1 && !abort_flag) {
             // drain 3: O -> fp32 staging in sA|sX (TMA store boxes of 32 columns);
             // P -> sP (P0 of the next chunk)
@@ -528,11 +541,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 #pragma unroll
                 for (int cb = 0; cb < D / 32; ++cb) tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, c * kL, head);
                 tma_store_commit();
-            }
-            if (has_next) {
-                issue_load(bQ, &mQ, tQ, c + 1);
-                if (MODE == 0) issue_load(bK, &mK, tK, c + 1);
-                issue_load(bV, &mV, tV, c + 1);
             }
         }
         first = false;
