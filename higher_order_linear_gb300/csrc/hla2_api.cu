@@ -150,12 +150,14 @@ int* device_status_word() {
 // leaving every segment's exclusive prefix in ws.prefix and, when wanted,
 // the inclusive totals in ws.tot.
 static int forward_scan(const FwdWorkspace& ws, int BH, SegPlan plan, int d, int dv, bool want_extra,
-                        bool want_tot, cudaStream_t s) {
+                        bool want_tot, bool use_tc, int* status, cudaStream_t s) {
     const RecOff ro = summary_offsets(d, dv);
     const size_t R = ro.R;
     cudaError_t e;
-    // 1. exclusive sums of S | C | m
-    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, R, 0, ro.X, want_tot ? ws.tot : nullptr, R, s);
+    // 1. exclusive sums of S (the walks read only S and P from a prefix;
+    //    C and m are summed too when the final state is wanted)
+    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, R, 0, want_tot ? ro.X : (size_t)d * d,
+                      want_tot ? ws.tot : nullptr, R, s);
     if (e != cudaSuccess) return cuda_fail(e, "scan: prefix sums of S, C, m");
     // 2. X_r = P_r + S_<r C_r  (and p_r + S_<r m_r)
     CrossArgs a{};
@@ -166,14 +168,15 @@ static int forward_scan(const FwdWorkspace& ws, int BH, SegPlan plan, int d, int
     a.basex = ws.summ + ro.x; a.sbasex = (long long)R;
     a.out = ws.prefix + ro.X; a.sout = (long long)R;
     a.outx = want_extra ? ws.prefix + ro.x : nullptr; a.soutx = (long long)R;
-    a.alpha = 1.f; a.d = d; a.dv = dv;
+    a.alpha = 1.f; a.d = d; a.dv = dv; a.status = status;
     for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
         CrossArgs c = a;
         const long long nb = (long long)BH * plan.nseg - b0;
         c.nb = (int)(nb < 65535 ? nb : 65535);
         c.A += b0 * R; c.B += b0 * R; if (c.bx) c.bx += b0 * R;
         c.base += b0 * R; c.basex += b0 * R; c.out += b0 * R; if (c.outx) c.outx += b0 * R;
-        e = launch_cross(c, s);
+        // tensor cores (split-bf16 operands) on the tensor-core path; exact fp32 otherwise
+        e = (use_tc && !want_extra) ? launch_tc_cross(c, s) : launch_cross(c, s);
         if (e != cudaSuccess) return cuda_fail(e, "scan: cross terms");
     }
     // 3. exclusive sums of the corrected part P | p (in place)
@@ -230,7 +233,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
     // exclusive scan of the summaries
-    rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, s);
+    rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
     if (rc) return rc;
     if (prof) cudaEventRecord(pe.ev[2], s);
     // outputs

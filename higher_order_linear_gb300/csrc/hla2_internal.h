@@ -100,6 +100,7 @@ struct CrossArgs {
     float* outx; long long soutx;
     float alpha;
     int d, dv, nb;
+    int* status;  // device status word (tensor-core variant's bounded wait)
 };
 cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s);
 
@@ -113,5 +114,8 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
                            float* O, const float* prefix, float* summ,
                            int BH, int T, int d, int dv, SegPlan plan, int* status,
                            cudaStream_t s);
+// Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
+// (d = dv in {64, 128}, no extra column).
+cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);
 
 }  // namespace hla2

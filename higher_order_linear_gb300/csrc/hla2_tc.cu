@@ -34,7 +34,8 @@ namespace hla2 {
 namespace {
 
 constexpr int kL = 128;          // tokens per chunk (MMA M)
-constexpr int kThreadsTC = 256;  // eight warps: two per 32-lane quarter of TMEM
+constexpr int kDrainWarps = 8;   // two per 32-lane quarter of TMEM
+constexpr int kThreadsTC = (kDrainWarps + 1) * 32;  // plus one issuing warp
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -249,43 +250,53 @@ struct Layout {
     static constexpr uint32_t kBytes = S + kSt + kPad;
 };
 
-// Eight warps: warp w drains TMEM lanes 32*(w%4).. (its lane quarter) and the
-// w/4-th half of each region's columns.  Thread 0 issues TMA and MMAs.
+// Warp roles.  Warps 0..7 drain tensor memory: warp w owns TMEM lane quarter
+// w % 4 (tile rows 32*(w%4)..+31) and column half w / 4 of every region.
+// Warp 8 (lane 0) issues every TMA copy and every MMA.  The roles meet only
+// on mbarriers: each group of MMAs is committed to its own barrier, and each
+// drained region is announced on a barrier (one arrival per drain warp) that
+// the issuer waits on before it overwrites the region or reads what the
+// drain wrote.  Drains thus overlap the MMAs that do not depend on them.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
     using LY = Layout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    __shared__ __align__(8) unsigned long long bars[5];  // Q, K, V loads; MMA completion; Q released
+    // loads | MMA commits | drains
+    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DWX, DO, DP, NBAR };
+    __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const bool issuer = warp == kDrainWarps;
     const int quarter = warp & 3;
-    const int half = warp >> 2;
-    const int row = quarter * 32 + (tid & 31);  // TMEM lane / tile row owned by this thread
+    const int half = (warp >> 2) & 1;
+    const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
     const int seg = blockIdx.x;
     const int head = blockIdx.y;
     const int c_begin = (int)((long long)seg * p.nchunk / p.nseg);
     const int c_end = (int)((long long)(seg + 1) * p.nchunk / p.nseg);
-    const bool state_rows = (D == 128) || quarter < D / 32;  // warp holds rows < D
+    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
+    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
     const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
-    const uint32_t bQ = smem_u32(&bars[0]), bK = smem_u32(&bars[1]), bV = smem_u32(&bars[2]), bM = smem_u32(&bars[3]);
-    const uint32_t bR = smem_u32(&bars[4]);
+    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bQ, 1);
-        mbar_init(bK, 1);
-        mbar_init(bV, 1);
-        mbar_init(bM, 1);
-        mbar_init(bR, 1);
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t cnt = 1;
+            if (i == DA || i == DX || i == DWX || i == DO) cnt = kDrainWarps;
+            if (i == DS || i == DP) cnt = kStateWarps;
+            mbar_init(bar(i), cnt);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -299,23 +310,22 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     // tensor-memory regions (column offsets)
-    const uint32_t tA_ = tmem + 0;           // A, then W, then O (mode 1); A then X (mode 0)
-    const uint32_t tX_ = tmem + 128;         // X, then packed bf16 W_lo (mode 1)
+    const uint32_t tA_ = tmem + 0;    // mode 1: A, then W, then O;  mode 0: A, then X
+    const uint32_t tX_ = tmem + 128;  // mode 1: Q S0, then X, then packed bf16 W_lo
     const uint32_t tS_ = tmem + (MODE == 1 ? 256 : 128);
     const uint32_t tP_ = tmem + (MODE == 1 ? 256 + D : 128 + D);
     const uint32_t tC_ = tmem + 128 + 2 * D;  // mode 0 only
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // this warp's column window in a 128-wide and in a D-wide region
-    const int c128 = half * 64;
-    const int cD = half * (D / 2);
+    const int c128 = half * 64;      // this drain warp's columns in a 128-wide region
+    const int cD = half * (D / 2);   // ... and in a D-wide region
 
-    uint32_t ph_load = 0, ph_mma = 0, ph_rel = 0;
     constexpr uint32_t kTileBytes = kL * D * 2;
-    auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
+    auto wait_bar = [&](int b, uint32_t parity) -> bool {
+        const uint32_t a = bar(b);
         if (abort_flag) return false;
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try(a, parity)) return true;
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try(bar, parity)) {
+        while (!mbar_try(a, parity)) {
             if (abort_flag) return false;
             if (globaltimer() - t0 > kWaitNs) {
                 abort_flag = 1;
@@ -325,29 +335,37 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         }
         return true;
     };
-    auto issue_load = [&](uint32_t bar, const CUtensorMap* map, const Tile& t, int chunk) {
-        mbar_expect_tx(bar, kTileBytes);
+    auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        mbar_expect_tx(bar(b), kTileBytes);
 #pragma unroll
-        for (int b = 0; b < D / 64; ++b) tma_load_3d(t.base + b * t.block_bytes(), map, b * 64, chunk * kL, head, bar);
+        for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
     };
-    // drain this warp's share of a 128-wide fp32 region into a bf16 tile
+    // a drain warp announces that its share of a region is done
+    auto drained = [&](int b) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
+    };
     auto drain128 = [&](uint32_t treg, const Tile& t, bool mask) {
         uint32_t r[64];
         tmem_ld_cols<64>(treg + lane_off + c128, r);
         put_row32(t, row, c128, r, mask);
         put_row32(t, row, c128 + 32, r + 32, mask);
     };
-    // drain this warp's share of a D-wide fp32 region into a bf16 tile
     auto drainD = [&](uint32_t treg, const Tile& t) {
         uint32_t r[64];
         tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
         put_row32(t, row, cD, r, false);
         if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
     };
+    // packed W_lo: drain warp h stores the pairs of its W columns [64h, 64h+64)
+    // over the X columns it has itself just drained, so no other warp's
+    // pending read is overwritten.  K-step ks reads 8 packed columns.
+    auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * (D / 2) + 8 * (ks & 3)); };
 
-    // ---- initial state ----
+    // ---- initial state (mode 1): S0, P0 fp32 into TMEM, bf16 into smem ----
     if (MODE == 1 && state_rows) {
-        // S0, P0 from the segment's exclusive prefix: fp32 into TMEM, bf16 into smem
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
         const float* S0 = pre;                          // S at offset 0
@@ -379,196 +397,347 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
 
-    if (tid == 0 && c_begin < c_end) {
-        issue_load(bQ, &mQ, tQ, c_begin);
-        issue_load(bK, &mK, tK, c_begin);
-        issue_load(bV, &mV, tV, c_begin);
-    }
-
     constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);   // 128 x 128, both K-major
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);     // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);       // both MN-major
-    bool first = true;
+    const int nchunks = c_end - c_begin;
 
-    for (int c = c_begin; c < c_end; ++c) {
-        const bool has_next = c + 1 < c_end;
-        // ================= phase 1 =================
-        if (tid == 0) {
-            if (MODE == 1) tma_store_wait_read();  // previous O tile has left sA|sX
-            wait_bar(bQ, ph_load);
-            wait_bar(bK, ph_load);
-            tc_fence_after();
-            if (!abort_flag) {
-                // A = Q K^T
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+    if (issuer) {
+        // ============================ issuer ============================
+        if (lane == 0 && nchunks > 0) {
+            issue_load(LQ, &mQ, tQ, c_begin);
+            issue_load(LK, &mK, tK, c_begin);
+            issue_load(LV, &mV, tV, c_begin);
+            int it = 0;
+            for (; it < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1, pph = (it + 1) & 1;
+                const bool has_next = it + 1 < nchunks;
+                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
                 if (MODE == 1) {
-                    // X = Q S0
+                    if (it > 0) {
+                        if (!wait_bar(DO, pph)) break;  // O of the previous chunk is staged; TMEM A free
+                        tc_fence_after();
+#pragma unroll
+                        for (int cb = 0; cb < D / 32; ++cb)
+                            tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, (c - 1) * kL, head);
+                        tma_store_commit();
+                    }
+                    tc_fence_after();
+                    // A = Q K^T
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                    tma_store_wait_read();  // the staged O has left sA|sX before drains rewrite them
+                    mma_commit(bar(CA));
+                    if (it > 0) {
+                        if (!wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
+                        tc_fence_after();
+                    }
+                    // X = Q S0 ; S += K^T K
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                }
-                // S += K^T K
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (MODE == 1 || !first || ks > 0) ? 1u : 0u);
-                mma_commit(bM);
-            }
-        }
-        __syncwarp();
-        wait_bar(bM, ph_mma);
-        ph_mma ^= 1;
-        tc_fence_after();
-        // drain 1: A -> sA (masked); mode 1 also X -> sX and S -> sS
-        if (!abort_flag) {
-            drain128(tA_, tA, true);
-            if (MODE == 1) {
-                drainD(tX_, tX);
-                if (state_rows) drainD(tS_, tS);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-
-        // ================= phase 2 =================
-        if (tid == 0 && !abort_flag) {
-            tc_fence_after();
-            if (MODE == 1) {
-                // W = A A^T + X Q^T   (X holds Q S0 here)
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tA.kmaj(ks), iSq, ks > 0);
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
-                // X = Q S0 + A K  (accumulate onto the fp32 Q S0 still in TMEM)
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-            } else {
-                // X = Q S_local + A K   (no S_local term on the segment's first chunk)
-                if (!first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
-            }
-            mma_commit(bM);
-        }
-        __syncwarp();
-        wait_bar(bM, ph_mma);
-        ph_mma ^= 1;
-        tc_fence_after();
-        // drain 2
-        if (!abort_flag) {
-            if (MODE == 1) {
-                // X -> sX; W -> hi in sA (masked), lo packed into the X region of TMEM
-                drainD(tX_, tX);
-                uint32_t lo[32];
-                {
-                    uint32_t r[64];
-                    tmem_ld_cols<64>(tA_ + lane_off + c128, r);
-                    put_row32_split(tA, row, c128, r, true, lo);
-                    put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
-                }
-                // both warps of this lane quarter have read X before it is overwritten
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-                tmem_st32(tX_ + lane_off + half * 32, lo);
-                tmem_st_wait();
-            } else {
-                // X -> sX ; S -> sS (S_local for the next chunk)
-                drainD(tA_, tX);
-                if (has_next && state_rows) drainD(tS_, tS);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-
-        // ================= phase 3 =================
-        if (tid == 0 && !abort_flag) {
-            if (has_next) issue_load(bK, &mK, tK, c + 1);  // sK was last read in phase 2
-            wait_bar(bV, ph_load);
-            tc_fence_after();
-            if (!abort_flag) {
-                // the products that read Q go first, with their own commit, so
-                // that the next chunk's Q can load while the rest runs
-                if (MODE == 1) {
-                    // O = Q P0 (+ W_hi V + W_lo V below)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CXS));
+                    if (!wait_bar(DA, ph)) break;  // sA = A
+                    tc_fence_after();
+                    // W = A A^T
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tA.kmaj(ks), iSq, ks > 0);
+                    if (!wait_bar(DX, ph)) break;  // sX = bf16(Q S0); TMEM X read
+                    tc_fence_after();
+                    // W += (Q S0) Q^T
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
+                    mma_commit(bar(CW));
+                    // X = Q S0 + A K
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                    mma_commit(bar(CX2));
+                    if (!wait_bar(DWX, ph)) break;  // sA = W_hi, TMEM W_lo, sX = X; TMEM A read
+                    tc_fence_after();
+                    if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
+                    if (it > 0) {
+                        if (!wait_bar(DP, pph)) break;  // sP = P0 of this chunk; TMEM P read
+                        tc_fence_after();
+                    }
+                    // O = Q P0 + W_hi V + W_lo V
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
-                } else {
-                    // C += Q^T V
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (!first || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(bR);
-                if (MODE == 1) {
+                    mma_commit(bar(CQ));
+                    if (!wait_bar(LV, ph)) break;
+                    tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + ks * 8, tV.mnmaj(ks), iKM, 1);
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
+                    mma_commit(bar(CO));
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CP));
+                    if (has_next) {
+                        if (!wait_bar(CQ, ph)) break;
+                        issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q P0
+                        if (!wait_bar(CP, ph)) break;
+                        issue_load(LV, &mV, tV, c + 1);  // V was last read by W V and X^T V
+                    }
                 } else {
+                    if (it > 0) {
+                        if (!wait_bar(DX, pph)) break;  // TMEM A (X of the previous chunk) read
+                        tc_fence_after();
+                    }
+                    // A = Q K^T
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                    mma_commit(bar(CA));
+                    if (it > 0) {
+                        if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
+                        tc_fence_after();
+                    }
+                    // S += K^T K
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CXS));
+                    if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
+                    tc_fence_after();
+                    // X = Q S_local + A K   (no S_local term on the segment's first chunk)
+                    if (it > 0)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CX2));
+                    if (!wait_bar(LV, ph)) break;
+                    tc_fence_after();
+                    // C += Q^T V
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CQ));
+                    if (!wait_bar(DX, ph)) break;  // sX = X
+                    tc_fence_after();
+                    if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (!first || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(bM);
-                const bool q_free = wait_bar(bR, ph_rel);
-                ph_rel ^= 1;
-                if (has_next && q_free) issue_load(bQ, &mQ, tQ, c + 1);
-            }
-        }
-        ph_load ^= 1;
-        __syncwarp();
-        wait_bar(bM, ph_mma);
-        ph_mma ^= 1;
-        tc_fence_after();
-        if (tid == 0 && has_next && !abort_flag) issue_load(bV, &mV, tV, c + 1);  // sV is free
-        if (MODE == 1 && !abort_flag) {
-            // drain 3: O -> fp32 staging in sA|sX (TMA store boxes of 32 columns);
-            // P -> sP (P0 of the next chunk)
-            {
-                uint32_t r[64];
-                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
-#pragma unroll
-                for (int g = 0; g < D / 64; ++g) {
-                    const int cb = (cD >> 5) + g;
-                    const uint32_t box = tA.base + (uint32_t)cb * 16384u + (uint32_t)row * 128u;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_shared_v4(box + (uint32_t)((q ^ (row & 7)) << 4), r[32 * g + 4 * q], r[32 * g + 4 * q + 1],
-                                     r[32 * g + 4 * q + 2], r[32 * g + 4 * q + 3]);
+                        mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CP));
+                    if (has_next) {
+                        if (!wait_bar(CQ, ph)) break;
+                        issue_load(LQ, &mQ, tQ, c + 1);
+                        if (!wait_bar(CP, ph)) break;
+                        issue_load(LV, &mV, tV, c + 1);
+                    }
                 }
             }
-            if (has_next && state_rows) drainD(tP_, tP);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && !abort_flag) {
-            if (MODE == 1) {
+            if (MODE == 1 && it == nchunks && wait_bar(DO, (it + 1) & 1)) {
+                // the last chunk's O
+                tc_fence_after();
 #pragma unroll
-                for (int cb = 0; cb < D / 32; ++cb) tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, c * kL, head);
+                for (int cb = 0; cb < D / 32; ++cb)
+                    tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, (c_end - 1) * kL, head);
                 tma_store_commit();
             }
+            tma_store_wait_all();
         }
-        first = false;
-    }
-
-    // ---- segment summary out (mode 0): S | C | m | P | p records, fp32 ----
-    if (MODE == 0 && !abort_flag && state_rows) {
-        const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
-        float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
-        float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // S, C, P
-        const uint32_t src[3] = {tS_, tC_, tP_};
+    } else {
+        // ========================== drain warps ==========================
+        for (int it = 0; it < nchunks; ++it) {
+            const uint32_t ph = it & 1;
+            const bool has_next = it + 1 < nchunks;
+            if (MODE == 1) {
+                if (!wait_bar(CA, ph)) break;
+                tc_fence_after();
+                drain128(tA_, tA, true);  // A -> sA (masked)
+                drained(DA);
+                if (!wait_bar(CXS, ph)) break;
+                tc_fence_after();
+                drainD(tX_, tX);  // bf16(Q S0) -> sX
+                drained(DX);
+                if (state_rows && has_next) {
+                    drainD(tS_, tS);  // S0 of the next chunk -> sS
+                    drained(DS);
+                }
+                if (!wait_bar(CW, ph) || !wait_bar(CX2, ph)) break;
+                tc_fence_after();
+                drainD(tX_, tX);  // X -> sX
+                {
+                    uint32_t lo[32];
+                    uint32_t r[64];
+                    tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                    put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
+                    put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
+                    tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
+                    tmem_st_wait();
+                }
+                drained(DWX);
+                if (!wait_bar(CO, ph) || !wait_bar(CP, ph)) break;
+                tc_fence_after();
+                {
+                    // O -> fp32 staging in sA|sX, TMA-store boxes of 32 columns
+                    uint32_t r[64];
+                    tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-            uint32_t r[64];
-            tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
+                    for (int g = 0; g < D / 64; ++g) {
+                        const int cb = (cD >> 5) + g;
+                        const uint32_t box = tA.base + (uint32_t)cb * 16384u + (uint32_t)row * 128u;
 #pragma unroll
-            for (int j = 0; j < D / 2; j += 4)
-                *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
-                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                __uint_as_float(r[j + 3]));
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(box + (uint32_t)((q ^ (row & 7)) << 4), r[32 * g + 4 * q],
+                                         r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2], r[32 * g + 4 * q + 3]);
+                    }
+                }
+                drained(DO);
+                if (state_rows && has_next) {
+                    drainD(tP_, tP);  // P0 of the next chunk -> sP
+                    drained(DP);
+                }
+            } else {
+                if (!wait_bar(CA, ph)) break;
+                tc_fence_after();
+                drain128(tA_, tA, true);  // A -> sA (masked)
+                drained(DA);
+                if (!wait_bar(CX2, ph)) break;
+                tc_fence_after();
+                drainD(tA_, tX);  // X -> sX
+                drained(DX);
+                if (state_rows && has_next) {
+                    drainD(tS_, tS);  // S_local of the next chunk -> sS
+                    drained(DS);
+                }
+            }
+        }
+        // ---- segment summary out (mode 0): S | C | m | P | p records, fp32 ----
+        if (MODE == 0 && state_rows && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
+            tc_fence_after();
+            const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
+            float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
+            float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // S, C, P
+            const uint32_t src[3] = {tS_, tC_, tP_};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
+#pragma unroll
+                for (int j = 0; j < D / 2; j += 4)
+                    *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                    __uint_as_float(r[j + 3]));
+            }
         }
     }
-    if (MODE == 1 && tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+
+// ------------------------------------------------------- cross products ----
+// out[b] = base[b] + A[b] B[b] for a batch of fp32 D x D matrices (the
+// scan's S_<r C_r terms).  Each fp32 operand x is split into bf16 parts
+// hi = bf16(x), lo = bf16(x - hi), and the product is taken as
+// A_hi B_hi + A_hi B_lo + A_lo B_hi on the tensor cores (fp32 accumulation),
+// which keeps about 16 significant bits of every operand.
+template <int D>
+struct CrossLayout {
+    static constexpr uint32_t kA = 128u * D * 2u;  // A tiles keep 128 rows (MMA M = 128)
+    static constexpr uint32_t kB = (uint32_t)D * D * 2u;
+    static constexpr uint32_t Ahi = 0, Alo = kA, Bhi = 2 * kA, Blo = 2 * kA + kB;
+    static constexpr uint32_t kBytes = 2 * kA + 2 * kB;
+};
+
+// Write the bf16 hi and lo parts of 4 fp32 values (columns c..c+3 of row r).
+__device__ __forceinline__ void put4_split(const Tile& hi, const Tile& lo, int r, int c, float4 x) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y), h1 = __floats2bfloat162_rn(x.z, x.w);
+    const uint32_t l0 = pack_bf16(x.x - __low2float(h0), x.y - __high2float(h0));
+    const uint32_t l1 = pack_bf16(x.z - __low2float(h1), x.w - __high2float(h1));
+    const uint32_t off = (uint32_t)((c & 7) >> 2) * 8u;  // which half of the 16-byte chunk
+    const uint32_t ah = hi.chunk(r, c >> 6, (c & 63) >> 3) + off;
+    const uint32_t al = lo.chunk(r, c >> 6, (c & 63) >> 3) + off;
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(ah), "r"(*reinterpret_cast<const uint32_t*>(&h0)),
+                 "r"(*reinterpret_cast<const uint32_t*>(&h1))
+                 : "memory");
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(al), "r"(l0), "r"(l1) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
+    using CL = CrossLayout<D>;
+    extern __shared__ __align__(1024) unsigned char dsm_raw[];
+    __shared__ __align__(8) unsigned long long bar_mma;
+    __shared__ uint32_t tmem_slot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const long long b = blockIdx.x;
+    const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
+    const Tile tAh{dsm + CL::Ahi, 128}, tAl{dsm + CL::Alo, 128}, tBh{dsm + CL::Bhi, D}, tBl{dsm + CL::Blo, D};
+    const float* A = a.A + b * a.sA;
+    const float* B = a.B + b * a.sB;
+    constexpr uint32_t kCols = D < 32 ? 32 : D;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar_mma), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // operands: A rows a (K-major, rows >= D zero), B rows b (read MN-major)
+    for (int i = tid; i < 128 * D / 4; i += 256) {
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        const float4 x = r < D ? *reinterpret_cast<const float4*>(A + (size_t)r * D + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        put4_split(tAh, tAl, r, c, x);
+    }
+    for (int i = tid; i < D * D / 4; i += 256) {
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        put4_split(tBh, tBl, r, c, *reinterpret_cast<const float4*>(B + (size_t)r * D + c));
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+    if (tid == 0) {
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBh.mnmaj(ks), idesc, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBl.mnmaj(ks), idesc, 1);
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAl.kmaj(ks), tBh.mnmaj(ks), idesc, 1);
+        mma_commit(smem_u32(&bar_mma));
+    }
+    __syncwarp();
+    // bounded wait for the products
+    bool ok = mbar_try(smem_u32(&bar_mma), 0);
+    if (!ok) {
+        const unsigned long long t0 = globaltimer();
+        while (!(ok = mbar_try(smem_u32(&bar_mma), 0)))
+            if (globaltimer() - t0 > kWaitNs) break;
+        if (!ok && lane == 0) atomicExch(a.status, (int)kDevWaitTimeout);
+    }
+    tc_fence_after();
+    if (ok && ((D == 128) || quarter < D / 32)) {
+        uint32_t r[64];
+        const int cD = half * (D / 2);
+        tmem_ld_cols<D / 2>(tmem + ((uint32_t)(quarter * 32) << 16) + cD, r);
+        const float* base = a.base + b * a.sbase;
+        float* out = a.out + b * a.sout;
+#pragma unroll
+        for (int j = 0; j < D / 2; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(base + (size_t)row * D + cD + j);
+            *reinterpret_cast<float4*>(out + (size_t)row * D + cD + j) =
+                make_float4(fmaf(a.alpha, x.x, __uint_as_float(r[j])), fmaf(a.alpha, x.y, __uint_as_float(r[j + 1])),
+                            fmaf(a.alpha, x.z, __uint_as_float(r[j + 2])), fmaf(a.alpha, x.w, __uint_as_float(r[j + 3])));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+}
+
+template <int D>
+cudaError_t launch_cross_t(const CrossArgs& a, cudaStream_t s) {
+    const size_t smem = CrossLayout<D>::kBytes + 1024;
+    auto kern = tc_cross_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.nb, 256, smem, s>>>(a);
+    note_launches(1);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ host side ----
@@ -651,6 +820,14 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
                                    : launch_t<128, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     if (d == 64) return mode == 0 ? launch_t<64, 0>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
                                   : launch_t<64, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s) {
+    if (a.nb == 0) return cudaSuccess;
+    if (a.d != a.dv || a.bx || a.outx) return cudaErrorInvalidValue;
+    if (a.d == 128) return launch_cross_t<128>(a, s);
+    if (a.d == 64) return launch_cross_t<64>(a, s);
     return cudaErrorInvalidValue;
 }
 
