@@ -70,14 +70,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -232,6 +224,7 @@ struct TCParams {
     int T, nseg, nchunk;
     float* summ;          // mode 0 output records
     const float* prefix;  // mode 1 input records
+    float* O;             // mode 1 outputs [BH][T][D]
     int* status;
 };
 
@@ -260,11 +253,11 @@ struct Layout {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
+               const __grid_constant__ CUtensorMap mV, TCParams p) {
     using LY = Layout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
-    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DWX, DO, DP, NBAR };
+    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -293,7 +286,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DWX || i == DO) cnt = kDrainWarps;
+            if (i == DA || i == DX || i == DW || i == DX2 || i == DO) cnt = kDrainWarps;
             if (i == DS || i == DP) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
@@ -416,18 +409,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 const bool has_next = it + 1 < nchunks;
                 if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
                 if (MODE == 1) {
-                    if (it > 0) {
-                        if (!wait_bar(DO, pph)) break;  // O of the previous chunk is staged; TMEM A free
-                        tc_fence_after();
-#pragma unroll
-                        for (int cb = 0; cb < D / 32; ++cb)
-                            tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, (c - 1) * kL, head);
-                        tma_store_commit();
-                    }
+                    if (it > 0 && !wait_bar(DO, pph)) break;  // O of the previous chunk read out of TMEM A
                     tc_fence_after();
                     // A = Q K^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
-                    tma_store_wait_read();  // the staged O has left sA|sX before drains rewrite them
                     mma_commit(bar(CA));
                     if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
@@ -449,7 +434,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // X = Q S0 + A K
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CX2));
-                    if (!wait_bar(DWX, ph)) break;  // sA = W_hi, TMEM W_lo, sX = X; TMEM A read
+                    if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
                     tc_fence_after();
                     if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
                     if (it > 0) {
@@ -464,6 +449,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CO));
+                    if (!wait_bar(DX2, ph)) break;  // sX = X
+                    tc_fence_after();
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                     mma_commit(bar(CP));
@@ -518,15 +505,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                 }
             }
-            if (MODE == 1 && it == nchunks && wait_bar(DO, (it + 1) & 1)) {
-                // the last chunk's O
-                tc_fence_after();
-#pragma unroll
-                for (int cb = 0; cb < D / 32; ++cb)
-                    tma_store_3d(&mO, tA.base + (uint32_t)cb * 16384u, cb * 32, (c_end - 1) * kL, head);
-                tma_store_commit();
-            }
-            tma_store_wait_all();
         }
     } else {
         // ========================== drain warps ==========================
@@ -548,35 +526,67 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 }
                 if (!wait_bar(CW, ph) || !wait_bar(CX2, ph)) break;
                 tc_fence_after();
-                drainD(tX_, tX);  // X -> sX
                 {
+                    // X is read out first (W_lo lands on this warp's X columns),
+                    // W is announced before X because the output products need it first
+                    uint32_t x[64];
+                    tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
                     uint32_t lo[32];
-                    uint32_t r[64];
-                    tmem_ld_cols<64>(tA_ + lane_off + c128, r);
-                    put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
-                    put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
+                    {
+                        uint32_t r[64];
+                        tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                        put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
+                        put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
+                    }
                     tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
                     tmem_st_wait();
+                    drained(DW);
+                    put_row32(tX, row, cD, x, false);  // X -> sX
+                    if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
+                    drained(DX2);
                 }
-                drained(DWX);
-                if (!wait_bar(CO, ph) || !wait_bar(CP, ph)) break;
+                if (!wait_bar(CO, ph)) break;
                 tc_fence_after();
                 {
-                    // O -> fp32 staging in sA|sX, TMA-store boxes of 32 columns
+                    // O (fp32) to global memory through a per-warp transpose: the
+                    // 4 KB of sA that hold this warp's own rows and column half
+                    // (W_hi there is dead once the output products completed) take
+                    // 32 rows x 32 columns at a time, then each store instruction
+                    // writes four whole 128-byte row pieces.
                     uint32_t r[64];
                     tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                    const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+                    const int t0 = (c_begin + it) * kL + quarter * 32;  // first token of this warp's rows
 #pragma unroll
                     for (int g = 0; g < D / 64; ++g) {
-                        const int cb = (cD >> 5) + g;
-                        const uint32_t box = tA.base + (uint32_t)cb * 16384u + (uint32_t)row * 128u;
+                        // this thread's row: 32 fp32 = 8 chunks of 16 bytes, swizzled
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            st_shared_v4(box + (uint32_t)((q ^ (row & 7)) << 4), r[32 * g + 4 * q],
-                                         r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2], r[32 * g + 4 * q + 3]);
+                            st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
+                                         r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
+                                         r[32 * g + 4 * q + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int lr = 4 * i + (lane >> 3);  // local row 0..31
+                            const int q = lane & 7;              // 16-byte piece of that row
+                            uint32_t w0, w1, w2, w3;
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                         : "r"(scratch + (uint32_t)lr * 128u + (uint32_t)((q ^ (lr & 7)) << 4)));
+                            const int t = t0 + lr;
+                            if (t < p.T)
+                                __stcs(reinterpret_cast<float4*>(p.O + ((size_t)head * p.T + t) * D + cD + 32 * g + 4 * q),
+                                       make_float4(__uint_as_float(w0), __uint_as_float(w1), __uint_as_float(w2),
+                                                   __uint_as_float(w3)));
+                        }
+                        __syncwarp();
                     }
                 }
                 drained(DO);
                 if (state_rows && has_next) {
+                    if (!wait_bar(CP, ph)) break;
+                    tc_fence_after();
                     drainD(tP_, tP);  // P0 of the next chunk -> sP
                     drained(DP);
                 }
@@ -776,23 +786,18 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 template <int D, int MODE>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
                      int T, SegPlan plan, int* status, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
-    if (MODE == 1) {
-        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32)) return cudaErrorInvalidValue;
-    } else {
-        mo = mq;  // unused
-    }
-    TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, status};
+    TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE>::kBytes + 1024;
     auto kern = tc_walk_kernel<D, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, prm);
+    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, prm);
     note_launches(1);
     return cudaGetLastError();
 }
