@@ -70,6 +70,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -253,7 +261,7 @@ struct Layout {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, TCParams p) {
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
     using LY = Layout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
@@ -514,6 +522,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             if (MODE == 1) {
                 if (!wait_bar(CA, ph)) break;
                 tc_fence_after();
+                if (lane == 0) tma_store_wait_read();  // this warp's O piece has left its sA rows
+                __syncwarp();
                 drain128(tA_, tA, true);  // A -> sA (masked)
                 drained(DA);
                 if (!wait_bar(CXS, ph)) break;
@@ -548,39 +558,32 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 if (!wait_bar(CO, ph)) break;
                 tc_fence_after();
                 {
-                    // O (fp32) to global memory through a per-warp transpose: the
-                    // 4 KB of sA that hold this warp's own rows and column half
-                    // (W_hi there is dead once the output products completed) take
-                    // 32 rows x 32 columns at a time, then each store instruction
-                    // writes four whole 128-byte row pieces.
+                    // O (fp32) leaves through the 4 KB of sA that hold this warp's
+                    // own rows and column half (W_hi there is dead once the output
+                    // products completed): 32 rows x 32 columns at a time, written
+                    // in the 128-byte-swizzled box layout and sent by a bulk tensor
+                    // store issued by this warp's lane 0.
                     uint32_t r[64];
                     tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
                     const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                     const int t0 = (c_begin + it) * kL + quarter * 32;  // first token of this warp's rows
 #pragma unroll
                     for (int g = 0; g < D / 64; ++g) {
-                        // this thread's row: 32 fp32 = 8 chunks of 16 bytes, swizzled
+                        if (g > 0) {
+                            if (lane == 0) tma_store_wait_read();  // previous piece has left the scratch
+                            __syncwarp();
+                        }
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
                                          r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
                                          r[32 * g + 4 * q + 3]);
+                        fence_proxy_async();
                         __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int lr = 4 * i + (lane >> 3);  // local row 0..31
-                            const int q = lane & 7;              // 16-byte piece of that row
-                            uint32_t w0, w1, w2, w3;
-                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                         : "r"(scratch + (uint32_t)lr * 128u + (uint32_t)((q ^ (lr & 7)) << 4)));
-                            const int t = t0 + lr;
-                            if (t < p.T)
-                                __stcs(reinterpret_cast<float4*>(p.O + ((size_t)head * p.T + t) * D + cD + 32 * g + 4 * q),
-                                       make_float4(__uint_as_float(w0), __uint_as_float(w1), __uint_as_float(w2),
-                                                   __uint_as_float(w3)));
+                        if (lane == 0) {
+                            tma_store_3d(&mO, scratch, cD + 32 * g, t0, head);
+                            tma_store_commit();
                         }
-                        __syncwarp();
                     }
                 }
                 drained(DO);
@@ -605,6 +608,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 }
             }
         }
+        if (MODE == 1 && lane == 0) tma_store_wait_all();
         // ---- segment summary out (mode 0): S | C | m | P | p records, fp32 ----
         if (MODE == 0 && state_rows && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
             tc_fence_after();
@@ -770,13 +774,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D map over [BH][T][cols] (innermost first), box {box_x, 128, 1}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int cols, int T, int BH, int box_x) {
+// 3-D map over [BH][T][cols] (innermost first), box {box_x, box_y, 1}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int cols, int T, int BH, int box_x,
+              int box_y = kL) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)cols * esize, (cuuint64_t)T * cols * esize};
-    cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)kL, 1};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_y, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -786,18 +791,24 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 template <int D, int MODE>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
                      int T, SegPlan plan, int* status, cudaStream_t s) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
+    if (MODE == 1) {
+        // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
+        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
+    } else {
+        mo = mq;  // unused
+    }
     TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE>::kBytes + 1024;
     auto kern = tc_walk_kernel<D, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, prm);
+    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, prm);
     note_launches(1);
     return cudaGetLastError();
 }
