@@ -51,6 +51,36 @@ exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t l
     if (total) total[(size_t)bh * total_stride + i] = run;
 }
 
+// Same scan, four consecutive elements per thread (16-byte accesses); used
+// when the element range, the record length and the pointers allow it.
+__global__ void __launch_bounds__(kScanThreads)
+exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
+               size_t total_stride) {
+    const size_t i = ((size_t)blockIdx.x * kScanThreads + threadIdx.x) * 4;
+    const int bh = blockIdx.y;
+    if (i >= len) return;
+    const float* pin = in + (size_t)bh * N * R + off + i;
+    float* pout = out + (size_t)bh * N * R + off + i;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    int r = 0;
+    for (; r + kScanUnroll <= N; r += kScanUnroll) {
+        float4 x[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
+            run.x += x[j].x; run.y += x[j].y; run.z += x[j].z; run.w += x[j].w;
+        }
+    }
+    for (; r < N; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(pin + (size_t)r * R);
+        *reinterpret_cast<float4*>(pout + (size_t)r * R) = run;
+        run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
+    }
+    if (total) *reinterpret_cast<float4*>(total + (size_t)bh * total_stride + i) = run;
+}
+
 // out = alpha*base + A [B | bx], 64 x 64 output tile per CTA, 4 x 4 per thread.
 constexpr int kTile = 64, kKs = 16;
 
@@ -127,8 +157,15 @@ __global__ void copy_strided_kernel(const float* src, long long s_src, float* ds
 cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
                           float* total, size_t total_stride, cudaStream_t s) {
     if (BH == 0 || len == 0) return cudaSuccess;
-    dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
-    exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+    const bool vec = ((off | len | R | total_stride) % 4 == 0) && ((reinterpret_cast<uintptr_t>(in) |
+                     reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(total)) % 16 == 0);
+    if (vec) {
+        dim3 grid((unsigned)((len / 4 + kScanThreads - 1) / kScanThreads), BH);
+        exscan4_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+    } else {
+        dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
+        exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+    }
     note_launches(1);
     return cudaGetLastError();
 }

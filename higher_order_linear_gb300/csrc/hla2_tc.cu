@@ -690,15 +690,28 @@ __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // operands: A rows a (K-major, rows >= D zero), B rows b (read MN-major)
-    for (int i = tid; i < 128 * D / 4; i += 256) {
-        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
-        const float4 x = r < D ? *reinterpret_cast<const float4*>(A + (size_t)r * D + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        put4_split(tAh, tAl, r, c, x);
-    }
-    for (int i = tid; i < D * D / 4; i += 256) {
-        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
-        put4_split(tBh, tBl, r, c, *reinterpret_cast<const float4*>(B + (size_t)r * D + c));
+    // operands: A rows a (K-major, rows >= D zero), B rows b (read MN-major).
+    // All of a thread's loads are issued before any conversion so that they
+    // overlap (the shared-memory stores are compiler barriers).
+    constexpr int kPer = D * D / 4 / 256;  // float4s of one D x D matrix per thread
+    {
+        float4 xa[kPer], xb[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * 256;
+            xa[j] = __ldg(reinterpret_cast<const float4*>(A) + i);
+            xb[j] = __ldg(reinterpret_cast<const float4*>(B) + i);
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * 256;
+            const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+            put4_split(tAh, tAl, r, c, xa[j]);
+            put4_split(tBh, tBl, r, c, xb[j]);
+        }
+        if (D < 128)
+            for (int i = D * D / 4 + tid; i < 128 * D / 4; i += 256)
+                put4_split(tAh, tAl, i / (D / 4), (i % (D / 4)) * 4, make_float4(0.f, 0.f, 0.f, 0.f));
     }
     fence_proxy_async();
     tc_fence_before();
