@@ -244,7 +244,8 @@ struct Layout {
     static constexpr uint32_t kSt = D * D * 2;        // S0 / P0 tiles
     static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq;
     static constexpr uint32_t P = X + kTok;                       // mode 1 only
-    static constexpr uint32_t S = (MODE == 1) ? P + kSt : X + kTok;
+    static constexpr uint32_t Q2 = X + kTok;                      // mode 0: second Q buffer
+    static constexpr uint32_t S = (MODE == 1) ? P + kSt : Q2 + kTok;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
@@ -265,7 +266,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     using LY = Layout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
-    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, NBAR };
+    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -287,6 +288,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
+    const Tile tQ2{dsm + LY::Q2, kL};  // summary walk: Q of odd chunks (two Q buffers)
     const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
@@ -410,12 +412,17 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             issue_load(LQ, &mQ, tQ, c_begin);
             issue_load(LK, &mK, tK, c_begin);
             issue_load(LV, &mV, tV, c_begin);
+            if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
             int it = 0;
             for (; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
+                // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
+                const bool qodd = MODE == 0 && (it & 1);
+                const Tile& tQc = qodd ? tQ2 : tQ;
+                const uint32_t qph = MODE == 0 ? (uint32_t)((it >> 1) & 1) : ph;
+                if (!wait_bar(qodd ? LQ2 : LQ, qph) || !wait_bar(LK, ph)) break;
                 if (MODE == 1) {
                     if (it > 0 && !wait_bar(DO, pph)) break;  // O of the previous chunk read out of TMEM A
                     tc_fence_after();
@@ -455,7 +462,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (!wait_bar(LV, ph)) break;
                     tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
+                    if (c == 0)  // W_lo V: the head's first chunk only (see the drain)
+                        for (int ks = 0; ks < kL / 16; ++ks)
+                            mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CO));
                     if (!wait_bar(DX2, ph)) break;  // sX = X
                     tc_fence_after();
@@ -474,7 +483,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         tc_fence_after();
                     }
                     // A = Q K^T
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                     mma_commit(bar(CA));
                     if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
@@ -488,7 +497,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     tc_fence_after();
                     // X = Q S_local + A K   (no S_local term on the segment's first chunk)
                     if (it > 0)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CX2));
@@ -496,7 +505,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     tc_fence_after();
                     // C += Q^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                        mma_bf16(tC_, tQc.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CQ));
                     if (!wait_bar(DX, ph)) break;  // sX = X
                     tc_fence_after();
@@ -505,9 +514,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CP));
-                    if (has_next) {
+                    if (it + 2 < nchunks) {
                         if (!wait_bar(CQ, ph)) break;
-                        issue_load(LQ, &mQ, tQ, c + 1);
+                        issue_load(qodd ? LQ2 : LQ, &mQ, tQc, c + 2);  // this buffer's next chunk
+                    }
+                    if (has_next) {
                         if (!wait_bar(CP, ph)) break;
                         issue_load(LV, &mV, tV, c + 1);
                     }
@@ -538,18 +549,26 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 tc_fence_after();
                 {
                     // X is read out first (W_lo lands on this warp's X columns),
-                    // W is announced before X because the output products need it first
+                    // W is announced before X because the output products need it first.
+                    // On the head's first chunk W is split into bf16 hi + lo: there an
+                    // output can be a single product (t = 0 gives (q.k)^2 v), so the
+                    // rounding of W is not averaged over many terms.  Later chunks
+                    // add the prefix term and many products, and plain bf16 W suffices.
                     uint32_t x[64];
                     tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
-                    uint32_t lo[32];
-                    {
-                        uint32_t r[64];
-                        tmem_ld_cols<64>(tA_ + lane_off + c128, r);
-                        put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
-                        put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
+                    if (c_begin + it == 0) {
+                        uint32_t lo[32];
+                        {
+                            uint32_t r[64];
+                            tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                            put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
+                            put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
+                        }
+                        tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
+                        tmem_st_wait();
+                    } else {
+                        drain128(tA_, tA, true);  // W -> sA (masked)
                     }
-                    tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
-                    tmem_st_wait();
                     drained(DW);
                     put_row32(tX, row, cD, x, false);  // X -> sX
                     if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
