@@ -229,7 +229,7 @@ def main():
         return
     import torch
     import torch.distributed as dist
-    from higher_order_linear_gb300 import build as hbuild, hla2, workloads as W
+    from higher_order_linear_gb300 import build as hbuild, hla2, replicas, workloads as W
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -249,11 +249,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return replicas.max_over_ranks(x, dev)
 
     peaks = load_peaks()
     w = W.WORKLOADS[FWD_WORKLOAD]
@@ -292,7 +288,7 @@ def main():
     status = hla2.hla2_device_status()
     if status != 0:
         raise SystemExit(f"device status {status}: {hla2.hla2_last_error_detail()}")
-    value = world * tokens / (ms_step_max / 1e3) if fwd_steps else 0.0
+    value = replicas.job_throughput(tokens, world, ms_step_max) if fwd_steps else 0.0
 
     # dominant kernel: segment outputs (phase 2)
     out_ms = phase_ms[2] / max(nfwd, 1)
