@@ -70,6 +70,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
         : "memory");
 }
+// Pull a tile into L2 ahead of its TMA load (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
@@ -413,11 +419,28 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             issue_load(LK, &mK, tK, c_begin);
             issue_load(LV, &mV, tV, c_begin);
             if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
+            if (nchunks > 1) {
+#pragma unroll
+                for (int k = 0; k < D / 64; ++k) {
+                    tma_prefetch_l2_3d(&mQ, k * 64, (c_begin + 1) * kL, head);
+                    tma_prefetch_l2_3d(&mK, k * 64, (c_begin + 1) * kL, head);
+                    tma_prefetch_l2_3d(&mV, k * 64, (c_begin + 1) * kL, head);
+                }
+            }
             int it = 0;
             for (; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
+                // the tiles two chunks ahead start moving into L2 now
+                if (it + 2 < nchunks) {
+#pragma unroll
+                    for (int k = 0; k < D / 64; ++k) {
+                        tma_prefetch_l2_3d(&mQ, k * 64, (c + 2) * kL, head);
+                        tma_prefetch_l2_3d(&mK, k * 64, (c + 2) * kL, head);
+                        tma_prefetch_l2_3d(&mV, k * 64, (c + 2) * kL, head);
+                    }
+                }
                 // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
                 const bool qodd = MODE == 0 && (it & 1);
                 const Tile& tQc = qodd ? tQ2 : tQ;
@@ -443,12 +466,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tA.kmaj(ks), iSq, ks > 0);
                     if (!wait_bar(DX, ph)) break;  // sX = bf16(Q S0); TMEM X read
                     tc_fence_after();
+                    // X = Q S0 + A K  (before the last W term, so that W completes last
+                    // and its drain, which also waits for this product, starts at once)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                    mma_commit(bar(CX2));
                     // W += (Q S0) Q^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                     mma_commit(bar(CW));
-                    // X = Q S0 + A K
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                    mma_commit(bar(CX2));
                     if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
                     tc_fence_after();
                     if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
