@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-forward", action="store_true", help="skip the forward (profiling the decode step alone)")
     p.add_argument("--T", type=int, default=None, help="override T (profiling a smaller case; not a bench line)")
     p.add_argument("--H", type=int, default=None, help="override H (profiling a smaller case; not a bench line)")
+    p.add_argument("--workload", type=int, default=FWD_WORKLOAD,
+                   help="forward workload id (0-3, see workloads.py); the bench line is workload 3")
     return p.parse_args()
 
 
@@ -170,11 +172,17 @@ def oracle_sample(w, seconds: float):
 
 
 # ----------------------------------------------------------------- config --
-def fwd_config(w, plan_segments=None):
+def fwd_config(w, plan_segments=None, l2_note=None):
     return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "input_dtype": w.dtype,
             "output_dtype": "fp32", "normalized": w.normalized, "segments_per_head": plan_segments,
-            "l2": "inputs exceed L2 (1.34 GB moved per step vs 129 MB L2); no flush",
+            "l2": l2_note or "inputs exceed L2 (1.34 GB moved per step vs 129 MB L2); no flush",
             "parallelism": "replicas (heads independent, no collective)"}
+
+
+def alg_flops(w, L=64):
+    """Algorithmic flops per token-head of the chunked forward (fixed count,
+    chunk L = 64): 2 [2 L d + L^2 + 2 d^2 + 2 L dv + 3 d dv]."""
+    return 2 * (2 * L * w.d + L * L + 2 * w.d * w.d + 2 * L * w.dv + 3 * w.d * w.dv)
 
 
 def segments_per_head(BH, T):
@@ -252,38 +260,58 @@ def main():
         return replicas.max_over_ranks(x, dev)
 
     peaks = load_peaks()
-    w = W.WORKLOADS[FWD_WORKLOAD]
+    w = W.WORKLOADS[args.workload]
     if args.T or args.H:
         import dataclasses
         w = dataclasses.replace(w, T=args.T or w.T, H=args.H or w.H, name=w.name + f"-override-H{args.H or w.H}-T{args.T or w.T}")
     tokens = w.BH * w.T
-    bytes_per_token = 2 * (2 * w.d + w.dv) + 4 * w.dv  # read Q,K,V bf16 once, write O fp32 once
+    esz = 2 if w.dtype == "bf16" else 4
+    bytes_per_token = esz * (2 * w.d + w.dv) + 4 * w.dv  # read Q,K,V once, write O fp32 once
     q, k, v = W.make_inputs_on(w, dev, seed=w.seed + 1000 * rank)
     O = torch.empty(w.B, w.H, w.T, w.dv, device=dev, dtype=torch.float32)
-    need = hla2.hla2_forward_workspace(w.B, w.H, w.T, w.d, w.dv, hla2.HLA2_DTYPE_BF16)
+    dcode = hla2.HLA2_DTYPE_BF16 if w.dtype == "bf16" else hla2.HLA2_DTYPE_F32
+    need = hla2.hla2_forward_workspace(w.B, w.H, w.T, w.d, w.dv, dcode)
     ws = torch.empty(need, device=dev, dtype=torch.uint8)
-    path = "tcgen05" if L.hla2_forward_path(w.d, w.dv, hla2.HLA2_DTYPE_BF16, 0, 0) == 1 else "cuda-core"
+    path = "tcgen05" if L.hla2_forward_path(w.d, w.dv, dcode, int(w.normalized), 0) == 1 else "cuda-core"
 
     clocks = ClockSampler(local)
     clocks.start()
     fwd_steps = 0 if args.no_forward else args.steps
     for _ in range(0 if args.no_forward else args.warmup):
-        hla2.hla2_forward(q, k, v, O, workspace=ws)
+        hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
     barrier()
     hla2.hla2_profile_read()
     hla2.hla2_profile_enable(True)
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Workloads whose step moves less than 4x the 129 MB L2 flush it (outside
+    # the timed events) before every step; larger ones stream from HBM anyway.
+    step_bytes = bytes_per_token * tokens
+    flush = step_bytes < 4 * 129e6
+    l2_note = ("L2 flushed before every step (256 MB write outside the timed events)" if flush else
+               f"inputs exceed L2 ({step_bytes / 1e9:.2f} GB moved per step vs 129 MB L2); no flush")
+    scratch = torch.empty(64 << 20, device=dev, dtype=torch.float32) if flush else None
     t_begin = time.time()
-    e0.record(stream)
-    for _ in range(fwd_steps):
-        hla2.hla2_forward(q, k, v, O, workspace=ws)
-    e1.record(stream)
-    barrier()
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(fwd_steps)]
+        for ea, eb in evs:
+            scratch.zero_()
+            ea.record(stream)
+            hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+            eb.record(stream)
+        barrier()
+        ms_total = sum(ea.elapsed_time(eb) for ea, eb in evs)
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(fwd_steps):
+            hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+        e1.record(stream)
+        barrier()
+        ms_total = e0.elapsed_time(e1)
     t_end = time.time()
     hla2.hla2_profile_enable(False)
     phase_ms, nfwd, launches = hla2.hla2_profile_read()
-    ms_step = e0.elapsed_time(e1) / max(fwd_steps, 1)
+    ms_step = ms_total / max(fwd_steps, 1)
     ms_step_max = max_over_ranks(ms_step)
     status = hla2.hla2_device_status()
     if status != 0:
@@ -302,7 +330,7 @@ def main():
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)" if peaks["source"] == "measured"
                 else "fallback 6.8 TB/s",
                 "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"] if fwd_steps else 0.0,
-                "tensor_frac_of_bf16_burst": (237568 * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
+                "tensor_frac_of_bf16_burst": (alg_flops(w) * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
                 if fwd_steps else 0.0}
 
     # ---- e2e through the public API with pinned host buffers ----
@@ -314,14 +342,14 @@ def main():
         dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         for _ in range(2):
             dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
-            hla2.hla2_forward(dq, dk, dvv, O, workspace=ws)
+            hla2.hla2_forward(dq, dk, dvv, O, normalized=w.normalized, workspace=ws)
             hO.copy_(O, non_blocking=True)
         barrier()
         e2 = torch.cuda.Event(enable_timing=True); e3 = torch.cuda.Event(enable_timing=True)
         e2.record(stream)
         for _ in range(n_e2e):
             dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
-            hla2.hla2_forward(dq, dk, dvv, O, workspace=ws)
+            hla2.hla2_forward(dq, dk, dvv, O, normalized=w.normalized, workspace=ws)
             hO.copy_(O, non_blocking=True)
         e3.record(stream)
         barrier()
@@ -358,7 +386,27 @@ def main():
                   "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC.get("step"),
                                "bytes_per_head_step": bytes_head}}
-        del toks, state
+        # the same stream on the compact P-form state (S | P | p), converted from the prefilled state
+        Rp = hla2.pform_record_len(wd.d, wd.dv)
+        del state
+        pstate = torch.zeros(wd.n, Rp, device=dev)
+        for t in range(wd.prefill):
+            hla2.hla2_step_pform(pstate, *toks[t])
+        barrier()
+        e6 = torch.cuda.Event(enable_timing=True); e7 = torch.cuda.Event(enable_timing=True)
+        e6.record(stream)
+        for t in range(wd.prefill, wd.prefill + wd.steps):
+            hla2.hla2_step_pform(pstate, *toks[t], o=o)
+        e7.record(stream)
+        barrier()
+        ms_pf = max_over_ranks(e6.elapsed_time(e7) / wd.steps)
+        bytes_pf = 8 * Rp + 4 * (2 * wd.d + 2 * wd.dv)
+        ach_pf = wd.n * bytes_pf / (ms_pf / 1e3) / 1e9
+        decode["pform"] = {"metric": "hla2_step_pform tokens/s (heads*steps/s)", "value": world * wd.n / (ms_pf / 1e3),
+                           "unit": "tokens/s", "ms_per_step": ms_pf,
+                           "roofline": {"bound": "hbm", "achieved": ach_pf, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": ach_pf / peaks["hbm_gbs"], "bytes_per_head_step": bytes_pf}}
+        del toks, pstate
     clk = clocks.stop(t_begin, t_end)
 
     cpu = None
@@ -370,7 +418,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
-                "config": fwd_config(w, segments_per_head(w.BH, w.T)), "path": path,
+                "config": fwd_config(w, segments_per_head(w.BH, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
                 "cpu_baseline": cpu, "decode": decode}
         print(json.dumps(line), flush=True)

@@ -8,9 +8,13 @@ from .hla2 import (  # noqa: F401
     hla2_chunk_summaries,
     hla2_device_status,
     hla2_forward,
+    hla2_forward_noalloc,
     hla2_forward_workspace,
     hla2_last_error_detail,
     hla2_scan,
+    hla2_state_to_pform,
     hla2_step,
+    hla2_step_pform,
+    pform_record_len,
     record_len,
 )

@@ -283,6 +283,51 @@ int hla2_step(float* state, const float* q, const float* k, const float* v, floa
     return HLA2_OK;
 }
 
+int hla2_step_pform(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,
+                    int normalized, hla2_stream_t stream) {
+    if (!state || !q || !k || !v || !o) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    auto pow2_4_128 = [](int x) { return x >= 4 && x <= 128 && (x & (x - 1)) == 0; };
+    if (!pow2_4_128(d) || !pow2_4_128(dv))
+        return fail(HLA2_ERR_UNSUPPORTED, "hla2_step_pform needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
+    cudaError_t e = launch_step_pform(state, q, k, v, o, n, d, dv, normalized, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_step_pform");
+    return HLA2_OK;
+}
+
+int hla2_state_to_pform(const float* gstate, float* pstate, int n, int d, int dv, hla2_stream_t stream) {
+    if (!gstate || !pstate) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(gstate) || !aligned16(pstate)) return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    if (d > 128 || dv > 128) return fail(HLA2_ERR_UNSUPPORTED, "d, dv must be <= 128");
+    const RecOff g = decode_offsets(d, dv);
+    const long long Rg = (long long)g.R;
+    const long long Rp = (long long)d * d + (long long)d * dv + d;
+    if (gstate < pstate + n * Rp && pstate < gstate + n * Rg) return fail(HLA2_ERR_INVALID, "gstate and pstate overlap");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (long long b0 = 0; b0 < n; b0 += 65535) {
+        const int nb = (int)((n - b0) < 65535 ? (n - b0) : 65535);
+        const float* gs = gstate + b0 * Rg;
+        float* ps = pstate + b0 * Rp;
+        cudaError_t e = launch_copy_strided(gs + g.S, Rg, ps, Rp, (size_t)d * d, nb, s);
+        if (e != cudaSuccess) return cuda_fail(e, "hla2_state_to_pform: copy S");
+        CrossArgs a{};
+        a.A = gs + g.S; a.sA = Rg;                 // S
+        a.B = gs + g.C; a.sB = Rg;                 // C
+        a.bx = gs + g.m; a.sbx = Rg;               // m (extra column)
+        a.base = gs + g.X; a.sbase = Rg;           // G
+        a.basex = gs + g.x; a.sbasex = Rg;         // h
+        a.out = ps + (size_t)d * d; a.sout = Rp;   // P = S C - G
+        a.outx = ps + (size_t)d * d + (size_t)d * dv; a.soutx = Rp;  // p = S m - h
+        a.alpha = -1.f; a.d = d; a.dv = dv; a.nb = nb;
+        e = launch_cross(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "hla2_state_to_pform: products");
+    }
+    return HLA2_OK;
+}
+
 int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* summ, int B, int H, int T, int d,
                          int dv, int L, int dtype, hla2_stream_t stream) {
     int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);

@@ -217,3 +217,138 @@ cudaError_t launch_step(float* state, const float* q, const float* k, const floa
 }
 
 }  // namespace hla2
+
+// ---------------------------------------------------------------------------
+// Compact P-form decode state: S (d x d) | P = S C - G (d x dv) | p = S m - h (d).
+// The same outputs with a third fewer state bytes at d = dv, because
+//   S_t = S + k k^T,  u = S_t q,  o = q^T P_{t-1} + (q . u) v,
+//   P_t = P + u v^T,  p_t = p + u,  den = q . p_t
+// (P_t - P_{t-1} = S_t q_t v_t^T).  Two passes: S (row reductions give u),
+// then P (column reductions give q^T P_{t-1} while P is updated).
+// ---------------------------------------------------------------------------
+namespace hla2 {
+namespace {
+
+__global__ void __launch_bounds__(kThreads)
+step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const float* __restrict__ k,
+                  const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized) {
+    __shared__ __align__(16) float sq[128], sk[128], sv[128], su[128], sy[128];
+    __shared__ __align__(16) float part[kThreads][4];
+    __shared__ float sdots[2];
+
+    const int head = blockIdx.x;
+    const int tid = threadIdx.x;
+    const size_t R = (size_t)d * d + (size_t)d * dv + (size_t)d;
+    float* S = state + (size_t)head * R;
+    float* P = S + (size_t)d * d;
+    float* p = P + (size_t)d * dv;
+
+    if (tid < d) {
+        sq[tid] = q[(size_t)head * d + tid];
+        sk[tid] = k[(size_t)head * d + tid];
+        su[tid] = 0.f;
+    }
+    if (tid < dv) sv[tid] = v[(size_t)head * dv + tid];
+    __syncthreads();
+
+    // ---- pass S: S' = S + k k^T ; u = S' q ---------------------------------
+    {
+        const int g = d >> 2;
+        const int nf = (d * d) >> 2;
+        for (int base = 0; base < nf; base += kThreads * kUnroll) {
+            float4 r[kUnroll];
+#pragma unroll
+            for (int i = 0; i < kUnroll; ++i) {
+                const int f = base + i * kThreads + tid;
+                if (f < nf) r[i] = ld_stream(S + 4 * (size_t)f);
+            }
+#pragma unroll
+            for (int i = 0; i < kUnroll; ++i) {
+                const int f = base + i * kThreads + tid;
+                float part_u = 0.f;
+                int a = 0;
+                if (f < nf) {
+                    a = f / g;
+                    const int b = (f - a * g) * 4;
+                    const float ka = sk[a];
+                    float4 x = r[i];
+                    x.x = fmaf(ka, sk[b + 0], x.x);
+                    x.y = fmaf(ka, sk[b + 1], x.y);
+                    x.z = fmaf(ka, sk[b + 2], x.z);
+                    x.w = fmaf(ka, sk[b + 3], x.w);
+                    st_stream(S + 4 * (size_t)f, x);
+                    part_u = x.x * sq[b] + x.y * sq[b + 1] + x.z * sq[b + 2] + x.w * sq[b + 3];
+                }
+                for (int off = g >> 1; off > 0; off >>= 1) part_u += __shfl_xor_sync(0xffffffffu, part_u, off);
+                if (f < nf && (tid & (g - 1)) == 0) su[a] += part_u;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- pass P: y = P^T q (old P), P' = P + u v^T -------------------------
+    const int gc = dv >> 2;
+    const int rows_per = kThreads / gc;
+    const int c4 = tid % gc;
+    const int rg = tid / gc;
+    {
+        float py[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4 v4 = *reinterpret_cast<const float4*>(&sv[4 * c4]);
+        for (int a0 = 0; a0 < d; a0 += rows_per * kUnroll) {
+            float4 r[kUnroll];
+#pragma unroll
+            for (int i = 0; i < kUnroll; ++i) {
+                const int a = a0 + i * rows_per + rg;
+                if (a < d) r[i] = ld_stream(P + (size_t)a * dv + 4 * c4);
+            }
+#pragma unroll
+            for (int i = 0; i < kUnroll; ++i) {
+                const int a = a0 + i * rows_per + rg;
+                if (a < d) {
+                    const float qa = sq[a], ua = su[a];
+                    float4 x = r[i];
+                    py[0] = fmaf(qa, x.x, py[0]); py[1] = fmaf(qa, x.y, py[1]);
+                    py[2] = fmaf(qa, x.z, py[2]); py[3] = fmaf(qa, x.w, py[3]);
+                    x.x = fmaf(ua, v4.x, x.x); x.y = fmaf(ua, v4.y, x.y);
+                    x.z = fmaf(ua, v4.z, x.z); x.w = fmaf(ua, v4.w, x.w);
+                    st_stream(P + (size_t)a * dv + 4 * c4, x);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[tid][j] = py[j];
+    }
+    // q . u and, normalised, p' = p + u and q . p'
+    if (tid < 32) {
+        float qu = 0.f, qp = 0.f;
+        for (int a = tid; a < d; a += 32) {
+            const float pn = p[a] + su[a];
+            qu += sq[a] * su[a];
+            qp += sq[a] * pn;
+            p[a] = pn;
+        }
+        qu = warp_sum(qu); qp = warp_sum(qp);
+        if (tid == 0) { sdots[0] = qu; sdots[1] = qp; }
+    }
+    __syncthreads();
+    if (tid < dv) {
+        const int cc = tid >> 2, j = tid & 3;
+        float y = 0.f;
+        for (int r = 0; r < rows_per; ++r) y += part[r * gc + cc][j];
+        float out = y + sdots[0] * sv[tid];
+        if (normalized) out = out / sdots[1];
+        o[(size_t)head * dv + tid] = out;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o, int n, int d,
+                              int dv, int normalized, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    step_pform_kernel<<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace hla2

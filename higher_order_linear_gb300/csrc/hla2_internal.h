@@ -68,6 +68,9 @@ struct SegPlan {
 // ---- decode step (hla2_decode.cu) ----
 cudaError_t launch_step(float* state, const float* q, const float* k, const float* v, float* o,
                         int n, int d, int dv, int normalized, cudaStream_t s);
+// Same step on the compact P-form state S | P | p.
+cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o,
+                              int n, int d, int dv, int normalized, cudaStream_t s);
 
 // ---- segment walks on CUDA cores (hla2_walk.cu) ----
 // mode 0: P-form segment summary  S|C|m|P|p from zero state.

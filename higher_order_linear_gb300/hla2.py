@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.hla2_forward_path.restype = i
             L.hla2_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
             L.hla2_forward_noalloc.restype = i
+            L.hla2_step_pform.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+            L.hla2_step_pform.restype = i
+            L.hla2_state_to_pform.argtypes = [vp, vp, i, i, i, vp]
+            L.hla2_state_to_pform.restype = i
             _lib = L
         return _lib
 
@@ -183,6 +187,40 @@ def hla2_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Te
                          n, d, dv, int(bool(normalized)), _stream(stream))
     _check(rc, "hla2_step")
     return o
+
+
+def pform_record_len(d: int, dv: int) -> int:
+    return d * d + d * dv + d
+
+
+def hla2_step_pform(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """Decode step on the compact P-form state [n, d*d + d*dv + d] (S | P | p)."""
+    n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * pform_record_len(d, dv):
+        raise ValueError("shape mismatch for hla2_step_pform")
+    if o is None:
+        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
+    rc = lib().hla2_step_pform(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
+                               _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
+                               _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized)), _stream(stream))
+    _check(rc, "hla2_step_pform")
+    return o
+
+
+def hla2_state_to_pform(gstate: torch.Tensor, d: int, dv: int, pstate: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """S|C|G|m|h decode states -> S|P|p (P = S C - G, p = S m - h)."""
+    n = gstate.numel() // record_len(d, dv)
+    if gstate.numel() != n * record_len(d, dv):
+        raise ValueError("gstate size is not a whole number of records")
+    if pstate is None:
+        pstate = torch.empty((n, pform_record_len(d, dv)), device=gstate.device, dtype=torch.float32)
+    rc = lib().hla2_state_to_pform(_dev(gstate, "gstate", torch.float32), _dev(pstate, "pstate", torch.float32),
+                                   n, d, dv, _stream(stream))
+    _check(rc, "hla2_state_to_pform")
+    return pstate
 
 
 def hla2_chunk_summaries(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, L: int,

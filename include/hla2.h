@@ -135,6 +135,26 @@ HLA2_API int hla2_step(float* state, const float* q, const float* k, const float
               int n, int d, int dv, int normalized, hla2_stream_t stream);
 
 /*
+ * hla2_step on the compact "P-form" decode state [HLA §1 online update,
+ * rewritten with P = S C - G and p = S m - h]:
+ *   state  [n][d*d + d*dv + d] fp32, per head S (d x d) | P (d x dv) | p (d).
+ * The step computes S' = S + k k^T, u = S' q, o = q^T P + (q.u) v,
+ * P' = P + u v^T, p' = p + u (normalised: o /= q.p'), i.e. the same o_t as
+ * hla2_step, moving a third fewer state bytes at d = dv.  Same argument
+ * rules and errors as hla2_step; a zero state is the empty prefix.
+ */
+HLA2_API int hla2_step_pform(float* state, const float* q, const float* k, const float* v, float* o,
+                             int n, int d, int dv, int normalized, hla2_stream_t stream);
+
+/*
+ * Converts n decode states from the hla2_step layout S|C|G|m|h to the P-form
+ * layout S|P|p (P = S C - G, p = S m - h, fp32 products).  gstate and
+ * pstate must not overlap.  Errors as for hla2_step (d, dv <= 128).
+ */
+HLA2_API int hla2_state_to_pform(const float* gstate, float* pstate, int n, int d, int dv,
+                                 hla2_stream_t stream);
+
+/*
  * Summary of every chunk of L consecutive tokens [HLA §4, segment summaries]:
  * the state the recurrence of [HLA §1] reaches from zero on that chunk alone.
  *   summ  [B][H][N][d*d + 2*d*dv + 2*d] fp32, N = ceil(T/L), record

@@ -187,6 +187,23 @@ def summary_to_decode_state(rec, d: int, dv: int) -> np.ndarray:
     return np.concatenate([S, C, G, m, h], axis=-1)
 
 
+def summary_to_pform_state(rec, d: int, dv: int) -> np.ndarray:
+    """Summary record S|C|m|G|h -> P-form decode state S|P|p with
+    P = S C - G and p = S m - h (HLA summary, section 1: G and h remove the
+    future terms of the naive product, so P and p are the masked products)."""
+    rec = _f64(rec)
+    nS, nC = d * d, d * dv
+    S = rec[..., :nS].reshape(*rec.shape[:-1], d, d)
+    C = rec[..., nS:nS + nC].reshape(*rec.shape[:-1], d, dv)
+    m = rec[..., nS + nC:nS + nC + d]
+    G = rec[..., nS + nC + d:nS + 2 * nC + d].reshape(*rec.shape[:-1], d, dv)
+    h = rec[..., nS + 2 * nC + d:]
+    P = S @ C - G
+    p = np.einsum("...ab,...b->...a", S, m) - h
+    lead = rec.shape[:-1]
+    return np.concatenate([S.reshape(*lead, nS), P.reshape(*lead, nC), p], axis=-1)
+
+
 def dense_causal_aatv(Q, K, V, normalized: bool = False) -> np.ndarray:
     """Independent statement through library matmuls: A = tril(Q K^T),
     O = tril(A A^T) V (HLA summary, section 2 names the A A^T V structure;

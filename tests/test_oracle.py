@@ -249,3 +249,21 @@ def test_planted_mistakes_fail_a_pin(mutant):
     b = oracle.chunk_summaries(Q[:, 5:], K[:, 5:], V[:, 5:], L=7, mutant=mutant)[0, 0]
     bad_combine = rel(oracle.combine(a, b, d, dv, mutant=mutant), whole) > 1e-6
     assert bad_serial or bad_combine
+
+
+def test_pform_state_is_the_masked_product():
+    """P = S C - G and p = S m - h equal the masked sums
+    sum_{i<=j} k_i k_i^T q_j v_j^T and sum_{i<=j} k_i (k_i . q_j) (explicit loops)."""
+    rng = np.random.default_rng(15)
+    d, dv, T = 4, 3, 11
+    Q, K, V = rand_inputs(rng, 1, T, d, dv)
+    rec = oracle.chunk_summaries(Q, K, V, L=T)[0, 0]
+    pst = oracle.summary_to_pform_state(rec, d, dv)
+    q, k, v = Q[0], K[0], V[0]
+    P = np.zeros((d, dv)); p = np.zeros(d)
+    for j in range(T):
+        for i in range(j + 1):
+            P += np.outer(k[i] * (k[i] @ q[j]), v[j])
+            p += k[i] * (k[i] @ q[j])
+    expect = np.concatenate([(k.T @ k).ravel(), P.ravel(), p])
+    assert rel(pst, expect) < 1e-13
