@@ -228,7 +228,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (prof) cudaEventRecord(pe.ev[0], s);
 
     // segment summaries
-    if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, plan, status, s);
+    if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, status, s);
     else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
@@ -237,7 +237,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (rc) return rc;
     if (prof) cudaEventRecord(pe.ev[2], s);
     // outputs
-    if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, plan, status, s);
+    if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, status, s);
     else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment outputs");
     if (prof) {

@@ -115,7 +115,7 @@ cudaError_t launch_copy_strided(const float* src, long long s_src, float* dst, l
 bool tc_supported(int d, int dv, int dtype, int normalized, int device);
 cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V,
                            float* O, const float* prefix, float* summ,
-                           int BH, int T, int d, int dv, SegPlan plan, int* status,
+                           int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
                            cudaStream_t s);
 // Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
 // (d = dv in {64, 128}, no extra column).

@@ -142,6 +142,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -216,6 +224,17 @@ __device__ __forceinline__ void put_row32_split(const Tile& t, int r, int col0, 
     }
 }
 
+// Same split, hi to tile `hi` and lo to tile `lo` (both bf16 operands).
+__device__ __forceinline__ void put_row32_split2(const Tile& hi, const Tile& lo, int r, int col0, const uint32_t* v,
+                                                 bool mask) {
+    uint32_t l[16];
+    put_row32_split(hi, r, col0, v, mask, l);
+    const int b = col0 >> 6;
+    const int c0 = (col0 & 63) >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) st_shared_v4(lo.chunk(r, b, c0 + q), l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+}
+
 // Load NC (32 or 64) consecutive TMEM columns of this thread's lane, one wait.
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) {
@@ -242,7 +261,7 @@ struct TCParams {
     int* status;
 };
 
-template <int D, int MODE>
+template <int D, int MODE, bool NORM = false>
 struct Layout {
     // byte offsets of the tiles inside the 1024-aligned dynamic shared memory
     static constexpr uint32_t kTok = kL * D * 2;      // Q, K, V, X tiles
@@ -252,10 +271,18 @@ struct Layout {
     static constexpr uint32_t P = X + kTok;                       // mode 1 only
     static constexpr uint32_t Q2 = X + kTok;                      // mode 0: second Q buffer
     static constexpr uint32_t S = (MODE == 1) ? P + kSt : Q2 + kTok;
+    static constexpr uint32_t kEnd = S + kSt;
+    // ratio-normalised walks: bf16 lo halves of the split operands, a tile of
+    // ones (16 x 128, the extra value column) and p0 as an operand (16 x D)
+    static constexpr uint32_t Alo = kEnd, Xlo = Alo + kSq, Slo = Xlo + kTok;
+    static constexpr uint32_t Plo = Slo + kSt;                    // mode 1 only
+    static constexpr uint32_t Ones = (MODE == 1) ? Plo + kSt : Slo + kSt;
+    static constexpr uint32_t P0h = Ones + 4096, P0l = P0h + 2048;  // mode 1 only
+    static constexpr uint32_t kNormEnd = (MODE == 1) ? P0l + 2048 : Ones + 4096;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
-    static constexpr uint32_t kBytes = S + kSt + kPad;
+    static constexpr uint32_t kBytes = (NORM ? kNormEnd : kEnd) + kPad;
 };
 
 // Warp roles.  Warps 0..7 drain tensor memory: warp w owns TMEM lane quarter
@@ -265,11 +292,19 @@ struct Layout {
 // drained region is announced on a barrier (one arrival per drain warp) that
 // the issuer waits on before it overwrites the region or reads what the
 // drain wrote.  Drains thus overlap the MMAs that do not depend on them.
-template <int D, int MODE>
+//
+// NORM (ratio-normalised variant, D = 64): every fp32 intermediate that
+// feeds a product (A, Q S0, X, W, S0, P0, p0) is split into bf16 hi + lo
+// parts and the product is taken on both parts (hi*hi + hi*lo + lo*hi for
+// A A^T), which keeps about 16 significant bits.  The extra value column of
+// ones (V -> [V | 1]) is a 16-column tile of ones: the denominator is
+// Q p0 + W 1 and p grows by X^T 1 (the summary walk also gathers m = Q^T 1),
+// all N = 16 products into their own tensor-memory columns.
+template <int D, int MODE, bool NORM>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
-    using LY = Layout<D, MODE>;
+    using LY = Layout<D, MODE, NORM>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
     enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, NBAR };
@@ -296,6 +331,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
     const Tile tQ2{dsm + LY::Q2, kL};  // summary walk: Q of odd chunks (two Q buffers)
     const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
+    // normalised walks only
+    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL}, tSl{dsm + LY::Slo, D}, tPl{dsm + LY::Plo, D};
+    const Tile tOnes{dsm + LY::Ones, 16}, tP0h{dsm + LY::P0h, 16}, tP0l{dsm + LY::P0l, 16};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
@@ -314,6 +352,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (NORM && tid < 256) {
+        // the ones tile (4 KB of bf16 1.0) and, in the output walk, zeroed p0 tiles
+        const uint32_t one2 = 0x3F803F80u;
+        st_shared_v4(tOnes.base + (uint32_t)tid * 16u, one2, one2, one2, one2);
+        if (MODE == 1) st_shared_v4(tP0h.base + (uint32_t)tid * 16u, 0u, 0u, 0u, 0u);  // P0h and P0l
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -324,6 +368,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const uint32_t tS_ = tmem + (MODE == 1 ? 256 : 128);
     const uint32_t tP_ = tmem + (MODE == 1 ? 256 + D : 128 + D);
     const uint32_t tC_ = tmem + 128 + 2 * D;  // mode 0 only
+    // normalised walks: p (16 columns, column 0 used) and the denominator
+    // (mode 1) or m (mode 0), after the regions above
+    const uint32_t tPn_ = tmem + (MODE == 1 ? 256 + 2 * D : 128 + 3 * D);
+    const uint32_t tDen_ = tPn_ + 16;  // mode 1: denominator;  mode 0: m
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int c128 = half * 64;      // this drain warp's columns in a 128-wide region
     const int cD = half * (D / 2);   // ... and in a D-wide region
@@ -368,6 +416,29 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         put_row32(t, row, cD, r, false);
         if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
     };
+    // split drains (normalised walks): hi to one tile, lo to another
+    auto drain128s = [&](uint32_t treg, const Tile& hi, const Tile& lo, bool mask) {
+        uint32_t r[64];
+        tmem_ld_cols<64>(treg + lane_off + c128, r);
+        put_row32_split2(hi, lo, row, c128, r, mask);
+        put_row32_split2(hi, lo, row, c128 + 32, r + 32, mask);
+    };
+    auto drainDs = [&](uint32_t treg, const Tile& hi, const Tile& lo) {
+        uint32_t r[64];
+        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        put_row32_split2(hi, lo, row, cD, r, false);
+        if (D == 128) put_row32_split2(hi, lo, row, cD + 32, r + 32, false);
+    };
+    // p0 (one fp32 per state row) as row 0 of the 16 x D operand tiles
+    auto put_p0 = [&](float x) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+        const uint32_t off = (uint32_t)(row & 7) * 2u;
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0h.chunk(0, row >> 6, (row & 63) >> 3) + off),
+                     "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0l.chunk(0, row >> 6, (row & 63) >> 3) + off),
+                     "h"(*reinterpret_cast<const unsigned short*>(&l)) : "memory");
+    };
     // packed W_lo: drain warp h stores the pairs of its W columns [64h, 64h+64)
     // over the X columns it has itself just drained, so no other warp's
     // pending read is overwritten.  K-step ks reads 8 packed columns.
@@ -389,7 +460,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
             }
             tmem_st32(tS_ + lane_off + cb, r);
-            put_row32(tS, row, cb, r, false);
+            if (NORM) put_row32_split2(tS, tSl, row, cb, r, false);
+            else put_row32(tS, row, cb, r, false);
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 x = *reinterpret_cast<const float4*>(P0 + (size_t)row * D + cb + j);
@@ -397,7 +469,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
             }
             tmem_st32(tP_ + lane_off + cb, r);
-            put_row32(tP, row, cb, r, false);
+            if (NORM) put_row32_split2(tP, tPl, row, cb, r, false);
+            else put_row32(tP, row, cb, r, false);
+        }
+        if (NORM && half == 0) {
+            // p0 = S0 m0 - h0 of the prefix (record slot after P)
+            const float p0 = pre[3 * (size_t)D * D + D + row];
+            tmem_st1(tPn_ + lane_off, __float_as_uint(p0));
+            put_p0(p0);
         }
         tmem_st_wait();
     }
@@ -410,6 +489,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);     // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);       // both MN-major
+    constexpr uint32_t iKK16 = idesc_bf16(128, 16, false, false);  // N = 16 (ones / p0), both K-major
+    constexpr uint32_t iMK16 = idesc_bf16(128, 16, true, false);   // N = 16, A MN-major
     const int nchunks = c_end - c_begin;
 
     if (issuer) {
@@ -458,20 +539,30 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     // X = Q S0 ; S += K^T K
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                    if (NORM)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tSl.kmaj(ks), iKK, 1);
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                     mma_commit(bar(CXS));
                     if (!wait_bar(DA, ph)) break;  // sA = A
                     tc_fence_after();
                     // W = A A^T
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tA.kmaj(ks), iSq, ks > 0);
+                    if (NORM) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tAl.kmaj(ks), iSq, 1);
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tA.kmaj(ks), iSq, 1);
+                    }
                     if (!wait_bar(DX, ph)) break;  // sX = bf16(Q S0); TMEM X read
                     tc_fence_after();
                     // X = Q S0 + A K  (before the last W term, so that W completes last
                     // and its drain, which also waits for this product, starts at once)
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                    if (NORM)
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CX2));
                     // W += (Q S0) Q^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
+                    if (NORM)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tXl.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                     mma_commit(bar(CW));
                     if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
                     tc_fence_after();
@@ -482,18 +573,36 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     // O = Q P0 + W_hi V + W_lo V
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
+                    if (NORM) {
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tPl.mnmaj(ks), iKM, 1);
+                        // denominator: Q p0 (+ W 1 below)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0h.kmaj(ks), iKK16, ks > 0);
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0l.kmaj(ks), iKK16, 1);
+                    }
                     mma_commit(bar(CQ));
                     if (!wait_bar(LV, ph)) break;
                     tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
-                    if (c == 0)  // W_lo V: the head's first chunk only (see the drain)
+                    if (NORM || c == 0)  // W_lo V: every chunk when normalised, else the head's first
                         for (int ks = 0; ks < kL / 16; ++ks)
                             mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
+                    if (NORM) {
+                        // denominator += W_hi 1 + W_lo 1
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tDen_, tA.kmaj(ks), tOnes.kmaj(ks), iKK16, 1);
+                        for (int ks = 0; ks < kL / 16; ++ks)
+                            mma_bf16_tmem_a(tDen_, tX_ + wlo_col(ks), tOnes.kmaj(ks), iKK16, 1);
+                    }
                     mma_commit(bar(CO));
                     if (!wait_bar(DX2, ph)) break;  // sX = X
                     tc_fence_after();
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                    if (NORM) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                        // p += X^T 1
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
+                    }
                     mma_commit(bar(CP));
                     if (has_next) {
                         if (!wait_bar(CQ, ph)) break;
@@ -520,16 +629,24 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
                     tc_fence_after();
                     // X = Q S_local + A K   (no S_local term on the segment's first chunk)
-                    if (it > 0)
+                    if (it > 0) {
                         for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                        if (NORM)
+                            for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tSl.kmaj(ks), iKK, 1);
+                    }
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
+                    if (NORM)
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CX2));
                     if (!wait_bar(LV, ph)) break;
                     tc_fence_after();
                     // C += Q^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tC_, tQc.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    if (NORM)  // m += Q^T 1
+                        for (int ks = 0; ks < kL / 16; ++ks)
+                            mma_bf16(tDen_, tQc.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CQ));
                     if (!wait_bar(DX, ph)) break;  // sX = X
                     tc_fence_after();
@@ -537,6 +654,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    if (NORM) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                        // p += X^T 1
+                        for (int ks = 0; ks < kL / 16; ++ks)
+                            mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
+                    }
                     mma_commit(bar(CP));
                     if (it + 2 < nchunks) {
                         if (!wait_bar(CQ, ph)) break;
@@ -559,14 +683,17 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 tc_fence_after();
                 if (lane == 0) tma_store_wait_read();  // this warp's O piece has left its sA rows
                 __syncwarp();
-                drain128(tA_, tA, true);  // A -> sA (masked)
+                if (NORM) drain128s(tA_, tA, tAl, true);
+                else drain128(tA_, tA, true);  // A -> sA (masked)
                 drained(DA);
                 if (!wait_bar(CXS, ph)) break;
                 tc_fence_after();
-                drainD(tX_, tX);  // bf16(Q S0) -> sX
+                if (NORM) drainDs(tX_, tX, tXl);
+                else drainD(tX_, tX);  // bf16(Q S0) -> sX
                 drained(DX);
                 if (state_rows && has_next) {
-                    drainD(tS_, tS);  // S0 of the next chunk -> sS
+                    if (NORM) drainDs(tS_, tS, tSl);
+                    else drainD(tS_, tS);  // S0 of the next chunk -> sS
                     drained(DS);
                 }
                 if (!wait_bar(CW, ph) || !wait_bar(CX2, ph)) break;
@@ -580,7 +707,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // add the prefix term and many products, and plain bf16 W suffices.
                     uint32_t x[64];
                     tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
-                    if (c_begin + it == 0) {
+                    if (NORM || c_begin + it == 0) {
                         uint32_t lo[32];
                         {
                             uint32_t r[64];
@@ -594,8 +721,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         drain128(tA_, tA, true);  // W -> sA (masked)
                     }
                     drained(DW);
-                    put_row32(tX, row, cD, x, false);  // X -> sX
-                    if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
+                    if (NORM) {
+                        put_row32_split2(tX, tXl, row, cD, x, false);  // X -> sX (hi, lo)
+                        if (D == 128) put_row32_split2(tX, tXl, row, cD + 32, x + 32, false);
+                    } else {
+                        put_row32(tX, row, cD, x, false);  // X -> sX
+                        if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
+                    }
                     drained(DX2);
                 }
                 if (!wait_bar(CO, ph)) break;
@@ -608,6 +740,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // store issued by this warp's lane 0.
                     uint32_t r[64];
                     tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                    if (NORM) {
+                        // ratio normalisation: o = num / den (plain IEEE division)
+                        const float den = __uint_as_float(tmem_ld1(tDen_ + lane_off));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) / den);
+                    }
                     const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                     const int t0 = (c_begin + it) * kL + quarter * 32;  // first token of this warp's rows
 #pragma unroll
@@ -633,20 +772,32 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 if (state_rows && has_next) {
                     if (!wait_bar(CP, ph)) break;
                     tc_fence_after();
-                    drainD(tP_, tP);  // P0 of the next chunk -> sP
+                    if (NORM) {
+                        drainDs(tP_, tP, tPl);  // P0 of the next chunk -> sP (hi, lo)
+                        if (half == 0) {
+                            const uint32_t pv = tmem_ld1(tPn_ + lane_off);  // p0 of the next chunk
+                            tmem_ld_wait();
+                            put_p0(__uint_as_float(pv));
+                        }
+                    } else {
+                        drainD(tP_, tP);  // P0 of the next chunk -> sP
+                    }
                     drained(DP);
                 }
             } else {
                 if (!wait_bar(CA, ph)) break;
                 tc_fence_after();
-                drain128(tA_, tA, true);  // A -> sA (masked)
+                if (NORM) drain128s(tA_, tA, tAl, true);
+                else drain128(tA_, tA, true);  // A -> sA (masked)
                 drained(DA);
                 if (!wait_bar(CX2, ph)) break;
                 tc_fence_after();
-                drainD(tA_, tX);  // X -> sX
+                if (NORM) drainDs(tA_, tX, tXl);
+                else drainD(tA_, tX);  // X -> sX
                 drained(DX);
                 if (state_rows && has_next) {
-                    drainD(tS_, tS);  // S_local of the next chunk -> sS
+                    if (NORM) drainDs(tS_, tS, tSl);
+                    else drainD(tS_, tS);  // S_local of the next chunk -> sS
                     drained(DS);
                 }
             }
@@ -668,6 +819,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
                         make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
                                     __uint_as_float(r[j + 3]));
+            }
+            if (NORM && half == 0) {
+                // m (after C) and p (after P), one value per state row
+                const uint32_t mv = tmem_ld1(tDen_ + lane_off);
+                const uint32_t pv = tmem_ld1(tPn_ + lane_off);
+                tmem_ld_wait();
+                out[2 * (size_t)D * D + row] = __uint_as_float(mv);
+                out[3 * (size_t)D * D + D + row] = __uint_as_float(pv);
             }
         }
     }
@@ -844,7 +1003,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool NORM>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
                      int T, SegPlan plan, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mo;
@@ -859,8 +1018,8 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
         mo = mq;  // unused
     }
     TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
-    const size_t smem = Layout<D, MODE>::kBytes + 1024;
-    auto kern = tc_walk_kernel<D, MODE>;
+    const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;
+    auto kern = tc_walk_kernel<D, MODE, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
@@ -872,7 +1031,8 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
 }  // namespace
 
 bool tc_supported(int d, int dv, int dtype, int normalized, int device) {
-    if (d != dv || (d != 64 && d != 128) || dtype != 1 || normalized) return false;
+    if (d != dv || (d != 64 && d != 128) || dtype != 1) return false;
+    if (normalized && d != 64) return false;  // the split operands fit in shared memory at d = 64
     static int cached[64] = {0};  // 0 unknown, 1 yes, 2 no
     if (device < 0 || device >= 64) return false;
     if (!cached[device]) {
@@ -885,13 +1045,19 @@ bool tc_supported(int d, int dv, int dtype, int normalized, int device) {
 }
 
 cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
-                           float* summ, int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s) {
+                           float* summ, int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
+                           cudaStream_t s) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
-    if (d == 128) return mode == 0 ? launch_t<128, 0>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
-                                   : launch_t<128, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
-    if (d == 64) return mode == 0 ? launch_t<64, 0>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
-                                  : launch_t<64, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    if (normalized) {
+        if (d != 64) return cudaErrorInvalidValue;
+        return mode == 0 ? launch_t<64, 0, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
+                         : launch_t<64, 1, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    }
+    if (d == 128) return mode == 0 ? launch_t<128, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
+                                   : launch_t<128, 1, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    if (d == 64) return mode == 0 ? launch_t<64, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
+                                  : launch_t<64, 1, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     return cudaErrorInvalidValue;
 }
 

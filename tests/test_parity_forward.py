@@ -37,7 +37,8 @@ def test_tensor_core_path_selected():
     L = hla2.lib()
     assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
     assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
-    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 0) == 0
+    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 0) == 1   # normalised: split operands
+    assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 1, 0) == 0
     assert L.hla2_forward_path(16, 16, hla2.HLA2_DTYPE_F32, 0, 0) == 0
     assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 1) == 0
 
@@ -53,6 +54,19 @@ def test_tensor_core_walk_lengths(T, d):
     v = (torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
     got = run_gpu(q, k, v)
     assert relerr(f64(got), oracle_forward(q, k, v)) < TOL_TC_BF16
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 1000, 3000])
+def test_tensor_core_normalized_lengths(T):
+    """Ratio-normalised variant on the tcgen05 walks (d = 64, split operands)."""
+    d = 64
+    g = torch.Generator().manual_seed(T * 11 + 5)
+    B, H = 2, 2
+    q = (torch.rand(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    k = (torch.rand(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    v = torch.randn(B, H, T, d, generator=g).to(torch.bfloat16)
+    got = run_gpu(q, k, v, normalized=True)
+    assert relerr(f64(got), oracle_forward(q, k, v, normalized=True)) < TOL_NORMALIZED
 
 
 # ------------------------------------------------------ seeded workloads ----
