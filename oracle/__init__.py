@@ -216,3 +216,103 @@ def dense_causal_aatv(Q, K, V, normalized: bool = False) -> np.ndarray:
     if normalized:
         O = O / W.sum(axis=-1, keepdims=True)
     return O
+
+
+# ------------------------------------------------------------------ AHLA ----
+# HLA summary, section 2 "AHLA": operator Q (K^T Q)(K^T V); masked reading
+#   o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j   (causal A A V, A = tril(Q K^T)).
+# Summary record M|P|m|E|n (M = sum k q^T, P = sum k v^T, m = sum k,
+# E = sum_i k_i q_i^T P_i, n = sum_i k_i (q_i . m_i)); decode state P|E|m|n.
+
+def _ahla_lib(mutant: int = 0) -> ctypes.CDLL:
+    lib = _lib(mutant)
+    if not getattr(lib, "_ahla_typed", False):
+        dp = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        lib.hla2_oracle_ahla_serial.argtypes = [dp, dp, dp, dp, i, i, i, i, i]
+        lib.hla2_oracle_ahla_bruteforce.argtypes = [dp, dp, dp, dp, i, i, i, i, i]
+        lib.hla2_oracle_ahla_chunk_summaries.argtypes = [dp, dp, dp, dp, i, i, i, i, i]
+        lib.hla2_oracle_ahla_chunked.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i]
+        lib.hla2_oracle_ahla_step.argtypes = [dp, dp, dp, dp, dp, i, i, i, i]
+        lib._ahla_typed = True
+    return lib
+
+
+def ahla_state_len(d: int, dv: int) -> int:
+    """Decode state P|E|m|n per head."""
+    return 2 * d * dv + 2 * d
+
+
+def ahla_serial(Q, K, V, normalized: bool = False, mutant: int = 0) -> np.ndarray:
+    """AHLA outputs by the serial recurrence."""
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _ahla_lib(mutant).hla2_oracle_ahla_serial(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized)):
+        raise RuntimeError("oracle ahla_serial failed")
+    return O.reshape(*lead, T, dv)
+
+
+def ahla_bruteforce(Q, K, V, normalized: bool = False, mutant: int = 0) -> np.ndarray:
+    """AHLA by its definition, O(T^3 d)."""
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _ahla_lib(mutant).hla2_oracle_ahla_bruteforce(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized)):
+        raise RuntimeError("oracle ahla_bruteforce failed")
+    return O.reshape(*lead, T, dv)
+
+
+def ahla_chunk_summaries(Q, K, V, L: int, mutant: int = 0) -> np.ndarray:
+    """[..., N, record] with record M|P|m|E|n of each L-token chunk."""
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    N = (T + L - 1) // L
+    out = np.zeros((BH, N, record_len(d, dv)))
+    if _ahla_lib(mutant).hla2_oracle_ahla_chunk_summaries(_p(Q), _p(K), _p(V), _p(out), BH, T, d, dv, int(L)):
+        raise RuntimeError("oracle ahla_chunk_summaries failed")
+    return out.reshape(*lead, N, record_len(d, dv))
+
+
+def ahla_chunked(Q, K, V, L: int, normalized: bool = False, mutant: int = 0) -> np.ndarray:
+    """AHLA chunk summaries + exclusive Blelloch scan + per-chunk restart."""
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _ahla_lib(mutant).hla2_oracle_ahla_chunked(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized),
+                                                  int(L)):
+        raise RuntimeError("oracle ahla_chunked failed")
+    return O.reshape(*lead, T, dv)
+
+
+def ahla_step(state, q, k, v, normalized: bool = False, mutant: int = 0):
+    """One AHLA decode step on n heads; returns (new_state, o).  State P|E|m|n."""
+    state = _f64(state).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n, d = q.shape
+    dv = v.shape[1]
+    o = np.zeros((n, dv))
+    if _ahla_lib(mutant).hla2_oracle_ahla_step(_p(state), _p(q), _p(k), _p(v), _p(o), n, d, dv, int(normalized)):
+        raise RuntimeError("oracle ahla_step failed")
+    return state, o
+
+
+def ahla_summary_to_state(rec, d: int, dv: int) -> np.ndarray:
+    """Summary record M|P|m|E|n -> decode state P|E|m|n (M is only needed to
+    combine segments, not to continue a sequence)."""
+    rec = _f64(rec)
+    nS, nC = d * d, d * dv
+    P = rec[..., nS:nS + nC]
+    m = rec[..., nS + nC:nS + nC + d]
+    E = rec[..., nS + nC + d:nS + 2 * nC + d]
+    n = rec[..., nS + 2 * nC + d:]
+    return np.concatenate([P, E, m, n], axis=-1)
+
+
+def dense_causal_aav(Q, K, V, normalized: bool = False) -> np.ndarray:
+    """Independent statement through library matmuls: A = tril(Q K^T),
+    O = (A A) V (HLA summary, section 2: A A V where HLA has A A^T V; A A is
+    lower triangular already).  Normalised: divide by the row sums of A A."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    A = np.tril(Q @ np.swapaxes(K, -1, -2))
+    W = A @ A
+    O = W @ V
+    if normalized:
+        O = O / W.sum(axis=-1, keepdims=True)
+    return O

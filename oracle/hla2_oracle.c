@@ -18,7 +18,10 @@
  *           o_t = q_t^T (S_t C_t - G_t),
  *         and a ratio-normalised variant that divides by a masked
  *         denominator built from the analogous summaries.
- *   [§2]  section "2. AHLA" contrasts HLA's symmetric A A^T V structure.
+ *   [§2]  section "2. AHLA": the asymmetric variant, operator
+ *         Q (K^T Q)(K^T V), i.e. an A A V structure where HLA has A A^T V,
+ *         with streaming summaries P^KV_t, m^K_t, E_t, n_t (the AHLA block
+ *         at the end of this file states the reading taken).
  *   [§4]  section "4. Parallel training via associative scans": segment
  *         summaries joined by a semidirect-product operator whose cross term
  *         is S_B C_A; an exclusive Blelloch scan over them reproduces the
@@ -48,7 +51,8 @@
  *
  * Build:  gcc -O2 -std=c11 -shared -fPIC -o libhla2_oracle.so hla2_oracle.c -lpthread
  * Defining HLA2_ORACLE_MUTANT=<n> plants one deliberate mistake (tests use
- * this to show that the pins catch it); never defined otherwise.
+ * this to show that the pins catch it); never defined otherwise.  1-4 are in
+ * the HLA functions, 5-6 in the AHLA ones.
  */
 #include <stdlib.h>
 #include <string.h>
@@ -486,3 +490,226 @@ int hla2_oracle_step(double* state, const double* q, const double* k, const doub
 
 /* Record length in doubles (same for summary and decode order). */
 long long hla2_oracle_record_len(int d, int dv) { return (long long)summary_len(d, dv); }
+
+/* ====================================================================== */
+/* AHLA: asymmetric second-order variant, HLA summary section 2.          */
+/*                                                                        */
+/* The pages give the operator Q (K^T Q)(K^T V) and name its streaming    */
+/* summaries P^KV_t, m^K_t, E_t, n_t, without printing their updates.     */
+/* Reading (pinned by brute force): causal A A V with A = tril(Q K^T),    */
+/*   o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j,                         */
+/* i.e. query t reaches key i, whose query i reaches key j <= i:          */
+/*   P_t = P_{t-1} + k_t v_t^T       m_t = m_{t-1} + k_t                  */
+/*   E_t = E_{t-1} + k_t (q_t^T P_t) n_t = n_{t-1} + k_t (q_t . m_t)      */
+/*   o_t = q_t^T E_t ;  normalised: o_t / (q_t^T n_t).                    */
+/* Segment summary record (same length as HLA's):                         */
+/*   M (d*d, = sum k q^T) | P (d*dv) | m (d) | E (d*dv) | n (d)            */
+/* and the combine (A earlier, B later) is HLA's with S->M, C->P, G->E:   */
+/*   M, P, m add;  E = E_A + E_B + M_B P_A;  n = n_A + n_B + M_B m_A.    */
+/* ====================================================================== */
+typedef struct {
+    int d, dv;
+    double *M, *P, *m, *E, *n; /* d*d, d*dv, d, d*dv, d */
+} astate_t;
+
+static int astate_alloc(astate_t* s, int d, int dv) {
+    double* p = (double*)calloc(summary_len(d, dv), sizeof(double));
+    if (!p) return -1;
+    s->d = d; s->dv = dv;
+    s->M = p;
+    s->P = s->M + (size_t)d * d;
+    s->m = s->P + (size_t)d * dv;
+    s->E = s->m + d;
+    s->n = s->E + (size_t)d * dv;
+    return 0;
+}
+static void astate_zero(astate_t* s) { memset(s->M, 0, sizeof(double) * summary_len(s->d, s->dv)); }
+
+/* absorb token t (P and m grow first: E and n use P_t and m_t) */
+static void ahla_absorb(astate_t* s, const double* q, const double* k, const double* v, double* w) {
+    const int d = s->d, dv = s->dv;
+#if HLA2_ORACLE_MUTANT == 5
+    /* mistake: E and n read P_{t-1}, m_{t-1} (drops the j = i terms) */
+    for (int e = 0; e < dv; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < d; ++a) acc += q[a] * s->P[(size_t)a * dv + e];
+        w[e] = acc;
+    }
+    double qm = 0.0;
+    for (int a = 0; a < d; ++a) qm += q[a] * s->m[a];
+#endif
+    for (int a = 0; a < d; ++a) {
+        for (int e = 0; e < dv; ++e) s->P[(size_t)a * dv + e] += k[a] * v[e];
+        s->m[a] += k[a];
+#if HLA2_ORACLE_MUTANT == 6
+        /* mistake: cross operand transposed (sum q k^T instead of k q^T) */
+        for (int b = 0; b < d; ++b) s->M[(size_t)a * d + b] += q[a] * k[b];
+#else
+        for (int b = 0; b < d; ++b) s->M[(size_t)a * d + b] += k[a] * q[b];
+#endif
+    }
+#if HLA2_ORACLE_MUTANT != 5
+    for (int e = 0; e < dv; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < d; ++a) acc += q[a] * s->P[(size_t)a * dv + e];
+        w[e] = acc;
+    }
+    double qm = 0.0;
+    for (int a = 0; a < d; ++a) qm += q[a] * s->m[a];
+#endif
+    for (int a = 0; a < d; ++a) {
+        for (int e = 0; e < dv; ++e) s->E[(size_t)a * dv + e] += k[a] * w[e];
+        s->n[a] += k[a] * qm;
+    }
+}
+static void ahla_emit(const astate_t* s, const double* q, double* o, int normalized) {
+    const int d = s->d, dv = s->dv;
+    for (int e = 0; e < dv; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < d; ++a) acc += q[a] * s->E[(size_t)a * dv + e];
+        o[e] = acc;
+    }
+    if (normalized) {
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += q[a] * s->n[a];
+        for (int e = 0; e < dv; ++e) o[e] /= den;
+    }
+}
+
+/* AHLA outputs by the serial recurrence. */
+int hla2_oracle_ahla_serial(const double* Q, const double* K, const double* V, double* O,
+                            int BH, int T, int d, int dv, int normalized) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    astate_t s;
+    if (astate_alloc(&s, d, dv)) return -1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)dv);
+    if (!w) { free(s.M); return -1; }
+    for (int bh = 0; bh < BH; ++bh) {
+        astate_zero(&s);
+        for (int t = 0; t < T; ++t) {
+            const double* q = Q + ((size_t)bh * T + t) * d;
+            ahla_absorb(&s, q, K + ((size_t)bh * T + t) * d, V + ((size_t)bh * T + t) * dv, w);
+            ahla_emit(&s, q, O + ((size_t)bh * T + t) * dv, normalized);
+        }
+    }
+    free(w);
+    free(s.M);
+    return 0;
+}
+
+/* The definition, O(T^3 d): o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j. */
+int hla2_oracle_ahla_bruteforce(const double* Q, const double* K, const double* V, double* O,
+                                int BH, int T, int d, int dv, int normalized) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    for (int bh = 0; bh < BH; ++bh) {
+        const double* Qh = Q + (size_t)bh * T * d;
+        const double* Kh = K + (size_t)bh * T * d;
+        const double* Vh = V + (size_t)bh * T * dv;
+        for (int t = 0; t < T; ++t) {
+            double* o = O + ((size_t)bh * T + t) * dv;
+            for (int e = 0; e < dv; ++e) o[e] = 0.0;
+            double den = 0.0;
+            for (int i = 0; i <= t; ++i) {
+                double qk_ti = 0.0;
+                for (int a = 0; a < d; ++a) qk_ti += Qh[(size_t)t * d + a] * Kh[(size_t)i * d + a];
+                for (int j = 0; j <= i; ++j) {
+                    double qk_ij = 0.0;
+                    for (int a = 0; a < d; ++a) qk_ij += Qh[(size_t)i * d + a] * Kh[(size_t)j * d + a];
+                    const double wgt = qk_ti * qk_ij;
+                    den += wgt;
+                    for (int e = 0; e < dv; ++e) o[e] += wgt * Vh[(size_t)j * dv + e];
+                }
+            }
+            if (normalized)
+                for (int e = 0; e < dv; ++e) o[e] /= den;
+        }
+    }
+    return 0;
+}
+
+/* AHLA chunk summaries M|P|m|E|n of every L-token chunk (state from zero). */
+int hla2_oracle_ahla_chunk_summaries(const double* Q, const double* K, const double* V,
+                                     double* summ, int BH, int T, int d, int dv, int L) {
+    if (!Q || !K || !V || !summ || BH < 0 || T < 0 || d <= 0 || dv <= 0 || L <= 0) return -1;
+    const int N = (T + L - 1) / L;
+    const size_t R = summary_len(d, dv);
+    astate_t s;
+    if (astate_alloc(&s, d, dv)) return -1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)dv);
+    if (!w) { free(s.M); return -1; }
+    for (int bh = 0; bh < BH; ++bh)
+        for (int c = 0; c < N; ++c) {
+            astate_zero(&s);
+            const int t1 = (c + 1) * L < T ? (c + 1) * L : T;
+            for (int t = c * L; t < t1; ++t)
+                ahla_absorb(&s, Q + ((size_t)bh * T + t) * d, K + ((size_t)bh * T + t) * d,
+                            V + ((size_t)bh * T + t) * dv, w);
+            memcpy(summ + ((size_t)bh * N + c) * R, s.M, sizeof(double) * R);
+        }
+    free(w);
+    free(s.M);
+    return 0;
+}
+
+/* AHLA chunked forward: chunk summaries, exclusive Blelloch scan with the
+ * combine above (the HLA combine routine, whose algebra is the same), then
+ * every chunk restarts the recurrence from its prefix. */
+int hla2_oracle_ahla_chunked(const double* Q, const double* K, const double* V, double* O,
+                             int BH, int T, int d, int dv, int normalized, int L) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0 || L <= 0) return -1;
+    const int N = (T + L - 1) / L;
+    const size_t R = summary_len(d, dv);
+    double* summ = (double*)malloc(sizeof(double) * R * (size_t)(N > 0 ? N : 1) * (size_t)(BH > 0 ? BH : 1));
+    double* pre = (double*)malloc(sizeof(double) * R * (size_t)(N > 0 ? N : 1) * (size_t)(BH > 0 ? BH : 1));
+    double* w = (double*)malloc(sizeof(double) * (size_t)dv);
+    astate_t s;
+    int rc = -1;
+    if (!summ || !pre || !w || astate_alloc(&s, d, dv)) goto out;
+    if (hla2_oracle_ahla_chunk_summaries(Q, K, V, summ, BH, T, d, dv, L) ||
+        hla2_oracle_scan_blelloch(summ, pre, BH, N, d, dv)) {
+        free(s.M);
+        goto out;
+    }
+    for (int bh = 0; bh < BH; ++bh)
+        for (int c = 0; c < N; ++c) {
+            memcpy(s.M, pre + ((size_t)bh * N + c) * R, sizeof(double) * R);
+            const int t1 = (c + 1) * L < T ? (c + 1) * L : T;
+            for (int t = c * L; t < t1; ++t) {
+                const double* q = Q + ((size_t)bh * T + t) * d;
+                ahla_absorb(&s, q, K + ((size_t)bh * T + t) * d, V + ((size_t)bh * T + t) * dv, w);
+                ahla_emit(&s, q, O + ((size_t)bh * T + t) * dv, normalized);
+            }
+        }
+    free(s.M);
+    rc = 0;
+out:
+    free(summ); free(pre); free(w);
+    return rc;
+}
+
+/* One AHLA decode step for n heads; state per head P|E|m|n (2 d dv + 2 d). */
+int hla2_oracle_ahla_step(double* state, const double* q, const double* k, const double* v,
+                          double* o, int n, int d, int dv, int normalized) {
+    if (!state || !q || !k || !v || !o || n < 0 || d <= 0 || dv <= 0) return -1;
+    astate_t s;
+    if (astate_alloc(&s, d, dv)) return -1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)dv);
+    if (!w) { free(s.M); return -1; }
+    const size_t nC = (size_t)d * dv, R = 2 * nC + 2 * (size_t)d;
+    for (int i = 0; i < n; ++i) {
+        double* r = state + (size_t)i * R;
+        memcpy(s.P, r, sizeof(double) * nC);
+        memcpy(s.E, r + nC, sizeof(double) * nC);
+        memcpy(s.m, r + 2 * nC, sizeof(double) * (size_t)d);
+        memcpy(s.n, r + 2 * nC + d, sizeof(double) * (size_t)d);
+        ahla_absorb(&s, q + (size_t)i * d, k + (size_t)i * d, v + (size_t)i * dv, w);
+        ahla_emit(&s, q + (size_t)i * d, o + (size_t)i * dv, normalized);
+        memcpy(r, s.P, sizeof(double) * nC);
+        memcpy(r + nC, s.E, sizeof(double) * nC);
+        memcpy(r + 2 * nC, s.m, sizeof(double) * (size_t)d);
+        memcpy(r + 2 * nC + d, s.n, sizeof(double) * (size_t)d);
+    }
+    free(w);
+    free(s.M);
+    return 0;
+}
