@@ -316,3 +316,65 @@ def dense_causal_aav(Q, K, V, normalized: bool = False) -> np.ndarray:
     if normalized:
         O = O / W.sum(axis=-1, keepdims=True)
     return O
+
+
+# -------------------------------------------------------------- unmasked ----
+# o_t = q_t^T S_t C_t = sum_{i<=t, j<=t} (q_t.k_i)(k_i.q_j) v_j (no G correction);
+# normalised by q_t^T S_t m_t.  Decode state S|C|m.
+
+def _unmasked_lib(mutant: int = 0) -> ctypes.CDLL:
+    lib = _lib(mutant)
+    if not getattr(lib, "_unmasked_typed", False):
+        dp = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        lib.hla2_oracle_unmasked_serial.argtypes = [dp, dp, dp, dp, i, i, i, i, i]
+        lib.hla2_oracle_unmasked_bruteforce.argtypes = [dp, dp, dp, dp, i, i, i, i, i]
+        lib.hla2_oracle_unmasked_step.argtypes = [dp, dp, dp, dp, dp, i, i, i, i]
+        lib._unmasked_typed = True
+    return lib
+
+
+def unmasked_state_len(d: int, dv: int) -> int:
+    return d * d + d * dv + d
+
+
+def unmasked_serial(Q, K, V, normalized: bool = False) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _unmasked_lib().hla2_oracle_unmasked_serial(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized)):
+        raise RuntimeError("oracle unmasked_serial failed")
+    return O.reshape(*lead, T, dv)
+
+
+def unmasked_bruteforce(Q, K, V, normalized: bool = False) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _unmasked_lib().hla2_oracle_unmasked_bruteforce(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized)):
+        raise RuntimeError("oracle unmasked_bruteforce failed")
+    return O.reshape(*lead, T, dv)
+
+
+def unmasked_step(state, q, k, v, normalized: bool = False):
+    """One unmasked decode step on n heads; returns (new_state, o).  State S|C|m."""
+    state = _f64(state).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n, d = q.shape
+    dv = v.shape[1]
+    o = np.zeros((n, dv))
+    if _unmasked_lib().hla2_oracle_unmasked_step(_p(state), _p(q), _p(k), _p(v), _p(o), n, d, dv, int(normalized)):
+        raise RuntimeError("oracle unmasked_step failed")
+    return state, o
+
+
+def dense_unmasked(Q, K, V, normalized: bool = False) -> np.ndarray:
+    """Independent statement through library routines: running sums
+    S_t = cumsum k k^T, C_t = cumsum q v^T, m_t = cumsum q, then q_t^T S_t C_t."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    S = np.cumsum(np.einsum("...ta,...tb->...tab", K, K), axis=-3)
+    C = np.cumsum(np.einsum("...ta,...te->...tae", Q, V), axis=-3)
+    u = np.einsum("...tab,...tb->...ta", S, Q)
+    O = np.einsum("...ta,...tae->...te", u, C)
+    if normalized:
+        m = np.cumsum(Q, axis=-2)
+        O = O / np.einsum("...ta,...ta->...t", u, m)[..., None]
+    return O

@@ -713,3 +713,106 @@ int hla2_oracle_ahla_step(double* state, const double* q, const double* k, const
     free(s.M);
     return 0;
 }
+
+/* ====================================================================== */
+/* Unmasked second-order HLA: o_t = q_t^T S_t C_t (HLA summary, section 1 */
+/* names the naive product S_t C_t that G_t corrects; the "Results and    */
+/* claims" section lists the unmasked operator among the variants).       */
+/*   o_t = sum_{i<=t} sum_{j<=t} (q_t.k_i)(k_i.q_j) v_j                   */
+/* normalised: o_t / (q_t^T S_t m_t).  State S, C, m only; segments join  */
+/* by plain addition (no cross term), so a scan is a running sum.         */
+/* Decode state per head: S (d*d) | C (d*dv) | m (d).                     */
+/* ====================================================================== */
+static void unmasked_absorb(double* S, double* C, double* m, const double* q, const double* k, const double* v,
+                            int d, int dv) {
+    for (int a = 0; a < d; ++a) {
+        for (int b = 0; b < d; ++b) S[(size_t)a * d + b] += k[a] * k[b];
+        for (int e = 0; e < dv; ++e) C[(size_t)a * dv + e] += q[a] * v[e];
+        m[a] += q[a];
+    }
+}
+static void unmasked_emit(const double* S, const double* C, const double* m, const double* q, double* o,
+                          double* u, int d, int dv, int normalized) {
+    for (int a = 0; a < d; ++a) {
+        double acc = 0.0;
+        for (int b = 0; b < d; ++b) acc += S[(size_t)a * d + b] * q[b];
+        u[a] = acc;
+    }
+    for (int e = 0; e < dv; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < d; ++a) acc += u[a] * C[(size_t)a * dv + e];
+        o[e] = acc;
+    }
+    if (normalized) {
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += u[a] * m[a];
+        for (int e = 0; e < dv; ++e) o[e] /= den;
+    }
+}
+
+/* Unmasked outputs by the serial recurrence. */
+int hla2_oracle_unmasked_serial(const double* Q, const double* K, const double* V, double* O,
+                                int BH, int T, int d, int dv, int normalized) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    const size_t n = (size_t)d * d + (size_t)d * dv + (size_t)d + (size_t)d;
+    double* buf = (double*)malloc(sizeof(double) * n);
+    if (!buf) return -1;
+    double *S = buf, *C = S + (size_t)d * d, *m = C + (size_t)d * dv, *u = m + d;
+    for (int bh = 0; bh < BH; ++bh) {
+        memset(buf, 0, sizeof(double) * n);
+        for (int t = 0; t < T; ++t) {
+            const double* q = Q + ((size_t)bh * T + t) * d;
+            unmasked_absorb(S, C, m, q, K + ((size_t)bh * T + t) * d, V + ((size_t)bh * T + t) * dv, d, dv);
+            unmasked_emit(S, C, m, q, O + ((size_t)bh * T + t) * dv, u, d, dv, normalized);
+        }
+    }
+    free(buf);
+    return 0;
+}
+
+/* The definition, O(T^3 d): every pair i <= t, j <= t. */
+int hla2_oracle_unmasked_bruteforce(const double* Q, const double* K, const double* V, double* O,
+                                    int BH, int T, int d, int dv, int normalized) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    for (int bh = 0; bh < BH; ++bh) {
+        const double* Qh = Q + (size_t)bh * T * d;
+        const double* Kh = K + (size_t)bh * T * d;
+        const double* Vh = V + (size_t)bh * T * dv;
+        for (int t = 0; t < T; ++t) {
+            double* o = O + ((size_t)bh * T + t) * dv;
+            for (int e = 0; e < dv; ++e) o[e] = 0.0;
+            double den = 0.0;
+            for (int i = 0; i <= t; ++i) {
+                double qk = 0.0;
+                for (int a = 0; a < d; ++a) qk += Qh[(size_t)t * d + a] * Kh[(size_t)i * d + a];
+                for (int j = 0; j <= t; ++j) {
+                    double kq = 0.0;
+                    for (int a = 0; a < d; ++a) kq += Kh[(size_t)i * d + a] * Qh[(size_t)j * d + a];
+                    den += qk * kq;
+                    for (int e = 0; e < dv; ++e) o[e] += qk * kq * Vh[(size_t)j * dv + e];
+                }
+            }
+            if (normalized)
+                for (int e = 0; e < dv; ++e) o[e] /= den;
+        }
+    }
+    return 0;
+}
+
+/* One unmasked decode step for n heads; state per head S|C|m. */
+int hla2_oracle_unmasked_step(double* state, const double* q, const double* k, const double* v,
+                              double* o, int n, int d, int dv, int normalized) {
+    if (!state || !q || !k || !v || !o || n < 0 || d <= 0 || dv <= 0) return -1;
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!u) return -1;
+    const size_t R = (size_t)d * d + (size_t)d * dv + (size_t)d;
+    for (int i = 0; i < n; ++i) {
+        double* S = state + (size_t)i * R;
+        double* C = S + (size_t)d * d;
+        double* m = C + (size_t)d * dv;
+        unmasked_absorb(S, C, m, q + (size_t)i * d, k + (size_t)i * d, v + (size_t)i * dv, d, dv);
+        unmasked_emit(S, C, m, q + (size_t)i * d, o + (size_t)i * dv, u, d, dv, normalized);
+    }
+    free(u);
+    return 0;
+}
