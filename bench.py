@@ -22,6 +22,7 @@ tokens / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -38,9 +39,19 @@ METRIC = "masked HLA-2 fwd tokens/s (B·H·T/s) at 1 GB300; % tensor/HBM rooflin
 UNIT = "tokens/s"
 FWD_WORKLOAD = 3          # B1 H16 T65536 d=dv=128 bf16
 BYTES_PER_TOKEN_FWD = None  # set from the workload: 2*(2d+dv) + 4*dv
-# ncu DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum), valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {}
+# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid only for the kernel source it was taken on, keyed by (kernel, workload).
+# Captured on smaller cases of the same kernels and scaled by the units
+# processed (profiles/*.md give the commands and the raw figures):
+#  - output walk tc_walk_kernel<128,1,false>, B1 H16 T16384: 244.9 MB read +
+#    97.5 MB written = 342.4 MB; x4 tokens for T = 65536;
+#  - decode step_kernel, 1024 heads: 204.0 + 143.3 = 347.3 MB; x4 heads.
+# Writes still in L2 when a small case ends are not counted, so both sit a
+# little below the algorithmic bytes.
+NCU_TRAFFIC = {
+    ("tcgen05", "hla2-fwd-B1H16T65536-d128-bf16"): 4 * 342.4e6,
+    ("step", "hla2-step-n4096-d128-fp32-prefill1024-steps512"): 4 * 347.3e6,
+}
 
 
 def parse():
@@ -56,6 +67,9 @@ def parse():
     p.add_argument("--no-forward", action="store_true", help="skip the forward (profiling the decode step alone)")
     p.add_argument("--T", type=int, default=None, help="override T (profiling a smaller case; not a bench line)")
     p.add_argument("--H", type=int, default=None, help="override H (profiling a smaller case; not a bench line)")
+    p.add_argument("--no-ahla", action="store_true", help="skip the AHLA forward and decode lines")
+    p.add_argument("--decode-n", type=int, default=None,
+                   help="override the number of decode heads (profiling a smaller case; not a bench line)")
     p.add_argument("--workload", type=int, default=FWD_WORKLOAD,
                    help="forward workload id (0-3, see workloads.py); the bench line is workload 3")
     return p.parse_args()
@@ -262,7 +276,6 @@ def main():
     peaks = load_peaks()
     w = W.WORKLOADS[args.workload]
     if args.T or args.H:
-        import dataclasses
         w = dataclasses.replace(w, T=args.T or w.T, H=args.H or w.H, name=w.name + f"-override-H{args.H or w.H}-T{args.T or w.T}")
     tokens = w.BH * w.T
     esz = 2 if w.dtype == "bf16" else 4
@@ -321,7 +334,7 @@ def main():
     # dominant kernel: segment outputs (phase 2)
     out_ms = phase_ms[2] / max(nfwd, 1)
     achieved = bytes_per_token * tokens / (out_ms / 1e3) / 1e9 if out_ms > 0 else 0.0
-    traffic = NCU_TRAFFIC.get(path)
+    traffic = NCU_TRAFFIC.get((path, w.name))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "kernel": f"segment outputs ({path})", "ms_per_launch": out_ms,
@@ -332,6 +345,32 @@ def main():
                 "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"] if fwd_steps else 0.0,
                 "tensor_frac_of_bf16_burst": (alg_flops(w) * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
                 if fwd_steps else 0.0}
+
+    # ---- AHLA (asymmetric variant) forward on the same inputs ----
+    ahla = None
+    if not args.no_ahla and fwd_steps:
+        apath = "tcgen05" if L.hla2_ahla_forward_path(w.d, w.dv, dcode, int(w.normalized), 0) == 1 else "cuda-core"
+        for _ in range(args.warmup):
+            hla2.hla2_ahla_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+        barrier()
+        n_a = max(1, min(args.steps, 50))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_a)]
+        for ea, eb in evs:
+            if flush:
+                scratch.zero_()
+            ea.record(stream)
+            hla2.hla2_ahla_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+            eb.record(stream)
+        barrier()
+        ms_a = max_over_ranks(sum(ea.elapsed_time(eb) for ea, eb in evs) / n_a)
+        if hla2.hla2_device_status() != 0:
+            raise SystemExit(f"device status after AHLA: {hla2.hla2_last_error_detail()}")
+        ach_a = bytes_per_token * tokens / (ms_a / 1e3) / 1e9
+        ahla = {"metric": "masked AHLA fwd tokens/s (B·H·T/s)", "value": replicas.job_throughput(tokens, world, ms_a),
+                "unit": UNIT, "ms_per_step": ms_a, "steps": n_a, "path": apath,
+                "roofline": {"bound": "hbm", "achieved": ach_a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": ach_a / peaks["hbm_gbs"], "traffic": None,
+                             "kernel": "whole AHLA forward step (summaries + scan + outputs)"}}
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
@@ -363,7 +402,8 @@ def main():
     # ---- decode: hla2_step on n=4096 heads, d=dv=128 ----
     decode = None
     if not args.no_decode:
-        wd = W.DECODE
+        wd = W.DECODE if args.decode_n is None else dataclasses.replace(
+            W.DECODE, n=args.decode_n, name=W.DECODE.name + f"-override-n{args.decode_n}")
         R = W.state_floats(wd.d, wd.dv)
         state = torch.zeros(wd.n, R, device=dev)
         toks = list(W.decode_tokens(wd, device=dev, seed=wd.seed + 1000 * rank))
@@ -384,7 +424,7 @@ def main():
                   "value": world * wd.n / (ms_dec / 1e3), "unit": "tokens/s", "ms_per_step": ms_dec,
                   "steps": wd.steps, "prefill": wd.prefill,
                   "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC.get("step"),
+                               "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC.get(("step", wd.name)),
                                "bytes_per_head_step": bytes_head}}
         # the same stream on the compact P-form state (S | P | p), converted from the prefilled state
         Rp = hla2.pform_record_len(wd.d, wd.dv)
@@ -406,6 +446,29 @@ def main():
                            "unit": "tokens/s", "ms_per_step": ms_pf,
                            "roofline": {"bound": "hbm", "achieved": ach_pf, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                         "frac": ach_pf / peaks["hbm_gbs"], "bytes_per_head_step": bytes_pf}}
+        if not args.no_ahla:
+            # AHLA decode on the same token stream: state P | E | m | n per head
+            Ra = hla2.ahla_state_len(wd.d, wd.dv)
+            del pstate
+            astate = torch.zeros(wd.n, Ra, device=dev)
+            for t in range(wd.prefill):
+                hla2.hla2_ahla_step(astate, *toks[t])
+            barrier()
+            e8 = torch.cuda.Event(enable_timing=True); e9 = torch.cuda.Event(enable_timing=True)
+            e8.record(stream)
+            for t in range(wd.prefill, wd.prefill + wd.steps):
+                hla2.hla2_ahla_step(astate, *toks[t], o=o)
+            e9.record(stream)
+            barrier()
+            ms_ah = max_over_ranks(e8.elapsed_time(e9) / wd.steps)
+            bytes_ah = 8 * Ra + 4 * (2 * wd.d + 2 * wd.dv)
+            ach_ah = wd.n * bytes_ah / (ms_ah / 1e3) / 1e9
+            decode["ahla"] = {"metric": "hla2_ahla_step tokens/s (heads*steps/s)",
+                              "value": world * wd.n / (ms_ah / 1e3), "unit": "tokens/s", "ms_per_step": ms_ah,
+                              "roofline": {"bound": "hbm", "achieved": ach_ah, "peak": peaks["hbm_gbs"],
+                                           "unit": "GB/s", "frac": ach_ah / peaks["hbm_gbs"],
+                                           "bytes_per_head_step": bytes_ah}}
+            pstate = astate
         del toks, pstate
     clk = clocks.stop(t_begin, t_end)
 
@@ -420,7 +483,7 @@ def main():
                 "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
                 "config": fwd_config(w, segments_per_head(w.BH, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-                "cpu_baseline": cpu, "decode": decode}
+                "cpu_baseline": cpu, "decode": decode, "ahla": ahla}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

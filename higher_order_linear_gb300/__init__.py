@@ -5,6 +5,9 @@ declared in ``include/hla2.h``; ``hla2`` is the thin Python binding.
 """
 from .hla2 import (  # noqa: F401
     HLA2Error,
+    ahla_state_len,
+    hla2_ahla_forward,
+    hla2_ahla_step,
     hla2_chunk_summaries,
     hla2_device_status,
     hla2_forward,
@@ -15,6 +18,9 @@ from .hla2 import (  # noqa: F401
     hla2_state_to_pform,
     hla2_step,
     hla2_step_pform,
+    hla2_unmasked_forward,
+    hla2_unmasked_step,
     pform_record_len,
     record_len,
+    unmasked_state_len,
 )

@@ -1,0 +1,464 @@
+// hla2_ahla_tc.cu -- tensor-core segment walks of masked AHLA on GB300
+// (sm_103a): tcgen05.mma with TMEM accumulators, TMA-staged tiles.
+//
+// HLA summary (arXiv 2510.27258), section 2 "AHLA": the operator
+// Q (K^T Q)(K^T V) under the causal mask, o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j,
+// kept as summaries P = sum k v^T, E = sum_i k_i q_i^T P_i (and, to join
+// segments, M = sum k q^T); section 4 for the chunk-parallel form.
+//
+// One CTA walks one segment of one head in chunks of L = 128 tokens.  With
+// the state (P0, E0) entering a chunk and the chunk's Q, K, V:
+//   A = tril(Q K^T)            (i <= t, diagonal kept)
+//   Y = Q P0 + A V             (row i is P_i^T q_i)
+//   O = Q E0 + A Y             (the chunk's outputs)
+//   E0 += K^T Y,   P0 += K^T V
+// The summary walk starts from zero and also accumulates M += K^T Q.  Every
+// product is a 128-row tcgen05.mma kind::f16 (bf16 operands in shared
+// memory, fp32 accumulators in tensor memory).  A, Y, P0 and E0 are rounded
+// to bf16 when written back as operands; P and E stay fp32 in tensor memory
+// for the whole segment.  On a head's first chunk (where an output can be a
+// single product: t = 0 gives (q.k)^2 v) A and Y are split into bf16 hi + lo
+// parts: Y = Q P0 + A_hi V + A_lo V, O = A_hi Y_hi + A_lo Y_hi + A_hi Y_lo,
+// E += K^T Y_hi + K^T Y_lo.  That chunk has P0 = E0 = 0, so at d = 128 the
+// E0 and P0 tiles hold the lo parts of A and Y (P0 of the next chunk is then
+// written only after every product of the first chunk has completed).
+//
+// Roles as in the HLA walk: warp 8 (lane 0) issues every TMA copy and MMA;
+// warps 0..7 drain tensor memory (warp w: lane quarter w % 4, column half
+// w / 4).  They meet only on mbarriers, every wait bounded in time.
+#include "hla2_tc_common.cuh"
+
+namespace hla2 {
+namespace {
+
+struct AParams {
+    int T, nseg, nchunk;
+    float* summ;          // summary walk: output records M|P|m|E|n
+    const float* prefix;  // output walk: input records (P, E read)
+    int* status;
+};
+
+template <int D, int MODE>
+struct ALayout {
+    static constexpr uint32_t kTok = kL * D * 2;  // Q, K, V, Y tiles
+    static constexpr uint32_t kSq = kL * kL * 2;  // A tile
+    static constexpr uint32_t kSt = D * D * 2;    // P0 / E0 tiles
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, Y = A + kSq;
+    static constexpr uint32_t P = Y + kTok;
+    static constexpr uint32_t E = P + kSt;  // output walk only
+    static constexpr uint32_t kEnd = (MODE == 1) ? E + kSt : E;
+    // lo parts of A and Y on a head's first chunk (output walk): the E0 and
+    // P0 tiles at D = 128 (same geometry, unused there), own tiles at D = 64
+    static constexpr uint32_t Alo = (D == 128) ? E : kEnd;
+    static constexpr uint32_t Ylo = (D == 128) ? P : kEnd + kSq;
+    static constexpr uint32_t kEnd2 = (MODE == 1 && D < 128) ? kEnd + kSq + kTok : kEnd;
+    // MN-major operands read with M = 128 > D see a second 64-column block
+    // one block past the tile: keep valid memory there when D = 64.
+    static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
+    static constexpr uint32_t kBytes = kEnd2 + kPad;
+};
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, AParams p) {
+    using LY = ALayout<D, MODE>;
+    extern __shared__ __align__(1024) unsigned char dsm_raw[];
+    // loads | MMA commits | drains
+    enum { LQ, LK, LV, CA, CY, CO, CE, DA, DY, DO, DP, DE, NBAR };
+    __shared__ __align__(8) unsigned long long bars[NBAR];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const bool issuer = warp == kDrainWarps;
+    const int quarter = warp & 3;
+    const int half = (warp >> 2) & 1;
+    const int row = quarter * 32 + lane;
+    const int seg = blockIdx.x;
+    const int head = blockIdx.y;
+    const int c_begin = (int)((long long)seg * p.nchunk / p.nseg);
+    const int c_end = (int)((long long)(seg + 1) * p.nchunk / p.nseg);
+    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
+
+    const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
+    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
+    const Tile tA{dsm + LY::A, kL}, tY{dsm + LY::Y, kL}, tAl{dsm + LY::Alo, kL}, tYl{dsm + LY::Ylo, kL};
+    const Tile tP{dsm + LY::P, D}, tE{dsm + LY::E, D};
+    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t cnt = 1;
+            if (i == DA || i == DY || i == DO) cnt = kDrainWarps;
+            if (i == DP || i == DE) cnt = kStateWarps;
+            mbar_init(bar(i), cnt);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    // tensor-memory regions (column offsets)
+    //   output walk:  A then O | Y | P | E
+    //   summary walk: A then Y | P | E | M
+    const uint32_t tA_ = tmem + 0;
+    const uint32_t tY_ = tmem + 128;  // output walk only
+    const uint32_t tP_ = tmem + (MODE == 1 ? 256 : 128);
+    const uint32_t tE_ = tP_ + D;
+    const uint32_t tM_ = tE_ + D;     // summary walk only
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c128 = half * 64;
+    const int cD = half * (D / 2);
+
+    constexpr uint32_t kTileBytes = kL * D * 2;
+    auto wait_bar = [&](int b, uint32_t parity) -> bool {
+        const uint32_t a = bar(b);
+        if (abort_flag) return false;
+        if (mbar_try(a, parity)) return true;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try(a, parity)) {
+            if (abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                abort_flag = 1;
+                atomicExch(p.status, (int)kDevWaitTimeout);
+                return false;
+            }
+        }
+        return true;
+    };
+    auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        mbar_expect_tx(bar(b), kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
+    };
+    auto prefetch = [&](int chunk) {
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) {
+            tma_prefetch_l2_3d(&mQ, k * 64, chunk * kL, head);
+            tma_prefetch_l2_3d(&mK, k * 64, chunk * kL, head);
+            tma_prefetch_l2_3d(&mV, k * 64, chunk * kL, head);
+        }
+    };
+    auto drained = [&](int b) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
+    };
+    auto drain128 = [&](uint32_t treg, const Tile& t, bool mask) {
+        uint32_t r[64];
+        tmem_ld_cols<64>(treg + lane_off + c128, r);
+        put_row32(t, row, c128, r, mask);
+        put_row32(t, row, c128 + 32, r + 32, mask);
+    };
+    auto drain128s = [&](uint32_t treg, const Tile& hi, const Tile& lo, bool mask) {
+        uint32_t r[64];
+        tmem_ld_cols<64>(treg + lane_off + c128, r);
+        put_row32_split2(hi, lo, row, c128, r, mask);
+        put_row32_split2(hi, lo, row, c128 + 32, r + 32, mask);
+    };
+    auto drainD = [&](uint32_t treg, const Tile& t) {
+        uint32_t r[64];
+        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        put_row32(t, row, cD, r, false);
+        if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
+    };
+    auto drainDs = [&](uint32_t treg, const Tile& hi, const Tile& lo) {
+        uint32_t r[64];
+        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        put_row32_split2(hi, lo, row, cD, r, false);
+        if (D == 128) put_row32_split2(hi, lo, row, cD + 32, r + 32, false);
+    };
+
+    // ---- initial state (output walk): P0, E0 fp32 into TMEM, bf16 into smem ----
+    if (MODE == 1 && state_rows) {
+        const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
+        const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
+        const float* src[2] = {pre + (size_t)D * D, pre + 2 * (size_t)D * D + D};  // P (after M), E (after m)
+        const uint32_t dst[2] = {tP_, tE_};
+        const Tile* til[2] = {&tP, &tE};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll 1
+            for (int cb = cD; cb < cD + D / 2; cb += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src[m] + (size_t)row * D + cb + j);
+                    r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
+                    r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
+                }
+                tmem_st32(dst[m] + lane_off + cb, r);
+                put_row32(*til[m], row, cb, r, false);
+            }
+        }
+        tmem_st_wait();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
+    constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
+    constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
+    const int nchunks = c_end - c_begin;
+
+    if (issuer) {
+        // ============================ issuer ============================
+        if (lane == 0 && nchunks > 0) {
+            issue_load(LQ, &mQ, tQ, c_begin);
+            issue_load(LK, &mK, tK, c_begin);
+            issue_load(LV, &mV, tV, c_begin);
+            if (nchunks > 1) prefetch(c_begin + 1);
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1, pph = (it + 1) & 1;
+                const bool has_next = it + 1 < nchunks;
+                if (it + 2 < nchunks) prefetch(c + 2);
+                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
+                if (MODE == 1) {
+                    const bool first = c == 0;  // P0 = E0 = 0; A and Y split into hi + lo
+                    if (it > 0 && !wait_bar(DO, pph)) break;  // O of the previous chunk read out of TMEM A
+                    tc_fence_after();
+                    // A = Q K^T
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                    mma_commit(bar(CA));
+                    if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P0 of this chunk; TMEM P read
+                    tc_fence_after();
+                    // Y = Q P0
+                    if (!first)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tY_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
+                    if (!wait_bar(LV, ph)) break;
+                    tc_fence_after();
+                    // P += K^T V
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tK.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                    if (!wait_bar(DA, ph)) break;  // sA = A (and its lo part on the first chunk)
+                    tc_fence_after();
+                    // Y += A V
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tY_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                    if (first)
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tY_, tAl.kmaj(ks), tV.mnmaj(ks), iKM, 1);
+                    mma_commit(bar(CY));
+                    if (!wait_bar(DY, ph)) break;  // sY = Y (and Y_lo on the first chunk); TMEM Y read
+                    tc_fence_after();
+                    if (has_next) issue_load(LV, &mV, tV, c + 1);
+                    if (it > 0 && !wait_bar(DE, pph)) break;  // sE = E0 of this chunk; TMEM E read
+                    tc_fence_after();
+                    // O = Q E0 + A Y
+                    if (!first)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tE.mnmaj(ks), iKM, ks > 0);
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tA_, tA.kmaj(ks), tY.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                    if (first) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tY.mnmaj(ks), iKM, 1);
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tYl.mnmaj(ks), iKM, 1);
+                    }
+                    mma_commit(bar(CO));
+                    // E += K^T Y
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, 1);
+                    if (first)
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tYl.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CE));
+                    if (has_next) {
+                        if (!wait_bar(CO, ph)) break;
+                        issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q E0
+                        if (!wait_bar(CE, ph)) break;
+                        issue_load(LK, &mK, tK, c + 1);  // K was last read by K^T Y
+                    }
+                } else {
+                    const uint32_t acc0 = it > 0 ? 1u : 0u;  // segment-local sums start at zero
+                    tc_fence_after();
+                    // A = Q K^T   (TMEM A is free: the previous Y was drained before its E product)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                    mma_commit(bar(CA));
+                    // M += K^T Q
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tM_, tK.mnmaj(ks), tQ.mnmaj(ks), iMM, (acc0 || ks > 0) ? 1u : 0u);
+                    if (!wait_bar(LV, ph)) break;
+                    if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P_local of this chunk; TMEM P read
+                    tc_fence_after();
+                    // P += K^T V
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tP_, tK.mnmaj(ks), tV.mnmaj(ks), iMM, (acc0 || ks > 0) ? 1u : 0u);
+                    if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
+                    tc_fence_after();
+                    // Y = Q P_local + A V   (no P_local term on the segment's first chunk)
+                    if (it > 0)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (acc0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CY));
+                    if (!wait_bar(DY, ph)) break;  // sY = Y; TMEM A read (Q and V no longer read)
+                    tc_fence_after();
+                    if (has_next) {
+                        issue_load(LQ, &mQ, tQ, c + 1);
+                        issue_load(LV, &mV, tV, c + 1);
+                    }
+                    // E += K^T Y
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, (acc0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(CE));
+                    if (has_next) {
+                        if (!wait_bar(CE, ph)) break;
+                        issue_load(LK, &mK, tK, c + 1);  // K was last read by K^T Y
+                    }
+                }
+            }
+        }
+    } else {
+        // ========================== drain warps ==========================
+        for (int it = 0; it < nchunks; ++it) {
+            const uint32_t ph = it & 1;
+            const bool has_next = it + 1 < nchunks;
+            if (MODE == 1) {
+                const bool first = c_begin + it == 0;
+                if (!wait_bar(CA, ph)) break;
+                tc_fence_after();
+                if (lane == 0) tma_store_wait_read();  // this warp's O piece has left its sA rows
+                __syncwarp();
+                if (first) drain128s(tA_, tA, tAl, true);  // A -> sA (hi), A_lo (masked)
+                else drain128(tA_, tA, true);              // A -> sA (masked)
+                drained(DA);
+                if (!wait_bar(CY, ph)) break;
+                tc_fence_after();
+                if (first) drainDs(tY_, tY, tYl);  // Y -> sY (hi), Y_lo
+                else drainD(tY_, tY);              // Y -> sY
+                drained(DY);
+                if (state_rows && has_next && !first) {
+                    drainD(tP_, tP);  // P0 of the next chunk -> sP (P += K^T V completed with Y)
+                    drained(DP);
+                }
+                if (!wait_bar(CO, ph)) break;
+                tc_fence_after();
+                {
+                    // O (fp32) leaves through the 4 KB of sA that hold this warp's own
+                    // rows and column half (A there is dead once the output products
+                    // completed), 32 rows x 32 columns per bulk tensor store.
+                    uint32_t r[64];
+                    tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                    const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+                    const int t0 = (c_begin + it) * kL + quarter * 32;
+#pragma unroll
+                    for (int g = 0; g < D / 64; ++g) {
+                        if (g > 0) {
+                            if (lane == 0) tma_store_wait_read();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
+                                         r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
+                                         r[32 * g + 4 * q + 3]);
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&mO, scratch, cD + 32 * g, t0, head);
+                            tma_store_commit();
+                        }
+                    }
+                }
+                drained(DO);
+                if (state_rows && has_next) {
+                    if (!wait_bar(CE, ph)) break;
+                    tc_fence_after();
+                    drainD(tE_, tE);  // E0 of the next chunk -> sE
+                    drained(DE);
+                    if (first) {
+                        drainD(tP_, tP);  // P0 of the next chunk -> sP, once Y_lo there is dead
+                        drained(DP);
+                    }
+                }
+            } else {
+                if (!wait_bar(CA, ph)) break;
+                tc_fence_after();
+                drain128(tA_, tA, true);  // A -> sA (masked)
+                drained(DA);
+                if (!wait_bar(CY, ph)) break;
+                tc_fence_after();
+                drainD(tA_, tY);  // Y -> sY
+                drained(DY);
+                if (state_rows && has_next) {
+                    drainD(tP_, tP);  // P_local of the next chunk -> sP
+                    drained(DP);
+                }
+            }
+        }
+        if (MODE == 1 && lane == 0) tma_store_wait_all();
+        // ---- segment summary out (summary walk): M | P | . | E | . records, fp32 ----
+        if (MODE == 0 && state_rows && nchunks > 0 && wait_bar(CE, (nchunks - 1) & 1)) {
+            tc_fence_after();
+            const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
+            float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
+            float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // M, P, E
+            const uint32_t src[3] = {tM_, tP_, tE_};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
+#pragma unroll
+                for (int j = 0; j < D / 2; j += 4)
+                    *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                    __uint_as_float(r[j + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+template <int D, int MODE>
+cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
+                     int T, SegPlan plan, int* status, cudaStream_t s) {
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
+        !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
+        !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
+        return cudaErrorInvalidValue;
+    if (MODE == 1) {
+        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
+    } else {
+        mo = mq;  // unused
+    }
+    AParams prm{T, plan.nseg, plan.nchunk, summ, prefix, status};
+    const size_t smem = ALayout<D, MODE>::kBytes + 1024;
+    auto kern = ahla_tc_walk_kernel<D, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.nseg, BH);
+    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, prm);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
+                                float* summ, int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s) {
+    if (BH == 0 || plan.nseg == 0) return cudaSuccess;
+    if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
+    if (d == 128) return mode == 0 ? launch_t<128, 0>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
+                                   : launch_t<128, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    if (d == 64) return mode == 0 ? launch_t<64, 0>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
+                                  : launch_t<64, 1>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hla2

@@ -186,6 +186,45 @@ static int forward_scan(const FwdWorkspace& ws, int BH, SegPlan plan, int d, int
     return HLA2_OK;
 }
 
+// AHLA scan over the segment summaries M|P|m|E|n (HLA summary, section 2 for
+// the summaries, section 4 for the combine).  E_AB = E_A + E_B + M_B P_A makes
+// the exclusive prefix unroll to E_<n = sum_{r<n} (E_r + M_r P_<r):
+//   1. exclusive sums of P (and m),
+//   2. Y_r = E_r + M_r P_<r (and n_r + M_r m_<r), one product per record,
+//   3. exclusive sums of Y in place.
+// M itself is never summed: no prefix or final state needs it.
+static int forward_scan_ahla(const FwdWorkspace& ws, int BH, SegPlan plan, int d, int dv, bool want_extra,
+                             bool want_tot, bool use_tc, int* status, cudaStream_t s) {
+    const RecOff ro = summary_offsets(d, dv);
+    const size_t R = ro.R;
+    cudaError_t e;
+    const size_t plen = want_extra ? (size_t)d * dv + d : (size_t)d * dv;  // P (| m)
+    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, R, ro.C, plen, want_tot ? ws.tot + ro.C : nullptr, R, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ahla scan: prefix sums of P, m");
+    CrossArgs a{};
+    a.A = ws.summ + ro.S;   a.sA = (long long)R;      // M_r
+    a.B = ws.prefix + ro.C; a.sB = (long long)R;      // P_<r
+    a.bx = want_extra ? ws.prefix + ro.m : nullptr; a.sbx = (long long)R;  // m_<r
+    a.base = ws.summ + ro.X; a.sbase = (long long)R;  // E_r
+    a.basex = ws.summ + ro.x; a.sbasex = (long long)R;  // n_r
+    a.out = ws.prefix + ro.X; a.sout = (long long)R;
+    a.outx = want_extra ? ws.prefix + ro.x : nullptr; a.soutx = (long long)R;
+    a.alpha = 1.f; a.d = d; a.dv = dv; a.status = status;
+    for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
+        CrossArgs c = a;
+        const long long nb = (long long)BH * plan.nseg - b0;
+        c.nb = (int)(nb < 65535 ? nb : 65535);
+        c.A += b0 * R; c.B += b0 * R; if (c.bx) c.bx += b0 * R;
+        c.base += b0 * R; c.basex += b0 * R; c.out += b0 * R; if (c.outx) c.outx += b0 * R;
+        e = (use_tc && !want_extra) ? launch_tc_cross(c, s) : launch_cross(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ahla scan: cross terms");
+    }
+    const size_t elen = want_extra ? (size_t)d * dv + d : (size_t)d * dv;  // E (| n)
+    e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, R, ro.X, elen, want_tot ? ws.tot + ro.X : nullptr, R, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ahla scan: prefix sums of E, n");
+    return HLA2_OK;
+}
+
 }  // namespace hla2
 
 using namespace hla2;
@@ -229,7 +268,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
 
     // segment summaries
     if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, status, s);
-    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, s);
+    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
     // exclusive scan of the summaries
@@ -238,7 +277,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (prof) cudaEventRecord(pe.ev[2], s);
     // outputs
     if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, status, s);
-    else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, s);
+    else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 0, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment outputs");
     if (prof) {
         cudaEventRecord(pe.ev[3], s);
@@ -340,7 +379,7 @@ int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* sum
     p.nchunk = (T + L - 1) / L;
     p.nseg = p.nchunk;  // one chunk per segment
     if (p.nseg > 65535) return fail(HLA2_ERR_UNSUPPORTED, "%d chunks per head exceeds 65535", p.nseg);
-    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, p,
+    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, p,
                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "hla2_chunk_summaries");
     return HLA2_OK;
@@ -448,6 +487,117 @@ int hla2_device_status(hla2_stream_t stream) {
                                                                            : v == kDevTmemAlloc ? "tensor memory allocation"
                                                                                                 : "unknown");
     }
+    return HLA2_OK;
+}
+
+
+int hla2_ahla_forward(const void* Q, const void* K, const void* V, float* O, int B, int H, int T, int d, int dv,
+                      int normalized, int dtype, void* workspace, size_t ws_bytes, float* state_out,
+                      hla2_stream_t stream) {
+    int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);
+    if (rc) return rc;
+    if (!O) return fail(HLA2_ERR_INVALID, "null output pointer");
+    if (!aligned16(O) || (state_out && !aligned16(state_out))) return fail(HLA2_ERR_INVALID, "output pointer not 16-byte aligned");
+    const size_t need = hla2_forward_workspace(B, H, T, d, dv, dtype);
+    if (!workspace || ws_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : (size_t)0, need);
+    if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const SegPlan plan = forward_plan(BH, T);
+    const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
+    const bool want_extra = normalized || state_out;  // m and n needed
+    int* status = device_status_word();
+    if (!status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    const bool use_tc = hla2_ahla_forward_path(d, dv, dtype, normalized, state_out != nullptr) == 1;
+    cudaError_t e = use_tc ? launch_ahla_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, plan, status, s)
+                           : launch_ahla_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized,
+                                              plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ahla segment summaries");
+    rc = forward_scan_ahla(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
+    if (rc) return rc;
+    e = use_tc ? launch_ahla_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, plan, status, s)
+               : launch_ahla_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ahla segment outputs");
+    if (state_out) {
+        // final state in decode order P|E|m|n from the scan totals
+        const RecOff so = summary_offsets(d, dv);
+        const long long R = (long long)so.R;
+        const long long Rs = 2LL * d * dv + 2LL * d;
+        const size_t nC = (size_t)d * dv;
+        e = launch_copy_strided(ws.tot + so.C, R, state_out, Rs, nC, BH, s);
+        if (e == cudaSuccess) e = launch_copy_strided(ws.tot + so.X, R, state_out + nC, Rs, nC, BH, s);
+        if (e == cudaSuccess) e = launch_copy_strided(ws.tot + so.m, R, state_out + 2 * nC, Rs, (size_t)d, BH, s);
+        if (e == cudaSuccess) e = launch_copy_strided(ws.tot + so.x, R, state_out + 2 * nC + d, Rs, (size_t)d, BH, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ahla state_out copy");
+    }
+    return HLA2_OK;
+}
+
+int hla2_ahla_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return (!normalized && !with_state_out && tc_supported(d, dv, dtype, 0, dev)) ? 1 : 0;
+}
+
+int hla2_ahla_step(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,
+                   int normalized, hla2_stream_t stream) {
+    if (!state || !q || !k || !v || !o) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    auto pow2_4_128 = [](int x) { return x >= 4 && x <= 128 && (x & (x - 1)) == 0; };
+    if (!pow2_4_128(d) || !pow2_4_128(dv))
+        return fail(HLA2_ERR_UNSUPPORTED, "hla2_ahla_step needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
+    cudaError_t e = launch_ahla_step(state, q, k, v, o, n, d, dv, normalized, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_ahla_step");
+    return HLA2_OK;
+}
+
+
+int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O, int B, int H, int T, int d, int dv,
+                          int normalized, int dtype, void* workspace, size_t ws_bytes, float* state_out,
+                          hla2_stream_t stream) {
+    int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);
+    if (rc) return rc;
+    if (!O) return fail(HLA2_ERR_INVALID, "null output pointer");
+    if (!aligned16(O) || (state_out && !aligned16(state_out))) return fail(HLA2_ERR_INVALID, "output pointer not 16-byte aligned");
+    const size_t need = hla2_forward_workspace(B, H, T, d, dv, dtype);
+    if (!workspace || ws_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : (size_t)0, need);
+    if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const SegPlan plan = forward_plan(BH, T);
+    const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
+    const RecOff ro = summary_offsets(d, dv);
+    // segment sums S|C|m, their exclusive prefix sums (the combine has no
+    // cross term here), then the walks from the prefixes
+    cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 1, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "unmasked segment sums");
+    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, ro.X, state_out ? ws.tot : nullptr, ro.R, s);
+    if (e != cudaSuccess) return cuda_fail(e, "unmasked prefix sums");
+    e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 1, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "unmasked segment outputs");
+    if (state_out) {
+        // final state S|C|m: the first d*d + d*dv + d floats of the totals
+        e = launch_copy_strided(ws.tot, (long long)ro.R, state_out, (long long)ro.X, ro.X, BH, s);
+        if (e != cudaSuccess) return cuda_fail(e, "unmasked state_out copy");
+    }
+    return HLA2_OK;
+}
+
+int hla2_unmasked_step(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,
+                       int normalized, hla2_stream_t stream) {
+    if (!state || !q || !k || !v || !o) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    auto pow2_4_128 = [](int x) { return x >= 4 && x <= 128 && (x & (x - 1)) == 0; };
+    if (!pow2_4_128(d) || !pow2_4_128(dv))
+        return fail(HLA2_ERR_UNSUPPORTED, "hla2_unmasked_step needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
+    cudaError_t e = launch_step_unmasked(state, q, k, v, o, n, d, dv, normalized, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_unmasked_step");
     return HLA2_OK;
 }
 

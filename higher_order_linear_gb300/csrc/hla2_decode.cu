@@ -225,10 +225,17 @@ cudaError_t launch_step(float* state, const float* q, const float* k, const floa
 //   P_t = P + u v^T,  p_t = p + u,  den = q . p_t
 // (P_t - P_{t-1} = S_t q_t v_t^T).  Two passes: S (row reductions give u),
 // then P (column reductions give q^T P_{t-1} while P is updated).
+//
+// The unmasked operator o_t = q_t^T S_t C_t (no G correction) has the same
+// two-pass shape on the state S | C | m, with the roles of q and u swapped in
+// the second pass:
+//   S_t = S + k k^T,  u = S_t q,  o = u^T C_{t-1} + (u . q) v,
+//   C_t = C + q v^T,  m_t = m + q,  den = u . m_t.
 // ---------------------------------------------------------------------------
 namespace hla2 {
 namespace {
 
+template <bool UNMASKED>
 __global__ void __launch_bounds__(kThreads)
 step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const float* __restrict__ k,
                   const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized) {
@@ -305,7 +312,8 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
             for (int i = 0; i < kUnroll; ++i) {
                 const int a = a0 + i * rows_per + rg;
                 if (a < d) {
-                    const float qa = sq[a], ua = su[a];
+                    // P-form: reduce with q, update with u;  unmasked: reduce with u, update with q
+                    const float qa = UNMASKED ? su[a] : sq[a], ua = UNMASKED ? sq[a] : su[a];
                     float4 x = r[i];
                     py[0] = fmaf(qa, x.x, py[0]); py[1] = fmaf(qa, x.y, py[1]);
                     py[2] = fmaf(qa, x.z, py[2]); py[3] = fmaf(qa, x.w, py[3]);
@@ -322,9 +330,9 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
     if (tid < 32) {
         float qu = 0.f, qp = 0.f;
         for (int a = tid; a < d; a += 32) {
-            const float pn = p[a] + su[a];
+            const float pn = p[a] + (UNMASKED ? sq[a] : su[a]);  // p + u  |  m + q
             qu += sq[a] * su[a];
-            qp += sq[a] * pn;
+            qp += (UNMASKED ? su[a] : sq[a]) * pn;               // q . p_t  |  u . m_t
             p[a] = pn;
         }
         qu = warp_sum(qu); qp = warp_sum(qp);
@@ -346,7 +354,15 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
 cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o, int n, int d,
                               int dv, int normalized, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    step_pform_kernel<<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
+    step_pform_kernel<false><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_step_unmasked(float* state, const float* q, const float* k, const float* v, float* o, int n,
+                                 int d, int dv, int normalized, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    step_pform_kernel<true><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
     note_launches(1);
     return cudaGetLastError();
 }

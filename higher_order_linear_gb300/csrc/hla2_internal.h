@@ -72,13 +72,19 @@ cudaError_t launch_step(float* state, const float* q, const float* k, const floa
 cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o,
                               int n, int d, int dv, int normalized, cudaStream_t s);
 
+// Unmasked operator o = q^T S C on the state S | C | m.
+cudaError_t launch_step_unmasked(float* state, const float* q, const float* k, const float* v, float* o,
+                                 int n, int d, int dv, int normalized, cudaStream_t s);
+
 // ---- segment walks on CUDA cores (hla2_walk.cu) ----
 // mode 0: P-form segment summary  S|C|m|P|p from zero state.
 // mode 1: outputs, starting from the prefix record S|.|.|P|p of the segment.
 // mode 2: G-form summary S|C|m|G|h from zero state (chunk summaries).
+// unmasked (modes 0, 1): o_t = q_t^T S_t C_t; mode 0 keeps S|C|m only, mode 1
+// starts from the prefix S|C|m.
 cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, int dtype,
                         float* O, const float* prefix, float* summ,
-                        int BH, int T, int d, int dv, int normalized, SegPlan plan,
+                        int BH, int T, int d, int dv, int normalized, int unmasked, SegPlan plan,
                         cudaStream_t s);
 
 // ---- scans (hla2_scan.cu) ----
@@ -111,12 +117,28 @@ cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s);
 cudaError_t launch_copy_strided(const float* src, long long s_src, float* dst, long long s_dst,
                                 size_t len, int nb, cudaStream_t s);
 
+// ---- AHLA on CUDA cores (hla2_ahla.cu) ----
+// mode 0: segment summary M|P|m|E|n (at the S|C|m|X|x offsets) from zero.
+// mode 1: outputs from the segment's prefix P, E (and m, n when normalised).
+cudaError_t launch_ahla_walk(int mode, const void* Q, const void* K, const void* V, int dtype,
+                             float* O, const float* prefix, float* summ,
+                             int BH, int T, int d, int dv, int normalized, SegPlan plan,
+                             cudaStream_t s);
+// One decode step on n heads, state P|E|m|n per head.
+cudaError_t launch_ahla_step(float* state, const float* q, const float* k, const float* v, float* o,
+                             int n, int d, int dv, int normalized, cudaStream_t s);
+
 // ---- tensor-core segment walks (hla2_tc.cu) ----
 bool tc_supported(int d, int dv, int dtype, int normalized, int device);
 cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V,
                            float* O, const float* prefix, float* summ,
                            int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
                            cudaStream_t s);
+// AHLA on tensor cores (hla2_ahla_tc.cu), d = dv in {64, 128}, bf16, unnormalised:
+// mode 0 writes the M|P|.|E|. parts of the segment summaries, mode 1 outputs.
+cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const void* V,
+                                float* O, const float* prefix, float* summ,
+                                int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s);
 // Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
 // (d = dv in {64, 128}, no extra column).
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);

@@ -17,6 +17,11 @@
 //           and emit o_t = q_t^T P_t (divided by q_t^T p_t when normalised).
 //   mode 2  G-form chunk summary from a zero state (S|C|m|G|h), by the
 //           recurrence G += k (C_{t-1}^T k), h += k (k . m_{t-1}).
+// With `unmasked` set, modes 0 and 1 compute the unmasked operator
+// o_t = q_t^T S_t C_t (section 1's naive product, no G correction): mode 0
+// keeps only the plain sums S, C, m, and mode 1 starts from the prefix
+// (S0, C0, m0) and takes, per token, S += k k^T, u = S q, C += q v^T,
+// o = u^T C (divided by u . m when normalised).
 // S is symmetric (a sum of outer products formed elementwise), so S q is
 // taken as a column reduction, which matches the thread layout of the walk.
 #include "hla2_internal.h"
@@ -53,7 +58,7 @@ template <typename Tin, int MODE>
 __global__ void __launch_bounds__(kWalkThreads)
 walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __restrict__ V,
             float* __restrict__ O, const float* __restrict__ prefix, float* __restrict__ summ,
-            int T, int d, int dv, int normalized, SegPlan plan) {
+            int T, int d, int dv, int normalized, int unmasked, SegPlan plan) {
     extern __shared__ float4 smem4[];
     float* sm = reinterpret_cast<float*>(smem4);
     const int mx = d > dv ? d : dv;
@@ -90,9 +95,11 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
     // ---- initial state ----
     if (MODE == 1) {
         const float* pre = prefix + ((size_t)head * plan.nseg + seg) * R;
+        // P-form: X = P, x = p;  unmasked: X = C, x = m
+        const size_t oX = unmasked ? ro.C : ro.X, ox = unmasked ? ro.m : ro.x;
         for (int i = tid; i < d * d; i += kWalkThreads) s.S[i] = pre[ro.S + i];
-        for (int i = tid; i < d * dv; i += kWalkThreads) s.X[i] = pre[ro.X + i];
-        for (int i = tid; i < d; i += kWalkThreads) s.x[i] = pre[ro.x + i];
+        for (int i = tid; i < d * dv; i += kWalkThreads) s.X[i] = pre[oX + i];
+        for (int i = tid; i < d; i += kWalkThreads) s.x[i] = pre[ox + i];
     } else {
         for (int i = tid; i < d * d; i += kWalkThreads) s.S[i] = 0.f;
         for (int i = tid; i < d * dv; i += kWalkThreads) { s.X[i] = 0.f; s.C[i] = 0.f; }
@@ -165,26 +172,45 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
                     float u = 0.f;
                     for (int r = 0; r < nrgs; ++r) u += s.part[r * mx + tid];
                     s.u[tid] = u;
-                    s.x[tid] += u;                       // p_t = p_{t-1} + u
+                    if (unmasked) {
+                        if (MODE == 1) s.x[tid] += q[tid];  // m_t = m_{t-1} + q
+                    } else {
+                        s.x[tid] += u;                       // p_t = p_{t-1} + u
+                    }
                     if (MODE == 0) s.m[tid] += q[tid];
                 }
                 __syncthreads();
                 // P_t = P_{t-1} + u v^T ; outputs o_e = sum_a q_a P_t[a][e]
                 if (act_v) {
                     float acc = 0.f;
-                    for (int a = rgv; a < d; a += nrgv) {
-                        const int i = a * dv + ev;
-                        const float pn = fmaf(s.u[a], v[ev], s.X[i]);
-                        s.X[i] = pn;
-                        if (MODE == 0) s.C[i] = fmaf(q[a], v[ev], s.C[i]);
-                        acc = fmaf(q[a], pn, acc);
+                    if (unmasked) {
+                        // mode 1: C_t = C_{t-1} + q v^T and o_e = sum_a u_a C_t[a][e]; mode 0: C only
+                        for (int a = rgv; a < d; a += nrgv) {
+                            const int i = a * dv + ev;
+                            if (MODE == 1) {
+                                const float cn = fmaf(q[a], v[ev], s.X[i]);
+                                s.X[i] = cn;
+                                acc = fmaf(s.u[a], cn, acc);
+                            } else {
+                                s.C[i] = fmaf(q[a], v[ev], s.C[i]);
+                            }
+                        }
+                    } else {
+                        for (int a = rgv; a < d; a += nrgv) {
+                            const int i = a * dv + ev;
+                            const float pn = fmaf(s.u[a], v[ev], s.X[i]);
+                            s.X[i] = pn;
+                            if (MODE == 0) s.C[i] = fmaf(q[a], v[ev], s.C[i]);
+                            acc = fmaf(q[a], pn, acc);
+                        }
                     }
                     if (MODE == 1) s.part[rgv * mx + ev] = acc;
                 }
                 if (MODE == 1 && normalized && tid >= kWalkThreads - 32) {
                     const int l = tid - (kWalkThreads - 32);
+                    const float* dv_ = unmasked ? s.u : q;  // den = u . m_t  (P-form: q . p_t)
                     float den = 0.f;
-                    for (int a = l; a < d; a += 32) den = fmaf(q[a], s.x[a], den);
+                    for (int a = l; a < d; a += 32) den = fmaf(dv_[a], s.x[a], den);
                     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
                     if (l == 0) s.misc[1] = den;
                 }
@@ -212,7 +238,7 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
 
 template <typename Tin, int MODE>
 cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O, const float* prefix,
-                          float* summ, int BH, int T, int d, int dv, int normalized, SegPlan plan,
+                          float* summ, int BH, int T, int d, int dv, int normalized, int unmasked, SegPlan plan,
                           cudaStream_t s) {
     const size_t bytes = walk_smem_floats(MODE, d, dv) * sizeof(float);
     auto kern = walk_kernel<Tin, MODE>;
@@ -221,7 +247,7 @@ cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O,
     dim3 grid(plan.nseg, BH);
     kern<<<grid, kWalkThreads, bytes, s>>>(static_cast<const Tin*>(Q), static_cast<const Tin*>(K),
                                            static_cast<const Tin*>(V), O, prefix, summ, T, d, dv, normalized,
-                                           plan);
+                                           unmasked, plan);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -230,19 +256,19 @@ cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O,
 
 cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, int dtype, float* O,
                         const float* prefix, float* summ, int BH, int T, int d, int dv, int normalized,
-                        SegPlan plan, cudaStream_t s) {
+                        int unmasked, SegPlan plan, cudaStream_t s) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (dtype == 1) {
         switch (mode) {
-            case 0: return launch_walk_t<__nv_bfloat16, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
-            case 1: return launch_walk_t<__nv_bfloat16, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
-            default: return launch_walk_t<__nv_bfloat16, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
+            case 0: return launch_walk_t<__nv_bfloat16, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+            case 1: return launch_walk_t<__nv_bfloat16, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+            default: return launch_walk_t<__nv_bfloat16, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
         }
     }
     switch (mode) {
-        case 0: return launch_walk_t<float, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
-        case 1: return launch_walk_t<float, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
-        default: return launch_walk_t<float, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, plan, s);
+        case 0: return launch_walk_t<float, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+        case 1: return launch_walk_t<float, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+        default: return launch_walk_t<float, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
     }
 }
 

@@ -72,6 +72,16 @@ def lib() -> ctypes.CDLL:
             L.hla2_step_pform.restype = i
             L.hla2_state_to_pform.argtypes = [vp, vp, i, i, i, vp]
             L.hla2_state_to_pform.restype = i
+            L.hla2_ahla_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
+            L.hla2_ahla_forward.restype = i
+            L.hla2_ahla_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+            L.hla2_ahla_step.restype = i
+            L.hla2_ahla_forward_path.argtypes = [i, i, i, i, i]
+            L.hla2_ahla_forward_path.restype = i
+            L.hla2_unmasked_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
+            L.hla2_unmasked_forward.restype = i
+            L.hla2_unmasked_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+            L.hla2_unmasked_step.restype = i
             _lib = L
         return _lib
 
@@ -266,3 +276,114 @@ def hla2_profile_read():
     nl = ctypes.c_longlong(0)
     _check(lib().hla2_profile_read(ms, 3, ctypes.byref(nf), ctypes.byref(nl)), "hla2_profile_read")
     return [float(x) for x in ms], int(nf.value), int(nl.value)
+
+
+# ------------------------------------------------------------------ AHLA ----
+def ahla_state_len(d: int, dv: int) -> int:
+    """AHLA decode state per head: P (d x dv) | E (d x dv) | m (d) | n (d)."""
+    return 2 * d * dv + 2 * d
+
+
+def hla2_ahla_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                      normalized: bool = False, workspace: torch.Tensor | None = None,
+                      state_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Masked AHLA forward (o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j).
+    Shapes and dtypes as for hla2_forward; ``state_out`` [B*H, 2*d*dv + 2*d]
+    fp32 receives the final P|E|m|n state if given."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    code = _dtype_code(Q)
+    if O is None:
+        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
+    elif O.shape != (B, H, T, dv):
+        raise ValueError("O has the wrong shape")
+    need = hla2_forward_workspace(B, H, T, d, dv, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
+    sptr = None
+    if state_out is not None:
+        if state_out.numel() != B * H * ahla_state_len(d, dv):
+            raise ValueError("state_out must hold B*H AHLA states")
+        sptr = _dev(state_out, "state_out", torch.float32)
+    rc = lib().hla2_ahla_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                                 B, H, T, d, dv, int(bool(normalized)), code,
+                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                 sptr, _stream(stream))
+    _check(rc, "hla2_ahla_forward")
+    return O
+
+
+def hla2_ahla_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                   o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """One AHLA decode step for n heads: state [n, 2*d*dv + 2*d] fp32 (P|E|m|n,
+    updated in place), q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
+    n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * ahla_state_len(d, dv):
+        raise ValueError("shape mismatch for hla2_ahla_step")
+    if o is None:
+        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
+    rc = lib().hla2_ahla_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
+                              _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
+                              n, d, dv, int(bool(normalized)), _stream(stream))
+    _check(rc, "hla2_ahla_step")
+    return o
+
+
+# -------------------------------------------------------------- unmasked ----
+def unmasked_state_len(d: int, dv: int) -> int:
+    """Unmasked decode state per head: S (d x d) | C (d x dv) | m (d)."""
+    return d * d + d * dv + d
+
+
+def hla2_unmasked_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                          normalized: bool = False, workspace: torch.Tensor | None = None,
+                          state_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Unmasked second-order forward o_t = q_t^T S_t C_t.  Shapes and dtypes
+    as for hla2_forward; ``state_out`` [B*H, d*d + d*dv + d] fp32 receives the
+    final S|C|m if given."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    code = _dtype_code(Q)
+    if O is None:
+        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
+    elif O.shape != (B, H, T, dv):
+        raise ValueError("O has the wrong shape")
+    need = hla2_forward_workspace(B, H, T, d, dv, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
+    sptr = None
+    if state_out is not None:
+        if state_out.numel() != B * H * unmasked_state_len(d, dv):
+            raise ValueError("state_out must hold B*H unmasked states")
+        sptr = _dev(state_out, "state_out", torch.float32)
+    rc = lib().hla2_unmasked_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                                     B, H, T, d, dv, int(bool(normalized)), code,
+                                     _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                     sptr, _stream(stream))
+    _check(rc, "hla2_unmasked_forward")
+    return O
+
+
+def hla2_unmasked_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """One unmasked decode step: state [n, d*d + d*dv + d] fp32 (S|C|m, in place)."""
+    n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * unmasked_state_len(d, dv):
+        raise ValueError("shape mismatch for hla2_unmasked_step")
+    if o is None:
+        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
+    rc = lib().hla2_unmasked_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
+                                  _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
+                                  _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized)), _stream(stream))
+    _check(rc, "hla2_unmasked_step")
+    return o

@@ -4,8 +4,9 @@
  *
  * Source of the method: the technical summary pages of "Higher-order Linear
  * Attention" (arXiv 2510.27258), Japanese and French editions (gist.science),
- * cited below as [HLA §1] ("Second-order HLA"), [HLA §4] ("Parallel training
- * via associative scans") and [HLA R] ("Results and claims").
+ * cited below as [HLA §1] ("Second-order HLA"), [HLA §2] ("AHLA"), [HLA §4]
+ * ("Parallel training via associative scans") and [HLA R] ("Results and
+ * claims").
  *
  * Per head, with tokens t = 0..T-1, q_t, k_t in R^d and v_t in R^dv:
  *   S_t = sum_{i<=t} k_i k_i^T      C_t = sum_{i<=t} q_i v_i^T     m_t = sum_{i<=t} q_i
@@ -182,6 +183,70 @@ HLA2_API int hla2_chunk_summaries(const void* Q, const void* K, const void* V, f
  */
 HLA2_API int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int dv,
               hla2_stream_t stream);
+
+/*
+ * AHLA, the asymmetric second-order variant [HLA §2]: the operator
+ * Q (K^T Q)(K^T V) with streaming summaries P^KV, m^K, E, n.  Under the
+ * causal mask (the reading this library computes; the pages print no update)
+ *   o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j            (A A V, A = tril(Q K^T))
+ *   P_t = P_{t-1} + k_t v_t^T      m_t = m_{t-1} + k_t
+ *   E_t = E_{t-1} + k_t (P_t^T q_t)^T      n_t = n_{t-1} + k_t (q_t . m_t)
+ *   o_t = E_t^T q_t;  ratio-normalised: o_t / (q_t . n_t).
+ * The forward runs like hla2_forward [HLA §4]: segment summaries
+ * M|P|m|E|n (M = sum k q^T, needed only to join segments), an exclusive scan
+ * with the combine E = E_A + E_B + M_B P_A, n = n_A + n_B + M_B m_A (HLA's
+ * combine with S -> M, C -> P, G -> E, h -> n), then segment walks from the
+ * prefixes.  Arguments, layouts, workspace (hla2_forward_workspace) and
+ * errors as for hla2_forward, except state_out:
+ *   state_out optional: [B*H][2*d*dv + 2*d] fp32, per head
+ *             P (d x dv) | E (d x dv) | m (d) | n (d), the hla2_ahla_step layout.
+ */
+HLA2_API int hla2_ahla_forward(const void* Q, const void* K, const void* V, float* O,
+                               int B, int H, int T, int d, int dv, int normalized, int dtype,
+                               void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * Which implementation hla2_ahla_forward picks on the current device:
+ * 1 = tensor-core segment walks (tcgen05; bf16 d = dv in {64, 128},
+ * unnormalised, no state_out), 0 = CUDA-core segment walks (fp32).
+ */
+HLA2_API int hla2_ahla_forward_path(int d, int dv, int dtype, int normalized, int with_state_out);
+
+/*
+ * One AHLA decode step for n heads [HLA §2 streaming summaries].
+ *   state  [n][2*d*dv + 2*d] fp32, per head P | E | m | n, updated in place;
+ *          a zero state is the empty prefix.
+ *   q, k [n][d], v [n][dv], o [n][dv], all fp32.
+ * The token is absorbed (P, m first, then E, n), then o = E^T q is emitted
+ * (divided by q.n when normalized).  Same size rules and errors as hla2_step.
+ */
+HLA2_API int hla2_ahla_step(float* state, const float* q, const float* k, const float* v, float* o,
+                            int n, int d, int dv, int normalized, hla2_stream_t stream);
+
+/*
+ * Unmasked second-order operator [HLA §1: S_t C_t is the naive product that
+ * G_t corrects; HLA R lists the unmasked operator as a variant]:
+ *   o_t = q_t^T S_t C_t = sum_{i<=t, j<=t} (q_t.k_i)(k_i.q_j) v_j,
+ *   ratio-normalised: o_t / (q_t^T S_t m_t).
+ * Segments carry only S, C, m, which join by plain addition, so the scan is a
+ * running sum [HLA §4 with no cross term].  Arguments, layouts, workspace
+ * (hla2_forward_workspace) and errors as for hla2_forward, except state_out:
+ *   state_out optional: [B*H][d*d + d*dv + d] fp32, per head S | C | m, the
+ *             hla2_unmasked_step layout.
+ * Runs on the CUDA-core segment walks (fp32 arithmetic).
+ */
+HLA2_API int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
+                                   int B, int H, int T, int d, int dv, int normalized, int dtype,
+                                   void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * One decode step of the unmasked operator for n heads.
+ *   state  [n][d*d + d*dv + d] fp32, per head S | C | m, updated in place.
+ * S, C, m grow by the token first, then o = (S q)^T C is emitted (divided by
+ * (S q) . m when normalized).  Same size rules and errors as hla2_step.
+ */
+HLA2_API int hla2_unmasked_step(float* state, const float* q, const float* k, const float* v, float* o,
+                                int n, int d, int dv, int normalized, hla2_stream_t stream);
 
 /*
  * Copies the calling host thread's last error reason (NUL-terminated,
