@@ -378,3 +378,80 @@ def dense_unmasked(Q, K, V, normalized: bool = False) -> np.ndarray:
         m = np.cumsum(Q, axis=-2)
         O = O / np.einsum("...ta,...ta->...t", u, m)[..., None]
     return O
+
+
+# ----------------------------------------------------------------- decay ----
+# o_t = sum_{i<=j<=t} gamma^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j: every prefix moment
+# decays by gamma per token.  Decode state in P-form: S|P|p.
+
+def _decay_lib() -> ctypes.CDLL:
+    lib = _lib(0)
+    if not getattr(lib, "_decay_typed", False):
+        dp = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        d_ = ctypes.c_double
+        lib.hla2_oracle_decay_serial.argtypes = [dp, dp, dp, dp, i, i, i, i, i, d_]
+        lib.hla2_oracle_decay_bruteforce.argtypes = [dp, dp, dp, dp, i, i, i, i, i, d_]
+        lib.hla2_oracle_decay_chunk_summaries.argtypes = [dp, dp, dp, dp, i, i, i, i, i, d_]
+        lib.hla2_oracle_decay_combine.argtypes = [dp, dp, dp, i, i, i, d_]
+        lib.hla2_oracle_decay_combine.restype = None
+        lib.hla2_oracle_decay_chunked.argtypes = [dp, dp, dp, dp, i, i, i, i, i, i, d_]
+        lib.hla2_oracle_decay_step_pform.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_]
+        lib._decay_typed = True
+    return lib
+
+
+def decay_serial(Q, K, V, gamma: float, normalized: bool = False) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _decay_lib().hla2_oracle_decay_serial(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized), float(gamma)):
+        raise RuntimeError("oracle decay_serial failed")
+    return O.reshape(*lead, T, dv)
+
+
+def decay_bruteforce(Q, K, V, gamma: float, normalized: bool = False) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _decay_lib().hla2_oracle_decay_bruteforce(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized),
+                                                 float(gamma)):
+        raise RuntimeError("oracle decay_bruteforce failed")
+    return O.reshape(*lead, T, dv)
+
+
+def decay_chunk_summaries(Q, K, V, L: int, gamma: float) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    N = (T + L - 1) // L
+    out = np.zeros((BH, N, record_len(d, dv)))
+    if _decay_lib().hla2_oracle_decay_chunk_summaries(_p(Q), _p(K), _p(V), _p(out), BH, T, d, dv, int(L),
+                                                      float(gamma)):
+        raise RuntimeError("oracle decay_chunk_summaries failed")
+    return out.reshape(*lead, N, record_len(d, dv))
+
+
+def decay_combine(a, b, d: int, dv: int, nB: int, gamma: float) -> np.ndarray:
+    a, b = _f64(a), _f64(b)
+    out = np.zeros(record_len(d, dv))
+    _decay_lib().hla2_oracle_decay_combine(_p(a), _p(b), _p(out), d, dv, int(nB), float(gamma))
+    return out
+
+
+def decay_chunked(Q, K, V, L: int, gamma: float, normalized: bool = False) -> np.ndarray:
+    Q, K, V, lead, BH, T, d, dv = _heads(Q, K, V)
+    O = np.zeros((BH, T, dv))
+    if _decay_lib().hla2_oracle_decay_chunked(_p(Q), _p(K), _p(V), _p(O), BH, T, d, dv, int(normalized), int(L),
+                                              float(gamma)):
+        raise RuntimeError("oracle decay_chunked failed")
+    return O.reshape(*lead, T, dv)
+
+
+def decay_step_pform(state, q, k, v, gamma: float, normalized: bool = False):
+    """One decayed decode step on the P-form state S|P|p; returns (new_state, o)."""
+    state = _f64(state).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n, d = q.shape
+    dv = v.shape[1]
+    o = np.zeros((n, dv))
+    if _decay_lib().hla2_oracle_decay_step_pform(_p(state), _p(q), _p(k), _p(v), _p(o), n, d, dv, int(normalized),
+                                                 float(gamma)):
+        raise RuntimeError("oracle decay_step_pform failed")
+    return state, o

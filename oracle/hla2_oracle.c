@@ -816,3 +816,215 @@ int hla2_oracle_unmasked_step(double* state, const double* q, const double* k, c
     free(u);
     return 0;
 }
+
+/* ====================================================================== */
+/* Exponentially decayed masked operator (HLA summary, section 4 lists     */
+/* decayed variants among the operators the scan covers; the decay form is */
+/* not printed).  Reading: one scalar gamma in (0, 1] decays every prefix  */
+/* moment per token,                                                       */
+/*   S_t = g S + k k^T,  C_t = g C + q v^T,  m_t = g m + q,                */
+/*   G_t = g^2 G + g k k^T C_{t-1},  h_t = g^2 h + g k k^T m_{t-1},        */
+/*   o_t = q_t^T (S_t C_t - G_t)                                           */
+/*       = sum_{i<=j<=t} g^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j,                 */
+/* normalised by q_t^T (S_t m_t - h_t).  gamma = 1 is the masked operator. */
+/* Compact (P-form) decode state S | P | p with P = S C - G, p = S m - h:  */
+/*   S_t = g S + k k^T, u = S_t q, P_t = g^2 P + u v^T, p_t = g^2 p + u.   */
+/* Segment combine (A earlier, B later, B spanning n_B tokens, f = g^n_B): */
+/*   S = f S_A + S_B, C = f C_A + C_B, m = f m_A + m_B,                    */
+/*   G = f^2 G_A + G_B + f S_B C_A,  h = f^2 h_A + h_B + f S_B m_A.        */
+/* ====================================================================== */
+static void decay_absorb(state_t* s, const double* q, const double* k, const double* v, double g, double* w) {
+    const int d = s->d, dv = s->dv;
+    for (int e = 0; e < dv; ++e) {
+        double acc = 0.0;
+        for (int a = 0; a < d; ++a) acc += s->C[(size_t)a * dv + e] * k[a];
+        w[e] = acc;
+    }
+    double km = 0.0;
+    for (int a = 0; a < d; ++a) km += k[a] * s->m[a];
+    for (int a = 0; a < d; ++a) {
+        for (int e = 0; e < dv; ++e)
+            s->G[(size_t)a * dv + e] = g * g * s->G[(size_t)a * dv + e] + g * k[a] * w[e];
+        s->h[a] = g * g * s->h[a] + g * k[a] * km;
+    }
+    for (int a = 0; a < d; ++a)
+        for (int b = 0; b < d; ++b) s->S[(size_t)a * d + b] = g * s->S[(size_t)a * d + b] + k[a] * k[b];
+    for (int a = 0; a < d; ++a)
+        for (int e = 0; e < dv; ++e) s->C[(size_t)a * dv + e] = g * s->C[(size_t)a * dv + e] + q[a] * v[e];
+    for (int a = 0; a < d; ++a) s->m[a] = g * s->m[a] + q[a];
+}
+
+/* Decayed outputs by the serial recurrence (G-form). */
+int hla2_oracle_decay_serial(const double* Q, const double* K, const double* V, double* O,
+                             int BH, int T, int d, int dv, int normalized, double gamma) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    state_t s;
+    if (state_alloc(&s, d, dv)) return -1;
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(d + dv));
+    if (!scratch) { state_free(&s); return -1; }
+    for (int bh = 0; bh < BH; ++bh) {
+        state_zero(&s);
+        for (int t = 0; t < T; ++t) {
+            const double* q = Q + ((size_t)bh * T + t) * d;
+            decay_absorb(&s, q, K + ((size_t)bh * T + t) * d, V + ((size_t)bh * T + t) * dv, gamma, scratch);
+            emit(&s, q, O + ((size_t)bh * T + t) * dv, normalized, scratch);
+        }
+    }
+    free(scratch);
+    state_free(&s);
+    return 0;
+}
+
+/* The definition, O(T^3 d): weights gamma^{2t-i-j} over i <= j <= t. */
+int hla2_oracle_decay_bruteforce(const double* Q, const double* K, const double* V, double* O,
+                                 int BH, int T, int d, int dv, int normalized, double gamma) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0) return -1;
+    for (int bh = 0; bh < BH; ++bh) {
+        const double* Qh = Q + (size_t)bh * T * d;
+        const double* Kh = K + (size_t)bh * T * d;
+        const double* Vh = V + (size_t)bh * T * dv;
+        for (int t = 0; t < T; ++t) {
+            double* o = O + ((size_t)bh * T + t) * dv;
+            for (int e = 0; e < dv; ++e) o[e] = 0.0;
+            double den = 0.0;
+            for (int i = 0; i <= t; ++i) {
+                double qk = 0.0;
+                for (int a = 0; a < d; ++a) qk += Qh[(size_t)t * d + a] * Kh[(size_t)i * d + a];
+                for (int j = i; j <= t; ++j) {
+                    double kq = 0.0;
+                    for (int a = 0; a < d; ++a) kq += Kh[(size_t)i * d + a] * Qh[(size_t)j * d + a];
+                    double wgt = qk * kq;
+                    for (int r = 0; r < 2 * t - i - j; ++r) wgt *= gamma;
+                    den += wgt;
+                    for (int e = 0; e < dv; ++e) o[e] += wgt * Vh[(size_t)j * dv + e];
+                }
+            }
+            if (normalized)
+                for (int e = 0; e < dv; ++e) o[e] /= den;
+        }
+    }
+    return 0;
+}
+
+/* Decayed chunk summaries S|C|m|G|h of every L-token chunk (state from zero). */
+int hla2_oracle_decay_chunk_summaries(const double* Q, const double* K, const double* V, double* summ,
+                                      int BH, int T, int d, int dv, int L, double gamma) {
+    if (!Q || !K || !V || !summ || BH < 0 || T < 0 || d <= 0 || dv <= 0 || L <= 0) return -1;
+    const int N = (T + L - 1) / L;
+    const size_t R = summary_len(d, dv);
+    state_t s;
+    if (state_alloc(&s, d, dv)) return -1;
+    double* w = (double*)malloc(sizeof(double) * (size_t)(d + dv));
+    if (!w) { state_free(&s); return -1; }
+    for (int bh = 0; bh < BH; ++bh)
+        for (int c = 0; c < N; ++c) {
+            state_zero(&s);
+            const int t1 = (c + 1) * L < T ? (c + 1) * L : T;
+            for (int t = c * L; t < t1; ++t)
+                decay_absorb(&s, Q + ((size_t)bh * T + t) * d, K + ((size_t)bh * T + t) * d,
+                             V + ((size_t)bh * T + t) * dv, gamma, w);
+            memcpy(summ + ((size_t)bh * N + c) * R, s.S, sizeof(double) * R);
+        }
+    free(w);
+    state_free(&s);
+    return 0;
+}
+
+/* Decayed combine: A earlier, B later spanning nB tokens. */
+void hla2_oracle_decay_combine(const double* A, const double* B, double* out, int d, int dv, int nB, double gamma) {
+    const size_t nS = (size_t)d * d, nC = (size_t)d * dv;
+    const double *SA = A, *CA = A + nS, *mA = CA + nC, *GA = mA + d, *hA = GA + nC;
+    const double *SB = B, *CB = B + nS, *mB = CB + nC, *GB = mB + d, *hB = GB + nC;
+    double *S = out, *C = out + nS, *m = C + nC, *G = m + d, *h = G + nC;
+    double f = 1.0;
+    for (int r = 0; r < nB; ++r) f *= gamma;
+    for (int a = 0; a < d; ++a) {
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int b = 0; b < d; ++b) acc += SB[(size_t)a * d + b] * CA[(size_t)b * dv + e];
+            G[(size_t)a * dv + e] = f * f * GA[(size_t)a * dv + e] + GB[(size_t)a * dv + e] + f * acc;
+        }
+        double acc = 0.0;
+        for (int b = 0; b < d; ++b) acc += SB[(size_t)a * d + b] * mA[b];
+        h[a] = f * f * hA[a] + hB[a] + f * acc;
+    }
+    for (size_t i = 0; i < nS; ++i) S[i] = f * SA[i] + SB[i];
+    for (size_t i = 0; i < nC; ++i) C[i] = f * CA[i] + CB[i];
+    for (int i = 0; i < d; ++i) m[i] = f * mA[i] + mB[i];
+}
+
+/* Decayed chunked forward: chunk summaries, an exclusive left fold with the
+ * decayed combine, then every chunk restarts the recurrence from its prefix. */
+int hla2_oracle_decay_chunked(const double* Q, const double* K, const double* V, double* O,
+                              int BH, int T, int d, int dv, int normalized, int L, double gamma) {
+    if (!Q || !K || !V || !O || BH < 0 || T < 0 || d <= 0 || dv <= 0 || L <= 0) return -1;
+    const int N = (T + L - 1) / L;
+    const size_t R = summary_len(d, dv);
+    const size_t NB = (size_t)(N > 0 ? N : 1) * (size_t)(BH > 0 ? BH : 1);
+    double* summ = (double*)malloc(sizeof(double) * R * NB);
+    double* pre = (double*)calloc(R * NB, sizeof(double));
+    double* w = (double*)malloc(sizeof(double) * (size_t)(d + dv));
+    state_t s;
+    int rc = -1;
+    if (!summ || !pre || !w || state_alloc(&s, d, dv)) goto out;
+    if (hla2_oracle_decay_chunk_summaries(Q, K, V, summ, BH, T, d, dv, L, gamma)) { state_free(&s); goto out; }
+    for (int bh = 0; bh < BH; ++bh)
+        for (int c = 1; c < N; ++c) {
+            const int nB = L;  /* chunk c-1 is never the last chunk, so it spans L tokens */
+            hla2_oracle_decay_combine(pre + ((size_t)bh * N + c - 1) * R, summ + ((size_t)bh * N + c - 1) * R,
+                                      pre + ((size_t)bh * N + c) * R, d, dv, nB, gamma);
+        }
+    for (int bh = 0; bh < BH; ++bh)
+        for (int c = 0; c < N; ++c) {
+            memcpy(s.S, pre + ((size_t)bh * N + c) * R, sizeof(double) * R);
+            const int t1 = (c + 1) * L < T ? (c + 1) * L : T;
+            for (int t = c * L; t < t1; ++t) {
+                const double* q = Q + ((size_t)bh * T + t) * d;
+                decay_absorb(&s, q, K + ((size_t)bh * T + t) * d, V + ((size_t)bh * T + t) * dv, gamma, w);
+                emit(&s, q, O + ((size_t)bh * T + t) * dv, normalized, w);
+            }
+        }
+    state_free(&s);
+    rc = 0;
+out:
+    free(summ); free(pre); free(w);
+    return rc;
+}
+
+/* One decayed decode step on the P-form state S|P|p for n heads. */
+int hla2_oracle_decay_step_pform(double* state, const double* q, const double* k, const double* v, double* o,
+                                 int n, int d, int dv, int normalized, double gamma) {
+    if (!state || !q || !k || !v || !o || n < 0 || d <= 0 || dv <= 0) return -1;
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!u) return -1;
+    const size_t R = (size_t)d * d + (size_t)d * dv + (size_t)d;
+    const double g = gamma;
+    for (int i = 0; i < n; ++i) {
+        double* S = state + (size_t)i * R;
+        double* P = S + (size_t)d * d;
+        double* p = P + (size_t)d * dv;
+        const double* qi = q + (size_t)i * d;
+        const double* ki = k + (size_t)i * d;
+        const double* vi = v + (size_t)i * dv;
+        for (int a = 0; a < d; ++a)
+            for (int b = 0; b < d; ++b) S[(size_t)a * d + b] = g * S[(size_t)a * d + b] + ki[a] * ki[b];
+        for (int a = 0; a < d; ++a) {
+            double acc = 0.0;
+            for (int b = 0; b < d; ++b) acc += S[(size_t)a * d + b] * qi[b];
+            u[a] = acc;
+        }
+        for (int a = 0; a < d; ++a) {
+            for (int e = 0; e < dv; ++e) P[(size_t)a * dv + e] = g * g * P[(size_t)a * dv + e] + u[a] * vi[e];
+            p[a] = g * g * p[a] + u[a];
+        }
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += qi[a] * p[a];
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int a = 0; a < d; ++a) acc += qi[a] * P[(size_t)a * dv + e];
+            o[(size_t)i * dv + e] = normalized ? acc / den : acc;
+        }
+    }
+    free(u);
+    return 0;
+}
