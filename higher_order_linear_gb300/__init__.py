@@ -9,6 +9,8 @@ from .hla2 import (  # noqa: F401
     hla2_ahla_forward,
     hla2_ahla_step,
     hla2_chunk_summaries,
+    hla2_decay_forward,
+    hla2_decay_step,
     hla2_device_status,
     hla2_forward,
     hla2_forward_noalloc,

@@ -65,7 +65,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     using LY = ALayout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
-    enum { LQ, LK, LV, CA, CY, CO, CE, DA, DY, DO, DP, DE, NBAR };
+    enum { LQ, LK, LV, CA, CY, CQ, CO, CE, DA, DY, DO, DP, DE, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -253,14 +253,24 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     if (first)
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tY_, tAl.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                     mma_commit(bar(CY));
-                    if (!wait_bar(DY, ph)) break;  // sY = Y (and Y_lo on the first chunk); TMEM Y read
-                    tc_fence_after();
-                    if (has_next) issue_load(LV, &mV, tV, c + 1);
                     if (it > 0 && !wait_bar(DE, pph)) break;  // sE = E0 of this chunk; TMEM E read
                     tc_fence_after();
-                    // O = Q E0 + A Y
+                    // O = Q E0 (TMEM A is free once A was drained); this is Q's last read
                     if (!first)
                         for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tE.mnmaj(ks), iKM, ks > 0);
+                    mma_commit(bar(CQ));
+                    if (has_next) {
+                        if (!wait_bar(CQ, ph)) break;
+                        issue_load(LQ, &mQ, tQ, c + 1);
+                    }
+                    if (!wait_bar(DY, ph)) break;  // sY = Y (and Y_lo on the first chunk); TMEM Y read
+                    tc_fence_after();
+                    if (has_next) issue_load(LV, &mV, tV, c + 1);  // V was last read by A V (CY)
+                    // E += K^T Y first (K's last read), then O += A Y
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, 1);
+                    if (first)
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tYl.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CE));
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tA_, tA.kmaj(ks), tY.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                     if (first) {
@@ -268,14 +278,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tYl.mnmaj(ks), iKM, 1);
                     }
                     mma_commit(bar(CO));
-                    // E += K^T Y
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, 1);
-                    if (first)
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tYl.mnmaj(ks), iMM, 1);
-                    mma_commit(bar(CE));
                     if (has_next) {
-                        if (!wait_bar(CO, ph)) break;
-                        issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q E0
                         if (!wait_bar(CE, ph)) break;
                         issue_load(LK, &mK, tK, c + 1);  // K was last read by K^T Y
                     }
@@ -350,6 +353,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     // completed), 32 rows x 32 columns per bulk tensor store.
                     uint32_t r[64];
                     tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                    drained(DO);  // TMEM A is free once O sits in registers
                     const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                     const int t0 = (c_begin + it) * kL + quarter * 32;
 #pragma unroll
@@ -371,7 +375,6 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                         }
                     }
                 }
-                drained(DO);
                 if (state_rows && has_next) {
                     if (!wait_bar(CE, ph)) break;
                     tc_fence_after();

@@ -268,7 +268,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
 
     // segment summaries
     if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, status, s);
-    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, plan, s);
+    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
     // exclusive scan of the summaries
@@ -277,7 +277,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (prof) cudaEventRecord(pe.ev[2], s);
     // outputs
     if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, status, s);
-    else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 0, plan, s);
+    else e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 0, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment outputs");
     if (prof) {
         cudaEventRecord(pe.ev[3], s);
@@ -379,7 +379,7 @@ int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* sum
     p.nchunk = (T + L - 1) / L;
     p.nseg = p.nchunk;  // one chunk per segment
     if (p.nseg > 65535) return fail(HLA2_ERR_UNSUPPORTED, "%d chunks per head exceeds 65535", p.nseg);
-    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, p,
+    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, 1.0f, p,
                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "hla2_chunk_summaries");
     return HLA2_OK;
@@ -573,11 +573,11 @@ int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
     const RecOff ro = summary_offsets(d, dv);
     // segment sums S|C|m, their exclusive prefix sums (the combine has no
     // cross term here), then the walks from the prefixes
-    cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 1, plan, s);
+    cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 1, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked segment sums");
     e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, ro.X, state_out ? ws.tot : nullptr, ro.R, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked prefix sums");
-    e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 1, plan, s);
+    e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 1, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked segment outputs");
     if (state_out) {
         // final state S|C|m: the first d*d + d*dv + d floats of the totals
@@ -598,6 +598,60 @@ int hla2_unmasked_step(float* state, const float* q, const float* k, const float
         return fail(HLA2_ERR_UNSUPPORTED, "hla2_unmasked_step needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
     cudaError_t e = launch_step_unmasked(state, q, k, v, o, n, d, dv, normalized, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "hla2_unmasked_step");
+    return HLA2_OK;
+}
+
+
+int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, int B, int H, int T, int d, int dv,
+                       int normalized, float gamma, int dtype, void* workspace, size_t ws_bytes, float* state_out,
+                       hla2_stream_t stream) {
+    int rc = check_common(Q, K, V, B, H, T, d, dv, dtype);
+    if (rc) return rc;
+    if (!O) return fail(HLA2_ERR_INVALID, "null output pointer");
+    if (!(gamma >= 0.f && gamma <= 1.f)) return fail(HLA2_ERR_INVALID, "gamma must lie in [0, 1] (got %g)", (double)gamma);
+    if (!aligned16(O) || (state_out && !aligned16(state_out))) return fail(HLA2_ERR_INVALID, "output pointer not 16-byte aligned");
+    const size_t need = hla2_forward_workspace(B, H, T, d, dv, dtype);
+    if (!workspace || ws_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : (size_t)0, need);
+    if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const SegPlan plan = forward_plan(BH, T);
+    const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
+    // P-form segment summaries with decay, the decayed sequential scan, walks
+    cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, gamma,
+                                plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decay segment summaries");
+    e = launch_decay_scan(ws.summ, ws.prefix, state_out ? ws.tot : nullptr, BH, T, d, dv, gamma, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decay scan");
+    e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 0, gamma, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decay segment outputs");
+    if (state_out) {
+        // final compact state S|P|p from the totals S|C|m|P|p
+        const RecOff so = summary_offsets(d, dv);
+        const long long R = (long long)so.R;
+        const long long Rp = (long long)d * d + (long long)d * dv + d;
+        e = launch_copy_strided(ws.tot + so.S, R, state_out, Rp, (size_t)d * d, BH, s);
+        if (e == cudaSuccess)
+            e = launch_copy_strided(ws.tot + so.X, R, state_out + (size_t)d * d, Rp, (size_t)d * dv + d, BH, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay state_out copy");
+    }
+    return HLA2_OK;
+}
+
+int hla2_decay_step(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,
+                    int normalized, float gamma, hla2_stream_t stream) {
+    if (!state || !q || !k || !v || !o) return fail(HLA2_ERR_INVALID, "null pointer");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(HLA2_ERR_INVALID, "pointer not 16-byte aligned");
+    if (n <= 0 || d <= 0 || dv <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (n=%d d=%d dv=%d)", n, d, dv);
+    if (!(gamma >= 0.f && gamma <= 1.f)) return fail(HLA2_ERR_INVALID, "gamma must lie in [0, 1] (got %g)", (double)gamma);
+    auto pow2_4_128 = [](int x) { return x >= 4 && x <= 128 && (x & (x - 1)) == 0; };
+    if (!pow2_4_128(d) || !pow2_4_128(dv))
+        return fail(HLA2_ERR_UNSUPPORTED, "hla2_decay_step needs d, dv powers of two in [4, 128] (d=%d dv=%d)", d, dv);
+    cudaError_t e = launch_step_pform_decay(state, q, k, v, o, n, d, dv, normalized, gamma,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "hla2_decay_step");
     return HLA2_OK;
 }
 

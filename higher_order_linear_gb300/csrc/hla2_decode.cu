@@ -226,6 +226,10 @@ cudaError_t launch_step(float* state, const float* q, const float* k, const floa
 // (P_t - P_{t-1} = S_t q_t v_t^T).  Two passes: S (row reductions give u),
 // then P (column reductions give q^T P_{t-1} while P is updated).
 //
+// With a per-token decay gamma of every prefix moment (the decayed masked
+// operator), S_t = gamma S + k k^T, P_t = gamma^2 P + u v^T, p_t = gamma^2 p + u
+// and o = gamma^2 q^T P_{t-1} + (q . u) v; gamma = 1 gives the lines above.
+//
 // The unmasked operator o_t = q_t^T S_t C_t (no G correction) has the same
 // two-pass shape on the state S | C | m, with the roles of q and u swapped in
 // the second pass:
@@ -238,7 +242,8 @@ namespace {
 template <bool UNMASKED>
 __global__ void __launch_bounds__(kThreads)
 step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const float* __restrict__ k,
-                  const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized) {
+                  const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized, float gamma) {
+    const float gm = gamma, gm2 = gamma * gamma;  // per-token decay (1: none)
     __shared__ __align__(16) float sq[128], sk[128], sv[128], su[128], sy[128];
     __shared__ __align__(16) float part[kThreads][4];
     __shared__ float sdots[2];
@@ -279,10 +284,10 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
                     const int b = (f - a * g) * 4;
                     const float ka = sk[a];
                     float4 x = r[i];
-                    x.x = fmaf(ka, sk[b + 0], x.x);
-                    x.y = fmaf(ka, sk[b + 1], x.y);
-                    x.z = fmaf(ka, sk[b + 2], x.z);
-                    x.w = fmaf(ka, sk[b + 3], x.w);
+                    x.x = fmaf(ka, sk[b + 0], gm * x.x);
+                    x.y = fmaf(ka, sk[b + 1], gm * x.y);
+                    x.z = fmaf(ka, sk[b + 2], gm * x.z);
+                    x.w = fmaf(ka, sk[b + 3], gm * x.w);
                     st_stream(S + 4 * (size_t)f, x);
                     part_u = x.x * sq[b] + x.y * sq[b + 1] + x.z * sq[b + 2] + x.w * sq[b + 3];
                 }
@@ -317,8 +322,8 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
                     float4 x = r[i];
                     py[0] = fmaf(qa, x.x, py[0]); py[1] = fmaf(qa, x.y, py[1]);
                     py[2] = fmaf(qa, x.z, py[2]); py[3] = fmaf(qa, x.w, py[3]);
-                    x.x = fmaf(ua, v4.x, x.x); x.y = fmaf(ua, v4.y, x.y);
-                    x.z = fmaf(ua, v4.z, x.z); x.w = fmaf(ua, v4.w, x.w);
+                    x.x = fmaf(ua, v4.x, gm2 * x.x); x.y = fmaf(ua, v4.y, gm2 * x.y);
+                    x.z = fmaf(ua, v4.z, gm2 * x.z); x.w = fmaf(ua, v4.w, gm2 * x.w);
                     st_stream(P + (size_t)a * dv + 4 * c4, x);
                 }
             }
@@ -330,7 +335,7 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
     if (tid < 32) {
         float qu = 0.f, qp = 0.f;
         for (int a = tid; a < d; a += 32) {
-            const float pn = p[a] + (UNMASKED ? sq[a] : su[a]);  // p + u  |  m + q
+            const float pn = fmaf(gm2, p[a], UNMASKED ? sq[a] : su[a]);  // gamma^2 p + u  |  m + q
             qu += sq[a] * su[a];
             qp += (UNMASKED ? su[a] : sq[a]) * pn;               // q . p_t  |  u . m_t
             p[a] = pn;
@@ -343,7 +348,7 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
         const int cc = tid >> 2, j = tid & 3;
         float y = 0.f;
         for (int r = 0; r < rows_per; ++r) y += part[r * gc + cc][j];
-        float out = y + sdots[0] * sv[tid];
+        float out = fmaf(gm2, y, sdots[0] * sv[tid]);
         if (normalized) out = out / sdots[1];
         o[(size_t)head * dv + tid] = out;
     }
@@ -354,7 +359,7 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
 cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o, int n, int d,
                               int dv, int normalized, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    step_pform_kernel<false><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
+    step_pform_kernel<false><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized, 1.0f);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -362,7 +367,15 @@ cudaError_t launch_step_pform(float* state, const float* q, const float* k, cons
 cudaError_t launch_step_unmasked(float* state, const float* q, const float* k, const float* v, float* o, int n,
                                  int d, int dv, int normalized, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    step_pform_kernel<true><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized);
+    step_pform_kernel<true><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized, 1.0f);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_step_pform_decay(float* state, const float* q, const float* k, const float* v, float* o, int n,
+                                    int d, int dv, int normalized, float gamma, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    step_pform_kernel<false><<<n, kThreads, 0, s>>>(state, q, k, v, o, d, dv, normalized, gamma);
     note_launches(1);
     return cudaGetLastError();
 }

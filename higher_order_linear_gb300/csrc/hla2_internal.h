@@ -71,6 +71,9 @@ cudaError_t launch_step(float* state, const float* q, const float* k, const floa
 // Same step on the compact P-form state S | P | p.
 cudaError_t launch_step_pform(float* state, const float* q, const float* k, const float* v, float* o,
                               int n, int d, int dv, int normalized, cudaStream_t s);
+// The same with per-token decay gamma of every prefix moment.
+cudaError_t launch_step_pform_decay(float* state, const float* q, const float* k, const float* v, float* o,
+                                    int n, int d, int dv, int normalized, float gamma, cudaStream_t s);
 
 // Unmasked operator o = q^T S C on the state S | C | m.
 cudaError_t launch_step_unmasked(float* state, const float* q, const float* k, const float* v, float* o,
@@ -81,11 +84,22 @@ cudaError_t launch_step_unmasked(float* state, const float* q, const float* k, c
 // mode 1: outputs, starting from the prefix record S|.|.|P|p of the segment.
 // mode 2: G-form summary S|C|m|G|h from zero state (chunk summaries).
 // unmasked (modes 0, 1): o_t = q_t^T S_t C_t; mode 0 keeps S|C|m only, mode 1
-// starts from the prefix S|C|m.
+// starts from the prefix S|C|m.  gamma (modes 0, 1, P-form): per-token decay
+// of every prefix moment (1 = none).
 cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, int dtype,
                         float* O, const float* prefix, float* summ,
-                        int BH, int T, int d, int dv, int normalized, int unmasked, SegPlan plan,
+                        int BH, int T, int d, int dv, int normalized, int unmasked, float gamma, SegPlan plan,
                         cudaStream_t s);
+
+// Decayed exclusive scan of P-form segment records S|C|m|P|p, sequential over
+// the nseg records of each head, fp32 on CUDA cores (gamma = 1: the masked
+// combine).  Segment r spans n_r tokens (from the plan and T); with
+// f = gamma^{n_r}:  S <- f S + S_r, C, m likewise,
+// P <- f^2 P + P_r + f S C_r, p <- f^2 p + p_r + f S m_r.
+// Writes S, P, p of every prefix record (and C, m when tot != nullptr) and,
+// if tot != nullptr, the inclusive totals S|C|m|P|p per head.
+cudaError_t launch_decay_scan(const float* summ, float* prefix, float* tot, int BH, int T, int d, int dv,
+                              float gamma, SegPlan plan, cudaStream_t s);
 
 // ---- scans (hla2_scan.cu) ----
 // Exclusive running sum along the record axis for the element range

@@ -146,6 +146,96 @@ cross_kernel(CrossArgs a) {
     }
 }
 
+// Decayed exclusive scan of P-form records, sequential over the records of
+// one head.  A CTA owns kRows consecutive state rows (of S, C, P and of the
+// vectors m, p) of one head and carries their running prefix in shared
+// memory; the cross terms S C_r and S m_r need the CTA's S rows against all
+// of C_r, read from global memory (coalesced along the value axis).
+constexpr int kRows = 16;
+
+__global__ void __launch_bounds__(256)
+decay_scan_kernel(const float* __restrict__ summ, float* __restrict__ prefix, float* __restrict__ tot,
+                  int T, int d, int dv, float gamma, SegPlan plan) {
+    extern __shared__ float dsm[];
+    const int head = blockIdx.y;
+    const int r0 = blockIdx.x * kRows;
+    const int nr = min(kRows, d - r0);
+    const RecOff ro = summary_offsets(d, dv);
+    float* sS = dsm;                      // kRows x d   running S rows
+    float* sC = sS + kRows * d;           // kRows x dv  running C rows
+    float* sP = sC + kRows * dv;          // kRows x dv  running P rows
+    float* sm = sP + kRows * dv;          // kRows       running m
+    float* sp = sm + kRows;               // kRows       running p
+    float* sX = sp + kRows;               // kRows x (dv + 1)  cross terms S C_r | S m_r
+    const int tid = threadIdx.x;
+    for (int i = tid; i < kRows * d; i += 256) sS[i] = 0.f;
+    for (int i = tid; i < kRows * dv; i += 256) { sC[i] = 0.f; sP[i] = 0.f; }
+    if (tid < kRows) { sm[tid] = 0.f; sp[tid] = 0.f; }
+    __syncthreads();
+    const int w = dv + 1;
+    for (int r = 0; r < plan.nseg; ++r) {
+        const long long c0 = (long long)r * plan.nchunk / plan.nseg;
+        const long long c1 = (long long)(r + 1) * plan.nchunk / plan.nseg;
+        const long long t1 = min((long long)T, c1 * plan.granule);
+        const int nb = (int)(t1 - c0 * plan.granule);  // tokens of segment r
+        // f = gamma^nb by repeated squaring in double precision (fp32 products
+        // over thousands of tokens would drift)
+        double fd = 1.0, base = (double)gamma;
+        for (int e = nb; e > 0; e >>= 1) {
+            if (e & 1) fd *= base;
+            base *= base;
+        }
+        const float f = (float)fd;
+        const float* rec = summ + ((size_t)head * plan.nseg + r) * ro.R;
+        float* pre = prefix + ((size_t)head * plan.nseg + r) * ro.R;
+        // the exclusive prefix of record r is the running state
+        for (int i = tid; i < nr * d; i += 256) pre[ro.S + (size_t)r0 * d + i] = sS[i];
+        for (int i = tid; i < nr * dv; i += 256) pre[ro.X + (size_t)r0 * dv + i] = sP[i];
+        if (tid < nr) pre[ro.x + r0 + tid] = sp[tid];
+        if (tot) {
+            for (int i = tid; i < nr * dv; i += 256) pre[ro.C + (size_t)r0 * dv + i] = sC[i];
+            if (tid < nr) pre[ro.m + r0 + tid] = sm[tid];
+        }
+        // cross terms with the running S (before it absorbs record r)
+        for (int i = tid; i < nr * w; i += 256) {
+            const int a = i / w, e = i % w;
+            const float* srow = sS + a * d;
+            float acc = 0.f;
+            if (e < dv)
+                for (int b = 0; b < d; ++b) acc = fmaf(srow[b], rec[ro.C + (size_t)b * dv + e], acc);
+            else
+                for (int b = 0; b < d; ++b) acc = fmaf(srow[b], rec[ro.m + b], acc);
+            sX[i] = acc;
+        }
+        __syncthreads();
+        const float f2 = f * f;
+        for (int i = tid; i < nr * dv; i += 256) {
+            const int a = i / dv, e = i % dv;
+            const size_t gi = (size_t)(r0 + a) * dv + e;
+            sP[i] = fmaf(f2, sP[i], fmaf(f, sX[a * w + e], rec[ro.X + gi]));
+            sC[i] = fmaf(f, sC[i], rec[ro.C + gi]);
+        }
+        if (tid < nr) {
+            sp[tid] = fmaf(f2, sp[tid], fmaf(f, sX[tid * w + dv], rec[ro.x + r0 + tid]));
+            sm[tid] = fmaf(f, sm[tid], rec[ro.m + r0 + tid]);
+        }
+        for (int i = tid; i < nr * d; i += 256) sS[i] = fmaf(f, sS[i], rec[ro.S + (size_t)r0 * d + i]);
+        __syncthreads();
+    }
+    if (tot) {
+        float* out = tot + (size_t)head * ro.R;
+        for (int i = tid; i < nr * d; i += 256) out[ro.S + (size_t)r0 * d + i] = sS[i];
+        for (int i = tid; i < nr * dv; i += 256) {
+            out[ro.C + (size_t)r0 * dv + i] = sC[i];
+            out[ro.X + (size_t)r0 * dv + i] = sP[i];
+        }
+        if (tid < nr) {
+            out[ro.m + r0 + tid] = sm[tid];
+            out[ro.x + r0 + tid] = sp[tid];
+        }
+    }
+}
+
 __global__ void copy_strided_kernel(const float* src, long long s_src, float* dst, long long s_dst, size_t len) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int b = blockIdx.y;
@@ -175,6 +265,17 @@ cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s) {
     const int ncol = a.dv + (a.bx ? 1 : 0);
     dim3 grid((ncol + kTile - 1) / kTile, (a.d + kTile - 1) / kTile, a.nb);
     cross_kernel<<<grid, 256, 0, s>>>(a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decay_scan(const float* summ, float* prefix, float* tot, int BH, int T, int d, int dv,
+                              float gamma, SegPlan plan, cudaStream_t s) {
+    if (BH == 0 || plan.nseg == 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * ((size_t)kRows * d + 2 * (size_t)kRows * dv + 2 * kRows +
+                                         (size_t)kRows * (dv + 1));
+    dim3 grid((d + kRows - 1) / kRows, BH);
+    decay_scan_kernel<<<grid, 256, smem, s>>>(summ, prefix, tot, T, d, dv, gamma, plan);
     note_launches(1);
     return cudaGetLastError();
 }

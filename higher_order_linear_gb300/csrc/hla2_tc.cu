@@ -343,9 +343,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (NORM)
                         for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tXl.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                     mma_commit(bar(CW));
+                    if (has_next) {
+                        if (!wait_bar(CX2, ph)) break;
+                        issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
+                    }
                     if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
                     tc_fence_after();
-                    if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
                     if (it > 0) {
                         if (!wait_bar(DP, pph)) break;  // sP = P0 of this chunk; TMEM P read
                         tc_fence_after();
@@ -360,6 +363,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     mma_commit(bar(CQ));
                     if (!wait_bar(LV, ph)) break;
+                    if (has_next) {
+                        // Q was last read by Q P0: the next chunk's Q starts moving now
+                        // (its first product waits on this load)
+                        if (!wait_bar(CQ, ph)) break;
+                        issue_load(LQ, &mQ, tQ, c + 1);
+                    }
                     tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                     if (NORM || c == 0)  // W_lo V: every chunk when normalised, else the head's first
@@ -384,8 +393,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     mma_commit(bar(CP));
                     if (has_next) {
-                        if (!wait_bar(CQ, ph)) break;
-                        issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q P0
                         if (!wait_bar(CP, ph)) break;
                         issue_load(LV, &mV, tV, c + 1);  // V was last read by W V and X^T V
                     }
@@ -427,9 +434,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         for (int ks = 0; ks < kL / 16; ++ks)
                             mma_bf16(tDen_, tQc.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CQ));
+                    if (has_next) {
+                        if (!wait_bar(CX2, ph)) break;
+                        issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
+                    }
                     if (!wait_bar(DX, ph)) break;  // sX = X
                     tc_fence_after();
-                    if (has_next) issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
                     // P += X^T V
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
@@ -526,6 +536,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 #pragma unroll
                         for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) / den);
                     }
+                    // TMEM A is free once O sits in registers: the next chunk's
+                    // A = Q K^T need not wait for the stores below
+                    drained(DO);
                     const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                     const int t0 = (c_begin + it) * kL + quarter * 32;  // first token of this warp's rows
 #pragma unroll
@@ -547,7 +560,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         }
                     }
                 }
-                drained(DO);
                 if (state_rows && has_next) {
                     if (!wait_bar(CP, ph)) break;
                     tc_fence_after();

@@ -17,6 +17,10 @@
 //           and emit o_t = q_t^T P_t (divided by q_t^T p_t when normalised).
 //   mode 2  G-form chunk summary from a zero state (S|C|m|G|h), by the
 //           recurrence G += k (C_{t-1}^T k), h += k (k . m_{t-1}).
+// `gamma` (modes 0 and 1, P-form) decays every prefix moment per token:
+// S = gamma S + k k^T, C = gamma C + q v^T, m = gamma m + q, and in P-form
+// P = gamma^2 P + u v^T, p = gamma^2 p + u (gamma = 1: the masked operator,
+// bit for bit, since the products by 1 are exact).
 // With `unmasked` set, modes 0 and 1 compute the unmasked operator
 // o_t = q_t^T S_t C_t (section 1's naive product, no G correction): mode 0
 // keeps only the plain sums S, C, m, and mode 1 starts from the prefix
@@ -58,7 +62,7 @@ template <typename Tin, int MODE>
 __global__ void __launch_bounds__(kWalkThreads)
 walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __restrict__ V,
             float* __restrict__ O, const float* __restrict__ prefix, float* __restrict__ summ,
-            int T, int d, int dv, int normalized, int unmasked, SegPlan plan) {
+            int T, int d, int dv, int normalized, int unmasked, float gamma, SegPlan plan) {
     extern __shared__ float4 smem4[];
     float* sm = reinterpret_cast<float*>(smem4);
     const int mx = d > dv ? d : dv;
@@ -91,6 +95,7 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
     const int es = tid % d, rgs = tid / d, nrgs = kWalkThreads / d;
     const bool act_v = rgv < nrgv;
     const bool act_s = rgs < nrgs;
+    const float g = gamma, g2 = gamma * gamma;
 
     // ---- initial state ----
     if (MODE == 1) {
@@ -157,9 +162,9 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
                 }
                 __syncthreads();
             } else {
-                // S_t = S_{t-1} + k k^T
+                // S_t = gamma S_{t-1} + k k^T
                 if (act_s)
-                    for (int a = rgs; a < d; a += nrgs) s.S[a * d + es] = fmaf(k[a], k[es], s.S[a * d + es]);
+                    for (int a = rgs; a < d; a += nrgs) s.S[a * d + es] = fmaf(k[a], k[es], g * s.S[a * d + es]);
                 __syncthreads();
                 // u = S_t q (column reduction; S symmetric)
                 if (act_s) {
@@ -175,9 +180,9 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
                     if (unmasked) {
                         if (MODE == 1) s.x[tid] += q[tid];  // m_t = m_{t-1} + q
                     } else {
-                        s.x[tid] += u;                       // p_t = p_{t-1} + u
+                        s.x[tid] = fmaf(g2, s.x[tid], u);    // p_t = gamma^2 p_{t-1} + u
                     }
-                    if (MODE == 0) s.m[tid] += q[tid];
+                    if (MODE == 0) s.m[tid] = fmaf(g, s.m[tid], q[tid]);
                 }
                 __syncthreads();
                 // P_t = P_{t-1} + u v^T ; outputs o_e = sum_a q_a P_t[a][e]
@@ -198,9 +203,9 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
                     } else {
                         for (int a = rgv; a < d; a += nrgv) {
                             const int i = a * dv + ev;
-                            const float pn = fmaf(s.u[a], v[ev], s.X[i]);
+                            const float pn = fmaf(s.u[a], v[ev], g2 * s.X[i]);
                             s.X[i] = pn;
-                            if (MODE == 0) s.C[i] = fmaf(q[a], v[ev], s.C[i]);
+                            if (MODE == 0) s.C[i] = fmaf(q[a], v[ev], g * s.C[i]);
                             acc = fmaf(q[a], pn, acc);
                         }
                     }
@@ -238,8 +243,8 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
 
 template <typename Tin, int MODE>
 cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O, const float* prefix,
-                          float* summ, int BH, int T, int d, int dv, int normalized, int unmasked, SegPlan plan,
-                          cudaStream_t s) {
+                          float* summ, int BH, int T, int d, int dv, int normalized, int unmasked, float gamma,
+                          SegPlan plan, cudaStream_t s) {
     const size_t bytes = walk_smem_floats(MODE, d, dv) * sizeof(float);
     auto kern = walk_kernel<Tin, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -247,7 +252,7 @@ cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O,
     dim3 grid(plan.nseg, BH);
     kern<<<grid, kWalkThreads, bytes, s>>>(static_cast<const Tin*>(Q), static_cast<const Tin*>(K),
                                            static_cast<const Tin*>(V), O, prefix, summ, T, d, dv, normalized,
-                                           unmasked, plan);
+                                           unmasked, gamma, plan);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -256,19 +261,19 @@ cudaError_t launch_walk_t(const void* Q, const void* K, const void* V, float* O,
 
 cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, int dtype, float* O,
                         const float* prefix, float* summ, int BH, int T, int d, int dv, int normalized,
-                        int unmasked, SegPlan plan, cudaStream_t s) {
+                        int unmasked, float gamma, SegPlan plan, cudaStream_t s) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (dtype == 1) {
         switch (mode) {
-            case 0: return launch_walk_t<__nv_bfloat16, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
-            case 1: return launch_walk_t<__nv_bfloat16, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
-            default: return launch_walk_t<__nv_bfloat16, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+            case 0: return launch_walk_t<__nv_bfloat16, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
+            case 1: return launch_walk_t<__nv_bfloat16, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
+            default: return launch_walk_t<__nv_bfloat16, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
         }
     }
     switch (mode) {
-        case 0: return launch_walk_t<float, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
-        case 1: return launch_walk_t<float, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
-        default: return launch_walk_t<float, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, plan, s);
+        case 0: return launch_walk_t<float, 0>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
+        case 1: return launch_walk_t<float, 1>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
+        default: return launch_walk_t<float, 2>(Q, K, V, O, prefix, summ, BH, T, d, dv, normalized, unmasked, gamma, plan, s);
     }
 }
 

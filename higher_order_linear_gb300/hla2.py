@@ -82,6 +82,10 @@ def lib() -> ctypes.CDLL:
             L.hla2_unmasked_forward.restype = i
             L.hla2_unmasked_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
             L.hla2_unmasked_step.restype = i
+            L.hla2_decay_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, vp, sz, vp, vp]
+            L.hla2_decay_forward.restype = i
+            L.hla2_decay_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp]
+            L.hla2_decay_step.restype = i
             _lib = L
         return _lib
 
@@ -386,4 +390,55 @@ def hla2_unmasked_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v:
                                   _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
                                   _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized)), _stream(stream))
     _check(rc, "hla2_unmasked_step")
+    return o
+
+
+# ----------------------------------------------------------------- decay ----
+def hla2_decay_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, gamma: float,
+                       O: torch.Tensor | None = None, normalized: bool = False,
+                       workspace: torch.Tensor | None = None, state_out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Decayed masked forward, o_t = sum_{i<=j<=t} gamma^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j.
+    Shapes and dtypes as for hla2_forward; ``state_out`` [B*H, d*d + d*dv + d]
+    fp32 receives the final compact state S|P|p if given."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    code = _dtype_code(Q)
+    if O is None:
+        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
+    elif O.shape != (B, H, T, dv):
+        raise ValueError("O has the wrong shape")
+    need = hla2_forward_workspace(B, H, T, d, dv, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
+    sptr = None
+    if state_out is not None:
+        if state_out.numel() != B * H * pform_record_len(d, dv):
+            raise ValueError("state_out must hold B*H compact states")
+        sptr = _dev(state_out, "state_out", torch.float32)
+    rc = lib().hla2_decay_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                                  B, H, T, d, dv, int(bool(normalized)), float(gamma), code,
+                                  _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                  sptr, _stream(stream))
+    _check(rc, "hla2_decay_forward")
+    return O
+
+
+def hla2_decay_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, gamma: float,
+                    o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """One decayed decode step on the compact state [n, d*d + d*dv + d] (S|P|p, in place)."""
+    n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * pform_record_len(d, dv):
+        raise ValueError("shape mismatch for hla2_decay_step")
+    if o is None:
+        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
+    rc = lib().hla2_decay_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
+                               _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
+                               n, d, dv, int(bool(normalized)), float(gamma), _stream(stream))
+    _check(rc, "hla2_decay_step")
     return o

@@ -249,6 +249,38 @@ HLA2_API int hla2_unmasked_step(float* state, const float* q, const float* k, co
                                 int n, int d, int dv, int normalized, hla2_stream_t stream);
 
 /*
+ * Exponentially decayed masked operator.  [HLA §4] names decayed operators
+ * among those the scan covers but prints no form; the reading this library
+ * computes decays every prefix moment by one scalar gamma per token:
+ *   S_t = gamma S + k k^T,  C_t = gamma C + q v^T,  m_t = gamma m + q,
+ *   G_t = gamma^2 G + gamma k k^T C_{t-1},  h_t = gamma^2 h + gamma k k^T m_{t-1},
+ *   o_t = q_t^T (S_t C_t - G_t) = sum_{i<=j<=t} gamma^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j,
+ * ratio-normalised by q_t^T (S_t m_t - h_t).  gamma = 1 is hla2_forward's
+ * operator.  Segments join with the decayed combine (B spanning n_B tokens,
+ * f = gamma^{n_B}): S = f S_A + S_B, ..., G = f^2 G_A + G_B + f S_B C_A.
+ * Runs on the CUDA-core segment walks (fp32) with a sequential fp32 scan.
+ *   gamma     in [0, 1] (else HLA2_ERR_INVALID).
+ *   state_out optional: [B*H][d*d + d*dv + d] fp32, per head the compact
+ *             state S | P = S C - G | p = S m - h, the hla2_decay_step layout.
+ * Other arguments, workspace (hla2_forward_workspace) and errors as for
+ * hla2_forward.
+ */
+HLA2_API int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O,
+                                int B, int H, int T, int d, int dv, int normalized, float gamma, int dtype,
+                                void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * One decayed decode step for n heads on the compact state
+ * [n][d*d + d*dv + d] fp32 (S | P | p, updated in place):
+ *   S = gamma S + k k^T, u = S q, P = gamma^2 P + u v^T, p = gamma^2 p + u,
+ *   o = q^T P (divided by q . p when normalized).
+ * gamma = 1 is hla2_step_pform.  Same size rules and errors as hla2_step,
+ * plus HLA2_ERR_INVALID for gamma outside [0, 1].
+ */
+HLA2_API int hla2_decay_step(float* state, const float* q, const float* k, const float* v, float* o,
+                             int n, int d, int dv, int normalized, float gamma, hla2_stream_t stream);
+
+/*
  * Copies the calling host thread's last error reason (NUL-terminated,
  * truncated to n bytes) into buf.  Returns the length of the full message.
  */
