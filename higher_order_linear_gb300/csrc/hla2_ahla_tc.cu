@@ -182,6 +182,17 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         if (D == 128) put_row32_split2(hi, lo, row, cD + 32, r + 32, false);
     };
 
+    const int nchunks = c_end - c_begin;
+    // The first chunk's tiles start moving now, while the drain warps load the
+    // segment prefix below (the barriers were initialised before the first
+    // __syncthreads, so the issuer may use them).
+    if (issuer && lane == 0 && nchunks > 0) {
+        issue_load(LQ, &mQ, tQ, c_begin);
+        issue_load(LK, &mK, tK, c_begin);
+        issue_load(LV, &mV, tV, c_begin);
+        if (nchunks > 1) prefetch(c_begin + 1);
+    }
+
     // ---- initial state (output walk): P0, E0 fp32 into TMEM, bf16 into smem ----
     if (MODE == 1 && state_rows) {
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
@@ -189,16 +200,23 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         const float* src[2] = {pre + (size_t)D * D, pre + 2 * (size_t)D * D + D};  // P (after M), E (after m)
         const uint32_t dst[2] = {tP_, tE_};
         const Tile* til[2] = {&tP, &tE};
+        // all loads of this thread's row pieces first: one memory latency, not four
+        float4 x4[2][D / 8];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) x4[m][j] = __ldg(reinterpret_cast<const float4*>(src[m] + (size_t)row * D + cD) + j);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-#pragma unroll 1
-            for (int cb = cD; cb < cD + D / 2; cb += 32) {
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                const int cb = cD + 32 * h;
                 uint32_t r[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(src[m] + (size_t)row * D + cb + j);
-                    r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
-                    r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 x = x4[m][8 * h + j];
+                    r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
+                    r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
                 }
                 tmem_st32(dst[m] + lane_off + cb, r);
                 put_row32(*til[m], row, cb, r, false);
@@ -214,15 +232,10 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
-    const int nchunks = c_end - c_begin;
 
     if (issuer) {
         // ============================ issuer ============================
         if (lane == 0 && nchunks > 0) {
-            issue_load(LQ, &mQ, tQ, c_begin);
-            issue_load(LK, &mK, tK, c_begin);
-            issue_load(LV, &mV, tV, c_begin);
-            if (nchunks > 1) prefetch(c_begin + 1);
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
@@ -404,20 +417,24 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         // ---- segment summary out (summary walk): M | P | . | E | . records, fp32 ----
         if (MODE == 0 && state_rows && nchunks > 0 && wait_bar(CE, (nchunks - 1) & 1)) {
             tc_fence_after();
-            const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
-            float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
-            float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // M, P, E
+            // M, P, E leave through 32 x 32 boxes and bulk tensor stores (mO maps
+            // the records as (3D + 2) rows of D floats: M at row 0, P at row D,
+            // E at row 2D + 1).  The last MMAs completed and no load is in
+            // flight, so each warp stages its boxes in its own part of the tiles.
             const uint32_t src[3] = {tM_, tP_, tE_};
+            const int row0[3] = {0, D, 2 * D + 1};
+            const uint32_t scratch = dsm + (uint32_t)warp * (3u * (D / 64) * 4096u);
+            const int rec = head * p.nseg + seg;
 #pragma unroll
             for (int m = 0; m < 3; ++m) {
                 uint32_t r[64];
                 tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
 #pragma unroll
-                for (int j = 0; j < D / 2; j += 4)
-                    *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
+                for (int g = 0; g < D / 64; ++g)
+                    box32_store(&mO, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
+                                row0[m] + quarter * 32, rec);
             }
+            if (lane == 0) tma_store_wait_all();
         }
     }
     tc_fence_before();
@@ -438,7 +455,9 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     if (MODE == 1) {
         if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
     } else {
-        mo = mq;  // unused
+        // the summary records as (3D + 2) rows of D floats each, 32 x 32 boxes
+        if (!make_map(&mo, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+            return cudaErrorInvalidValue;
     }
     AParams prm{T, plan.nseg, plan.nchunk, summ, prefix, status};
     const size_t smem = ALayout<D, MODE>::kBytes + 1024;

@@ -223,29 +223,57 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     // pending read is overwritten.  K-step ks reads 8 packed columns.
     auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * (D / 2) + 8 * (ks & 3)); };
 
+    const int nchunks = c_end - c_begin;
+    // The first chunk's tiles start moving now, while the drain warps load the
+    // segment prefix below (the barriers were initialised before the first
+    // __syncthreads, so the issuer may use them).
+    if (issuer && lane == 0 && nchunks > 0) {
+        issue_load(LQ, &mQ, tQ, c_begin);
+        issue_load(LK, &mK, tK, c_begin);
+        issue_load(LV, &mV, tV, c_begin);
+        if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
+        if (nchunks > 1) {
+#pragma unroll
+            for (int k = 0; k < D / 64; ++k) {
+                tma_prefetch_l2_3d(&mQ, k * 64, (c_begin + 1) * kL, head);
+                tma_prefetch_l2_3d(&mK, k * 64, (c_begin + 1) * kL, head);
+                tma_prefetch_l2_3d(&mV, k * 64, (c_begin + 1) * kL, head);
+            }
+        }
+    }
+
     // ---- initial state (mode 1): S0, P0 fp32 into TMEM, bf16 into smem ----
     if (MODE == 1 && state_rows) {
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
         const float* S0 = pre;                          // S at offset 0
         const float* P0 = pre + 2 * (size_t)D * D + D;  // P after S, C, m
-#pragma unroll 1
-        for (int cb = cD; cb < cD + D / 2; cb += 32) {
+        // every load of this thread's row pieces is issued before the first use,
+        // so the CTA pays one memory latency here instead of one per piece
+        float4 xs[D / 8], xp[D / 8];
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+            xs[j] = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)row * D + cD) + j);
+            xp[j] = __ldg(reinterpret_cast<const float4*>(P0 + (size_t)row * D + cD) + j);
+        }
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+            const int cb = cD + 32 * h;
             uint32_t r[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(S0 + (size_t)row * D + cb + j);
-                r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
-                r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
+            for (int j = 0; j < 8; ++j) {
+                const float4 x = xs[8 * h + j];
+                r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
+                r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
             }
             tmem_st32(tS_ + lane_off + cb, r);
             if (NORM) put_row32_split2(tS, tSl, row, cb, r, false);
             else put_row32(tS, row, cb, r, false);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(P0 + (size_t)row * D + cb + j);
-                r[j] = __float_as_uint(x.x); r[j + 1] = __float_as_uint(x.y);
-                r[j + 2] = __float_as_uint(x.z); r[j + 3] = __float_as_uint(x.w);
+            for (int j = 0; j < 8; ++j) {
+                const float4 x = xp[8 * h + j];
+                r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
+                r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
             }
             tmem_st32(tP_ + lane_off + cb, r);
             if (NORM) put_row32_split2(tP, tPl, row, cb, r, false);
@@ -270,23 +298,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);       // both MN-major
     constexpr uint32_t iKK16 = idesc_bf16(128, 16, false, false);  // N = 16 (ones / p0), both K-major
     constexpr uint32_t iMK16 = idesc_bf16(128, 16, true, false);   // N = 16, A MN-major
-    const int nchunks = c_end - c_begin;
 
     if (issuer) {
         // ============================ issuer ============================
         if (lane == 0 && nchunks > 0) {
-            issue_load(LQ, &mQ, tQ, c_begin);
-            issue_load(LK, &mK, tK, c_begin);
-            issue_load(LV, &mV, tV, c_begin);
-            if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
-            if (nchunks > 1) {
-#pragma unroll
-                for (int k = 0; k < D / 64; ++k) {
-                    tma_prefetch_l2_3d(&mQ, k * 64, (c_begin + 1) * kL, head);
-                    tma_prefetch_l2_3d(&mK, k * 64, (c_begin + 1) * kL, head);
-                    tma_prefetch_l2_3d(&mV, k * 64, (c_begin + 1) * kL, head);
-                }
-            }
             int it = 0;
             for (; it < nchunks; ++it) {
                 const int c = c_begin + it;
@@ -599,18 +614,25 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             tc_fence_after();
             const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
             float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
-            float* dst[3] = {out, out + (size_t)D * D, out + 2 * (size_t)D * D + D};  // S, C, P
+            // S, C, P leave through 32 x 32 boxes and bulk tensor stores (mO maps
+            // the records as (3D + 2) rows of D floats: S at row 0, C at row D,
+            // P at row 2D + 1).  Every tile is dead now: the last MMAs completed
+            // and no load is in flight, so each warp stages its boxes in its own
+            // 3 * D / 16 KB of the tile area.
             const uint32_t src[3] = {tS_, tC_, tP_};
+            const int row0[3] = {0, D, 2 * D + 1};
+            const uint32_t scratch = dsm + (uint32_t)warp * (3u * (D / 64) * 4096u);
+            const int rec = head * p.nseg + seg;
 #pragma unroll
             for (int m = 0; m < 3; ++m) {
                 uint32_t r[64];
                 tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
 #pragma unroll
-                for (int j = 0; j < D / 2; j += 4)
-                    *reinterpret_cast<float4*>(dst[m] + (size_t)row * D + cD + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
+                for (int g = 0; g < D / 64; ++g)
+                    box32_store(&mO, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
+                                row0[m] + quarter * 32, rec);
             }
+            if (lane == 0) tma_store_wait_all();
             if (NORM && half == 0) {
                 // m (after C) and p (after P), one value per state row
                 const uint32_t mv = tmem_ld1(tDen_ + lane_off);
@@ -773,7 +795,9 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
         // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
         if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
     } else {
-        mo = mq;  // unused
+        // the summary records as (3D + 2) rows of D floats each, 32 x 32 boxes
+        if (!make_map(&mo, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+            return cudaErrorInvalidValue;
     }
     TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;

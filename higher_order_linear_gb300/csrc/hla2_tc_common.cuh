@@ -223,6 +223,25 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) 
     tmem_ld_wait();
 }
 
+// One lane-row of 32 fp32 values per lane (the warp's 32 lanes are the box's
+// 32 rows) written as a 4 KB box in the 128-byte-swizzled layout a tensor map
+// with SWIZZLE_128B expects, then sent to global memory by a bulk tensor store
+// at (x, y, z) that lane 0 issues and commits.  The caller waits for the bulk
+// group before reusing `scratch` and before the CTA exits.
+__device__ __forceinline__ void box32_store(const CUtensorMap* map, uint32_t scratch, const uint32_t* v, int lane,
+                                            int x, int y, int z) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1],
+                     v[4 * q + 2], v[4 * q + 3]);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(map, scratch, x, y, z);
+        tma_store_commit();
+    }
+}
+
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                 uint32_t acc) {
     asm volatile(
