@@ -61,11 +61,13 @@ struct ALayout {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, AParams p) {
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
+                    const __grid_constant__ CUtensorMap mR, AParams p) {
     using LY = ALayout<D, MODE>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
-    enum { LQ, LK, LV, CA, CY, CQ, CO, CE, DA, DY, DO, DP, DE, NBAR };
+    // (PB + w: drain warp w's prefix boxes, output walk)
+    enum { LQ, LK, LV, CA, CY, CQ, CO, CE, DA, DY, DO, DP, DE, PB, NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -197,30 +199,34 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     if (MODE == 1 && state_rows) {
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
-        const float* src[2] = {pre + (size_t)D * D, pre + 2 * (size_t)D * D + D};  // P (after M), E (after m)
-        const uint32_t dst[2] = {tP_, tE_};
-        const Tile* til[2] = {&tP, &tE};
-        // all loads of this thread's row pieces first: one memory latency, not four
-        float4 x4[2][D / 8];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int j = 0; j < D / 8; ++j) x4[m][j] = __ldg(reinterpret_cast<const float4*>(src[m] + (size_t)row * D + cD) + j);
-#pragma unroll
+        // P0 (record row D) and E0 (record row 2D + 1) arrive as this warp's
+        // 32 x 32 fp32 boxes by bulk tensor loads (mR maps the records as
+        // (3D + 2) rows of D floats) into a private staging area in the A / Y
+        // tiles, which nothing else touches before the first chunk
+        (void)pre;
+        const int rec = head * p.nseg + seg;
+        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+#pragma unroll 1
         for (int m = 0; m < 2; ++m) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                const int cb = cD + 32 * h;
-                uint32_t r[32];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 x = x4[m][8 * h + j];
-                    r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
-                    r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
-                }
-                tmem_st32(dst[m] + lane_off + cb, r);
-                put_row32(*til[m], row, cb, r, false);
+                for (int g = 0; g < D / 64; ++g)
+                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? D : 2 * D + 1) + quarter * 32, rec,
+                                bar(PB + warp));
             }
+            __syncwarp();
+            if (!wait_bar(PB + warp, (uint32_t)m)) break;
+#pragma unroll
+            for (int g = 0; g < D / 64; ++g) {
+                const int cb = cD + 32 * g;
+                uint32_t r[32];
+                box32_read(stage + (uint32_t)g * 4096u, lane, r);
+                tmem_st32((m == 0 ? tP_ : tE_) + lane_off + cb, r);
+                put_row32(m == 0 ? tP : tE, row, cb, r, false);
+            }
+            __syncwarp();  // every lane has read the boxes before the next load reuses them
         }
         tmem_st_wait();
     }
@@ -431,7 +437,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
 #pragma unroll
                 for (int g = 0; g < D / 64; ++g)
-                    box32_store(&mO, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
+                    box32_store(&mR, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
                                 row0[m] + quarter * 32, rec);
             }
             if (lane == 0) tma_store_wait_all();
@@ -452,12 +458,16 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
+    // mR: the segment records (prefixes read by the output walk, summaries
+    // written by the summary walk) as (3D + 2) rows of D floats, 32 x 32 boxes
+    CUtensorMap mr;
+    if (!make_map(&mr, MODE == 1 ? static_cast<const void*>(prefix) : static_cast<const void*>(summ),
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+        return cudaErrorInvalidValue;
     if (MODE == 1) {
         if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
     } else {
-        // the summary records as (3D + 2) rows of D floats each, 32 x 32 boxes
-        if (!make_map(&mo, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
-            return cudaErrorInvalidValue;
+        mo = mr;  // unused
     }
     AParams prm{T, plan.nseg, plan.nchunk, summ, prefix, status};
     const size_t smem = ALayout<D, MODE>::kBytes + 1024;
@@ -465,7 +475,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, prm);
+    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -82,11 +82,14 @@ struct Layout {
 template <int D, int MODE, bool NORM>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TCParams p) {
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
+               const __grid_constant__ CUtensorMap mR, TCParams p) {
     using LY = Layout<D, MODE, NORM>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
-    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, NBAR };
+    // (PB + w: drain warp w's prefix boxes, output walk)
+    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, PB,
+           NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -246,38 +249,34 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     if (MODE == 1 && state_rows) {
         const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
         const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
-        const float* S0 = pre;                          // S at offset 0
-        const float* P0 = pre + 2 * (size_t)D * D + D;  // P after S, C, m
-        // every load of this thread's row pieces is issued before the first use,
-        // so the CTA pays one memory latency here instead of one per piece
-        float4 xs[D / 8], xp[D / 8];
+        // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
+        // 32 x 32 fp32 boxes by bulk tensor loads (mR maps the records as
+        // (3D + 2) rows of D floats) into a private staging area in the A / X
+        // tiles, which nothing else touches before the first chunk
+        const int rec = head * p.nseg + seg;
+        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+#pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            xs[j] = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)row * D + cD) + j);
-            xp[j] = __ldg(reinterpret_cast<const float4*>(P0 + (size_t)row * D + cD) + j);
-        }
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-            const int cb = cD + 32 * h;
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = xs[8 * h + j];
-                r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
-                r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
+                for (int g = 0; g < D / 64; ++g)
+                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? 0 : 2 * D + 1) + quarter * 32, rec,
+                                bar(PB + warp));
             }
-            tmem_st32(tS_ + lane_off + cb, r);
-            if (NORM) put_row32_split2(tS, tSl, row, cb, r, false);
-            else put_row32(tS, row, cb, r, false);
+            __syncwarp();
+            if (!wait_bar(PB + warp, (uint32_t)m)) break;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = xp[8 * h + j];
-                r[4 * j] = __float_as_uint(x.x); r[4 * j + 1] = __float_as_uint(x.y);
-                r[4 * j + 2] = __float_as_uint(x.z); r[4 * j + 3] = __float_as_uint(x.w);
+            for (int g = 0; g < D / 64; ++g) {
+                const int cb = cD + 32 * g;
+                uint32_t r[32];
+                box32_read(stage + (uint32_t)g * 4096u, lane, r);
+                tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cb, r);
+                if (NORM) put_row32_split2(m == 0 ? tS : tP, m == 0 ? tSl : tPl, row, cb, r, false);
+                else put_row32(m == 0 ? tS : tP, row, cb, r, false);
             }
-            tmem_st32(tP_ + lane_off + cb, r);
-            if (NORM) put_row32_split2(tP, tPl, row, cb, r, false);
-            else put_row32(tP, row, cb, r, false);
+            __syncwarp();  // every lane has read the boxes before the next load reuses them
         }
         if (NORM && half == 0) {
             // p0 = S0 m0 - h0 of the prefix (record slot after P)
@@ -629,7 +628,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
 #pragma unroll
                 for (int g = 0; g < D / 64; ++g)
-                    box32_store(&mO, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
+                    box32_store(&mR, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
                                 row0[m] + quarter * 32, rec);
             }
             if (lane == 0) tma_store_wait_all();
@@ -791,13 +790,17 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
+    // mR: the segment records (prefixes read by the output walk, summaries
+    // written by the summary walk) as (3D + 2) rows of D floats, 32 x 32 boxes
+    CUtensorMap mr;
+    if (!make_map(&mr, MODE == 1 ? static_cast<const void*>(prefix) : static_cast<const void*>(summ),
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+        return cudaErrorInvalidValue;
     if (MODE == 1) {
         // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
         if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
     } else {
-        // the summary records as (3D + 2) rows of D floats each, 32 x 32 boxes
-        if (!make_map(&mo, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
-            return cudaErrorInvalidValue;
+        mo = mr;  // unused
     }
     TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;
@@ -805,7 +808,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, prm);
+    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -242,6 +242,19 @@ __device__ __forceinline__ void box32_store(const CUtensorMap* map, uint32_t scr
     }
 }
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
+// Reads back this lane's row (32 fp32 values) of a 32 x 32 box that a tensor
+// load with SWIZZLE_128B wrote at `scratch` (the layout box32_store writes).
+__device__ __forceinline__ void box32_read(uint32_t scratch, int lane, uint32_t* v) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        ld_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1],
+                     v[4 * q + 2], v[4 * q + 3]);
+}
+
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                 uint32_t acc) {
     asm volatile(
