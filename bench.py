@@ -200,9 +200,16 @@ def alg_flops(w, L=64):
 
 
 def segments_per_head(BH, T):
-    # mirrors the library's segment plan (two waves of 152 SMs, 128-token chunks)
+    # mirrors the library's segment plan: 128-token chunks, the segment count
+    # minimising waves * (chunks per segment + 2) + nseg / 2 on 152 SMs
     nchunk = (T + 127) // 128
-    return min(max(1, (304 + BH - 1) // BH), nchunk)
+    best, best_cost = 1, None
+    for n in range(1, min(nchunk, 4096) + 1):
+        waves = (BH * n + 151) // 152
+        cost2 = 2 * waves * ((nchunk + n - 1) // n + 2) + n
+        if best_cost is None or cost2 < best_cost:
+            best, best_cost = n, cost2
+    return best
 
 
 def reference_arm(args):

@@ -43,19 +43,33 @@ constexpr int kMaxDevices = 64;
 int* g_status_addr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
-// Segments per head for the forward: enough CTAs to fill two waves of the
-// GB300's 152 SMs, never more than the head's 128-token chunks.
+// Segments per head for the forward.  Every segment is one CTA, and a
+// tensor-core walk holds a whole SM (its shared memory), so the walks run in
+// waves of 152 CTAs; each CTA pays a ramp (prefix and first tiles) of about
+// two chunks, and every segment adds work to the scan.  The plan takes the
+// segment count that minimises
+//   waves * (chunks per segment + 2) + nseg / 2      (in units of one chunk)
+// over 1 <= nseg <= min(chunks per head, 4096).
 constexpr int kGranule = 128;
-constexpr int kTargetCtas = 2 * 152;
+constexpr int kSMs = 152;
 
 SegPlan forward_plan(int BH, int T) {
     SegPlan p;
     p.granule = kGranule;
     p.nchunk = (T + kGranule - 1) / kGranule;
-    int want = (kTargetCtas + BH - 1) / BH;
-    if (want < 1) want = 1;
-    p.nseg = want < p.nchunk ? want : p.nchunk;
-    if (p.nseg > 65535) p.nseg = 65535;
+    const int top = p.nchunk < 4096 ? p.nchunk : 4096;
+    long long best_cost = -1;
+    int best = 1;
+    for (int n = 1; n <= top; ++n) {
+        const long long waves = ((long long)BH * n + kSMs - 1) / kSMs;
+        const long long per = (p.nchunk + n - 1) / n;
+        const long long cost2 = 2 * waves * (per + 2) + n;  // twice the cost above, in integers
+        if (best_cost < 0 || cost2 < best_cost) {
+            best_cost = cost2;
+            best = n;
+        }
+    }
+    p.nseg = best;
     return p;
 }
 
