@@ -77,6 +77,7 @@ struct FwdWorkspace {
     float* summ;    // [BH][nseg][R]
     float* prefix;  // [BH][nseg][R]
     float* tot;     // [BH][R]
+    float* fac;     // [2][nseg] decay factors of the segments (decayed operator)
     size_t bytes;
 };
 
@@ -89,7 +90,8 @@ FwdWorkspace carve(void* base, int BH, SegPlan p, int d, int dv) {
     w.summ = reinterpret_cast<float*>(c);
     w.prefix = reinterpret_cast<float*>(c + up(seg_floats) * 4);
     w.tot = reinterpret_cast<float*>(c + 2 * up(seg_floats) * 4);
-    w.bytes = (2 * up(seg_floats) + up((size_t)BH * R)) * 4;
+    w.fac = reinterpret_cast<float*>(c + (2 * up(seg_floats) + up((size_t)BH * R)) * 4);
+    w.bytes = (2 * up(seg_floats) + up((size_t)BH * R) + up(2 * (size_t)p.nseg)) * 4;
     return w;
 }
 
@@ -636,8 +638,42 @@ int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, in
     cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, gamma,
                                 plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "decay segment summaries");
-    e = launch_decay_scan(ws.summ, ws.prefix, state_out ? ws.tot : nullptr, BH, T, d, dv, gamma, plan, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decay scan");
+    // decayed scan (f_r = gamma^{n_r}, segment r spanning n_r tokens):
+    //   S_<r+1 = f_r S_<r + S_r (C, m likewise),
+    //   P_<r+1 = f_r^2 P_<r + P_r + f_r S_<r C_r (p likewise with m_r),
+    // as decayed running sums of (S, C, m), one product per record, and
+    // decayed running sums of the corrected part with f_r^2
+    {
+        const RecOff ro = summary_offsets(d, dv);
+        float* tot = state_out ? ws.tot : nullptr;
+        e = launch_decay_factors(ws.fac, T, gamma, plan, s);
+        if (e == cudaSuccess)
+            e = launch_decay_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, ro.X, tot, ro.R, ws.fac, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of S, C, m");
+        CrossArgs a{};
+        a.A = ws.prefix + ro.S; a.sA = (long long)ro.R;
+        a.B = ws.summ + ro.C;   a.sB = (long long)ro.R;
+        a.bx = ws.summ + ro.m;  a.sbx = (long long)ro.R;
+        a.base = ws.summ + ro.X; a.sbase = (long long)ro.R;
+        a.basex = ws.summ + ro.x; a.sbasex = (long long)ro.R;
+        a.out = ws.prefix + ro.X; a.sout = (long long)ro.R;
+        a.outx = ws.prefix + ro.x; a.soutx = (long long)ro.R;
+        a.alpha = 1.f; a.d = d; a.dv = dv;
+        a.pscale = ws.fac; a.pscale_mod = plan.nseg;
+        for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
+            CrossArgs c = a;
+            const long long nb = (long long)BH * plan.nseg - b0;
+            c.nb = (int)(nb < 65535 ? nb : 65535);
+            c.pscale_off = b0;
+            c.A += b0 * ro.R; c.B += b0 * ro.R; c.bx += b0 * ro.R;
+            c.base += b0 * ro.R; c.basex += b0 * ro.R; c.out += b0 * ro.R; c.outx += b0 * ro.R;
+            e = launch_cross(c, s);
+            if (e != cudaSuccess) return cuda_fail(e, "decay scan: cross terms");
+        }
+        e = launch_decay_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, ro.R - ro.X,
+                                tot ? tot + ro.X : nullptr, ro.R, ws.fac + plan.nseg, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of P, p");
+    }
     e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 0, gamma, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "decay segment outputs");
     if (state_out) {

@@ -91,15 +91,15 @@ cudaError_t launch_walk(int mode, const void* Q, const void* K, const void* V, i
                         int BH, int T, int d, int dv, int normalized, int unmasked, float gamma, SegPlan plan,
                         cudaStream_t s);
 
-// Decayed exclusive scan of P-form segment records S|C|m|P|p, sequential over
-// the nseg records of each head, fp32 on CUDA cores (gamma = 1: the masked
-// combine).  Segment r spans n_r tokens (from the plan and T); with
-// f = gamma^{n_r}:  S <- f S + S_r, C, m likewise,
-// P <- f^2 P + P_r + f S C_r, p <- f^2 p + p_r + f S m_r.
-// Writes S, P, p of every prefix record (and C, m when tot != nullptr) and,
-// if tot != nullptr, the inclusive totals S|C|m|P|p per head.
-cudaError_t launch_decay_scan(const float* summ, float* prefix, float* tot, int BH, int T, int d, int dv,
-                              float gamma, SegPlan plan, cudaStream_t s);
+// Decay factors of the segment plan: fac[r] = gamma^{n_r} and
+// fac[nseg + r] = gamma^{2 n_r}, n_r the tokens of segment r.
+cudaError_t launch_decay_factors(float* fac, int T, float gamma, SegPlan plan, cudaStream_t s);
+
+// Decayed exclusive running sum along the record axis over the element range
+// [off, off+len): out[b][0][i] = 0, out[b][n+1][i] = fac[n] out[b][n][i] + in[b][n][i].
+// in may equal out; total (if not null) receives the inclusive sums.
+cudaError_t launch_decay_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
+                                float* total, size_t total_stride, const float* fac, cudaStream_t s);
 
 // ---- scans (hla2_scan.cu) ----
 // Exclusive running sum along the record axis for the element range
@@ -124,6 +124,11 @@ struct CrossArgs {
     float alpha;
     int d, dv, nb;
     int* status;  // device status word (tensor-core variant's bounded wait)
+    // optional per-item scale of the product (fp32 kernel only): item i of the
+    // batch uses pscale[(pscale_off + i) % pscale_mod]
+    const float* pscale;
+    long long pscale_off;
+    int pscale_mod;
 };
 cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s);
 

@@ -128,6 +128,13 @@ cross_kernel(CrossArgs a) {
     const float* basex = a.basex ? a.basex + (long long)nb * a.sbasex : nullptr;
     float* out = a.out + (long long)nb * a.sout;
     float* outx = a.outx ? a.outx + (long long)nb * a.soutx : nullptr;
+    if (a.pscale) {
+        const float sc = a.pscale[(a.pscale_off + nb) % a.pscale_mod];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] *= sc;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = row0 + ty * 4 + i;
@@ -146,94 +153,52 @@ cross_kernel(CrossArgs a) {
     }
 }
 
-// Decayed exclusive scan of P-form records, sequential over the records of
-// one head.  A CTA owns kRows consecutive state rows (of S, C, P and of the
-// vectors m, p) of one head and carries their running prefix in shared
-// memory; the cross terms S C_r and S m_r need the CTA's S rows against all
-// of C_r, read from global memory (coalesced along the value axis).
-constexpr int kRows = 16;
+// Decayed scans (the decayed operator's segment combine): per-record factors
+// and an exclusive running sum that decays the running value by the factor of
+// the record it passes.
+__global__ void decay_factors_kernel(float* fac, int T, float gamma, SegPlan plan) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= plan.nseg) return;
+    const long long c0 = (long long)r * plan.nchunk / plan.nseg;
+    const long long c1 = (long long)(r + 1) * plan.nchunk / plan.nseg;
+    const long long t1 = min((long long)T, c1 * plan.granule);
+    // gamma^n by repeated squaring in double precision (fp32 products over
+    // thousands of tokens would drift)
+    double f = 1.0, base = (double)gamma;
+    for (long long e = t1 - c0 * plan.granule; e > 0; e >>= 1) {
+        if (e & 1) f *= base;
+        base *= base;
+    }
+    fac[r] = (float)f;
+    fac[plan.nseg + r] = (float)(f * f);
+}
 
-__global__ void __launch_bounds__(256)
-decay_scan_kernel(const float* __restrict__ summ, float* __restrict__ prefix, float* __restrict__ tot,
-                  int T, int d, int dv, float gamma, SegPlan plan) {
-    extern __shared__ float dsm[];
-    const int head = blockIdx.y;
-    const int r0 = blockIdx.x * kRows;
-    const int nr = min(kRows, d - r0);
-    const RecOff ro = summary_offsets(d, dv);
-    float* sS = dsm;                      // kRows x d   running S rows
-    float* sC = sS + kRows * d;           // kRows x dv  running C rows
-    float* sP = sC + kRows * dv;          // kRows x dv  running P rows
-    float* sm = sP + kRows * dv;          // kRows       running m
-    float* sp = sm + kRows;               // kRows       running p
-    float* sX = sp + kRows;               // kRows x (dv + 1)  cross terms S C_r | S m_r
-    const int tid = threadIdx.x;
-    for (int i = tid; i < kRows * d; i += 256) sS[i] = 0.f;
-    for (int i = tid; i < kRows * dv; i += 256) { sC[i] = 0.f; sP[i] = 0.f; }
-    if (tid < kRows) { sm[tid] = 0.f; sp[tid] = 0.f; }
-    __syncthreads();
-    const int w = dv + 1;
-    for (int r = 0; r < plan.nseg; ++r) {
-        const long long c0 = (long long)r * plan.nchunk / plan.nseg;
-        const long long c1 = (long long)(r + 1) * plan.nchunk / plan.nseg;
-        const long long t1 = min((long long)T, c1 * plan.granule);
-        const int nb = (int)(t1 - c0 * plan.granule);  // tokens of segment r
-        // f = gamma^nb by repeated squaring in double precision (fp32 products
-        // over thousands of tokens would drift)
-        double fd = 1.0, base = (double)gamma;
-        for (int e = nb; e > 0; e >>= 1) {
-            if (e & 1) fd *= base;
-            base *= base;
-        }
-        const float f = (float)fd;
-        const float* rec = summ + ((size_t)head * plan.nseg + r) * ro.R;
-        float* pre = prefix + ((size_t)head * plan.nseg + r) * ro.R;
-        // the exclusive prefix of record r is the running state
-        for (int i = tid; i < nr * d; i += 256) pre[ro.S + (size_t)r0 * d + i] = sS[i];
-        for (int i = tid; i < nr * dv; i += 256) pre[ro.X + (size_t)r0 * dv + i] = sP[i];
-        if (tid < nr) pre[ro.x + r0 + tid] = sp[tid];
-        if (tot) {
-            for (int i = tid; i < nr * dv; i += 256) pre[ro.C + (size_t)r0 * dv + i] = sC[i];
-            if (tid < nr) pre[ro.m + r0 + tid] = sm[tid];
-        }
-        // cross terms with the running S (before it absorbs record r)
-        for (int i = tid; i < nr * w; i += 256) {
-            const int a = i / w, e = i % w;
-            const float* srow = sS + a * d;
-            float acc = 0.f;
-            if (e < dv)
-                for (int b = 0; b < d; ++b) acc = fmaf(srow[b], rec[ro.C + (size_t)b * dv + e], acc);
-            else
-                for (int b = 0; b < d; ++b) acc = fmaf(srow[b], rec[ro.m + b], acc);
-            sX[i] = acc;
-        }
-        __syncthreads();
-        const float f2 = f * f;
-        for (int i = tid; i < nr * dv; i += 256) {
-            const int a = i / dv, e = i % dv;
-            const size_t gi = (size_t)(r0 + a) * dv + e;
-            sP[i] = fmaf(f2, sP[i], fmaf(f, sX[a * w + e], rec[ro.X + gi]));
-            sC[i] = fmaf(f, sC[i], rec[ro.C + gi]);
-        }
-        if (tid < nr) {
-            sp[tid] = fmaf(f2, sp[tid], fmaf(f, sX[tid * w + dv], rec[ro.x + r0 + tid]));
-            sm[tid] = fmaf(f, sm[tid], rec[ro.m + r0 + tid]);
-        }
-        for (int i = tid; i < nr * d; i += 256) sS[i] = fmaf(f, sS[i], rec[ro.S + (size_t)r0 * d + i]);
-        __syncthreads();
-    }
-    if (tot) {
-        float* out = tot + (size_t)head * ro.R;
-        for (int i = tid; i < nr * d; i += 256) out[ro.S + (size_t)r0 * d + i] = sS[i];
-        for (int i = tid; i < nr * dv; i += 256) {
-            out[ro.C + (size_t)r0 * dv + i] = sC[i];
-            out[ro.X + (size_t)r0 * dv + i] = sP[i];
-        }
-        if (tid < nr) {
-            out[ro.m + r0 + tid] = sm[tid];
-            out[ro.x + r0 + tid] = sp[tid];
+__global__ void __launch_bounds__(kScanThreads)
+decay_exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
+                    size_t total_stride, const float* __restrict__ fac) {
+    const size_t i = (size_t)blockIdx.x * kScanThreads + threadIdx.x;
+    const int bh = blockIdx.y;
+    if (i >= len) return;
+    const float* pin = in + (size_t)bh * N * R + off + i;
+    float* pout = out + (size_t)bh * N * R + off + i;
+    float run = 0.f;
+    int r = 0;
+    for (; r + kScanUnroll <= N; r += kScanUnroll) {
+        float x[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) x[j] = pin[(size_t)(r + j) * R];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            pout[(size_t)(r + j) * R] = run;
+            run = fmaf(fac[r + j], run, x[j]);
         }
     }
+    for (; r < N; ++r) {
+        const float x = pin[(size_t)r * R];
+        pout[(size_t)r * R] = run;
+        run = fmaf(fac[r], run, x);
+    }
+    if (total) total[(size_t)bh * total_stride + i] = run;
 }
 
 __global__ void copy_strided_kernel(const float* src, long long s_src, float* dst, long long s_dst, size_t len) {
@@ -269,13 +234,18 @@ cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_decay_scan(const float* summ, float* prefix, float* tot, int BH, int T, int d, int dv,
-                              float gamma, SegPlan plan, cudaStream_t s) {
-    if (BH == 0 || plan.nseg == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((size_t)kRows * d + 2 * (size_t)kRows * dv + 2 * kRows +
-                                         (size_t)kRows * (dv + 1));
-    dim3 grid((d + kRows - 1) / kRows, BH);
-    decay_scan_kernel<<<grid, 256, smem, s>>>(summ, prefix, tot, T, d, dv, gamma, plan);
+cudaError_t launch_decay_factors(float* fac, int T, float gamma, SegPlan plan, cudaStream_t s) {
+    if (plan.nseg == 0) return cudaSuccess;
+    decay_factors_kernel<<<(plan.nseg + 255) / 256, 256, 0, s>>>(fac, T, gamma, plan);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decay_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
+                                float* total, size_t total_stride, const float* fac, cudaStream_t s) {
+    if (BH == 0 || len == 0) return cudaSuccess;
+    dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
+    decay_exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride, fac);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -39,10 +39,11 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_workspace_query(L):
     R = lambda d, dv: d * d + 2 * d * dv + 2 * d
-    # one head, T=64: one segment -> summary + prefix + total records (256-byte rounded)
+    # one head, T=64: one segment -> summary + prefix + total records and the
+    # two decay factors of the segment, each rounded to 256 bytes
     ws = hla2.hla2_forward_workspace(1, 1, 64, 16, 16, 0)
     up = lambda n: (n + 63) // 64 * 64
-    assert ws == 4 * (2 * up(R(16, 16)) + up(R(16, 16)))
+    assert ws == 4 * (2 * up(R(16, 16)) + up(R(16, 16)) + up(2))
     big = hla2.hla2_forward_workspace(1, 16, 65536, 128, 128, 1)
     assert big > 0 and big % 256 == 0
     assert hla2.hla2_forward_workspace(1, 1, 64, 200, 16, 0) == 0   # unsupported d
