@@ -185,7 +185,9 @@ def oracle_sample(w, seconds: float):
 # ----------------------------------------------------------------- config --
 def fwd_config(w, plan_segments=None, l2_note=None):
     return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "input_dtype": w.dtype,
-            "output_dtype": "fp32", "normalized": w.normalized, "segments_per_head": plan_segments,
+            "output_dtype": "fp32", "normalized": w.normalized,
+            "segments_per_head": plan_segments[0] if plan_segments else None,
+            "chunks_per_segment": plan_segments[1] if plan_segments else None,
             "l2": l2_note or "inputs exceed L2 (1.34 GB moved per step vs 129 MB L2); no flush",
             "parallelism": "replicas (heads independent, no collective)"}
 
@@ -197,16 +199,33 @@ def alg_flops(w, L=64):
 
 
 def segments_per_head(BH, T):
-    # mirrors the library's segment plan: 128-token chunks, the segment count
-    # minimising waves * (chunks per segment + 2) + nseg / 2 on 152 SMs
+    """Mirrors the library's segment plan: runs of `seglen` 128-token chunks
+    (the last may be shorter), the run length minimising the dispatch makespan
+    on 152 SMs (a CTA costs its chunks + 2) plus nseg / 2.  Returns (nseg, seglen)."""
+    import heapq
     nchunk = (T + 127) // 128
-    best, best_cost = 1, None
-    for n in range(1, min(nchunk, 4096) + 1):
-        waves = (BH * n + 151) // 152
-        cost2 = 2 * waves * ((nchunk + n - 1) // n + 2) + n
-        if best_cost is None or cost2 < best_cost:
-            best, best_cost = n, cost2
-    return best
+    best = None
+    for ln in range(max(1, (nchunk + 4095) // 4096), nchunk + 1):
+        ns = (nchunk + ln - 1) // ln
+        tail = nchunk - (ns - 1) * ln
+        short = ns > 1 and tail < ln
+        full = BH * (ns - 1) if short else BH * ns
+        q, r = divmod(full, 152)
+        span = (q + 1 if r else q) * (ln + 2)
+        if short:
+            if BH > 20000:
+                span += -(-BH // 152) * (tail + 2)
+            else:
+                load = [(q + 1) * (ln + 2) if i < r else q * (ln + 2) for i in range(152)]
+                heapq.heapify(load)
+                for _ in range(BH):
+                    t = heapq.heappop(load) + tail + 2
+                    heapq.heappush(load, t)
+                    span = max(span, t)
+        cost2 = 2 * span + ns
+        if best is None or cost2 < best[0]:
+            best = (cost2, ns, ln)
+    return best[1], best[2]
 
 
 def reference_arm(args):

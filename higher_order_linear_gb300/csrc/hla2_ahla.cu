@@ -76,10 +76,10 @@ ahla_walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin
     s.misc = s.partB + kWalkThreads;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = blockIdx.x;
-    const int head = blockIdx.y;
-    const long long c0 = (long long)seg * plan.nchunk / plan.nseg;
-    const long long c1 = (long long)(seg + 1) * plan.nchunk / plan.nseg;
+    int head, seg;
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const long long c0 = seg_chunk_begin(plan, seg);
+    const long long c1 = seg_chunk_begin(plan, seg + 1);
     const int t0 = (int)(c0 * plan.granule);
     const int t1 = (int)min((long long)T, c1 * plan.granule);
     const RecOff ro = summary_offsets(d, dv);  // M|P|m|E|n at the S|C|m|X|x offsets

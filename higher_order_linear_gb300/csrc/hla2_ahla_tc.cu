@@ -32,7 +32,7 @@ namespace hla2 {
 namespace {
 
 struct AParams {
-    int T, nseg, nchunk;
+    int T, nseg, nchunk, seglen;
     float* summ;          // summary walk: output records M|P|m|E|n
     const float* prefix;  // output walk: input records (P, E read)
     int* status;
@@ -79,10 +79,11 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
-    const int seg = blockIdx.x;
-    const int head = blockIdx.y;
-    const int c_begin = (int)((long long)seg * p.nchunk / p.nseg);
-    const int c_end = (int)((long long)(seg + 1) * p.nchunk / p.nseg);
+    int head, seg;
+    const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const int c_begin = seg_chunk_begin(plan, seg);
+    const int c_end = seg_chunk_begin(plan, seg + 1);
     const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
@@ -469,7 +470,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     } else {
         mo = mr;  // unused
     }
-    AParams prm{T, plan.nseg, plan.nchunk, summ, prefix, status};
+    AParams prm{T, plan.nseg, plan.nchunk, plan.seglen, summ, prefix, status};
     const size_t smem = ALayout<D, MODE>::kBytes + 1024;
     auto kern = ahla_tc_walk_kernel<D, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -7,7 +7,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -44,32 +46,70 @@ int* g_status_addr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
 // Segments per head for the forward.  Every segment is one CTA, and a
-// tensor-core walk holds a whole SM (its shared memory), so the walks run in
-// waves of 152 CTAs; each CTA pays a ramp (prefix and first tiles) of about
-// two chunks, and every segment adds work to the scan.  The plan takes the
-// segment count that minimises
-//   waves * (chunks per segment + 2) + nseg / 2      (in units of one chunk)
-// over 1 <= nseg <= min(chunks per head, 4096).
+// tensor-core walk holds a whole SM (its shared memory).  A head's chunks are
+// cut into runs of seglen chunks (the last run may be shorter); the CTAs of
+// full runs are dispatched first and the short ones last (block_segment).
+// The plan takes the run length that minimises
+//   makespan + nseg / 2          (in units of one chunk)
+// where the makespan comes from dispatching every CTA, in that order, to the
+// first free of the 152 SMs, a CTA costing its chunks plus two for its ramp
+// (prefix and first tiles), and nseg / 2 stands for the scan work a segment
+// adds.  Plans are cached per (BH, T).
 constexpr int kGranule = 128;
 constexpr int kSMs = 152;
 
+namespace {
+long long plan_makespan2(long long BH, int nchunk, int seglen, int nseg) {
+    // twice the makespan, in chunk units (a CTA costs its chunks + 2)
+    const int tail = nchunk - (nseg - 1) * seglen;
+    const bool short_tail = nseg > 1 && tail < seglen;
+    const long long full = short_tail ? BH * (nseg - 1) : BH * nseg;
+    const long long a = seglen + 2, b = tail + 2;
+    // full-length CTAs first: equal jobs fill the SMs round by round
+    const long long q = full / kSMs, r = full % kSMs;
+    long long span = (r > 0 ? q + 1 : q) * a;
+    if (!short_tail) return 2 * span;
+    if (BH > 20000) {  // too many to place one by one: treat them as one more round
+        return 2 * (span + ((BH + kSMs - 1) / kSMs) * b);
+    }
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> load;
+    for (long long i = 0; i < kSMs; ++i) load.push(i < r ? (q + 1) * a : q * a);
+    for (long long i = 0; i < BH; ++i) {
+        const long long t = load.top() + b;
+        load.pop();
+        load.push(t);
+        if (t > span) span = t;
+    }
+    return 2 * span;
+}
+}  // namespace
+
 SegPlan forward_plan(int BH, int T) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, SegPlan> cache;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find({BH, T});
+        if (it != cache.end()) return it->second;
+    }
     SegPlan p;
     p.granule = kGranule;
     p.nchunk = (T + kGranule - 1) / kGranule;
-    const int top = p.nchunk < 4096 ? p.nchunk : 4096;
     long long best_cost = -1;
-    int best = 1;
-    for (int n = 1; n <= top; ++n) {
-        const long long waves = ((long long)BH * n + kSMs - 1) / kSMs;
-        const long long per = (p.nchunk + n - 1) / n;
-        const long long cost2 = 2 * waves * (per + 2) + n;  // twice the cost above, in integers
+    p.nseg = 1;
+    p.seglen = p.nchunk;
+    const int len0 = (p.nchunk + 4095) / 4096;  // at most 4096 segments per head
+    for (int len = len0 > 0 ? len0 : 1; len <= p.nchunk; ++len) {
+        const int nseg = (p.nchunk + len - 1) / len;
+        const long long cost2 = plan_makespan2(BH, p.nchunk, len, nseg) + nseg;
         if (best_cost < 0 || cost2 < best_cost) {
             best_cost = cost2;
-            best = n;
+            p.nseg = nseg;
+            p.seglen = len;
         }
     }
-    p.nseg = best;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[{BH, T}] = p;
     return p;
 }
 
@@ -394,6 +434,7 @@ int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* sum
     p.granule = L;
     p.nchunk = (T + L - 1) / L;
     p.nseg = p.nchunk;  // one chunk per segment
+    p.seglen = 1;
     if (p.nseg > 65535) return fail(HLA2_ERR_UNSUPPORTED, "%d chunks per head exceeds 65535", p.nseg);
     cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, 1.0f, p,
                                 reinterpret_cast<cudaStream_t>(stream));

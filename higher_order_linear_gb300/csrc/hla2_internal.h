@@ -57,13 +57,39 @@ __host__ __device__ inline RecOff decode_offsets(int d, int dv) {
     return o;
 }
 
-// Segment partition: a head's ceil(T/granule) chunks are split into nseg
-// contiguous runs; segment s owns chunks [s*nc/nseg, (s+1)*nc/nseg).
+// Segment partition: a head's nchunk = ceil(T/granule) chunks are split into
+// nseg contiguous runs of seglen chunks; the last run may be shorter.
+// Segment s owns chunks [seg_chunk_begin(s), seg_chunk_begin(s + 1)).
 struct SegPlan {
     int granule;  // tokens per chunk
     int nchunk;   // chunks per head
     int nseg;     // segments per head
+    int seglen;   // chunks per segment (all but the last)
 };
+__host__ __device__ inline int seg_chunk_begin(const SegPlan& p, int s) {
+    const long long c = (long long)s * p.seglen;
+    return c < p.nchunk ? (int)c : p.nchunk;
+}
+// The (head, segment) a CTA of a (nseg, BH) grid works on, from its linear
+// block index b.  When each head's last segment is shorter than the others,
+// the CTAs of all full-length segments come first (head-major) and the short
+// ones last, so that the short segments go to the SMs that free up first.
+__host__ __device__ inline void block_segment(const SegPlan& p, int BH, long long b, int& head, int& seg) {
+    const bool short_tail = p.nseg > 1 && (long long)p.nseg * p.seglen > p.nchunk;
+    if (!short_tail) {
+        head = (int)(b / p.nseg);
+        seg = (int)(b % p.nseg);
+        return;
+    }
+    const long long nfull = (long long)BH * (p.nseg - 1);
+    if (b < nfull) {
+        head = (int)(b / (p.nseg - 1));
+        seg = (int)(b % (p.nseg - 1));
+    } else {
+        head = (int)(b - nfull);
+        seg = p.nseg - 1;
+    }
+}
 
 // ---- decode step (hla2_decode.cu) ----
 cudaError_t launch_step(float* state, const float* q, const float* k, const float* v, float* o,

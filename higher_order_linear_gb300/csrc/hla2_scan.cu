@@ -159,8 +159,8 @@ cross_kernel(CrossArgs a) {
 __global__ void decay_factors_kernel(float* fac, int T, float gamma, SegPlan plan) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= plan.nseg) return;
-    const long long c0 = (long long)r * plan.nchunk / plan.nseg;
-    const long long c1 = (long long)(r + 1) * plan.nchunk / plan.nseg;
+    const long long c0 = seg_chunk_begin(plan, r);
+    const long long c1 = seg_chunk_begin(plan, r + 1);
     const long long t1 = min((long long)T, c1 * plan.granule);
     // gamma^n by repeated squaring in double precision (fp32 products over
     // thousands of tokens would drift)

@@ -33,7 +33,7 @@ namespace {
 
 // ------------------------------------------------------------- kernel ----
 struct TCParams {
-    int T, nseg, nchunk;
+    int T, nseg, nchunk, seglen;
     float* summ;          // mode 0 output records
     const float* prefix;  // mode 1 input records
     float* O;             // mode 1 outputs [BH][T][D]
@@ -101,10 +101,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
-    const int seg = blockIdx.x;
-    const int head = blockIdx.y;
-    const int c_begin = (int)((long long)seg * p.nchunk / p.nseg);
-    const int c_end = (int)((long long)(seg + 1) * p.nchunk / p.nseg);
+    int head, seg;
+    const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const int c_begin = seg_chunk_begin(plan, seg);
+    const int c_end = seg_chunk_begin(plan, seg + 1);
     const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
@@ -802,7 +803,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     } else {
         mo = mr;  // unused
     }
-    TCParams prm{T, plan.nseg, plan.nchunk, summ, prefix, O, status};
+    TCParams prm{T, plan.nseg, plan.nchunk, plan.seglen, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;
     auto kern = tc_walk_kernel<D, MODE, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

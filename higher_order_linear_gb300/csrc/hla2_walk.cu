@@ -81,10 +81,10 @@ walk_kernel(const Tin* __restrict__ Q, const Tin* __restrict__ K, const Tin* __r
     s.misc = s.part + (size_t)(kWalkThreads / mn) * mx;
 
     const int tid = threadIdx.x;
-    const int seg = blockIdx.x;
-    const int head = blockIdx.y;
-    const long long c0 = (long long)seg * plan.nchunk / plan.nseg;
-    const long long c1 = (long long)(seg + 1) * plan.nchunk / plan.nseg;
+    int head, seg;
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const long long c0 = seg_chunk_begin(plan, seg);
+    const long long c1 = seg_chunk_begin(plan, seg + 1);
     const int t0 = (int)(c0 * plan.granule);
     const int t1 = (int)min((long long)T, c1 * plan.granule);
     const size_t R = record_len(d, dv);
