@@ -351,13 +351,22 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 const bool first = c_begin + it == 0;
                 if (!wait_bar(CA, ph)) break;
                 tc_fence_after();
-                if (lane == 0) tma_store_wait_read();  // this warp's O piece has left its sA rows
+                // this warp's first O piece has left its sA rows (at D = 128 the
+                // second piece, staged in sY, may still be in flight)
+                if (lane == 0) {
+                    if (D == 128) tma_store_wait_read_all_but_1();
+                    else tma_store_wait_read();
+                }
                 __syncwarp();
                 if (first) drain128s(tA_, tA, tAl, true);  // A -> sA (hi), A_lo (masked)
                 else drain128(tA_, tA, true);              // A -> sA (masked)
                 drained(DA);
                 if (!wait_bar(CY, ph)) break;
                 tc_fence_after();
+                if (D == 128) {
+                    if (lane == 0) tma_store_wait_read();  // the second O piece has left its sY rows
+                    __syncwarp();
+                }
                 if (first) drainDs(tY_, tY, tYl);  // Y -> sY (hi), Y_lo
                 else drainD(tY_, tY);              // Y -> sY
                 drained(DY);
@@ -374,26 +383,13 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     uint32_t r[64];
                     tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
                     drained(DO);  // TMEM A is free once O sits in registers
-                    const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+                    // piece 0 through this warp's 4 KB of sA, piece 1 (D = 128) through the
+                    // same rows of sY: both dead once the output products (and K^T Y,
+                    // committed before them) completed
+                    const uint32_t wofs = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                     const int t0 = (c_begin + it) * kL + quarter * 32;
-#pragma unroll
-                    for (int g = 0; g < D / 64; ++g) {
-                        if (g > 0) {
-                            if (lane == 0) tma_store_wait_read();
-                            __syncwarp();
-                        }
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
-                                         r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
-                                         r[32 * g + 4 * q + 3]);
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_3d(&mO, scratch, cD + 32 * g, t0, head);
-                            tma_store_commit();
-                        }
-                    }
+                    box32_store(&mO, tA.base + wofs, r, lane, cD, t0, head);
+                    if (D == 128) box32_store(&mO, tY.base + wofs, r + 32, lane, cD + 32, t0, head);
                 }
                 if (state_rows && has_next) {
                     if (!wait_bar(CE, ph)) break;
