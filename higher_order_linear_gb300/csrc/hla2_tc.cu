@@ -31,6 +31,12 @@
 namespace hla2 {
 namespace {
 
+// Chunks ahead whose tiles a walk pulls into L2 before their TMA loads.  Zero:
+// on the headline (B1 H16 T65536 d128) prefetching one, two or four chunks
+// ahead made the output walk 4-8% slower; its loads are issued as early as
+// the single-buffered tiles allow and HBM is busy with the O stores.
+constexpr int kAhead = 0;
+
 // ------------------------------------------------------------- kernel ----
 struct TCParams {
     int T, nseg, nchunk, seglen;
@@ -180,6 +186,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
     };
+    auto prefetch = [&](int chunk) {
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) {
+            tma_prefetch_l2_3d(&mQ, k * 64, chunk * kL, head);
+            tma_prefetch_l2_3d(&mK, k * 64, chunk * kL, head);
+            tma_prefetch_l2_3d(&mV, k * 64, chunk * kL, head);
+        }
+    };
     // a drain warp announces that its share of a region is done
     auto drained = [&](int b) {
         fence_proxy_async();
@@ -236,14 +250,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
         if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
-        if (nchunks > 1) {
-#pragma unroll
-            for (int k = 0; k < D / 64; ++k) {
-                tma_prefetch_l2_3d(&mQ, k * 64, (c_begin + 1) * kL, head);
-                tma_prefetch_l2_3d(&mK, k * 64, (c_begin + 1) * kL, head);
-                tma_prefetch_l2_3d(&mV, k * 64, (c_begin + 1) * kL, head);
-            }
-        }
+        for (int a = 1; a < kAhead && a < nchunks; ++a) prefetch(c_begin + a);
     }
 
     // ---- initial state (mode 1): S0, P0 fp32 into TMEM, bf16 into smem ----
@@ -307,15 +314,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                // the tiles two chunks ahead start moving into L2 now
-                if (it + 2 < nchunks) {
-#pragma unroll
-                    for (int k = 0; k < D / 64; ++k) {
-                        tma_prefetch_l2_3d(&mQ, k * 64, (c + 2) * kL, head);
-                        tma_prefetch_l2_3d(&mK, k * 64, (c + 2) * kL, head);
-                        tma_prefetch_l2_3d(&mV, k * 64, (c + 2) * kL, head);
-                    }
-                }
+                // the tiles kAhead chunks ahead start moving into L2 now
+                if (kAhead > 0 && it + kAhead < nchunks) prefetch(c + kAhead);
                 // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
                 const bool qodd = MODE == 0 && (it & 1);
                 const Tile& tQc = qodd ? tQ2 : tQ;
