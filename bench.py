@@ -43,13 +43,10 @@ BYTES_PER_TOKEN_FWD = None  # set from the workload: 2*(2d+dv) + 4*dv
 # valid only for the kernel source it was taken on, keyed by (kernel, workload).
 # Captured on smaller cases of the same kernels and scaled by the units
 # processed (profiles/*.md give the commands and the raw figures):
-#  - output walk tc_walk_kernel<128,1,false> at full size (a one-pass metric
-#    set, so no scaling): 888.2 MB read + 496.5 MB written per launch;
 #  - decode step_kernel, 1024 heads: 204.0 + 143.3 = 347.3 MB; x4 heads.
 # Writes still in L2 when a kernel ends are not counted, so the write side
 # sits a little below the algorithmic bytes.
 NCU_TRAFFIC = {
-    ("tcgen05", "hla2-fwd-B1H16T65536-d128-bf16"): 888.2e6 + 496.5e6,
     ("step", "hla2-step-n4096-d128-fp32-prefill1024-steps512"): 4 * 347.3e6,
 }
 
