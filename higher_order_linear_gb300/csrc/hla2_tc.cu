@@ -328,6 +328,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                     mma_commit(bar(CA));
                     if (it > 0) {
+                        // this chunk's V: the previous chunk's X^T V was V's last read (the
+                        // load waits here, behind A, rather than holding up A at the end of
+                        // the previous chunk)
+                        if (!wait_bar(CP, pph)) break;
+                        issue_load(LV, &mV, tV, c);
+                    }
+                    if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
                         tc_fence_after();
                     }
@@ -407,10 +414,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
                     }
                     mma_commit(bar(CP));
-                    if (has_next) {
-                        if (!wait_bar(CP, ph)) break;
-                        issue_load(LV, &mV, tV, c + 1);  // V was last read by W V and X^T V
-                    }
                 } else {
                     if (it > 0) {
                         if (!wait_bar(DX, pph)) break;  // TMEM A (X of the previous chunk) read
@@ -419,6 +422,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // A = Q K^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                     mma_commit(bar(CA));
+                    if (it > 0) {
+                        // this chunk's V: the previous chunk's X^T V was V's last read
+                        if (!wait_bar(CP, pph)) break;
+                        issue_load(LV, &mV, tV, c);
+                    }
                     if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
                         tc_fence_after();
@@ -469,10 +477,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (it + 2 < nchunks) {
                         if (!wait_bar(CQ, ph)) break;
                         issue_load(qodd ? LQ2 : LQ, &mQ, tQc, c + 2);  // this buffer's next chunk
-                    }
-                    if (has_next) {
-                        if (!wait_bar(CP, ph)) break;
-                        issue_load(LV, &mV, tV, c + 1);
                     }
                 }
             }
