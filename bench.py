@@ -65,6 +65,8 @@ def parse():
     p.add_argument("--T", type=int, default=None, help="override T (profiling a smaller case; not a bench line)")
     p.add_argument("--H", type=int, default=None, help="override H (profiling a smaller case; not a bench line)")
     p.add_argument("--no-ahla", action="store_true", help="skip the AHLA forward and decode lines")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the unmasked and decayed forward and decode lines")
     p.add_argument("--decode-n", type=int, default=None,
                    help="override the number of decode heads (profiling a smaller case; not a bench line)")
     p.add_argument("--workload", type=int, default=FWD_WORKLOAD,
@@ -395,6 +397,35 @@ def main():
                              "frac": ach_a / peaks["hbm_gbs"], "traffic": None,
                              "kernel": "whole AHLA forward step (summaries + scan + outputs)"}}
 
+    # ---- the other operators on the same inputs: unmasked and decayed ----
+    # (CUDA-core walks; a few timed steps keep the run short)
+    variants = None
+    if not args.no_variants and fwd_steps:
+        variants = {}
+        gamma = 0.999
+        for name, call in (("unmasked", lambda: hla2.hla2_unmasked_forward(q, k, v, O, normalized=w.normalized,
+                                                                           workspace=ws)),
+                           ("decay", lambda: hla2.hla2_decay_forward(q, k, v, gamma, O, normalized=w.normalized,
+                                                                     workspace=ws))):
+            call()
+            barrier()
+            n_v = 3
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(n_v):
+                call()
+            ev1.record(stream)
+            barrier()
+            ms_v = max_over_ranks(ev0.elapsed_time(ev1) / n_v)
+            if hla2.hla2_device_status() != 0:
+                raise SystemExit(f"device status after {name}: {hla2.hla2_last_error_detail()}")
+            ach_v = bytes_per_token * tokens / (ms_v / 1e3) / 1e9
+            variants[name] = {"metric": f"{name} fwd tokens/s (B·H·T/s)", "value": replicas.job_throughput(tokens, world, ms_v),
+                              "unit": UNIT, "ms_per_step": ms_v, "steps": n_v, "path": "cuda-core",
+                              "roofline": {"bound": "alu", "hbm_frac": ach_v / peaks["hbm_gbs"],
+                                           "note": "fp32 CUDA-core walks; HBM fraction given for scale"}}
+        variants["decay"]["gamma"] = gamma
+
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
     if not args.no_e2e and not args.no_forward:
@@ -492,6 +523,32 @@ def main():
                                            "unit": "GB/s", "frac": ach_ah / peaks["hbm_gbs"],
                                            "bytes_per_head_step": bytes_ah}}
             pstate = astate
+        if not args.no_variants:
+            # unmasked (S | C | m) and decayed (S | P | p) decode steps on the same stream
+            Rp = hla2.pform_record_len(wd.d, wd.dv)
+            del pstate
+            for name, step in (("unmasked", lambda st, t: hla2.hla2_unmasked_step(st, *t, o=o)),
+                               ("decay", lambda st, t: hla2.hla2_decay_step(st, *t, 0.999, o=o))):
+                vstate = torch.zeros(wd.n, Rp, device=dev)
+                for t in range(64):  # the state's values do not change the work per step
+                    step(vstate, toks[t])
+                barrier()
+                e10 = torch.cuda.Event(enable_timing=True); e11 = torch.cuda.Event(enable_timing=True)
+                e10.record(stream)
+                for t in range(wd.prefill, wd.prefill + wd.steps):
+                    step(vstate, toks[t])
+                e11.record(stream)
+                barrier()
+                ms_s = max_over_ranks(e10.elapsed_time(e11) / wd.steps)
+                bytes_s = 8 * Rp + 4 * (2 * wd.d + 2 * wd.dv)
+                ach_s = wd.n * bytes_s / (ms_s / 1e3) / 1e9
+                decode[name] = {"metric": f"{name} decode tokens/s (heads*steps/s)",
+                                "value": world * wd.n / (ms_s / 1e3), "unit": "tokens/s", "ms_per_step": ms_s,
+                                "roofline": {"bound": "hbm", "achieved": ach_s, "peak": peaks["hbm_gbs"],
+                                             "unit": "GB/s", "frac": ach_s / peaks["hbm_gbs"],
+                                             "bytes_per_head_step": bytes_s}}
+                del vstate
+            pstate = None
         del toks, pstate
     clk = clocks.stop(t_begin, t_end)
 
@@ -506,7 +563,7 @@ def main():
                 "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
                 "config": fwd_config(w, segments_per_head(w.BH, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-                "cpu_baseline": cpu, "decode": decode, "ahla": ahla}
+                "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

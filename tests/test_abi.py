@@ -93,3 +93,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(hla2, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         hla2.lib()
+
+
+@pytest.mark.parametrize("B,H,T,d", [(1, 16, 65536, 128), (4, 16, 4096, 64), (2, 8, 2048, 64), (1, 1, 65536, 128),
+                                     (3, 1, 5000, 64), (1, 40, 200, 32), (1, 128, 16384, 128)])
+def test_bench_plan_mirror_matches_library(B, H, T, d):
+    """bench.py reports the segment plan from a Python copy of the library's
+    plan search; the workspace size (summaries, prefixes, totals, decay
+    factors) pins the two to the same segment count."""
+    import bench
+    nseg, seglen = bench.segments_per_head(B * H, T)
+    nchunk = (T + 127) // 128
+    assert (nchunk + seglen - 1) // seglen == nseg
+    R = d * d + 2 * d * d + 2 * d
+    up = lambda n: (n + 63) // 64 * 64
+    BH = B * H
+    expect = 4 * (2 * up(BH * nseg * R) + up(BH * R) + up(2 * nseg))
+    assert hla2.hla2_forward_workspace(B, H, T, d, d, hla2.HLA2_DTYPE_BF16) == expect
