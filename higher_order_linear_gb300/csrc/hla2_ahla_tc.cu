@@ -71,7 +71,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
     // (PB + w: drain warp w's prefix boxes, output walk)
-    enum { LQ, LK, LV, CA, CY, CQ, CO, CE, DA, DY, DO, DP, DE, PB, NBAR = PB + kDrainWarps };
+    enum { LQ, LK, LV, CA, CY, CQ, CO, CE, DA, DY, DO, DP, DE, FIN, PB, NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -345,6 +345,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     }
                 }
             }
+            if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
     } else {
         // ========================== drain warps ==========================

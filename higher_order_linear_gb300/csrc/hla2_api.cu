@@ -628,13 +628,20 @@ int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
     const SegPlan plan = forward_plan(BH, T);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
     const RecOff ro = summary_offsets(d, dv);
-    // segment sums S|C|m, their exclusive prefix sums (the combine has no
-    // cross term here), then the walks from the prefixes
-    cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 1, 1.0f, plan, s);
+    const bool use_tc = hla2_unmasked_forward_path(d, dv, dtype, normalized, state_out != nullptr) == 1;
+    int* status = nullptr;
+    if (use_tc && !(status = device_status_word())) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    // segment sums S|C|m (S|C on tensor cores), their exclusive prefix sums
+    // (the combine has no cross term here), then the walks from the prefixes
+    cudaError_t e = use_tc ? launch_unm_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, plan, status, s)
+                           : launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 1, 1.0f,
+                                         plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked segment sums");
-    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, ro.X, state_out ? ws.tot : nullptr, ro.R, s);
+    e = launch_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, use_tc ? ro.m : ro.X, state_out ? ws.tot : nullptr,
+                      ro.R, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked prefix sums");
-    e = launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 1, 1.0f, plan, s);
+    e = use_tc ? launch_unm_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, plan, status, s)
+               : launch_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, 1, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "unmasked segment outputs");
     if (state_out) {
         // final state S|C|m: the first d*d + d*dv + d floats of the totals
@@ -642,6 +649,12 @@ int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
         if (e != cudaSuccess) return cuda_fail(e, "unmasked state_out copy");
     }
     return HLA2_OK;
+}
+
+int hla2_unmasked_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return (!normalized && !with_state_out && tc_supported(d, dv, dtype, 0, dev)) ? 1 : 0;
 }
 
 int hla2_unmasked_step(float* state, const float* q, const float* k, const float* v, float* o, int n, int d, int dv,

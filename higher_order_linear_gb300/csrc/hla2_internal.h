@@ -184,6 +184,12 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
 cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const void* V,
                                 float* O, const float* prefix, float* summ,
                                 int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s);
+// Unmasked operator on tensor cores (hla2_unm_tc.cu), d = dv in {64, 128}, bf16,
+// unnormalised: mode 0 writes the S|C parts of the segment sums, mode 1 outputs
+// from the prefix S|C.
+cudaError_t launch_unm_tc_walk(int mode, const void* Q, const void* K, const void* V,
+                               float* O, const float* prefix, float* summ,
+                               int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s);
 // Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
 // (d = dv in {64, 128}, no extra column).
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);

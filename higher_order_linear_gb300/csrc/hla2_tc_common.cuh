@@ -220,6 +220,18 @@ __device__ __forceinline__ void put_row32_split2(const Tile& hi, const Tile& lo,
     for (int q = 0; q < 4; ++q) st_shared_v4(lo.chunk(r, b, c0 + q), l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
 }
 
+// Commits every tcgen05 operation this thread issued to `mbar` (one arrival,
+// used for nothing else, phase 0) and waits for them, at most kWaitNs, so that
+// no MMA is still writing tensor memory or reading shared memory when the CTA
+// releases them.  False when the wait ran out.
+__device__ __forceinline__ bool mma_wait_all(uint32_t mbar) {
+    mma_commit(mbar);
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try(mbar, 0))
+        if (globaltimer() - t0 > kWaitNs) return false;
+    return true;
+}
+
 // Load NC (32 or 64) consecutive TMEM columns of this thread's lane, one wait.
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) {

@@ -233,11 +233,19 @@ HLA2_API int hla2_ahla_step(float* state, const float* q, const float* k, const 
  * (hla2_forward_workspace) and errors as for hla2_forward, except state_out:
  *   state_out optional: [B*H][d*d + d*dv + d] fp32, per head S | C | m, the
  *             hla2_unmasked_step layout.
- * Runs on the CUDA-core segment walks (fp32 arithmetic).
+ * Implementation: see hla2_unmasked_forward_path.
  */
 HLA2_API int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
                                    int B, int H, int T, int d, int dv, int normalized, int dtype,
                                    void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * Which implementation hla2_unmasked_forward picks on the current device:
+ * 1 = tensor-core segment walks (tcgen05 with fp32 accumulators; bf16
+ * d = dv in {64, 128}, unnormalised, no state_out), 0 = CUDA-core segment
+ * walks (fp32 arithmetic).
+ */
+HLA2_API int hla2_unmasked_forward_path(int d, int dv, int dtype, int normalized, int with_state_out);
 
 /*
  * One decode step of the unmasked operator for n heads.

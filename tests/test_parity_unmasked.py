@@ -7,11 +7,20 @@ import torch
 
 import oracle
 from higher_order_linear_gb300 import hla2, workloads as W
-from tests._parity import TOL_NORMALIZED, TOL_STEP_FP32, f64, relerr
+from tests._parity import TOL_NORMALIZED, TOL_STEP_FP32, TOL_TC_BF16, f64, relerr
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 TOL_FP32 = 1e-4  # CUDA-core walks, fp32 arithmetic from exact inputs
+
+
+def tol(dtype, d, dv, norm):
+    """Tensor-core walks (bf16 operands) get the bf16 bound, the CUDA-core
+    walks the fp32 one, the normalised variant its own."""
+    if norm:
+        return TOL_NORMALIZED
+    code = hla2.HLA2_DTYPE_BF16 if dtype == torch.bfloat16 else hla2.HLA2_DTYPE_F32
+    return TOL_TC_BF16 if hla2.lib().hla2_unmasked_forward_path(d, dv, code, 0, 0) == 1 else TOL_FP32
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,12 +64,43 @@ def ref(q, k, v, normalized=False):
 def test_forward_shapes(B, H, T, d, dv, dtype, norm):
     q, k, v = inputs(B, H, T, d, dv, dtype, norm, seed=B * 1000 + H * 100 + T + d + 9)
     got = run_gpu(q, k, v, normalized=norm)
-    assert relerr(f64(got), ref(q, k, v, norm)) < (TOL_NORMALIZED if norm else TOL_FP32)
+    assert relerr(f64(got), ref(q, k, v, norm)) < tol(dtype, d, dv, norm)
+
+
+def test_tensor_core_path_selected():
+    L = hla2.lib()
+    assert L.hla2_unmasked_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
+    assert L.hla2_unmasked_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 0, 0) == 1
+    assert L.hla2_unmasked_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 0) == 0   # normalised: CUDA cores
+    assert L.hla2_unmasked_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 1) == 0  # state_out: CUDA cores
+    assert L.hla2_unmasked_forward_path(128, 64, hla2.HLA2_DTYPE_BF16, 0, 0) == 0
+    assert L.hla2_unmasked_forward_path(64, 64, hla2.HLA2_DTYPE_F32, 0, 0) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 127, 128, 129, 383, 2000, 5000])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_walk_lengths(T, d):
+    """Chunk boundaries, ragged tails, the split first chunk and multi-segment
+    heads on the tcgen05 unmasked walks."""
+    q, k, v = inputs(1, 3, T, d, d, torch.bfloat16, False, seed=T * 17 + d)
+    got = run_gpu(q, k, v)
+    assert relerr(f64(got), ref(q, k, v)) < TOL_TC_BF16
+
+
+def test_tensor_core_matches_cuda_core_walk():
+    """The tcgen05 walk and the fp32 CUDA-core walk (reached through
+    state_out) agree on the same bf16 inputs within the bf16 bound."""
+    q, k, v = inputs(2, 2, 1500, 128, 128, torch.bfloat16, False, seed=31)
+    tc = run_gpu(q, k, v)
+    st = torch.empty(4, hla2.unmasked_state_len(128, 128), device=DEV)
+    cc = run_gpu(q, k, v, state_out=st)
+    assert relerr(f64(tc), f64(cc)) < TOL_TC_BF16
 
 
 def test_workload1_full():
-    q, k, v = W.make_inputs(W.WORKLOADS[1])
-    assert relerr(f64(run_gpu(q, k, v)), ref(q, k, v)) < TOL_FP32
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w)
+    assert relerr(f64(run_gpu(q, k, v)), ref(q, k, v)) < tol(q.dtype, w.d, w.dv, False)
 
 
 def test_workload2_normalized_full():
