@@ -423,11 +423,14 @@ def main():
             if hla2.hla2_device_status() != 0:
                 raise SystemExit(f"device status after {name}: {hla2.hla2_last_error_detail()}")
             ach_v = bytes_per_token * tokens / (ms_v / 1e3) / 1e9
-            tc_v = name == "unmasked" and L.hla2_unmasked_forward_path(w.d, w.dv, dcode, int(w.normalized), 0) == 1
+            if name == "unmasked":
+                tc_v = L.hla2_unmasked_forward_path(w.d, w.dv, dcode, int(w.normalized), 0) == 1
+            else:
+                tc_v = L.hla2_decay_forward_path(w.d, w.dv, dcode, int(w.normalized), 0, gamma) == 1
             if tc_v:
                 roof_v = {"bound": "hbm", "achieved": ach_v, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": ach_v / peaks["hbm_gbs"], "traffic": None,
-                          "kernel": "whole unmasked forward step (sums + scan + outputs)"}
+                          "kernel": f"whole {name} forward step (summaries + scan + outputs)"}
             else:
                 roof_v = {"bound": "alu", "hbm_frac": ach_v / peaks["hbm_gbs"],
                           "note": "fp32 CUDA-core walks; HBM fraction given for scale"}

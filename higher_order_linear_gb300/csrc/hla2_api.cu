@@ -651,6 +651,12 @@ int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
     return HLA2_OK;
 }
 
+int hla2_decay_forward_path(int d, int dv, int dtype, int normalized, int with_state_out, float gamma) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return (!normalized && !with_state_out && decay_tc_gamma_ok(gamma) && tc_supported(d, dv, dtype, 0, dev)) ? 1 : 0;
+}
+
 int hla2_unmasked_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -688,7 +694,44 @@ int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, in
     const int BH = B * H;
     const SegPlan plan = forward_plan(BH, T);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
-    // P-form segment summaries with decay, the decayed sequential scan, walks
+    const bool use_tc = hla2_decay_forward_path(d, dv, dtype, normalized, state_out != nullptr, gamma) == 1;
+    int* status = nullptr;
+    if (use_tc && !(status = device_status_word())) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    if (use_tc) {
+        // tensor cores: segment summaries S|C|.|P|. from the walks, the decayed
+        // scan of S, the cross terms f_r S_<r C_r on tensor cores, the decayed
+        // scan of P with f_r^2, then the output walks
+        const RecOff ro = summary_offsets(d, dv);
+        cudaError_t e = launch_decay_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, gamma, plan, status, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay segment summaries");
+        e = launch_decay_factors(ws.fac, T, gamma, plan, s);
+        if (e == cudaSuccess)
+            e = launch_decay_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, (size_t)d * d, nullptr, ro.R, ws.fac, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of S");
+        CrossArgs a{};
+        a.A = ws.prefix + ro.S; a.sA = (long long)ro.R;
+        a.B = ws.summ + ro.C;   a.sB = (long long)ro.R;
+        a.base = ws.summ + ro.X; a.sbase = (long long)ro.R;
+        a.out = ws.prefix + ro.X; a.sout = (long long)ro.R;
+        a.alpha = 1.f; a.d = d; a.dv = dv; a.status = status;
+        a.pscale = ws.fac; a.pscale_mod = plan.nseg;
+        for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
+            CrossArgs c = a;
+            const long long nb = (long long)BH * plan.nseg - b0;
+            c.nb = (int)(nb < 65535 ? nb : 65535);
+            c.pscale_off = b0;
+            c.A += b0 * ro.R; c.B += b0 * ro.R; c.base += b0 * ro.R; c.out += b0 * ro.R;
+            e = launch_tc_cross(c, s);
+            if (e != cudaSuccess) return cuda_fail(e, "decay scan: cross terms");
+        }
+        e = launch_decay_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, (size_t)d * dv, nullptr, ro.R,
+                                ws.fac + plan.nseg, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of P");
+        e = launch_decay_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, gamma, plan, status, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay segment outputs");
+        return HLA2_OK;
+    }
+    // P-form segment summaries with decay, the decayed scan, walks
     cudaError_t e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, gamma,
                                 plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "decay segment summaries");

@@ -1,0 +1,695 @@
+// hla2_decay_tc.cu -- tensor-core segment walks of the exponentially decayed
+// masked operator on GB300 (sm_103a): tcgen05.mma with TMEM accumulators,
+// TMA tiles.
+//
+// Operator (HLA summary, arXiv 2510.27258, section 4 names decayed operators
+// among those the scan covers): every prefix moment decays by gamma per token,
+//   S_t = g S + k k^T,   P_t = g^2 P + S_t q_t v_t^T,   o_t = q_t^T P_t,
+// i.e. o_t = sum_{i<=j<=t} g^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j (P = S C - G).
+//
+// Chunk form.  For a chunk of L tokens (local index t, 128 rows, L real) with
+// the state (S0, P0) at its start, a_t = g^{t+1}, b_t = g^{L-1-t}:
+//   X^g_t = a_t S0 q_t + sum_{i<=t} g^{t-i} (q_t.k_i) k_i      (= S_t q_t)
+//   o_t   = a_t^2 q_t^T P0 + sum_{j<=t} g^{2(t-j)} (q_t.X^g_j) v_j
+//   S'    = g^L S0 + K^T diag(b) K,   P' = g^{2L} P0 + X^g^T diag(b^2) V.
+// Every per-token factor is moved into an operand that is rounded to bf16
+// anyway, or into a factor common to a whole accumulator row, so that Q, K, V
+// enter the products exactly:
+//   A~  = tril(Q K^T) * g^{-(i+1)}            (column factor)
+//   X'  = Q S0 + A~ K                          (= X^g_t / a_t)
+//   sX  = g^{2L-1-t} X'_t                      (= b_t^2 X^g_t: the P update's operand)
+//   W~  = g^{-2L} tril(Q sX^T)                 (constant factor)
+//   O'  = Q P0 + W~ V,  o_t = g^{2(t+1)} O'_t  (row factor)
+//   S  += (diag(b) K)^T K after TMEM S was scaled by g^L (P by g^{2L}).
+// The negative powers stay within g^{-2L}; with g >= 0.8 every intermediate is
+// a finite fp32 / bf16 number (products too small to represent only drop terms
+// that are negligible against the output).  W~ is split into bf16 hi + lo on
+// every chunk (the lo part packed in tensor memory), and on a head's first
+// chunk A~ and sX are split as well.
+//
+// Summary walk (mode 0): per segment S (running), and C, P accumulated in the
+// frame of the segment's last token: chunk c contributes with the factor
+// F_c = g^{(tokens of the segment after chunk c)}, C += Q^T diag(F_c b) V,
+// P += (F_c^2 b^2 X^g)^T V, so neither needs rescaling from chunk to chunk.
+//
+// Roles as in the other walks: warp 8 (lane 0) issues every copy and MMA,
+// warps 0..7 drain tensor memory; they meet only on mbarriers, every wait
+// bounded in time.
+#include <cmath>
+
+#include "hla2_tc_common.cuh"
+
+namespace hla2 {
+namespace {
+
+struct DParams {
+    int T, nseg, nchunk, seglen;
+    float lg;  // log2(gamma)
+    int* status;
+};
+
+__device__ __forceinline__ float gpow(float lg, float n) { return exp2f(n * lg); }
+__device__ __forceinline__ int chunk_len(int T, int c) { return min(kL, T - c * kL); }
+
+// 32 fp32 values (columns col0.., row r, scaled in place) times a column
+// factor cf[col] (and a scalar s), optionally masked to columns <= r, written
+// as bf16 (hi) to `hi` and, when split is set, the rounding remainder to `lo`.
+__device__ __forceinline__ void put_row32_cf(const Tile& hi, const Tile& lo, bool split, int r, int col0, uint32_t* v,
+                                             const float* cf, float s, bool mask) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float f = __uint_as_float(v[j]) * (cf ? cf[col0 + j] : 1.f) * s;
+        if (mask && col0 + j > r) f = 0.f;
+        v[j] = __float_as_uint(f);
+    }
+    if (split) put_row32_split2(hi, lo, r, col0, v, false);
+    else put_row32(hi, r, col0, v, false);
+}
+
+// Row r, columns [col0, col0 + 8n) of bf16 tile `src`, times s, to the same
+// place of tile `dst` (same geometry).
+template <int N8>
+__device__ __forceinline__ void scale_row(const Tile& src, const Tile& dst, int r, int col0, float s) {
+#pragma unroll
+    for (int q = 0; q < N8; ++q) {
+        const int col = col0 + 8 * q;
+        const uint32_t a = src.chunk(r, col >> 6, (col & 63) >> 3);
+        uint32_t w[4];
+        ld_shared_v4(a, w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+            w[h] = pack_bf16(__low2float(p) * s, __high2float(p) * s);
+        }
+        st_shared_v4(dst.chunk(r, col >> 6, (col & 63) >> 3), w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ------------------------------------------------------------- outputs ----
+template <int D>
+struct DOutLayout {
+    static constexpr uint32_t kTok = kL * D * 2;  // Q, K, V, X tiles
+    static constexpr uint32_t kSq = kL * kL * 2;  // A~ / W~ tile
+    static constexpr uint32_t kSt = D * D * 2;    // S0 / P0 tiles
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq;
+    static constexpr uint32_t S = X + kTok, P = S + kSt;
+    static constexpr uint32_t kEnd = P + kSt;
+    // a head's first chunk: A~_lo in the S0 tile and sX_lo in the P0 tile at
+    // D = 128 (the state is zero there); own tiles at D = 64
+    static constexpr uint32_t Alo = (D == 128) ? S : kEnd;
+    static constexpr uint32_t Xlo = (D == 128) ? P : kEnd + kSq;
+    static constexpr uint32_t kEnd2 = (D == 128) ? kEnd : kEnd + kSq + kTok;
+    static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
+    static constexpr uint32_t kBytes = kEnd2 + kPad;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
+                    const __grid_constant__ CUtensorMap mR, DParams p) {
+    using LY = DOutLayout<D>;
+    extern __shared__ __align__(1024) unsigned char dsm_raw[];
+    enum { LQ, LK, LV, CA, CX, CW, CO, CP, DA, DX, DW, DO, DS, DP, FIN, PB, NBAR = PB + kDrainWarps };
+    __shared__ __align__(8) unsigned long long bars[NBAR];
+    __shared__ float colf[kL];  // g^{-(i+1)}
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer = warp == kDrainWarps;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int row = quarter * 32 + lane;
+    int head, seg;
+    const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
+    const int nchunks = c_end - c_begin;
+    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
+    const float lg = p.lg;
+
+    const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
+    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
+    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
+    const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
+    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL};
+    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
+
+    if (tid < kL) colf[tid] = gpow(lg, -(float)(tid + 1));
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t cnt = 1;
+            if (i == DA || i == DX || i == DW || i == DO) cnt = kDrainWarps;
+            if (i == DS || i == DP) cnt = kStateWarps;
+            mbar_init(bar(i), cnt);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    // tensor memory: A~, then W', then O' | X', then packed W~_lo | S | P
+    const uint32_t tA_ = tmem + 0, tX_ = tmem + 128, tS_ = tmem + 256, tP_ = tmem + 256 + D;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c128 = half * 64;
+    const int cD = half * (D / 2);
+    // packed W~_lo: warp half h holds W columns [64h, 64h + 64) as 32 packed
+    // columns at X' column h * D/2 (a K-step ks reads 8 of them)
+    auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * (D / 2) + 8 * (ks & 3)); };
+
+    constexpr uint32_t kTileBytes = kL * D * 2;
+    auto wait_bar = [&](int b, uint32_t parity) -> bool {
+        const uint32_t a = bar(b);
+        if (abort_flag) return false;
+        if (mbar_try(a, parity)) return true;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try(a, parity)) {
+            if (abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                abort_flag = 1;
+                atomicExch(p.status, (int)kDevWaitTimeout);
+                return false;
+            }
+        }
+        return true;
+    };
+    auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        mbar_expect_tx(bar(b), kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
+    };
+    auto drained = [&](int b) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
+    };
+    // TMEM state rows (D columns of this warp's half) -> bf16 tile; the TMEM
+    // copy is multiplied by `decay` for the next chunk's update
+    auto drain_state = [&](uint32_t treg, const Tile& t, float decay) {
+        uint32_t r[64];
+        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        put_row32(t, row, cD, r, false);
+        if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
+#pragma unroll
+        for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+        tmem_st32(treg + lane_off + cD, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        if (D == 128) tmem_st32(treg + lane_off + cD + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_st_wait();
+    };
+
+    if (issuer && lane == 0 && nchunks > 0) {
+        issue_load(LQ, &mQ, tQ, c_begin);
+        issue_load(LK, &mK, tK, c_begin);
+        issue_load(LV, &mV, tV, c_begin);
+    }
+    // ---- initial state: S0 (record row 0), P0 (record row 2D+1) by bulk
+    // tensor loads into per-warp staging in the A / X tiles; bf16 copies as
+    // they are, TMEM copies decayed over the first chunk (g^L, g^{2L})
+    if (state_rows && nchunks > 0) {
+        const int rec = head * p.nseg + seg;
+        const float L0 = (float)chunk_len(p.T, c_begin);
+        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+#pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
+#pragma unroll
+                for (int g = 0; g < D / 64; ++g)
+                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? 0 : 2 * D + 1) + quarter * 32,
+                                rec, bar(PB + warp));
+            }
+            __syncwarp();
+            if (!wait_bar(PB + warp, (uint32_t)m)) break;
+            const float decay = gpow(lg, (m == 0 ? 1.f : 2.f) * L0);
+#pragma unroll
+            for (int g = 0; g < D / 64; ++g) {
+                const int cb = cD + 32 * g;
+                uint32_t r[32];
+                box32_read(stage + (uint32_t)g * 4096u, lane, r);
+                put_row32(m == 0 ? tS : tP, row, cb, r, false);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+                tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cb, r);
+            }
+            __syncwarp();
+        }
+        tmem_st_wait();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
+    constexpr uint32_t iKK = idesc_bf16(128, D, false, false);    // N = D, both K-major
+    constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
+    constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
+
+    if (issuer) {
+        // ============================ issuer ============================
+        if (lane == 0 && nchunks > 0) {
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1, pph = (it + 1) & 1;
+                const bool has_next = it + 1 < nchunks;
+                const bool first = c == 0;  // S0 = P0 = 0; A~ and sX split into hi + lo
+                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
+                if (it > 0 && !wait_bar(DO, pph)) break;  // O' of the previous chunk read out of TMEM A
+                tc_fence_after();
+                // A = Q K^T
+                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                mma_commit(bar(CA));
+                if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0; TMEM S decayed
+                if (!wait_bar(DA, ph)) break;              // sA = A~ (A~_lo), sX = diag(b) K
+                tc_fence_after();
+                // X' = Q S0 + A~ K ; S += (diag(b) K)^T K
+                if (!first)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                if (first)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                if (has_next)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tX.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                mma_commit(bar(CX));
+                if (has_next) {
+                    if (!wait_bar(CX, ph)) break;
+                    issue_load(LK, &mK, tK, c + 1);  // K was last read by A~ K and the S update
+                }
+                if (!wait_bar(DX, ph)) break;  // sX = g^{2L-1-t} X' (and its lo part); TMEM X' read
+                tc_fence_after();
+                // W' = Q sX^T
+                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tX.kmaj(ks), iSq, ks > 0);
+                if (first)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tXl.kmaj(ks), iSq, 1);
+                mma_commit(bar(CW));
+                if (!wait_bar(DW, ph)) break;              // sA = W~_hi, TMEM X' columns = W~_lo; TMEM A read
+                if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P0; TMEM P decayed
+                tc_fence_after();
+                // O' = Q P0 + W~_hi V + W~_lo V
+                if (!first)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
+                if (!wait_bar(LV, ph)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
+                mma_commit(bar(CO));
+                if (has_next) {
+                    // P += sX^T V
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CP));
+                    if (!wait_bar(CO, ph)) break;
+                    issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q P0
+                    if (!wait_bar(CP, ph)) break;
+                    issue_load(LV, &mV, tV, c + 1);  // V was last read by the P update
+                }
+            }
+            if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
+    } else {
+        // ========================== drain warps ==========================
+        for (int it = 0; it < nchunks; ++it) {
+            const int c = c_begin + it;
+            const uint32_t ph = it & 1, pph = (it + 1) & 1;
+            const bool has_next = it + 1 < nchunks;
+            const bool first = c == 0;
+            const float L = (float)chunk_len(p.T, c);
+            if (!wait_bar(CA, ph)) break;
+            if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
+            tc_fence_after();
+            // this warp's O pieces have left sA and sX
+            if (lane == 0) tma_store_wait_read();
+            __syncwarp();
+            {
+                // A~ = tril(A) g^{-(i+1)} -> sA (A~_lo -> its tile on the first chunk)
+                uint32_t r[64];
+                tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                put_row32_cf(tA, tAl, first, row, c128, r, colf, 1.f, true);
+                put_row32_cf(tA, tAl, first, row, c128 + 32, r + 32, colf, 1.f, true);
+            }
+            // diag(b) K -> sX (row = token; b = g^{L-1-t})
+            scale_row<D / 16>(tK, tX, row, cD, gpow(lg, L - 1.f - (float)row));
+            drained(DA);
+            if (!wait_bar(CX, ph)) break;
+            tc_fence_after();
+            {
+                // sX = g^{2L-1-t} X'  (hi, and lo on the first chunk)
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(tX_ + lane_off + cD, r);
+                const float xs = gpow(lg, 2.f * L - 1.f - (float)row);
+                put_row32_cf(tX, tXl, first, row, cD, r, nullptr, xs, false);
+                if (D == 128) put_row32_cf(tX, tXl, first, row, cD + 32, r + 32, nullptr, xs, false);
+            }
+            drained(DX);
+            if (state_rows && has_next) {
+                drain_state(tS_, tS, gpow(lg, (float)chunk_len(p.T, c + 1)));  // S0 of the next chunk
+                drained(DS);
+            }
+            if (!wait_bar(CW, ph)) break;
+            tc_fence_after();
+            {
+                // W~ = g^{-2L} tril(W'): hi -> sA, lo packed -> TMEM over this warp's X' columns
+                // (32 columns at a time to bound the live registers)
+                uint32_t lo[32];
+                const float ws = gpow(lg, -2.f * L);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[32];
+                    tmem_ld32(tA_ + lane_off + c128 + 32 * hh, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * ws);
+                    put_row32_split(tA, row, c128 + 32 * hh, r, true, lo + 16 * hh);
+                }
+                tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);
+                tmem_st_wait();
+            }
+            drained(DW);
+            if (!wait_bar(CO, ph)) break;
+            tc_fence_after();
+            {
+                // o_t = g^{2(t+1)} O'_t: piece 0 through this warp's 4 KB of sA,
+                // piece 1 (D = 128) through the same rows of sX once the P update has read it
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                drained(DO);
+                const float os = gpow(lg, 2.f * (float)(row + 1));
+#pragma unroll
+                for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * os);
+                const uint32_t wofs = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+                const int t0 = c * kL + quarter * 32;
+                box32_store(&mO, tA.base + wofs, r, lane, cD, t0, head);
+                if (D == 128) {
+                    if (has_next && !wait_bar(CP, ph)) break;
+                    tc_fence_after();
+                    box32_store(&mO, tX.base + wofs, r + 32, lane, cD + 32, t0, head);
+                }
+            }
+            if (state_rows && has_next) {
+                if (!wait_bar(CP, ph)) break;
+                tc_fence_after();
+                drain_state(tP_, tP, gpow(lg, 2.f * (float)chunk_len(p.T, c + 1)));  // P0 of the next chunk
+                drained(DP);
+            }
+        }
+        if (lane == 0) tma_store_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ----------------------------------------------------------- summaries ----
+template <int D>
+struct DSumLayout {
+    static constexpr uint32_t kTok = kL * D * 2;
+    static constexpr uint32_t kSq = kL * kL * 2;
+    static constexpr uint32_t kSt = D * D * 2;
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq, S = X + kTok;
+    static constexpr uint32_t kEnd = S + kSt;
+    static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
+    static constexpr uint32_t kBytes = kEnd + kPad;
+    static_assert(kEnd >= 8u * 3u * (D / 64) * 4096u || D < 128, "record staging must fit the tiles");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mR, DParams p) {
+    using LY = DSumLayout<D>;
+    extern __shared__ __align__(1024) unsigned char dsm_raw[];
+    enum { LQ, LK, LV, CA, CX, CC, CP, DA, DX, DV, DS, FIN, NBAR };
+    __shared__ __align__(8) unsigned long long bars[NBAR];
+    __shared__ float colf[kL];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer = warp == kDrainWarps;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int row = quarter * 32 + lane;
+    int head, seg;
+    const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
+    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
+    const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
+    const int nchunks = c_end - c_begin;
+    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
+    const float lg = p.lg;
+    const int seg_end_tok = min(p.T, c_end * kL);
+
+    const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
+    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
+    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tS{dsm + LY::S, D};
+    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
+
+    if (tid < kL) colf[tid] = gpow(lg, -(float)(tid + 1));
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t cnt = 1;
+            if (i == DA || i == DX || i == DV) cnt = kDrainWarps;
+            if (i == DS) cnt = kStateWarps;
+            mbar_init(bar(i), cnt);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    // tensor memory: A~, then X' | S (running) | C, P (segment-end frame)
+    const uint32_t tA_ = tmem + 0, tS_ = tmem + 128, tC_ = tmem + 128 + D, tP_ = tmem + 128 + 2 * D;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c128 = half * 64;
+    const int cD = half * (D / 2);
+
+    constexpr uint32_t kTileBytes = kL * D * 2;
+    auto wait_bar = [&](int b, uint32_t parity) -> bool {
+        const uint32_t a = bar(b);
+        if (abort_flag) return false;
+        if (mbar_try(a, parity)) return true;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try(a, parity)) {
+            if (abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                abort_flag = 1;
+                atomicExch(p.status, (int)kDevWaitTimeout);
+                return false;
+            }
+        }
+        return true;
+    };
+    auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        mbar_expect_tx(bar(b), kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
+    };
+    auto drained = [&](int b) {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
+    };
+
+    constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t iKK = idesc_bf16(128, D, false, false);
+    constexpr uint32_t iKM = idesc_bf16(128, D, false, true);
+    constexpr uint32_t iMM = idesc_bf16(128, D, true, true);
+
+    if (issuer) {
+        if (lane == 0 && nchunks > 0) {
+            issue_load(LQ, &mQ, tQ, c_begin);
+            issue_load(LK, &mK, tK, c_begin);
+            issue_load(LV, &mV, tV, c_begin);
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1, pph = (it + 1) & 1;
+                const bool has_next = it + 1 < nchunks;
+                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
+                if (it > 0 && !wait_bar(DX, pph)) break;  // TMEM A (X' of the previous chunk) read
+                tc_fence_after();
+                // A = Q K^T
+                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                mma_commit(bar(CA));
+                if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0; TMEM S decayed
+                if (!wait_bar(DA, ph)) break;              // sA = A~, sX = diag(b) K
+                tc_fence_after();
+                // X' = Q S0 + A~ K   (S0 = 0 on the segment's first chunk) ; S += (diag(b) K)^T K
+                if (it > 0)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tS_, tX.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CX));
+                if (has_next) {
+                    if (!wait_bar(CX, ph)) break;
+                    issue_load(LK, &mK, tK, c + 1);
+                }
+                if (!wait_bar(DV, ph)) break;  // sA = diag(F b) V
+                tc_fence_after();
+                // C += Q^T diag(F b) V
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tC_, tQ.mnmaj(ks), tA.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CC));
+                if (!wait_bar(DX, ph)) break;  // sX = F^2 g^{2L-1-t} X'
+                tc_fence_after();
+                // P += sX^T V
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CP));
+                if (has_next) {
+                    if (!wait_bar(CC, ph)) break;
+                    issue_load(LQ, &mQ, tQ, c + 1);
+                    if (!wait_bar(CP, ph)) break;
+                    issue_load(LV, &mV, tV, c + 1);
+                }
+            }
+            // FIN completes once every product has: the records can be read out
+            if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
+    } else if (nchunks > 0) {
+        // ========================== drain warps ==========================
+        for (int it = 0; it < nchunks; ++it) {
+            const int c = c_begin + it;
+            const uint32_t ph = it & 1, pph = (it + 1) & 1;
+            const bool has_next = it + 1 < nchunks;
+            const float L = (float)chunk_len(p.T, c);
+            const float F = gpow(lg, (float)(seg_end_tok - min(p.T, (c + 1) * kL)));
+            if (!wait_bar(CA, ph)) break;
+            // sA and sX of the previous chunk were read by its C and P updates
+            if (it > 0 && (!wait_bar(CC, pph) || !wait_bar(CP, pph))) break;
+            tc_fence_after();
+            {
+                uint32_t r[64];
+                tmem_ld_cols<64>(tA_ + lane_off + c128, r);
+                put_row32_cf(tA, tA, false, row, c128, r, colf, 1.f, true);
+                put_row32_cf(tA, tA, false, row, c128 + 32, r + 32, colf, 1.f, true);
+            }
+            scale_row<D / 16>(tK, tX, row, cD, gpow(lg, L - 1.f - (float)row));
+            drained(DA);
+            if (!wait_bar(CX, ph)) break;
+            tc_fence_after();
+            {
+                // sX = F^2 g^{2L-1-t} X'
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                const float xs = F * F * gpow(lg, 2.f * L - 1.f - (float)row);
+                put_row32_cf(tX, tX, false, row, cD, r, nullptr, xs, false);
+                if (D == 128) put_row32_cf(tX, tX, false, row, cD + 32, r + 32, nullptr, xs, false);
+            }
+            drained(DX);
+            if (!wait_bar(LV, ph)) break;
+            // diag(F b) V -> sA (A~ was read by X')
+            scale_row<D / 16>(tV, tA, row, cD, F * gpow(lg, L - 1.f - (float)row));
+            drained(DV);
+            if (state_rows && has_next) {
+                // S0 of the next chunk -> sS; TMEM S decayed over the next chunk
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(tS_ + lane_off + cD, r);
+                put_row32(tS, row, cD, r, false);
+                if (D == 128) put_row32(tS, row, cD + 32, r + 32, false);
+                const float decay = gpow(lg, (float)chunk_len(p.T, c + 1));
+#pragma unroll
+                for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+                tmem_st32(tS_ + lane_off + cD, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                if (D == 128) tmem_st32(tS_ + lane_off + cD + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_st_wait();
+                drained(DS);
+            }
+        }
+        // records S (row 0), C (row D), P (row 2D+1) through the dead tiles once
+        // every product has completed
+        if (state_rows && !abort_flag && wait_bar(FIN, 0)) {
+            tc_fence_after();
+            const uint32_t src[3] = {tS_, tC_, tP_};
+            const int rows0[3] = {0, D, 2 * D + 1};
+            const uint32_t scratch = dsm + (uint32_t)warp * (3u * (D / 64) * 4096u);
+            const int rec = head * p.nseg + seg;
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                uint32_t r[64];
+                tmem_ld_cols<D / 2>(src[m] + lane_off + cD, r);
+#pragma unroll
+                for (int g = 0; g < D / 64; ++g)
+                    box32_store(&mR, scratch + (uint32_t)(m * (D / 64) + g) * 4096u, r + 32 * g, lane, cD + 32 * g,
+                                rows0[m] + quarter * 32, rec);
+            }
+            if (lane == 0) tma_store_wait_all();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+template <int D>
+cudaError_t launch_d(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
+                     float* summ, int BH, int T, float gamma, SegPlan plan, int* status, cudaStream_t s) {
+    CUtensorMap mq, mk, mv, mo, mr;
+    if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
+        !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
+        !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
+        return cudaErrorInvalidValue;
+    if (!make_map(&mr, mode == 1 ? static_cast<const void*>(prefix) : static_cast<const void*>(summ),
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+        return cudaErrorInvalidValue;
+    DParams prm{T, plan.nseg, plan.nchunk, plan.seglen, (float)std::log2((double)gamma), status};
+    dim3 grid(plan.nseg, BH);
+    cudaError_t e;
+    if (mode == 0) {
+        const size_t smem = DSumLayout<D>::kBytes + 1024;
+        auto kern = decay_tc_sum_kernel<D>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mr, prm);
+    } else {
+        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
+        const size_t smem = DOutLayout<D>::kBytes + 1024;
+        auto kern = decay_tc_out_kernel<D>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decay_tc_gamma_ok(float gamma) { return gamma >= kDecayTcMinGamma && gamma <= 1.f; }
+
+cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
+                                 float* summ, int BH, int T, int d, int dv, float gamma, SegPlan plan, int* status,
+                                 cudaStream_t s) {
+    if (BH == 0 || plan.nseg == 0) return cudaSuccess;
+    if (plan.granule != kL || d != dv || !decay_tc_gamma_ok(gamma)) return cudaErrorInvalidValue;
+    if (d == 128) return launch_d<128>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
+    if (d == 64) return launch_d<64>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hla2

@@ -150,8 +150,8 @@ struct CrossArgs {
     float alpha;
     int d, dv, nb;
     int* status;  // device status word (tensor-core variant's bounded wait)
-    // optional per-item scale of the product (fp32 kernel only): item i of the
-    // batch uses pscale[(pscale_off + i) % pscale_mod]
+    // optional per-item scale of the product: item i of the batch uses
+    // pscale[(pscale_off + i) % pscale_mod]
     const float* pscale;
     long long pscale_off;
     int pscale_mod;
@@ -190,6 +190,15 @@ cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const vo
 cudaError_t launch_unm_tc_walk(int mode, const void* Q, const void* K, const void* V,
                                float* O, const float* prefix, float* summ,
                                int BH, int T, int d, int dv, SegPlan plan, int* status, cudaStream_t s);
+// Decayed operator on tensor cores (hla2_decay_tc.cu), d = dv in {64, 128},
+// bf16, unnormalised, gamma in [kDecayTcMinGamma, 1]: mode 0 writes the S|C|.|P|.
+// parts of the segment summaries, mode 1 outputs from the prefix S|.|.|P|.
+constexpr float kDecayTcMinGamma = 0.8f;
+bool decay_tc_gamma_ok(float gamma);
+cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const void* V,
+                                 float* O, const float* prefix, float* summ,
+                                 int BH, int T, int d, int dv, float gamma, SegPlan plan, int* status,
+                                 cudaStream_t s);
 // Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
 // (d = dv in {64, 128}, no extra column).
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);

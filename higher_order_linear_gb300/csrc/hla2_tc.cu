@@ -761,12 +761,15 @@ __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
         tmem_ld_cols<D / 2>(tmem + ((uint32_t)(quarter * 32) << 16) + cD, r);
         const float* base = a.base + b * a.sbase;
         float* out = a.out + b * a.sout;
+        const float sc = a.pscale ? a.pscale[(a.pscale_off + b) % a.pscale_mod] : 1.f;
 #pragma unroll
         for (int j = 0; j < D / 2; j += 4) {
             const float4 x = *reinterpret_cast<const float4*>(base + (size_t)row * D + cD + j);
             *reinterpret_cast<float4*>(out + (size_t)row * D + cD + j) =
-                make_float4(fmaf(a.alpha, x.x, __uint_as_float(r[j])), fmaf(a.alpha, x.y, __uint_as_float(r[j + 1])),
-                            fmaf(a.alpha, x.z, __uint_as_float(r[j + 2])), fmaf(a.alpha, x.w, __uint_as_float(r[j + 3])));
+                make_float4(fmaf(a.alpha, x.x, sc * __uint_as_float(r[j])),
+                            fmaf(a.alpha, x.y, sc * __uint_as_float(r[j + 1])),
+                            fmaf(a.alpha, x.z, sc * __uint_as_float(r[j + 2])),
+                            fmaf(a.alpha, x.w, sc * __uint_as_float(r[j + 3])));
         }
     }
     tc_fence_before();

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             L.hla2_ahla_forward_path.restype = i
             L.hla2_unmasked_forward_path.argtypes = [i, i, i, i, i]
             L.hla2_unmasked_forward_path.restype = i
+            L.hla2_decay_forward_path.argtypes = [i, i, i, i, i, ctypes.c_float]
+            L.hla2_decay_forward_path.restype = i
             L.hla2_unmasked_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
             L.hla2_unmasked_forward.restype = i
             L.hla2_unmasked_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]

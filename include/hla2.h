@@ -265,8 +265,9 @@ HLA2_API int hla2_unmasked_step(float* state, const float* q, const float* k, co
  *   o_t = q_t^T (S_t C_t - G_t) = sum_{i<=j<=t} gamma^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j,
  * ratio-normalised by q_t^T (S_t m_t - h_t).  gamma = 1 is hla2_forward's
  * operator.  Segments join with the decayed combine (B spanning n_B tokens,
- * f = gamma^{n_B}): S = f S_A + S_B, ..., G = f^2 G_A + G_B + f S_B C_A.
- * Runs on the CUDA-core segment walks (fp32) with a sequential fp32 scan.
+ * f = gamma^{n_B}): S = f S_A + S_B, ..., G = f^2 G_A + G_B + f S_B C_A,
+ * computed as decayed running sums along the segment axis with one cross
+ * product per segment.  Implementation: see hla2_decay_forward_path.
  *   gamma     in [0, 1] (else HLA2_ERR_INVALID).
  *   state_out optional: [B*H][d*d + d*dv + d] fp32, per head the compact
  *             state S | P = S C - G | p = S m - h, the hla2_decay_step layout.
@@ -276,6 +277,15 @@ HLA2_API int hla2_unmasked_step(float* state, const float* q, const float* k, co
 HLA2_API int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O,
                                 int B, int H, int T, int d, int dv, int normalized, float gamma, int dtype,
                                 void* workspace, size_t ws_bytes, float* state_out, hla2_stream_t stream);
+
+/*
+ * Which implementation hla2_decay_forward picks on the current device:
+ * 1 = tensor-core segment walks (tcgen05 with fp32 accumulators; bf16
+ * d = dv in {64, 128}, unnormalised, no state_out, gamma in [0.8, 1]: the
+ * chunk form there carries per-token factors down to gamma^{-256}, which stay
+ * finite), 0 = CUDA-core segment walks (fp32 arithmetic).
+ */
+HLA2_API int hla2_decay_forward_path(int d, int dv, int dtype, int normalized, int with_state_out, float gamma);
 
 /*
  * One decayed decode step for n heads on the compact state

@@ -8,11 +8,20 @@ import torch
 
 import oracle
 from higher_order_linear_gb300 import hla2, workloads as W
-from tests._parity import TOL_NORMALIZED, TOL_STEP_FP32, f64, relerr
+from tests._parity import TOL_NORMALIZED, TOL_STEP_FP32, TOL_TC_BF16, f64, relerr
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 TOL_FP32 = 1e-4  # CUDA-core walks and fp32 scan
+
+
+def tol(dtype, d, dv, norm, gamma):
+    """Tensor-core walks (bf16 operands) get the bf16 bound, the CUDA-core
+    walks the fp32 one, the normalised variant its own."""
+    if norm:
+        return TOL_NORMALIZED
+    code = hla2.HLA2_DTYPE_BF16 if dtype == torch.bfloat16 else hla2.HLA2_DTYPE_F32
+    return TOL_TC_BF16 if hla2.lib().hla2_decay_forward_path(d, dv, code, 0, 0, gamma) == 1 else TOL_FP32
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,18 +68,54 @@ def ref(q, k, v, gamma, normalized=False):
 def test_forward_shapes(B, H, T, d, dv, dtype, norm, gamma):
     q, k, v = inputs(B, H, T, d, dv, dtype, norm, seed=B * 1000 + H * 100 + T + d + 11)
     got = run_gpu(q, k, v, g32(gamma), normalized=norm)
-    assert relerr(f64(got), ref(q, k, v, gamma, norm)) < (TOL_NORMALIZED if norm else TOL_FP32)
+    assert relerr(f64(got), ref(q, k, v, gamma, norm)) < tol(dtype, d, dv, norm, g32(gamma))
+
+
+def test_tensor_core_path_selected():
+    L = hla2.lib()
+    bf = hla2.HLA2_DTYPE_BF16
+    assert L.hla2_decay_forward_path(128, 128, bf, 0, 0, g32(0.999)) == 1
+    assert L.hla2_decay_forward_path(64, 64, bf, 0, 0, 1.0) == 1
+    assert L.hla2_decay_forward_path(64, 64, bf, 0, 0, 0.8) == 1
+    assert L.hla2_decay_forward_path(64, 64, bf, 0, 0, g32(0.79)) == 0   # below the tensor-core range
+    assert L.hla2_decay_forward_path(64, 64, bf, 1, 0, g32(0.99)) == 0   # normalised: CUDA cores
+    assert L.hla2_decay_forward_path(128, 128, bf, 0, 1, g32(0.99)) == 0  # state_out: CUDA cores
+    assert L.hla2_decay_forward_path(128, 64, bf, 0, 0, g32(0.99)) == 0
+    assert L.hla2_decay_forward_path(64, 64, hla2.HLA2_DTYPE_F32, 0, 0, g32(0.99)) == 0
+
+
+@pytest.mark.parametrize("gamma", [1.0, 0.999, 0.95, 0.8])
+@pytest.mark.parametrize("T", [1, 2, 127, 129, 383, 2000, 5000])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_walk_lengths(T, d, gamma):
+    """Chunk boundaries, ragged tails, the split first chunk, multi-segment
+    heads and the ends of the tensor-core gamma range on the tcgen05 walks."""
+    q, k, v = inputs(1, 3, T, d, d, torch.bfloat16, False, seed=T * 19 + d)
+    got = run_gpu(q, k, v, g32(gamma))
+    assert relerr(f64(got), ref(q, k, v, g32(gamma))) < TOL_TC_BF16
+
+
+def test_tensor_core_matches_cuda_core_walk():
+    """The tcgen05 walk and the fp32 CUDA-core walk (reached through
+    state_out) agree on the same bf16 inputs within the bf16 bound."""
+    q, k, v = inputs(2, 2, 1500, 128, 128, torch.bfloat16, False, seed=32)
+    gamma = g32(0.97)
+    tc = run_gpu(q, k, v, gamma)
+    st = torch.empty(4, hla2.pform_record_len(128, 128), device=DEV)
+    cc = run_gpu(q, k, v, gamma, state_out=st)
+    assert relerr(f64(tc), f64(cc)) < TOL_TC_BF16
 
 
 def test_gamma_one_matches_the_masked_oracle():
     q, k, v = inputs(1, 2, 2000, 64, 64, torch.bfloat16, False, seed=3)
     got = run_gpu(q, k, v, 1.0)
-    assert relerr(f64(got), oracle.serial(f64(q), f64(k), f64(v))) < TOL_FP32
+    assert relerr(f64(got), oracle.serial(f64(q), f64(k), f64(v))) < tol(q.dtype, 64, 64, False, 1.0)
 
 
 def test_workload1_full():
-    q, k, v = W.make_inputs(W.WORKLOADS[1])
-    assert relerr(f64(run_gpu(q, k, v, g32(0.999))), ref(q, k, v, 0.999)) < TOL_FP32
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w)
+    assert relerr(f64(run_gpu(q, k, v, g32(0.999))), ref(q, k, v, 0.999)) < tol(q.dtype, w.d, w.dv, False, g32(0.999))
 
 
 def test_causality_bit_exact():
