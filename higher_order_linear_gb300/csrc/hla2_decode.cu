@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads)
 step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const float* __restrict__ k,
                   const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized, float gamma) {
     const float gm = gamma, gm2 = gamma * gamma;  // per-token decay (1: none)
-    __shared__ __align__(16) float sq[128], sk[128], sv[128], su[128], sy[128];
+    __shared__ __align__(16) float sq[128], sk[128], sv[128], su[128];
     __shared__ __align__(16) float part[kThreads][4];
     __shared__ float sdots[2];
 

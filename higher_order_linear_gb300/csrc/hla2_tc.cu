@@ -31,11 +31,13 @@
 namespace hla2 {
 namespace {
 
-// Chunks ahead whose tiles a walk pulls into L2 before their TMA loads.  Zero:
-// on the headline (B1 H16 T65536 d128) prefetching one, two or four chunks
-// ahead made the output walk 4-8% slower; its loads are issued as early as
-// the single-buffered tiles allow and HBM is busy with the O stores.
-constexpr int kAhead = 0;
+// Chunks ahead whose tiles a walk pulls into L2 before their TMA loads, per
+// walk.  On the headline (B1 H16 T65536 d128): the output walk is fastest
+// with none (one, two or four chunks ahead made it 4-8% slower; its loads are
+// issued as early as the single-buffered tiles allow and HBM is busy with the
+// O stores); the summary walk gains 3% with one (two: 0.5%, four: 12% slower).
+template <int MODE>
+constexpr int ahead() { return MODE == 0 ? 1 : 0; }
 
 // ------------------------------------------------------------- kernel ----
 struct TCParams {
@@ -250,7 +252,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
         if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
-        for (int a = 1; a < kAhead && a < nchunks; ++a) prefetch(c_begin + a);
+        for (int a = 1; a < ahead<MODE>() && a < nchunks; ++a) prefetch(c_begin + a);
     }
 
     // ---- initial state (mode 1): S0, P0 fp32 into TMEM, bf16 into smem ----
@@ -314,8 +316,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                // the tiles kAhead chunks ahead start moving into L2 now
-                if (kAhead > 0 && it + kAhead < nchunks) prefetch(c + kAhead);
+                // the tiles ahead<MODE>() chunks ahead start moving into L2 now
+                if (ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
                 // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
                 const bool qodd = MODE == 0 && (it & 1);
                 const Tile& tQc = qodd ? tQ2 : tQ;
