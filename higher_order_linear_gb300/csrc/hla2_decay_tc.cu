@@ -20,7 +20,8 @@
 //   sX  = g^{2L-1-t} X'_t                      (= b_t^2 X^g_t: the P update's operand)
 //   W~  = g^{-2L} tril(Q sX^T)                 (constant factor)
 //   O'  = Q P0 + W~ V,  o_t = g^{2(t+1)} O'_t  (row factor)
-//   S  += (diag(b) K)^T K after TMEM S was scaled by g^L (P by g^{2L}).
+//   S  += K'^T K' with K' = diag(sqrt(b)) K (K scaled in place once its
+//         other products are done), after TMEM S was scaled by g^L (P by g^{2L}).
 // The negative powers stay within g^{-2L}; with g >= 0.8 every intermediate is
 // a finite fp32 / bf16 number (products too small to represent only drop terms
 // that are negligible against the output).  W~ is split into bf16 hi + lo on
@@ -110,7 +111,7 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     const __grid_constant__ CUtensorMap mR, DParams p) {
     using LY = DOutLayout<D>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    enum { LQ, LK, LV, CA, CX, CW, CO, CP, DA, DX, DW, DO, DS, DP, FIN, PB, NBAR = PB + kDrainWarps };
+    enum { LQ, LK, LV, CA, CX, CS, CW, CO, CP, DA, DX, DK, DW, DO, DS, DP, FIN, PB, NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ float colf[kL];  // g^{-(i+1)}
     __shared__ uint32_t tmem_slot;
@@ -141,7 +142,7 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DW || i == DO) cnt = kDrainWarps;
+            if (i == DA || i == DX || i == DK || i == DW || i == DO) cnt = kDrainWarps;
             if (i == DS || i == DP) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
@@ -271,22 +272,16 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                 mma_commit(bar(CA));
                 if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0; TMEM S decayed
-                if (!wait_bar(DA, ph)) break;              // sA = A~ (A~_lo), sX = diag(b) K
+                if (!wait_bar(DA, ph)) break;              // sA = A~ (A~_lo)
                 tc_fence_after();
-                // X' = Q S0 + A~ K ; S += (diag(b) K)^T K
+                // X' = Q S0 + A~ K
                 if (!first)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                if (has_next)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tX.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                 mma_commit(bar(CX));
-                if (has_next) {
-                    if (!wait_bar(CX, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);  // K was last read by A~ K and the S update
-                }
                 if (!wait_bar(DX, ph)) break;  // sX = g^{2L-1-t} X' (and its lo part); TMEM X' read
                 tc_fence_after();
                 // W' = Q sX^T
@@ -294,6 +289,15 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 if (first)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tXl.kmaj(ks), iSq, 1);
                 mma_commit(bar(CW));
+                if (has_next) {
+                    // S += K'^T K' (K' = diag(sqrt(b)) K, scaled in place by the drains)
+                    if (!wait_bar(DK, ph)) break;
+                    tc_fence_after();
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CS));
+                    if (!wait_bar(CS, ph)) break;
+                    issue_load(LK, &mK, tK, c + 1);  // K was last read by the S update
+                }
                 if (!wait_bar(DW, ph)) break;              // sA = W~_hi, TMEM X' columns = W~_lo; TMEM A read
                 if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P0; TMEM P decayed
                 tc_fence_after();
@@ -327,7 +331,6 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             const bool first = c == 0;
             const float L = (float)chunk_len(p.T, c);
             if (!wait_bar(CA, ph)) break;
-            if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
             tc_fence_after();
             // this warp's O pieces have left sA and sX
             if (lane == 0) tma_store_wait_read();
@@ -339,10 +342,9 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 put_row32_cf(tA, tAl, first, row, c128, r, colf, 1.f, true);
                 put_row32_cf(tA, tAl, first, row, c128 + 32, r + 32, colf, 1.f, true);
             }
-            // diag(b) K -> sX (row = token; b = g^{L-1-t})
-            scale_row<D / 16>(tK, tX, row, cD, gpow(lg, L - 1.f - (float)row));
             drained(DA);
             if (!wait_bar(CX, ph)) break;
+            if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
             tc_fence_after();
             {
                 // sX = g^{2L-1-t} X'  (hi, and lo on the first chunk)
@@ -353,9 +355,11 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 if (D == 128) put_row32_cf(tX, tXl, first, row, cD + 32, r + 32, nullptr, xs, false);
             }
             drained(DX);
-            if (state_rows && has_next) {
-                drain_state(tS_, tS, gpow(lg, (float)chunk_len(p.T, c + 1)));  // S0 of the next chunk
-                drained(DS);
+            if (has_next) {
+                // K' = diag(sqrt(b)) K in place (row = token; b = g^{L-1-t}): its
+                // other products (A, A~ K) have completed
+                scale_row<D / 16>(tK, tK, row, cD, gpow(lg, 0.5f * (L - 1.f - (float)row)));
+                drained(DK);
             }
             if (!wait_bar(CW, ph)) break;
             tc_fence_after();
@@ -377,6 +381,12 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 tmem_st_wait();
             }
             drained(DW);
+            if (state_rows && has_next) {
+                if (!wait_bar(CS, ph)) break;
+                tc_fence_after();
+                drain_state(tS_, tS, gpow(lg, (float)chunk_len(p.T, c + 1)));  // S0 of the next chunk
+                drained(DS);
+            }
             if (!wait_bar(CO, ph)) break;
             tc_fence_after();
             {
@@ -420,7 +430,8 @@ struct DSumLayout {
     static constexpr uint32_t kSq = kL * kL * 2;
     static constexpr uint32_t kSt = D * D * 2;
     static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq, S = X + kTok;
-    static constexpr uint32_t kEnd = S + kSt;
+    static constexpr uint32_t Vb = S + kSt;  // diag(F b) V, the C update's operand
+    static constexpr uint32_t kEnd = Vb + kTok;
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
     static constexpr uint32_t kBytes = kEnd + kPad;
     static_assert(kEnd >= 8u * 3u * (D / 64) * 4096u || D < 128, "record staging must fit the tiles");
@@ -432,7 +443,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mR, DParams p) {
     using LY = DSumLayout<D>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    enum { LQ, LK, LV, CA, CX, CC, CP, DA, DX, DV, DS, FIN, NBAR };
+    enum { LQ, LK, LV, CA, CX, CS, CC, CP, DA, DX, DK, DV, DS, FIN, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ float colf[kL];
     __shared__ uint32_t tmem_slot;
@@ -454,7 +465,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
-    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tS{dsm + LY::S, D};
+    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tS{dsm + LY::S, D}, tVb{dsm + LY::Vb, kL};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid < kL) colf[tid] = gpow(lg, -(float)(tid + 1));
@@ -462,7 +473,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DV) cnt = kDrainWarps;
+            if (i == DA || i == DX || i == DK || i == DV) cnt = kDrainWarps;
             if (i == DS) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
@@ -533,25 +544,29 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                 mma_commit(bar(CA));
                 if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0; TMEM S decayed
-                if (!wait_bar(DA, ph)) break;              // sA = A~, sX = diag(b) K
+                if (!wait_bar(DA, ph)) break;              // sA = A~
                 tc_fence_after();
-                // X' = Q S0 + A~ K   (S0 = 0 on the segment's first chunk) ; S += (diag(b) K)^T K
+                // X' = Q S0 + A~ K   (S0 = 0 on the segment's first chunk)
                 if (it > 0)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tS_, tX.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CX));
+                // S += K'^T K' (K' = diag(sqrt(b)) K, scaled in place by the drains)
+                if (!wait_bar(DK, ph)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CS));
                 if (has_next) {
-                    if (!wait_bar(CX, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);
+                    if (!wait_bar(CS, ph)) break;
+                    issue_load(LK, &mK, tK, c + 1);  // K was last read by the S update
                 }
-                if (!wait_bar(DV, ph)) break;  // sA = diag(F b) V
+                if (!wait_bar(DV, ph)) break;  // sVb = diag(F b) V
                 tc_fence_after();
                 // C += Q^T diag(F b) V
                 for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tC_, tQ.mnmaj(ks), tA.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_bf16(tC_, tQ.mnmaj(ks), tVb.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CC));
                 if (!wait_bar(DX, ph)) break;  // sX = F^2 g^{2L-1-t} X'
                 tc_fence_after();
@@ -578,8 +593,6 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             const float L = (float)chunk_len(p.T, c);
             const float F = gpow(lg, (float)(seg_end_tok - min(p.T, (c + 1) * kL)));
             if (!wait_bar(CA, ph)) break;
-            // sA and sX of the previous chunk were read by its C and P updates
-            if (it > 0 && (!wait_bar(CC, pph) || !wait_bar(CP, pph))) break;
             tc_fence_after();
             {
                 uint32_t r[64];
@@ -587,9 +600,9 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 put_row32_cf(tA, tA, false, row, c128, r, colf, 1.f, true);
                 put_row32_cf(tA, tA, false, row, c128 + 32, r + 32, colf, 1.f, true);
             }
-            scale_row<D / 16>(tK, tX, row, cD, gpow(lg, L - 1.f - (float)row));
             drained(DA);
             if (!wait_bar(CX, ph)) break;
+            if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
             tc_fence_after();
             {
                 // sX = F^2 g^{2L-1-t} X'
@@ -600,11 +613,17 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 if (D == 128) put_row32_cf(tX, tX, false, row, cD + 32, r + 32, nullptr, xs, false);
             }
             drained(DX);
+            // K' = diag(sqrt(b)) K in place (A and A~ K have completed)
+            scale_row<D / 16>(tK, tK, row, cD, gpow(lg, 0.5f * (L - 1.f - (float)row)));
+            drained(DK);
             if (!wait_bar(LV, ph)) break;
-            // diag(F b) V -> sA (A~ was read by X')
-            scale_row<D / 16>(tV, tA, row, cD, F * gpow(lg, L - 1.f - (float)row));
+            if (it > 0 && !wait_bar(CC, pph)) break;  // the previous C update has read sVb
+            // diag(F b) V -> sVb
+            scale_row<D / 16>(tV, tVb, row, cD, F * gpow(lg, L - 1.f - (float)row));
             drained(DV);
             if (state_rows && has_next) {
+                if (!wait_bar(CS, ph)) break;
+                tc_fence_after();
                 // S0 of the next chunk -> sS; TMEM S decayed over the next chunk
                 uint32_t r[64];
                 tmem_ld_cols<D / 2>(tS_ + lane_off + cD, r);

@@ -201,6 +201,38 @@ decay_exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, si
     if (total) total[(size_t)bh * total_stride + i] = run;
 }
 
+// Same decayed scan, four consecutive elements per thread (16-byte accesses).
+__global__ void __launch_bounds__(kScanThreads)
+decay_exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
+                     size_t total_stride, const float* __restrict__ fac) {
+    const size_t i = ((size_t)blockIdx.x * kScanThreads + threadIdx.x) * 4;
+    const int bh = blockIdx.y;
+    if (i >= len) return;
+    const float* pin = in + (size_t)bh * N * R + off + i;
+    float* pout = out + (size_t)bh * N * R + off + i;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    int r = 0;
+    for (; r + kScanUnroll <= N; r += kScanUnroll) {
+        float4 x[kScanUnroll];
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
+#pragma unroll
+        for (int j = 0; j < kScanUnroll; ++j) {
+            *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
+            const float f = fac[r + j];
+            run = make_float4(fmaf(f, run.x, x[j].x), fmaf(f, run.y, x[j].y), fmaf(f, run.z, x[j].z),
+                              fmaf(f, run.w, x[j].w));
+        }
+    }
+    for (; r < N; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(pin + (size_t)r * R);
+        *reinterpret_cast<float4*>(pout + (size_t)r * R) = run;
+        const float f = fac[r];
+        run = make_float4(fmaf(f, run.x, x.x), fmaf(f, run.y, x.y), fmaf(f, run.z, x.z), fmaf(f, run.w, x.w));
+    }
+    if (total) *reinterpret_cast<float4*>(total + (size_t)bh * total_stride + i) = run;
+}
+
 __global__ void copy_strided_kernel(const float* src, long long s_src, float* dst, long long s_dst, size_t len) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int b = blockIdx.y;
@@ -244,8 +276,15 @@ cudaError_t launch_decay_factors(float* fac, int T, float gamma, SegPlan plan, c
 cudaError_t launch_decay_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
                                 float* total, size_t total_stride, const float* fac, cudaStream_t s) {
     if (BH == 0 || len == 0) return cudaSuccess;
-    dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
-    decay_exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride, fac);
+    const bool vec = ((off | len | R | total_stride) % 4 == 0) && ((reinterpret_cast<uintptr_t>(in) |
+                     reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(total)) % 16 == 0);
+    if (vec) {
+        dim3 grid((unsigned)((len / 4 + kScanThreads - 1) / kScanThreads), BH);
+        decay_exscan4_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride, fac);
+    } else {
+        dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
+        decay_exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride, fac);
+    }
     note_launches(1);
     return cudaGetLastError();
 }
