@@ -68,6 +68,8 @@ def parse():
     p.add_argument("--T", type=int, default=None, help="override T (profiling a smaller case; not a bench line)")
     p.add_argument("--H", type=int, default=None, help="override H (profiling a smaller case; not a bench line)")
     p.add_argument("--no-ahla", action="store_true", help="skip the AHLA forward and decode lines")
+    p.add_argument("--no-small", action="store_true",
+                   help="skip the B2 H8 T2048 d64 forward timed eagerly and as a CUDA graph")
     p.add_argument("--no-variants", action="store_true",
                    help="skip the unmasked and decayed forward and decode lines")
     p.add_argument("--decode-n", type=int, default=None,
@@ -439,6 +441,56 @@ def main():
                               "path": "tcgen05" if tc_v else "cuda-core", "roofline": roof_v}
         variants["decay"]["gamma"] = gamma
 
+    # ---- the latency-scale workload (B2 H8 T2048 d64): eager launches and a
+    # CUDA graph of the same forwards, replayed ----
+    small = None
+    if not args.no_small and not args.no_forward and rank == 0:
+        ws1 = W.WORKLOADS[1]
+        sq, sk, sv = W.make_inputs_on(ws1, dev)
+        sO = torch.empty(ws1.B, ws1.H, ws1.T, ws1.dv, device=dev, dtype=torch.float32)
+        sws = torch.empty(max(hla2.hla2_forward_workspace(ws1.B, ws1.H, ws1.T, ws1.d, ws1.dv,
+                                                          hla2.HLA2_DTYPE_BF16), 16), device=dev, dtype=torch.uint8)
+        n_in = 20  # forwards per graph
+        for _ in range(3):
+            hla2.hla2_forward(sq, sk, sv, sO, workspace=sws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(100):
+            hla2.hla2_forward(sq, sk, sv, sO, workspace=sws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_eager = e0.elapsed_time(e1) / 100
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cs):
+            hla2.hla2_forward(sq, sk, sv, sO, workspace=sws)  # first call outside the capture
+            cs.synchronize()
+            with torch.cuda.graph(g, stream=cs):
+                for _ in range(n_in):
+                    hla2.hla2_forward(sq, sk, sv, sO, workspace=sws)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(5):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_graph = e0.elapsed_time(e1) / (5 * n_in)
+        if hla2.hla2_device_status() != 0:
+            raise SystemExit(f"device status after the graph replays: {hla2.hla2_last_error_detail()}")
+        ntok = ws1.B * ws1.H * ws1.T
+        small = {"workload": ws1.name, "metric": "masked HLA-2 fwd tokens/s (B·H·T/s)",
+                 "eager": {"value": ntok / (ms_eager / 1e3), "ms_per_forward": ms_eager, "forwards": 100},
+                 "graph": {"value": ntok / (ms_graph / 1e3), "ms_per_forward": ms_graph,
+                           "forwards": 5 * n_in, "forwards_per_graph": n_in},
+                 "unit": UNIT, "inputs_in_l2": True,
+                 "note": "inputs (12.6 MB) stay in L2 between forwards: a latency-scale case, not an HBM roofline"}
+        del sq, sk, sv, sO, sws, g
+
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
     if not args.no_e2e and not args.no_forward:
@@ -576,7 +628,7 @@ def main():
                 "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
                 "config": fwd_config(w, segments_per_head(w.BH, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-                "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants}
+                "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants, "small": small}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -211,3 +211,44 @@ def test_state_out_then_step_continues(dtype, norm):
         outs.append(hla2.hla2_step(state, qt, kt, vt, normalized=norm))
     got = torch.stack(outs, dim=1).reshape(B, H, extra, dv)
     assert relerr(f64(got), ref[..., T:, :]) < 1e-4
+
+
+@pytest.mark.parametrize("op", ["hla", "ahla", "unmasked", "decay"])
+def test_cuda_graph_replay_matches_eager(op):
+    """The forwards issue only stream-ordered work (no allocation, no host
+    synchronisation), so they can be captured in a CUDA graph: replays on new
+    inputs give the eager results bit for bit."""
+    calls = {"hla": lambda q, k, v, O, ws: hla2.hla2_forward(q, k, v, O, workspace=ws),
+             "ahla": lambda q, k, v, O, ws: hla2.hla2_ahla_forward(q, k, v, O, workspace=ws),
+             "unmasked": lambda q, k, v, O, ws: hla2.hla2_unmasked_forward(q, k, v, O, workspace=ws),
+             "decay": lambda q, k, v, O, ws: hla2.hla2_decay_forward(q, k, v, 0.99, O, workspace=ws)}
+    call = calls[op]
+    w = W.WORKLOADS[1]
+    q, k, v = (x.to(DEV) for x in W.make_inputs(w))
+    q2, k2, v2 = (x.to(DEV) for x in W.make_inputs(w, seed=77))
+    ws = torch.empty(hla2.hla2_forward_workspace(w.B, w.H, w.T, w.d, w.dv, hla2.HLA2_DTYPE_BF16),
+                     device=DEV, dtype=torch.uint8)
+    O = torch.empty(w.B, w.H, w.T, w.dv, device=DEV)
+    call(q2, k2, v2, O, ws)
+    ref2 = O.clone()
+    call(q, k, v, O, ws)
+    ref1 = O.clone()
+    sq, sk, sv = q.clone(), k.clone(), v.clone()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        call(sq, sk, sv, O, ws)
+        cs.synchronize()
+        with torch.cuda.graph(g, stream=cs):
+            call(sq, sk, sv, O, ws)
+    torch.cuda.synchronize()
+    O.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(O, ref1)
+    sq.copy_(q2); sk.copy_(k2); sv.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(O, ref2)
+    assert hla2.hla2_device_status() == 0
