@@ -30,7 +30,7 @@
 //
 // Summary walk (mode 0): per segment S (running), and C, P accumulated in the
 // frame of the segment's last token: chunk c contributes with the factor
-// F_c = g^{(tokens of the segment after chunk c)}, C += Q^T diag(F_c b) V,
+// F_c = g^{(tokens of the segment after chunk c)}, C += (diag(F_c b) Q)^T V,
 // P += (F_c^2 b^2 X^g)^T V, so neither needs rescaling from chunk to chunk.
 //
 // Roles as in the other walks: warp 8 (lane 0) issues every copy and MMA,
@@ -424,14 +424,18 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 }
 
 // ----------------------------------------------------------- summaries ----
+// Q is double-buffered (chunk it uses buffer it & 1); once a chunk's A and X'
+// products have completed, the drains scale its K tile in place by sqrt(b)
+// (for S += K'^T K') and its Q tile by F_c b (for C += Q'^T V), so the segment
+// sums need no staged copies and V enters unscaled.
 template <int D>
 struct DSumLayout {
     static constexpr uint32_t kTok = kL * D * 2;
     static constexpr uint32_t kSq = kL * kL * 2;
     static constexpr uint32_t kSt = D * D * 2;
-    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq, S = X + kTok;
-    static constexpr uint32_t Vb = S + kSt;  // diag(F b) V, the C update's operand
-    static constexpr uint32_t kEnd = Vb + kTok;
+    static constexpr uint32_t Q = 0, Q2 = Q + kTok, K = Q2 + kTok, V = K + kTok, A = V + kTok, X = A + kSq;
+    static constexpr uint32_t S = X + kTok;
+    static constexpr uint32_t kEnd = S + kSt;
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
     static constexpr uint32_t kBytes = kEnd + kPad;
     static_assert(kEnd >= 8u * 3u * (D / 64) * 4096u || D < 128, "record staging must fit the tiles");
@@ -443,7 +447,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mR, DParams p) {
     using LY = DSumLayout<D>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    enum { LQ, LK, LV, CA, CX, CS, CC, CP, DA, DX, DK, DV, DS, FIN, NBAR };
+    enum { LQ, LQ2, LK, LV, CA, CX, CS, CC, CP, DA, DX, DK, DQ, DS, FIN, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ float colf[kL];
     __shared__ uint32_t tmem_slot;
@@ -464,8 +468,8 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     const int seg_end_tok = min(p.T, c_end * kL);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
-    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
-    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tS{dsm + LY::S, D}, tVb{dsm + LY::Vb, kL};
+    const Tile tQa{dsm + LY::Q, kL}, tQb{dsm + LY::Q2, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
+    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tS{dsm + LY::S, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid < kL) colf[tid] = gpow(lg, -(float)(tid + 1));
@@ -473,7 +477,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DK || i == DV) cnt = kDrainWarps;
+            if (i == DA || i == DX || i == DK || i == DQ) cnt = kDrainWarps;
             if (i == DS) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
@@ -530,14 +534,17 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 
     if (issuer) {
         if (lane == 0 && nchunks > 0) {
-            issue_load(LQ, &mQ, tQ, c_begin);
+            issue_load(LQ, &mQ, tQa, c_begin);
             issue_load(LK, &mK, tK, c_begin);
             issue_load(LV, &mV, tV, c_begin);
+            if (nchunks > 1) issue_load(LQ2, &mQ, tQb, c_begin + 1);
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
+                const bool qodd = it & 1;  // Q buffer of this chunk
+                const Tile& tQ = qodd ? tQb : tQa;
+                if (!wait_bar(qodd ? LQ2 : LQ, (uint32_t)((it >> 1) & 1)) || !wait_bar(LK, ph)) break;
                 if (it > 0 && !wait_bar(DX, pph)) break;  // TMEM A (X' of the previous chunk) read
                 tc_fence_after();
                 // A = Q K^T
@@ -562,11 +569,11 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     if (!wait_bar(CS, ph)) break;
                     issue_load(LK, &mK, tK, c + 1);  // K was last read by the S update
                 }
-                if (!wait_bar(DV, ph)) break;  // sVb = diag(F b) V
+                // C += Q'^T V (Q' = diag(F b) Q, scaled in place by the drains)
+                if (!wait_bar(DQ, ph) || !wait_bar(LV, ph)) break;
                 tc_fence_after();
-                // C += Q^T diag(F b) V
                 for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tC_, tQ.mnmaj(ks), tVb.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CC));
                 if (!wait_bar(DX, ph)) break;  // sX = F^2 g^{2L-1-t} X'
                 tc_fence_after();
@@ -574,9 +581,11 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CP));
-                if (has_next) {
+                if (it + 2 < nchunks) {
                     if (!wait_bar(CC, ph)) break;
-                    issue_load(LQ, &mQ, tQ, c + 1);
+                    issue_load(qodd ? LQ2 : LQ, &mQ, tQ, c + 2);  // this buffer's next chunk
+                }
+                if (has_next) {
                     if (!wait_bar(CP, ph)) break;
                     issue_load(LV, &mV, tV, c + 1);
                 }
@@ -590,6 +599,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             const int c = c_begin + it;
             const uint32_t ph = it & 1, pph = (it + 1) & 1;
             const bool has_next = it + 1 < nchunks;
+            const Tile& tQ = (it & 1) ? tQb : tQa;
             const float L = (float)chunk_len(p.T, c);
             const float F = gpow(lg, (float)(seg_end_tok - min(p.T, (c + 1) * kL)));
             if (!wait_bar(CA, ph)) break;
@@ -601,7 +611,11 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 put_row32_cf(tA, tA, false, row, c128 + 32, r + 32, colf, 1.f, true);
             }
             drained(DA);
-            if (!wait_bar(CX, ph)) break;
+            if (!wait_bar(CX, ph)) break;  // A and X' have read Q and K
+            tc_fence_after();
+            // K' = diag(sqrt(b)) K in place (row = token; b = g^{L-1-t})
+            scale_row<D / 16>(tK, tK, row, cD, gpow(lg, 0.5f * (L - 1.f - (float)row)));
+            drained(DK);
             if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
             tc_fence_after();
             {
@@ -613,14 +627,9 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 if (D == 128) put_row32_cf(tX, tX, false, row, cD + 32, r + 32, nullptr, xs, false);
             }
             drained(DX);
-            // K' = diag(sqrt(b)) K in place (A and A~ K have completed)
-            scale_row<D / 16>(tK, tK, row, cD, gpow(lg, 0.5f * (L - 1.f - (float)row)));
-            drained(DK);
-            if (!wait_bar(LV, ph)) break;
-            if (it > 0 && !wait_bar(CC, pph)) break;  // the previous C update has read sVb
-            // diag(F b) V -> sVb
-            scale_row<D / 16>(tV, tVb, row, cD, F * gpow(lg, L - 1.f - (float)row));
-            drained(DV);
+            // Q' = diag(F b) Q in place
+            scale_row<D / 16>(tQ, tQ, row, cD, F * gpow(lg, L - 1.f - (float)row));
+            drained(DQ);
             if (state_rows && has_next) {
                 if (!wait_bar(CS, ph)) break;
                 tc_fence_after();
