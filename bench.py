@@ -491,32 +491,33 @@ def main():
                  "note": "inputs (12.6 MB) stay in L2 between forwards: a latency-scale case, not an HBM roofline"}
         del sq, sk, sv, sO, sws, g
 
-    # ---- e2e through the public API with pinned host buffers ----
+    # ---- e2e through the C ABI with pinned host buffers: hla2_forward_host
+    # copies Q, K, V in and O out itself, pipelined over groups of heads ----
     e2e = None
     if not args.no_e2e and not args.no_forward:
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         hO = torch.empty(O.shape, dtype=torch.float32).pin_memory()
         n_e2e = max(2, min(args.steps, 10))
-        dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        del ws  # the host call has its own device buffer (two slots and a workspace)
+        dcode_e = hla2.HLA2_DTYPE_BF16 if w.dtype == "bf16" else hla2.HLA2_DTYPE_F32
+        hdev = torch.empty(hla2.hla2_forward_host_workspace(w.B, w.H, w.T, w.d, w.dv, dcode_e, 0),
+                           dtype=torch.uint8, device=dev)
         for _ in range(2):
-            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
-            hla2.hla2_forward(dq, dk, dvv, O, normalized=w.normalized, workspace=ws)
-            hO.copy_(O, non_blocking=True)
+            hla2.hla2_forward_host(hq, hk, hv, hO, normalized=w.normalized, dev=hdev)
         barrier()
         e2 = torch.cuda.Event(enable_timing=True); e3 = torch.cuda.Event(enable_timing=True)
         e2.record(stream)
         for _ in range(n_e2e):
-            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dvv.copy_(hv, non_blocking=True)
-            hla2.hla2_forward(dq, dk, dvv, O, normalized=w.normalized, workspace=ws)
-            hO.copy_(O, non_blocking=True)
+            hla2.hla2_forward_host(hq, hk, hv, hO, normalized=w.normalized, dev=hdev)
         e3.record(stream)
         barrier()
         ms_e2e = max_over_ranks(e2.elapsed_time(e3) / n_e2e)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
         d2h = hO.numel() * hO.element_size()
         e2e = {"value": world * tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e}
-        del dq, dk, dvv, hq, hk, hv, hO
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
+               "api": "hla2_forward_host (copies in, forward and copy out pipelined over groups of heads)"}
+        del hq, hk, hv, hO, hdev
 
     # ---- decode: hla2_step on n=4096 heads, d=dv=128 ----
     decode = None

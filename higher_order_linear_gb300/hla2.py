@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.hla2_forward_path.restype = i
             L.hla2_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
             L.hla2_forward_noalloc.restype = i
+            L.hla2_forward_host_workspace.argtypes = [i, i, i, i, i, i, i]
+            L.hla2_forward_host_workspace.restype = sz
+            L.hla2_forward_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, vp, sz, vp]
+            L.hla2_forward_host.restype = i
             L.hla2_step_pform.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
             L.hla2_step_pform.restype = i
             L.hla2_state_to_pform.argtypes = [vp, vp, i, i, i, vp]
@@ -187,6 +191,52 @@ def hla2_forward_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: t
     rc = lib().hla2_forward_noalloc(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
                                     B, H, T, d, dv, int(bool(normalized)), _dtype_code(Q), _stream(stream))
     _check(rc, "hla2_forward_noalloc")
+    return O
+
+
+def _host(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def hla2_forward_host_workspace(B: int, H: int, T: int, d: int, dv: int, dtype: int, heads_per_group: int = 0) -> int:
+    return int(lib().hla2_forward_host_workspace(B, H, T, d, dv, dtype, heads_per_group))
+
+
+def hla2_forward_host(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                      normalized: bool = False, heads_per_group: int = 0, dev: torch.Tensor | None = None,
+                      stream=None, device=None) -> torch.Tensor:
+    """Masked forward on host tensors (pinned for overlap): Q, K [B,H,T,d],
+    V [B,H,T,dv] on the CPU -> O [B,H,T,dv] fp32 on the CPU.  The library
+    copies groups of heads in, runs the forward and copies O out as a
+    pipeline on the current CUDA device; O is complete once ``stream`` (the
+    current stream by default) has been synchronised.  ``dev`` is the device
+    buffer of hla2_forward_host_workspace(...) bytes (allocated here when
+    None)."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share a dtype")
+    B, H, T, d = Q.shape
+    dv = V.shape[-1]
+    code = _dtype_code(Q)
+    if O is None:
+        O = torch.empty((B, H, T, dv), dtype=torch.float32, pin_memory=Q.is_pinned())
+    elif O.shape != (B, H, T, dv):
+        raise ValueError("O has the wrong shape")
+    need = hla2_forward_host_workspace(B, H, T, d, dv, code, heads_per_group)
+    if dev is None:
+        dev = torch.empty(max(need, 256), dtype=torch.uint8,
+                          device=device if device is not None else torch.device("cuda", torch.cuda.current_device()))
+    rc = lib().hla2_forward_host(_host(Q, "Q"), _host(K, "K"), _host(V, "V"), _host(O, "O", torch.float32),
+                                 B, H, T, d, dv, int(bool(normalized)), code, int(heads_per_group),
+                                 _dev(dev, "dev"), dev.numel() * dev.element_size(), _stream(stream))
+    _check(rc, "hla2_forward_host")
     return O
 
 

@@ -121,6 +121,36 @@ HLA2_API int hla2_forward_noalloc(const void* Q, const void* K, const void* V, f
                                   hla2_stream_t stream);
 
 /*
+ * The forward on HOST buffers: the masked operator of hla2_forward, with the
+ * copies in and out made by the library.  The pages have no counterpart (it
+ * is the end-to-end entry point).  Heads are independent, so the B*H heads
+ * are cut into groups of heads_per_group (0: about an eighth of them) and
+ * each group's host-to-device copy of Q, K, V, its forward and the
+ * device-to-host copy of its O run as a pipeline: the copy of one group
+ * overlaps the forward of the previous one and the copy-out of the one
+ * before.  The copies run on two streams the library creates once per device
+ * and keeps (with eight events); the forwards run on `stream`, which, when
+ * the call returns, carries all of the call's work: O is complete once
+ * `stream` has been synchronised.
+ *   Qh, Kh [B][H][T][d], Vh [B][H][T][dv] on the host in `dtype`, Oh
+ *   [B][H][T][dv] fp32 on the host.  They should be page-locked (pinned):
+ *   copies from pageable memory run, but without overlap.
+ *   dev: device buffer of hla2_forward_host_workspace(...) bytes, 256-byte
+ *   aligned, owned by the caller: two slots of a group's Q, K, V, O and one
+ *   forward workspace.
+ * Results equal hla2_forward's within its tolerances (each group is planned
+ * as its own problem, so segment boundaries, and with them rounding, can
+ * differ).  Calls on one device enqueue one at a time (a lock); their copies
+ * share the library's two copy streams.  Errors as for hla2_forward, plus
+ * HLA2_ERR_WORKSPACE for a missing or small `dev`; work enqueued before an
+ * error is left on the streams.
+ */
+HLA2_API size_t hla2_forward_host_workspace(int B, int H, int T, int d, int dv, int dtype, int heads_per_group);
+HLA2_API int hla2_forward_host(const void* Qh, const void* Kh, const void* Vh, float* Oh,
+                               int B, int H, int T, int d, int dv, int normalized, int dtype,
+                               int heads_per_group, void* dev, size_t dev_bytes, hla2_stream_t stream);
+
+/*
  * One streaming decode step for n independent heads [HLA §1, online update;
  * HLA R: O(d^2 + d dv) per token, independent of the prefix length].
  *   state  [n][d*d + 2*d*dv + 2*d] fp32, per head S (d x d) | C (d x dv) |

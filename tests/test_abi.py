@@ -110,3 +110,30 @@ def test_bench_plan_mirror_matches_library(B, H, T, d):
     BH = B * H
     expect = 4 * (2 * up(BH * nseg * R) + up(BH * R) + up(2 * nseg))
     assert hla2.hla2_forward_workspace(B, H, T, d, d, hla2.HLA2_DTYPE_BF16) == expect
+
+
+def test_host_forward_workspace_and_checks(L):
+    """The host-buffer forward's device buffer holds two slots (a group's
+    Q, K, V and O) and one forward workspace; its argument checks run on the
+    host before any CUDA call."""
+    up = lambda n: (n + 255) // 256 * 256
+    B, H, T, d, dv, G = 1, 16, 4096, 64, 64, 3
+    bf = hla2.HLA2_DTYPE_BF16
+    slot = 2 * up(G * T * d * 2) + up(G * T * dv * 2) + up(G * T * dv * 4)
+    last = B * H - (B * H + G - 1) // G * G + G  # heads in the last group
+    ws = max(hla2.hla2_forward_workspace(1, G, T, d, dv, bf), hla2.hla2_forward_workspace(1, last, T, d, dv, bf))
+    assert hla2.hla2_forward_host_workspace(B, H, T, d, dv, bf, G) == 2 * slot + up(ws)
+    assert hla2.hla2_forward_host_workspace(B, H, T, d, dv, bf, 0) == hla2.hla2_forward_host_workspace(B, H, T, d, dv, bf, 2)
+    assert hla2.hla2_forward_host_workspace(B, H, T, d, dv, bf, -1) == 0
+    assert hla2.hla2_forward_host_workspace(B, H, T, 200, dv, bf, 0) == 0
+    p = _fake()
+    need = hla2.hla2_forward_host_workspace(B, H, T, d, dv, bf, G)
+    dev = _fake(1 << 20)
+    assert L.hla2_forward_host(None, p, p, p, B, H, T, d, dv, 0, bf, G, dev, need, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_forward_host(p, p, p, p, B, H, T, d, dv, 0, bf, -1, dev, need, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_forward_host(p, p, p, p, B, H, T, d, dv, 0, bf, G, dev, need - 1, None) == hla2.HLA2_ERR_WORKSPACE
+    assert L.hla2_forward_host(p, p, p, p, B, H, T, d, dv, 0, bf, G, None, need, None) == hla2.HLA2_ERR_WORKSPACE
+    assert L.hla2_forward_host(p, p, p, p, B, H, T, d, dv, 0, bf, G, _fake((1 << 20) + 16), need, None) == \
+        hla2.HLA2_ERR_INVALID
+    assert "aligned" in hla2.hla2_last_error_detail()
+    assert L.hla2_forward_host(p, p, p, p, B, H, T, 200, dv, 0, bf, G, dev, need, None) == hla2.HLA2_ERR_UNSUPPORTED
