@@ -356,17 +356,27 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     if (!wait_bar(DX, ph)) break;  // sX = bf16(Q S0); TMEM X read
                     tc_fence_after();
-                    // X = Q S0 + A K  (before the last W term, so that W completes last
-                    // and its drain, which also waits for this product, starts at once)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                    if (NORM)
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                    mma_commit(bar(CX2));
+                    // On a head's first chunk and in the normalised walk the W drain
+                    // writes W_lo over X's TMEM columns, so it reads X first: there
+                    // X = Q S0 + A K goes before the last W term (W then completes
+                    // last).  Otherwise W completes first and X after it, so that
+                    // W's drain, on the chain to O, does not wait for A K.
+                    const bool x_first = NORM || c == 0;
+                    if (x_first) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                        if (NORM)
+                            for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                        mma_commit(bar(CX2));
+                    }
                     // W += (Q S0) Q^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                     if (NORM)
                         for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tXl.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                     mma_commit(bar(CW));
+                    if (!x_first) {
+                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                        mma_commit(bar(CX2));
+                    }
                     if (has_next) {
                         if (!wait_bar(CX2, ph)) break;
                         issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
@@ -507,18 +517,33 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     else drainD(tS_, tS);  // S0 of the next chunk -> sS
                     drained(DS);
                 }
-                if (!wait_bar(CW, ph) || !wait_bar(CX2, ph)) break;
+                const bool x_first = NORM || c_begin + it == 0;  // as in the issuer
+                if (!wait_bar(CW, ph) || (x_first && !wait_bar(CX2, ph))) break;
                 tc_fence_after();
                 {
-                    // X is read out first (W_lo lands on this warp's X columns),
-                    // W is announced before X because the output products need it first.
-                    // On the head's first chunk W is split into bf16 hi + lo: there an
-                    // output can be a single product (t = 0 gives (q.k)^2 v), so the
-                    // rounding of W is not averaged over many terms.  Later chunks
-                    // add the prefix term and many products, and plain bf16 W suffices.
-                    uint32_t x[64];
-                    tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
-                    if (NORM || c_begin + it == 0) {
+                    // W is announced before X because the output products need it
+                    // first.  On the head's first chunk W is split into bf16 hi + lo:
+                    // there an output can be a single product (t = 0 gives (q.k)^2 v),
+                    // so the rounding of W is not averaged over many terms; W_lo lands
+                    // on this warp's X columns, so X is read out before it.  Later
+                    // chunks add the prefix term and many products, and plain bf16 W
+                    // suffices; there X completes after W and is read out after it.
+                    // X -> sX (hi, and lo in the normalised walk)
+                    auto put_x = [&](const uint32_t* x) {
+                        if (NORM) {
+                            put_row32_split2(tX, tXl, row, cD, x, false);
+                            if (D == 128) put_row32_split2(tX, tXl, row, cD + 32, x + 32, false);
+                        } else {
+                            put_row32(tX, row, cD, x, false);
+                            if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
+                        }
+                    };
+                    if (x_first) {
+                        uint32_t x[64];
+                        tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
+                        // at D = 128 X goes to shared memory before W is read out, which
+                        // keeps the live registers within the 168 this launch allows
+                        if (!NORM) put_x(x);
                         uint32_t lo[32];
                         {
                             uint32_t r[64];
@@ -528,16 +553,16 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         }
                         tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
                         tmem_st_wait();
+                        drained(DW);
+                        if (NORM) put_x(x);
                     } else {
                         drain128(tA_, tA, true);  // W -> sA (masked)
-                    }
-                    drained(DW);
-                    if (NORM) {
-                        put_row32_split2(tX, tXl, row, cD, x, false);  // X -> sX (hi, lo)
-                        if (D == 128) put_row32_split2(tX, tXl, row, cD + 32, x + 32, false);
-                    } else {
-                        put_row32(tX, row, cD, x, false);  // X -> sX
-                        if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
+                        drained(DW);
+                        if (!wait_bar(CX2, ph)) break;
+                        tc_fence_after();
+                        uint32_t x[64];
+                        tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
+                        put_x(x);
                     }
                     drained(DX2);
                 }
