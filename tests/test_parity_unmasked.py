@@ -156,3 +156,15 @@ def test_step_from_shared_fp32_state(d, dv, n, prefill, steps, norm):
         assert relerr(f64(o), o_ref) < (TOL_NORMALIZED if norm else TOL_STEP_FP32)
     torch.cuda.synchronize()
     assert relerr(f64(st_gpu), st_ref) < 1e-5
+
+
+def test_workload3_full_size_sampled_heads():
+    """B1 H16 T65536 d=dv=128 (the benchmark's inputs and launch
+    configuration): all heads on the GPU, three checked token by token."""
+    w = W.WORKLOADS[3]
+    q, k, v = W.make_inputs(w)
+    got = run_gpu(q, k, v)
+    heads = [0, 8, 15]
+    r = ref(q[:, heads], k[:, heads], v[:, heads])
+    assert relerr(f64(got[:, heads]), r) < tol(q.dtype, w.d, w.dv, False)
+    assert torch.isfinite(got).all()
