@@ -45,12 +45,10 @@ BYTES_PER_TOKEN_FWD = None  # set from the workload: 2*(2d+dv) + 4*dv
 # step on a smaller case and scaled by the units processed (profiles/*.md give
 # the commands and the raw figures):
 #  - tc_walk_kernel<128,1,false>, B1 H16 T65536: 826.5 + 495.4 MB;
-#  - decode step_kernel, 1024 heads: 204.0 + 143.3 = 347.3 MB; x4 heads.
 # Writes still in L2 when a kernel ends are not counted, so the write side
 # sits a little below the algorithmic bytes.
 NCU_TRAFFIC = {
     ("tcgen05", "hla2-fwd-B1H16T65536-d128-bf16"): 826540800 + 495391488,
-    ("step", "hla2-step-n4096-d128-fp32-prefill1024-steps512"): 4 * 347.3e6,
 }
 
 

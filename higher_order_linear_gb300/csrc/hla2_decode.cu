@@ -91,22 +91,31 @@ step_kernel(float* __restrict__ state, const float* __restrict__ q, const float*
             }
         }
     }
-    __syncthreads();
-
-    // ---- pass C: w = C^T k, y = C^T u (old C), C' = C + q v^T -------------
     const int gc = dv >> 2;        // float4 columns per row
     const int rows_per = kThreads / gc;  // rows covered per sweep (gc divides 256)
     const int c4 = tid % gc;
     const int rg = tid / gc;
+    // The first batch of C is loaded before the barrier that ends pass S (its
+    // loads need nothing from that pass), so the stream does not pause there.
+    float4 r[kUnroll];
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+        const int a = i * rows_per + rg;
+        if (a < d) r[i] = ld_stream(C + (size_t)a * dv + 4 * c4);
+    }
+    __syncthreads();
+
+    // ---- pass C: w = C^T k, y = C^T u (old C), C' = C + q v^T -------------
     {
         float pw[4] = {0.f, 0.f, 0.f, 0.f}, py[4] = {0.f, 0.f, 0.f, 0.f};
         const float4 v4 = *reinterpret_cast<const float4*>(&sv[4 * c4]);
         for (int a0 = 0; a0 < d; a0 += rows_per * kUnroll) {
-            float4 r[kUnroll];
+            if (a0 > 0) {
 #pragma unroll
-            for (int i = 0; i < kUnroll; ++i) {
-                const int a = a0 + i * rows_per + rg;
-                if (a < d) r[i] = ld_stream(C + (size_t)a * dv + 4 * c4);
+                for (int i = 0; i < kUnroll; ++i) {
+                    const int a = a0 + i * rows_per + rg;
+                    if (a < d) r[i] = ld_stream(C + (size_t)a * dv + 4 * c4);
+                }
             }
 #pragma unroll
             for (int i = 0; i < kUnroll; ++i) {
@@ -127,6 +136,12 @@ step_kernel(float* __restrict__ state, const float* __restrict__ q, const float*
 #pragma unroll
         for (int j = 0; j < 4; ++j) { part[0][tid][j] = pw[j]; part[1][tid][j] = py[j]; }
     }
+    // likewise the first batch of G before the barrier that ends pass C
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+        const int a = i * rows_per + rg;
+        if (a < d) r[i] = ld_stream(G + (size_t)a * dv + 4 * c4);
+    }
     __syncthreads();
     if (tid < dv) {
         const int cc = tid >> 2, j = tid & 3;
@@ -142,11 +157,12 @@ step_kernel(float* __restrict__ state, const float* __restrict__ q, const float*
         float pz[4] = {0.f, 0.f, 0.f, 0.f};
         const float4 w4 = *reinterpret_cast<const float4*>(&sw[4 * c4]);
         for (int a0 = 0; a0 < d; a0 += rows_per * kUnroll) {
-            float4 r[kUnroll];
+            if (a0 > 0) {
 #pragma unroll
-            for (int i = 0; i < kUnroll; ++i) {
-                const int a = a0 + i * rows_per + rg;
-                if (a < d) r[i] = ld_stream(G + (size_t)a * dv + 4 * c4);
+                for (int i = 0; i < kUnroll; ++i) {
+                    const int a = a0 + i * rows_per + rg;
+                    if (a < d) r[i] = ld_stream(G + (size_t)a * dv + 4 * c4);
+                }
             }
 #pragma unroll
             for (int i = 0; i < kUnroll; ++i) {
