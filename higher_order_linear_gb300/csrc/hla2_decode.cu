@@ -312,22 +312,30 @@ step_pform_kernel(float* __restrict__ state, const float* __restrict__ q, const 
             }
         }
     }
-    __syncthreads();
-
-    // ---- pass P: y = P^T q (old P), P' = P + u v^T -------------------------
     const int gc = dv >> 2;
     const int rows_per = kThreads / gc;
     const int c4 = tid % gc;
     const int rg = tid / gc;
+    // the first batch of P is loaded before the barrier that ends pass S
+    float4 r[kUnroll];
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+        const int a = i * rows_per + rg;
+        if (a < d) r[i] = ld_stream(P + (size_t)a * dv + 4 * c4);
+    }
+    __syncthreads();
+
+    // ---- pass P: y = P^T q (old P), P' = P + u v^T -------------------------
     {
         float py[4] = {0.f, 0.f, 0.f, 0.f};
         const float4 v4 = *reinterpret_cast<const float4*>(&sv[4 * c4]);
         for (int a0 = 0; a0 < d; a0 += rows_per * kUnroll) {
-            float4 r[kUnroll];
+            if (a0 > 0) {
 #pragma unroll
-            for (int i = 0; i < kUnroll; ++i) {
-                const int a = a0 + i * rows_per + rg;
-                if (a < d) r[i] = ld_stream(P + (size_t)a * dv + 4 * c4);
+                for (int i = 0; i < kUnroll; ++i) {
+                    const int a = a0 + i * rows_per + rg;
+                    if (a < d) r[i] = ld_stream(P + (size_t)a * dv + 4 * c4);
+                }
             }
 #pragma unroll
             for (int i = 0; i < kUnroll; ++i) {
