@@ -32,8 +32,8 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// d and dv are powers of two in [4, 128].
-__global__ void __launch_bounds__(kThreads)
+// d and dv are powers of two in [4, 128].  Four CTAs per SM (64 registers).
+__global__ void __launch_bounds__(kThreads, 4)
 step_kernel(float* __restrict__ state, const float* __restrict__ q, const float* __restrict__ k,
             const float* __restrict__ v, float* __restrict__ o, int d, int dv, int normalized) {
     __shared__ __align__(16) float sq[128], sk[128], sv[128], su[128], sw[128], sy[128], sz[128];
