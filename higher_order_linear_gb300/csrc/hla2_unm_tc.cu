@@ -236,7 +236,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    // tensor-memory regions: A then W then O | X | S | C
+    // tensor-memory regions: A then W then W V | X then X C0 | S | C
     const uint32_t tA_ = tmem + 0, tX_ = tmem + 128, tS_ = tmem + 256, tC_ = tmem + 256 + D;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int c128 = half * 64;
@@ -379,16 +379,19 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 if (first)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tXl.kmaj(ks), tQ.kmaj(ks), iSq, 1);
                 mma_commit(bar(CW));
+                if (!first) {
+                    // X C0 into TMEM X (read out at DX): it runs while W is drained, and
+                    // the O drain adds it to W V
+                    if (it > 0 && !wait_bar(DC, pph)) break;  // sC = C0 of this chunk; TMEM C read
+                    tc_fence_after();
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tX.kmaj(ks), tC.mnmaj(ks), iKM, ks > 0);
+                }
                 if (!wait_bar(DW, ph)) break;  // sA = W (and W_lo); TMEM A read
-                if (it > 0 && !wait_bar(DC, pph)) break;  // sC = C0 of this chunk; TMEM C read
                 tc_fence_after();
-                // O = X C0 + W V
-                if (!first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tC.mnmaj(ks), iKM, ks > 0);
+                // O = W V  (+ X C0 from TMEM X)
                 if (!wait_bar(LV, ph)) break;
                 tc_fence_after();
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, ks > 0 ? 1u : 0u);
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tWl.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CO));
@@ -447,6 +450,18 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 // the same rows of sX (both dead once the output products completed)
                 uint32_t r[64];
                 tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
+                if (!first) {
+                    // + X C0 (TMEM X), 32 columns at a time
+#pragma unroll
+                    for (int g = 0; g < D / 64; ++g) {
+                        uint32_t t[32];
+                        tmem_ld32(tX_ + lane_off + cD + 32 * g, t);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            r[32 * g + j] = __float_as_uint(__uint_as_float(r[32 * g + j]) + __uint_as_float(t[j]));
+                    }
+                }
                 drained(DO);
                 const uint32_t wofs = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                 const int t0 = (c_begin + it) * kL + quarter * 32;
