@@ -73,6 +73,10 @@ def parse():
                    help="skip the unmasked and decayed forward and decode lines")
     p.add_argument("--decode-n", type=int, default=None,
                    help="override the number of decode heads (profiling a smaller case; not a bench line)")
+    p.add_argument("--no-normalized", action="store_true",
+                   help="skip the ratio-normalised B4 H16 T4096 d64 forward line")
+    p.add_argument("--no-chunk-level", action="store_true",
+                   help="skip timing hla2_chunk_summaries (L = 64) and hla2_scan on the headline inputs")
     p.add_argument("--workload", type=int, default=FWD_WORKLOAD,
                    help="forward workload id (0-3, see workloads.py); the bench line is workload 3")
     return p.parse_args()
@@ -204,34 +208,12 @@ def alg_flops(w, L=64):
     return 2 * (2 * L * w.d + L * L + 2 * w.d * w.d + 2 * L * w.dv + 3 * w.d * w.dv)
 
 
-def segments_per_head(BH, T):
-    """Mirrors the library's segment plan: runs of `seglen` 128-token chunks
-    (the last may be shorter), the run length minimising the dispatch makespan
-    on 152 SMs (a CTA costs its chunks + 2) plus nseg / 2.  Returns (nseg, seglen)."""
-    import heapq
-    nchunk = (T + 127) // 128
-    best = None
-    for ln in range(max(1, (nchunk + 4095) // 4096), nchunk + 1):
-        ns = (nchunk + ln - 1) // ln
-        tail = nchunk - (ns - 1) * ln
-        short = ns > 1 and tail < ln
-        full = BH * (ns - 1) if short else BH * ns
-        q, r = divmod(full, 152)
-        span = (q + 1 if r else q) * (ln + 2)
-        if short:
-            if BH > 20000:
-                span += -(-BH // 152) * (tail + 2)
-            else:
-                load = [(q + 1) * (ln + 2) if i < r else q * (ln + 2) for i in range(152)]
-                heapq.heapify(load)
-                for _ in range(BH):
-                    t = heapq.heappop(load) + tail + 2
-                    heapq.heappush(load, t)
-                    span = max(span, t)
-        cost2 = 2 * span + ns
-        if best is None or cost2 < best[0]:
-            best = (cost2, ns, ln)
-    return best[1], best[2]
+def segments_per_head(B, H, T):
+    """The library's segment plan for the current device (its SM count
+    queried by the library): (segments per head, chunks per segment)."""
+    from higher_order_linear_gb300 import hla2
+    nseg, seglen, _ = hla2.hla2_forward_plan(B, H, T)
+    return nseg, seglen
 
 
 def reference_arm(args):
@@ -266,7 +248,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": fwd_config(w, segments_per_head(w.BH, w.T)),
+            "config": fwd_config(w, segments_per_head(w.B, w.H, w.T)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -322,8 +304,6 @@ def main():
     for _ in range(0 if args.no_forward else args.warmup):
         hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
     barrier()
-    hla2.hla2_profile_read()
-    hla2.hla2_profile_enable(True)
     stream = torch.cuda.current_stream()
     # Workloads whose step moves less than 4x the 129 MB L2 flush it (outside
     # the timed events) before every step; larger ones stream from HBM anyway.
@@ -331,49 +311,144 @@ def main():
     flush = step_bytes < 4 * 129e6
     l2_note = ("L2 flushed before every step (256 MB write outside the timed events)" if flush else
                f"inputs exceed L2 ({step_bytes / 1e9:.2f} GB moved per step vs 129 MB L2); no flush")
-    scratch = torch.empty(64 << 20, device=dev, dtype=torch.float32) if flush else None
-    t_begin = time.time()
-    if flush:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(fwd_steps)]
-        for ea, eb in evs:
-            scratch.zero_()
-            ea.record(stream)
-            hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
-            eb.record(stream)
-        barrier()
-        ms_total = sum(ea.elapsed_time(eb) for ea, eb in evs)
-    else:
+    scratch = torch.empty(64 << 20, device=dev, dtype=torch.float32)  # 256 MB: flushes L2 where asked
+
+    def timed(call, n, flush_each):
+        """Mean ms of `call` over n steps, CUDA events on the launching stream;
+        with flush_each, L2 is flushed before every step outside the events."""
+        if flush_each:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for ea, eb in evs:
+                scratch.zero_()
+                ea.record(stream)
+                call()
+                eb.record(stream)
+            barrier()
+            return sum(ea.elapsed_time(eb) for ea, eb in evs) / n
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(fwd_steps):
-            hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+        for _ in range(n):
+            call()
         e1.record(stream)
         barrier()
-        ms_total = e0.elapsed_time(e1)
-    t_end = time.time()
+        return e0.elapsed_time(e1) / n
+
+    fwd = lambda: hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws)
+    # The headline is timed bare (no per-phase events recorded); the library's
+    # launch counter, which costs nothing on the GPU, counts its launches.
     hla2.hla2_profile_enable(False)
-    phase_ms, nfwd, launches = hla2.hla2_profile_read()
-    ms_step = ms_total / max(fwd_steps, 1)
+    hla2.hla2_profile_read()  # resets the launch counter
+    t_begin = time.time()
+    ms_step = timed(fwd, fwd_steps, flush) if fwd_steps else 0.0
+    t_end = time.time()
+    _, _, launches = hla2.hla2_profile_read()
     ms_step_max = max_over_ranks(ms_step)
     status = hla2.hla2_device_status()
     if status != 0:
         raise SystemExit(f"device status {status}: {hla2.hla2_last_error_detail()}")
     value = replicas.job_throughput(tokens, world, ms_step_max) if fwd_steps else 0.0
 
+    def phase_split(call, n, flush_each):
+        """A separate instrumented run: the library records CUDA events on the
+        launching stream around each phase (summaries, scan, outputs) of n
+        forwards.  Returns (per-phase ms per forward, ms per instrumented step)."""
+        hla2.hla2_profile_read()
+        hla2.hla2_profile_enable(True)
+        ms_instr = timed(call, n, flush_each)
+        hla2.hla2_profile_enable(False)
+        ph, nf, _ = hla2.hla2_profile_read()
+        return [x / max(nf, 1) for x in ph], ms_instr
+
+    n_prof = max(1, min(args.steps, 20))
+    phase, ms_instr = phase_split(fwd, n_prof, flush) if fwd_steps else ([0.0, 0.0, 0.0], 0.0)
+
     # dominant kernel: segment outputs (phase 2)
-    out_ms = phase_ms[2] / max(nfwd, 1)
+    out_ms = phase[2]
     achieved = bytes_per_token * tokens / (out_ms / 1e3) / 1e9 if out_ms > 0 else 0.0
     traffic = NCU_TRAFFIC.get((path, w.name))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "kernel": f"segment outputs ({path})", "ms_per_launch": out_ms,
-                "phase_ms_per_step": {"summaries": phase_ms[0] / max(nfwd, 1), "scan": phase_ms[1] / max(nfwd, 1),
-                                      "outputs": out_ms},
+                "phase_ms_per_step": {"summaries": phase[0], "scan": phase[1], "outputs": out_ms},
+                "phase_source": f"separate instrumented run of {n_prof} forwards "
+                                f"({ms_instr:.4f} ms per step with the per-phase events)",
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)" if peaks["source"] == "measured"
                 else "fallback 6.8 TB/s",
                 "step_frac": bytes_per_token * tokens / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"] if fwd_steps else 0.0,
                 "tensor_frac_of_bf16_burst": (alg_flops(w) * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
                 if fwd_steps else 0.0}
+
+    # ---- the ratio-normalised workload (B4 H16 T4096 d=dv=64, q, k >= 0) ----
+    normalized = None
+    if not args.no_normalized and fwd_steps and args.workload == FWD_WORKLOAD and not (args.T or args.H):
+        wn = W.WORKLOADS[2]
+        nq, nk, nv = W.make_inputs_on(wn, dev, seed=wn.seed + 1000 * rank)
+        nO = torch.empty(wn.B, wn.H, wn.T, wn.dv, device=dev, dtype=torch.float32)
+        ncode = hla2.HLA2_DTYPE_BF16
+        nws = torch.empty(max(hla2.hla2_forward_workspace(wn.B, wn.H, wn.T, wn.d, wn.dv, ncode), 16),
+                          device=dev, dtype=torch.uint8)
+        npath = "tcgen05" if L.hla2_forward_path(wn.d, wn.dv, ncode, 1, 0) == 1 else "cuda-core"
+        nfwd = lambda: hla2.hla2_forward(nq, nk, nv, nO, normalized=True, workspace=nws)
+        for _ in range(args.warmup):
+            nfwd()
+        barrier()
+        ntok = wn.B * wn.H * wn.T
+        nbytes_tok = 2 * (2 * wn.d + wn.dv) + 4 * wn.dv
+        nflush = nbytes_tok * ntok < 4 * 129e6
+        n_n = max(1, min(args.steps, 50))
+        ms_n = max_over_ranks(timed(nfwd, n_n, nflush))
+        nphase, nms_instr = phase_split(nfwd, max(1, min(n_n, 20)), nflush)
+        if hla2.hla2_device_status() != 0:
+            raise SystemExit(f"device status after the normalised forward: {hla2.hla2_last_error_detail()}")
+        n_ach = nbytes_tok * ntok / (nphase[2] / 1e3) / 1e9 if nphase[2] > 0 else 0.0
+        normalized = {
+            "metric": "ratio-normalised HLA-2 fwd tokens/s (B·H·T/s)", "workload": wn.name,
+            "value": replicas.job_throughput(ntok, world, ms_n), "unit": UNIT, "ms_per_step": ms_n, "steps": n_n,
+            "path": npath,
+            "l2": (f"L2 flushed before every step (256 MB write outside the timed events); "
+                   f"{nbytes_tok * ntok / 1e6:.1f} MB moved per step vs 129 MB L2") if nflush else "no flush",
+            "roofline": {"bound": "hbm", "achieved": n_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": n_ach / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": f"segment outputs ({npath}, normalised)", "ms_per_launch": nphase[2],
+                         "bytes_per_token_head": nbytes_tok,
+                         "phase_ms_per_step": {"summaries": nphase[0], "scan": nphase[1], "outputs": nphase[2]},
+                         "step_frac": nbytes_tok * ntok / (ms_n / 1e3) / 1e9 / peaks["hbm_gbs"]}}
+        del nq, nk, nv, nO, nws
+
+    # ---- the chunk-level calls of the boundary on the headline inputs:
+    # hla2_chunk_summaries (L = 64: 1024 chunks per head) and hla2_scan ----
+    chunk_level = None
+    if not args.no_chunk_level and fwd_steps and args.workload == FWD_WORKLOAD and not (args.T or args.H):
+        Lc = 64
+        N = (w.T + Lc - 1) // Lc
+        R = hla2.record_len(w.d, w.dv)
+        summ = torch.empty(w.B, w.H, N, R, device=dev, dtype=torch.float32)
+        pref = torch.empty_like(summ)
+        cs = lambda: hla2.hla2_chunk_summaries(q, k, v, Lc, summ=summ)
+        sc = lambda: hla2.hla2_scan(summ, w.d, w.dv, prefix=pref)
+        cs()
+        sc()
+        barrier()
+        n_c = max(1, min(args.steps, 3))
+        ms_cs = max_over_ranks(timed(cs, n_c, False))
+        ms_sc = max_over_ranks(timed(sc, n_c, False))
+        if hla2.hla2_device_status() != 0:
+            raise SystemExit(f"device status after the chunk-level calls: {hla2.hla2_last_error_detail()}")
+        rec_bytes = w.BH * N * R * 4
+        cs_bytes = esz * (2 * w.d + w.dv) * tokens + rec_bytes  # read Q, K, V; write the records
+        sc_bytes = 2 * rec_bytes                                 # read the records; write the prefixes
+        chunk_level = {
+            "L": Lc, "chunks_per_head": N, "record_bytes": R * 4,
+            "chunk_summaries": {"ms": ms_cs, "steps": n_c, "algorithmic_bytes": cs_bytes,
+                                "roofline": {"bound": "hbm", "achieved": cs_bytes / (ms_cs / 1e3) / 1e9,
+                                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                             "frac": cs_bytes / (ms_cs / 1e3) / 1e9 / peaks["hbm_gbs"]}},
+            "scan": {"ms": ms_sc, "steps": n_c, "algorithmic_bytes": sc_bytes,
+                     "roofline": {"bound": "hbm", "achieved": sc_bytes / (ms_sc / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": sc_bytes / (ms_sc / 1e3) / 1e9 / peaks["hbm_gbs"]}},
+            "note": "records are S|C|m|G|h fp32 per chunk; both calls are bound by writing / reading them"}
+        del summ, pref
 
     # ---- AHLA (asymmetric variant) forward on the same inputs ----
     ahla = None
@@ -626,9 +701,10 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if path == "tcgen05" else "f32", "data": "synthetic",
-                "config": fwd_config(w, segments_per_head(w.BH, w.T), l2_note), "path": path,
+                "config": fwd_config(w, segments_per_head(w.B, w.H, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-                "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants, "small": small}
+                "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants, "small": small,
+                "normalized": normalized, "chunk_level": chunk_level}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

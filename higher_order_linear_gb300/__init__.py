@@ -14,6 +14,7 @@ from .hla2 import (  # noqa: F401
     hla2_device_status,
     hla2_forward,
     hla2_forward_noalloc,
+    hla2_forward_plan,
     hla2_forward_workspace,
     hla2_last_error_detail,
     hla2_scan,

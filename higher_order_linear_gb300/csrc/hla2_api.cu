@@ -11,6 +11,7 @@
 #include <mutex>
 #include <queue>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "../../include/hla2.h"
@@ -52,28 +53,49 @@ std::mutex g_status_mu;
 // The plan takes the run length that minimises
 //   makespan + nseg / 2          (in units of one chunk)
 // where the makespan comes from dispatching every CTA, in that order, to the
-// first free of the 152 SMs, a CTA costing its chunks plus two for its ramp
-// (prefix and first tiles), and nseg / 2 stands for the scan work a segment
-// adds.  Plans are cached per (BH, T).
+// first free of the device's SMs, a CTA costing its chunks plus two for its
+// ramp (prefix and first tiles), and nseg / 2 stands for the scan work a
+// segment adds.  Plans are cached per (BH, T, SM count).
 constexpr int kGranule = 128;
-constexpr int kSMs = 152;
+// SM count assumed when no device can be queried (a machine without a
+// visible GPU asking for a workspace size): GB300's 152.  A forward always
+// plans with the count of the device it runs on, queried once per device.
+constexpr int kFallbackSMs = 152;
+
+int current_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();  // clear the (non-sticky) error of a machine without a device
+        return kFallbackSMs;
+    }
+    static std::atomic<int> cache[kMaxDevices];
+    const int known = cache[dev].load(std::memory_order_relaxed);
+    if (known > 0) return known;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return kFallbackSMs;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 namespace {
-long long plan_makespan2(long long BH, int nchunk, int seglen, int nseg) {
+long long plan_makespan2(long long BH, int nchunk, int seglen, int nseg, int sms) {
     // twice the makespan, in chunk units (a CTA costs its chunks + 2)
     const int tail = nchunk - (nseg - 1) * seglen;
     const bool short_tail = nseg > 1 && tail < seglen;
     const long long full = short_tail ? BH * (nseg - 1) : BH * nseg;
     const long long a = seglen + 2, b = tail + 2;
     // full-length CTAs first: equal jobs fill the SMs round by round
-    const long long q = full / kSMs, r = full % kSMs;
+    const long long q = full / sms, r = full % sms;
     long long span = (r > 0 ? q + 1 : q) * a;
     if (!short_tail) return 2 * span;
     if (BH > 20000) {  // too many to place one by one: treat them as one more round
-        return 2 * (span + ((BH + kSMs - 1) / kSMs) * b);
+        return 2 * (span + ((BH + sms - 1) / sms) * b);
     }
     std::priority_queue<long long, std::vector<long long>, std::greater<long long>> load;
-    for (long long i = 0; i < kSMs; ++i) load.push(i < r ? (q + 1) * a : q * a);
+    for (long long i = 0; i < sms; ++i) load.push(i < r ? (q + 1) * a : q * a);
     for (long long i = 0; i < BH; ++i) {
         const long long t = load.top() + b;
         load.pop();
@@ -84,12 +106,13 @@ long long plan_makespan2(long long BH, int nchunk, int seglen, int nseg) {
 }
 }  // namespace
 
-SegPlan forward_plan(int BH, int T) {
+SegPlan forward_plan(int BH, int T, int sms) {
+    if (sms <= 0) sms = current_sm_count();
     static std::mutex mu;
-    static std::map<std::pair<int, int>, SegPlan> cache;
+    static std::map<std::tuple<int, int, int>, SegPlan> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
-        auto it = cache.find({BH, T});
+        auto it = cache.find({BH, T, sms});
         if (it != cache.end()) return it->second;
     }
     SegPlan p;
@@ -101,7 +124,7 @@ SegPlan forward_plan(int BH, int T) {
     const int len0 = (p.nchunk + 4095) / 4096;  // at most 4096 segments per head
     for (int len = len0 > 0 ? len0 : 1; len <= p.nchunk; ++len) {
         const int nseg = (p.nchunk + len - 1) / len;
-        const long long cost2 = plan_makespan2(BH, p.nchunk, len, nseg) + nseg;
+        const long long cost2 = plan_makespan2(BH, p.nchunk, len, nseg, sms) + nseg;
         if (best_cost < 0 || cost2 < best_cost) {
             best_cost = cost2;
             p.nseg = nseg;
@@ -109,7 +132,7 @@ SegPlan forward_plan(int BH, int T) {
         }
     }
     std::lock_guard<std::mutex> lk(mu);
-    cache[{BH, T}] = p;
+    cache[{BH, T, sms}] = p;
     return p;
 }
 
@@ -292,8 +315,20 @@ size_t hla2_forward_workspace(int B, int H, int T, int d, int dv, int dtype) {
     if (dtype != HLA2_DTYPE_F32 && dtype != HLA2_DTYPE_BF16) return 0;
     if ((long long)B * H > 65535) return 0;
     const int BH = B * H;
-    SegPlan p = forward_plan(BH, T);
+    SegPlan p = forward_plan(BH, T, 0);
     return carve(nullptr, BH, p, d, dv).bytes;
+}
+
+int hla2_forward_plan(int B, int H, int T, int sm_count, int* nseg, int* chunks_per_segment, int* sm_count_used) {
+    if (B <= 0 || H <= 0 || T <= 0) return fail(HLA2_ERR_INVALID, "sizes must be positive (B=%d H=%d T=%d)", B, H, T);
+    if (!nseg || !chunks_per_segment) return fail(HLA2_ERR_INVALID, "null output pointer");
+    if ((long long)B * H > 65535) return fail(HLA2_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", (long long)B * H);
+    const int sms = sm_count > 0 ? sm_count : current_sm_count();
+    const SegPlan p = forward_plan(B * H, T, sms);
+    *nseg = p.nseg;
+    *chunks_per_segment = p.seglen;
+    if (sm_count_used) *sm_count_used = sms;
+    return HLA2_OK;
 }
 
 int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, int H, int T, int d, int dv,
@@ -309,7 +344,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int BH = B * H;
-    const SegPlan plan = forward_plan(BH, T);
+    const SegPlan plan = forward_plan(BH, T, 0);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
     const bool want_extra = normalized || state_out;  // p (and m) needed
     int dev = 0;
@@ -561,7 +596,7 @@ int hla2_ahla_forward(const void* Q, const void* K, const void* V, float* O, int
     if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int BH = B * H;
-    const SegPlan plan = forward_plan(BH, T);
+    const SegPlan plan = forward_plan(BH, T, 0);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
     const bool want_extra = normalized || state_out;  // m and n needed
     int* status = device_status_word();
@@ -625,7 +660,7 @@ int hla2_unmasked_forward(const void* Q, const void* K, const void* V, float* O,
     if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int BH = B * H;
-    const SegPlan plan = forward_plan(BH, T);
+    const SegPlan plan = forward_plan(BH, T, 0);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
     const RecOff ro = summary_offsets(d, dv);
     const bool use_tc = hla2_unmasked_forward_path(d, dv, dtype, normalized, state_out != nullptr) == 1;
@@ -692,7 +727,7 @@ int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, in
     if (!aligned16(workspace)) return fail(HLA2_ERR_INVALID, "workspace not 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int BH = B * H;
-    const SegPlan plan = forward_plan(BH, T);
+    const SegPlan plan = forward_plan(BH, T, 0);
     const FwdWorkspace ws = carve(workspace, BH, plan, d, dv);
     const bool use_tc = hla2_decay_forward_path(d, dv, dtype, normalized, state_out != nullptr, gamma) == 1;
     int* status = nullptr;

@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.hla2_forward_workspace.argtypes = [i, i, i, i, i, i]
             L.hla2_forward_workspace.restype = sz
+            L.hla2_forward_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i)]
+            L.hla2_forward_plan.restype = i
             L.hla2_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
             L.hla2_forward.restype = i
             L.hla2_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
@@ -135,45 +137,105 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported input dtype {t.dtype}")
 
 
+def _same_device(device: torch.device, **tensors) -> None:
+    """Every tensor must live on ``device`` (the first input's): the library
+    launches on the current device, which the calls below make ``device``."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+
+
+def _qkv(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor):
+    """Shape, dtype and device checks shared by the forwards; returns
+    (B, H, T, d, dv, dtype code).  Runs before anything touches the library."""
+    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
+        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError(f"Q, K, V must share a dtype (got {Q.dtype}, {K.dtype}, {V.dtype})")
+    _same_device(Q.device, K=K, V=V)
+    B, H, T, d = Q.shape
+    return B, H, T, d, V.shape[-1], _dtype_code(Q)
+
+
+def _out(O: torch.Tensor | None, shape, device: torch.device) -> torch.Tensor:
+    """The caller's output tensor, checked, or a new fp32 one."""
+    if O is None:
+        return torch.empty(shape, device=device, dtype=torch.float32)
+    if tuple(O.shape) != tuple(shape):
+        raise ValueError(f"O has shape {tuple(O.shape)}, expected {tuple(shape)}")
+    if O.dtype != torch.float32:
+        raise ValueError(f"O must be float32, got {O.dtype}")
+    if not O.is_contiguous():
+        raise ValueError("O must be contiguous")
+    _same_device(device, O=O)
+    return O
+
+
 def hla2_forward_workspace(B: int, H: int, T: int, d: int, dv: int, dtype: int) -> int:
     return int(lib().hla2_forward_workspace(B, H, T, d, dv, dtype))
+
+
+def hla2_forward_plan(B: int, H: int, T: int, sm_count: int = 0):
+    """The forward's segment plan: (segments per head, chunks of 128 tokens
+    per segment, SM count planned for).  sm_count <= 0 plans for the current
+    device, as hla2_forward does."""
+    ns, ln, used = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().hla2_forward_plan(B, H, T, int(sm_count), ctypes.byref(ns), ctypes.byref(ln), ctypes.byref(used)),
+           "hla2_forward_plan")
+    return int(ns.value), int(ln.value), int(used.value)
 
 
 def record_len(d: int, dv: int) -> int:
     return d * d + 2 * d * dv + 2 * d
 
 
+def _cuda_device(t: torch.Tensor, name: str) -> torch.device:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.device
+
+
+def _forward(entry: str, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None,
+             normalized: bool, workspace: torch.Tensor | None, state_out: torch.Tensor | None, stream,
+             state_len: int | None, gamma: float | None = None) -> torch.Tensor:
+    """Common marshalling of the four forwards (same C signature, plus gamma
+    before the dtype for the decayed one).  Every check runs before the
+    library is touched; the call itself runs with Q's device current, so the
+    default stream and the library's per-device state are that device's."""
+    B, H, T, d, dv, code = _qkv(Q, K, V)
+    O = _out(O, (B, H, T, dv), Q.device)
+    if state_out is not None:
+        if state_len is None or state_out.numel() != B * H * state_len:
+            raise ValueError(f"state_out must hold B*H = {B * H} states of {state_len} floats")
+    _same_device(Q.device, workspace=workspace, state_out=state_out)
+    dev = _cuda_device(Q, "Q")
+    with torch.cuda.device(dev):
+        need = hla2_forward_workspace(B, H, T, d, dv, code)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+        sptr = _dev(state_out, "state_out", torch.float32) if state_out is not None else None
+        args = [_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                B, H, T, d, dv, int(bool(normalized))]
+        if gamma is not None:
+            args.append(float(gamma))
+        args += [code, _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), sptr,
+                 _stream(stream)]
+        rc = getattr(lib(), entry)(*args)
+    _check(rc, entry)
+    return O
+
+
 def hla2_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
                  normalized: bool = False, workspace: torch.Tensor | None = None,
                  state_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Masked second-order HLA forward.  Q, K [B,H,T,d], V [B,H,T,dv] (fp32 or
-    bf16, same dtype) -> O [B,H,T,dv] fp32.  ``state_out`` [B*H, record] fp32
-    receives the final decode state if given."""
-    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
-        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
-    if not (Q.dtype == K.dtype == V.dtype):
-        raise ValueError("Q, K, V must share a dtype")
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
-    code = _dtype_code(Q)
-    if O is None:
-        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
-    elif O.shape != (B, H, T, dv):
-        raise ValueError("O has the wrong shape")
-    need = hla2_forward_workspace(B, H, T, d, dv, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
-    sptr = None
-    if state_out is not None:
-        if state_out.numel() != B * H * record_len(d, dv):
-            raise ValueError("state_out must hold B*H records")
-        sptr = _dev(state_out, "state_out", torch.float32)
-    rc = lib().hla2_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
-                            B, H, T, d, dv, int(bool(normalized)), code,
-                            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-                            sptr, _stream(stream))
-    _check(rc, "hla2_forward")
-    return O
+    bf16, same dtype, same device) -> O [B,H,T,dv] fp32.  ``state_out``
+    [B*H, record] fp32 receives the final decode state S|C|G|m|h if given."""
+    return _forward("hla2_forward", Q, K, V, O, normalized, workspace, state_out, stream, record_len(*_dims(Q, V)))
+
+
+def _dims(Q: torch.Tensor, V: torch.Tensor):
+    return (Q.shape[-1] if Q.dim() else 0), (V.shape[-1] if V.dim() else 0)
 
 
 def hla2_forward_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
@@ -181,15 +243,14 @@ def hla2_forward_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: t
     """hla2_forward for callers that cannot allocate device scratch: the
     library uses its own fixed 64 MiB device array instead of a workspace
     (larger problems raise).  Only O is allocated here, and only when the
-    caller passes none."""
-    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
-        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
-    if O is None:
-        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
-    rc = lib().hla2_forward_noalloc(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
-                                    B, H, T, d, dv, int(bool(normalized)), _dtype_code(Q), _stream(stream))
+    caller passes none.  The arguments are checked as for hla2_forward
+    before anything is launched."""
+    B, H, T, d, dv, code = _qkv(Q, K, V)
+    O = _out(O, (B, H, T, dv), Q.device)
+    dev = _cuda_device(Q, "Q")
+    with torch.cuda.device(dev):
+        rc = lib().hla2_forward_noalloc(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
+                                        B, H, T, d, dv, int(bool(normalized)), code, _stream(stream))
     _check(rc, "hla2_forward_noalloc")
     return O
 
@@ -214,10 +275,11 @@ def hla2_forward_host(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torc
     """Masked forward on host tensors (pinned for overlap): Q, K [B,H,T,d],
     V [B,H,T,dv] on the CPU -> O [B,H,T,dv] fp32 on the CPU.  The library
     copies groups of heads in, runs the forward and copies O out as a
-    pipeline on the current CUDA device; O is complete once ``stream`` (the
-    current stream by default) has been synchronised.  ``dev`` is the device
-    buffer of hla2_forward_host_workspace(...) bytes (allocated here when
-    None)."""
+    pipeline on the GPU that holds ``dev`` (else ``device``, else the current
+    one), which is made current for the call; O is complete once ``stream``
+    (that device's current stream by default) has been synchronised.  ``dev``
+    is the device buffer of hla2_forward_host_workspace(...) bytes (allocated
+    here when None)."""
     if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
         raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
     if not (Q.dtype == K.dtype == V.dtype):
@@ -229,32 +291,55 @@ def hla2_forward_host(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torc
         O = torch.empty((B, H, T, dv), dtype=torch.float32, pin_memory=Q.is_pinned())
     elif O.shape != (B, H, T, dv):
         raise ValueError("O has the wrong shape")
-    need = hla2_forward_host_workspace(B, H, T, d, dv, code, heads_per_group)
-    if dev is None:
-        dev = torch.empty(max(need, 256), dtype=torch.uint8,
-                          device=device if device is not None else torch.device("cuda", torch.cuda.current_device()))
-    rc = lib().hla2_forward_host(_host(Q, "Q"), _host(K, "K"), _host(V, "V"), _host(O, "O", torch.float32),
-                                 B, H, T, d, dv, int(bool(normalized)), code, int(heads_per_group),
-                                 _dev(dev, "dev"), dev.numel() * dev.element_size(), _stream(stream))
+    if dev is not None:
+        gpu = _cuda_device(dev, "dev")
+        if device is not None and torch.device(device) != gpu:
+            raise ValueError(f"dev is on {gpu}, device is {device}")
+    else:
+        gpu = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(gpu):
+        need = hla2_forward_host_workspace(B, H, T, d, dv, code, heads_per_group)
+        if dev is None:
+            dev = torch.empty(max(need, 256), dtype=torch.uint8, device=gpu)
+        rc = lib().hla2_forward_host(_host(Q, "Q"), _host(K, "K"), _host(V, "V"), _host(O, "O", torch.float32),
+                                     B, H, T, d, dv, int(bool(normalized)), code, int(heads_per_group),
+                                     _dev(dev, "dev"), dev.numel() * dev.element_size(), _stream(stream))
     _check(rc, "hla2_forward_host")
     return O
 
 
-def hla2_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
-              o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
-    """One decode step for n heads.  state [n, record] fp32 (updated in place),
-    q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
+def _step(entry: str, state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+          o: torch.Tensor | None, normalized: bool, stream, state_len_fn, gamma: float | None = None) -> torch.Tensor:
+    """Common marshalling of the decode steps: state [n, state_len] fp32
+    (updated in place), q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
+    if q.dim() != 2 or k.shape != q.shape or v.dim() != 2 or v.shape[0] != q.shape[0]:
+        raise ValueError(f"{entry}: expected q, k [n,d] and v [n,dv]")
     n, d = q.shape
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * record_len(d, dv):
-        raise ValueError("shape mismatch for hla2_step")
-    if o is None:
-        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
-    rc = lib().hla2_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
-                         _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
-                         n, d, dv, int(bool(normalized)), _stream(stream))
-    _check(rc, "hla2_step")
+    if state.numel() != n * state_len_fn(d, dv):
+        raise ValueError(f"{entry}: state must hold n = {n} states of {state_len_fn(d, dv)} floats")
+    if o is not None and tuple(o.shape) != (n, dv):
+        raise ValueError(f"{entry}: o has shape {tuple(o.shape)}, expected {(n, dv)}")
+    _same_device(q.device, k=k, v=v, state=state, o=o)
+    dev = _cuda_device(q, "q")
+    with torch.cuda.device(dev):
+        if o is None:
+            o = torch.empty((n, dv), device=dev, dtype=torch.float32)
+        args = [_dev(state, "state", torch.float32), _dev(q, "q", torch.float32), _dev(k, "k", torch.float32),
+                _dev(v, "v", torch.float32), _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized))]
+        if gamma is not None:
+            args.append(float(gamma))
+        args.append(_stream(stream))
+        rc = getattr(lib(), entry)(*args)
+    _check(rc, entry)
     return o
+
+
+def hla2_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+              o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
+    """One decode step for n heads.  state [n, record] fp32 (S|C|G|m|h,
+    updated in place), q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
+    return _step("hla2_step", state, q, k, v, o, normalized, stream, record_len)
 
 
 def pform_record_len(d: int, dv: int) -> int:
@@ -264,17 +349,7 @@ def pform_record_len(d: int, dv: int) -> int:
 def hla2_step_pform(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
     """Decode step on the compact P-form state [n, d*d + d*dv + d] (S | P | p)."""
-    n, d = q.shape
-    dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * pform_record_len(d, dv):
-        raise ValueError("shape mismatch for hla2_step_pform")
-    if o is None:
-        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
-    rc = lib().hla2_step_pform(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
-                               _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
-                               _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized)), _stream(stream))
-    _check(rc, "hla2_step_pform")
-    return o
+    return _step("hla2_step_pform", state, q, k, v, o, normalized, stream, pform_record_len)
 
 
 def hla2_state_to_pform(gstate: torch.Tensor, d: int, dv: int, pstate: torch.Tensor | None = None,
@@ -283,10 +358,15 @@ def hla2_state_to_pform(gstate: torch.Tensor, d: int, dv: int, pstate: torch.Ten
     n = gstate.numel() // record_len(d, dv)
     if gstate.numel() != n * record_len(d, dv):
         raise ValueError("gstate size is not a whole number of records")
-    if pstate is None:
-        pstate = torch.empty((n, pform_record_len(d, dv)), device=gstate.device, dtype=torch.float32)
-    rc = lib().hla2_state_to_pform(_dev(gstate, "gstate", torch.float32), _dev(pstate, "pstate", torch.float32),
-                                   n, d, dv, _stream(stream))
+    if pstate is not None and pstate.numel() != n * pform_record_len(d, dv):
+        raise ValueError(f"pstate must hold n = {n} states of {pform_record_len(d, dv)} floats")
+    _same_device(gstate.device, pstate=pstate)
+    dev = _cuda_device(gstate, "gstate")
+    with torch.cuda.device(dev):
+        if pstate is None:
+            pstate = torch.empty((n, pform_record_len(d, dv)), device=dev, dtype=torch.float32)
+        rc = lib().hla2_state_to_pform(_dev(gstate, "gstate", torch.float32), _dev(pstate, "pstate", torch.float32),
+                                       n, d, dv, _stream(stream))
     _check(rc, "hla2_state_to_pform")
     return pstate
 
@@ -294,26 +374,39 @@ def hla2_state_to_pform(gstate: torch.Tensor, d: int, dv: int, pstate: torch.Ten
 def hla2_chunk_summaries(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, L: int,
                          summ: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """[B,H,N,record] fp32 chunk summaries S|C|m|G|h, N = ceil(T/L)."""
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
+    B, H, T, d, dv, code = _qkv(Q, K, V)
+    if L <= 0:
+        raise ValueError("chunk length L must be positive")
     N = (T + L - 1) // L
-    if summ is None:
-        summ = torch.empty((B, H, N, record_len(d, dv)), device=Q.device, dtype=torch.float32)
-    rc = lib().hla2_chunk_summaries(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(summ, "summ", torch.float32),
-                                    B, H, T, d, dv, int(L), _dtype_code(Q), _stream(stream))
+    if summ is not None and summ.numel() != B * H * N * record_len(d, dv):
+        raise ValueError(f"summ must hold B*H*N = {B * H * N} records of {record_len(d, dv)} floats")
+    _same_device(Q.device, summ=summ)
+    dev = _cuda_device(Q, "Q")
+    with torch.cuda.device(dev):
+        if summ is None:
+            summ = torch.empty((B, H, N, record_len(d, dv)), device=dev, dtype=torch.float32)
+        rc = lib().hla2_chunk_summaries(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(summ, "summ", torch.float32),
+                                        B, H, T, d, dv, int(L), code, _stream(stream))
     _check(rc, "hla2_chunk_summaries")
     return summ
 
 
 def hla2_scan(summ: torch.Tensor, d: int, dv: int, prefix: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Exclusive scan of [B,H,N,record] summaries with the semidirect combine."""
+    if summ.dim() != 4:
+        raise ValueError("summ must be [B,H,N,record]")
     B, H, N, R = summ.shape
     if R != record_len(d, dv):
         raise ValueError("record length does not match d, dv")
-    if prefix is None:
-        prefix = torch.empty_like(summ)
-    rc = lib().hla2_scan(_dev(summ, "summ", torch.float32), _dev(prefix, "prefix", torch.float32),
-                         B, H, N, d, dv, _stream(stream))
+    if prefix is not None and tuple(prefix.shape) != tuple(summ.shape):
+        raise ValueError("prefix must have the shape of summ")
+    _same_device(summ.device, prefix=prefix)
+    dev = _cuda_device(summ, "summ")
+    with torch.cuda.device(dev):
+        if prefix is None:
+            prefix = torch.empty_like(summ)
+        rc = lib().hla2_scan(_dev(summ, "summ", torch.float32), _dev(prefix, "prefix", torch.float32),
+                             B, H, N, d, dv, _stream(stream))
     _check(rc, "hla2_scan")
     return prefix
 
@@ -348,48 +441,15 @@ def hla2_ahla_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torc
     """Masked AHLA forward (o_t = sum_{j<=i<=t} (q_t.k_i)(q_i.k_j) v_j).
     Shapes and dtypes as for hla2_forward; ``state_out`` [B*H, 2*d*dv + 2*d]
     fp32 receives the final P|E|m|n state if given."""
-    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
-        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
-    if not (Q.dtype == K.dtype == V.dtype):
-        raise ValueError("Q, K, V must share a dtype")
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
-    code = _dtype_code(Q)
-    if O is None:
-        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
-    elif O.shape != (B, H, T, dv):
-        raise ValueError("O has the wrong shape")
-    need = hla2_forward_workspace(B, H, T, d, dv, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
-    sptr = None
-    if state_out is not None:
-        if state_out.numel() != B * H * ahla_state_len(d, dv):
-            raise ValueError("state_out must hold B*H AHLA states")
-        sptr = _dev(state_out, "state_out", torch.float32)
-    rc = lib().hla2_ahla_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
-                                 B, H, T, d, dv, int(bool(normalized)), code,
-                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-                                 sptr, _stream(stream))
-    _check(rc, "hla2_ahla_forward")
-    return O
+    return _forward("hla2_ahla_forward", Q, K, V, O, normalized, workspace, state_out, stream,
+                    ahla_state_len(*_dims(Q, V)))
 
 
 def hla2_ahla_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                    o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
     """One AHLA decode step for n heads: state [n, 2*d*dv + 2*d] fp32 (P|E|m|n,
     updated in place), q, k [n, d], v [n, dv] fp32 -> o [n, dv] fp32."""
-    n, d = q.shape
-    dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * ahla_state_len(d, dv):
-        raise ValueError("shape mismatch for hla2_ahla_step")
-    if o is None:
-        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
-    rc = lib().hla2_ahla_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
-                              _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
-                              n, d, dv, int(bool(normalized)), _stream(stream))
-    _check(rc, "hla2_ahla_step")
-    return o
+    return _step("hla2_ahla_step", state, q, k, v, o, normalized, stream, ahla_state_len)
 
 
 # -------------------------------------------------------------- unmasked ----
@@ -404,47 +464,14 @@ def hla2_unmasked_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: 
     """Unmasked second-order forward o_t = q_t^T S_t C_t.  Shapes and dtypes
     as for hla2_forward; ``state_out`` [B*H, d*d + d*dv + d] fp32 receives the
     final S|C|m if given."""
-    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
-        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
-    if not (Q.dtype == K.dtype == V.dtype):
-        raise ValueError("Q, K, V must share a dtype")
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
-    code = _dtype_code(Q)
-    if O is None:
-        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
-    elif O.shape != (B, H, T, dv):
-        raise ValueError("O has the wrong shape")
-    need = hla2_forward_workspace(B, H, T, d, dv, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
-    sptr = None
-    if state_out is not None:
-        if state_out.numel() != B * H * unmasked_state_len(d, dv):
-            raise ValueError("state_out must hold B*H unmasked states")
-        sptr = _dev(state_out, "state_out", torch.float32)
-    rc = lib().hla2_unmasked_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
-                                     B, H, T, d, dv, int(bool(normalized)), code,
-                                     _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-                                     sptr, _stream(stream))
-    _check(rc, "hla2_unmasked_forward")
-    return O
+    return _forward("hla2_unmasked_forward", Q, K, V, O, normalized, workspace, state_out, stream,
+                    unmasked_state_len(*_dims(Q, V)))
 
 
 def hla2_unmasked_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                        o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
     """One unmasked decode step: state [n, d*d + d*dv + d] fp32 (S|C|m, in place)."""
-    n, d = q.shape
-    dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * unmasked_state_len(d, dv):
-        raise ValueError("shape mismatch for hla2_unmasked_step")
-    if o is None:
-        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
-    rc = lib().hla2_unmasked_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
-                                  _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
-                                  _dev(o, "o", torch.float32), n, d, dv, int(bool(normalized)), _stream(stream))
-    _check(rc, "hla2_unmasked_step")
-    return o
+    return _step("hla2_unmasked_step", state, q, k, v, o, normalized, stream, unmasked_state_len)
 
 
 # ----------------------------------------------------------------- decay ----
@@ -455,44 +482,11 @@ def hla2_decay_forward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, gamma:
     """Decayed masked forward, o_t = sum_{i<=j<=t} gamma^{2t-i-j} (q_t.k_i)(k_i.q_j) v_j.
     Shapes and dtypes as for hla2_forward; ``state_out`` [B*H, d*d + d*dv + d]
     fp32 receives the final compact state S|P|p if given."""
-    if Q.dim() != 4 or K.shape != Q.shape or V.dim() != 4 or V.shape[:3] != Q.shape[:3]:
-        raise ValueError("expected Q, K [B,H,T,d] and V [B,H,T,dv]")
-    if not (Q.dtype == K.dtype == V.dtype):
-        raise ValueError("Q, K, V must share a dtype")
-    B, H, T, d = Q.shape
-    dv = V.shape[-1]
-    code = _dtype_code(Q)
-    if O is None:
-        O = torch.empty((B, H, T, dv), device=Q.device, dtype=torch.float32)
-    elif O.shape != (B, H, T, dv):
-        raise ValueError("O has the wrong shape")
-    need = hla2_forward_workspace(B, H, T, d, dv, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=Q.device, dtype=torch.uint8)
-    sptr = None
-    if state_out is not None:
-        if state_out.numel() != B * H * pform_record_len(d, dv):
-            raise ValueError("state_out must hold B*H compact states")
-        sptr = _dev(state_out, "state_out", torch.float32)
-    rc = lib().hla2_decay_forward(_dev(Q, "Q"), _dev(K, "K"), _dev(V, "V"), _dev(O, "O", torch.float32),
-                                  B, H, T, d, dv, int(bool(normalized)), float(gamma), code,
-                                  _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-                                  sptr, _stream(stream))
-    _check(rc, "hla2_decay_forward")
-    return O
+    return _forward("hla2_decay_forward", Q, K, V, O, normalized, workspace, state_out, stream,
+                    pform_record_len(*_dims(Q, V)), gamma=gamma)
 
 
 def hla2_decay_step(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, gamma: float,
                     o: torch.Tensor | None = None, normalized: bool = False, stream=None) -> torch.Tensor:
     """One decayed decode step on the compact state [n, d*d + d*dv + d] (S|P|p, in place)."""
-    n, d = q.shape
-    dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[0] != n or state.numel() != n * pform_record_len(d, dv):
-        raise ValueError("shape mismatch for hla2_decay_step")
-    if o is None:
-        o = torch.empty((n, dv), device=q.device, dtype=torch.float32)
-    rc = lib().hla2_decay_step(_dev(state, "state", torch.float32), _dev(q, "q", torch.float32),
-                               _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), _dev(o, "o", torch.float32),
-                               n, d, dv, int(bool(normalized)), float(gamma), _stream(stream))
-    _check(rc, "hla2_decay_step")
-    return o
+    return _step("hla2_decay_step", state, q, k, v, o, normalized, stream, pform_record_len, gamma=gamma)

@@ -67,8 +67,25 @@ enum { HLA2_DTYPE_F32 = 0, HLA2_DTYPE_BF16 = 1 };
 /*
  * Bytes of device workspace hla2_forward needs for this problem (valid for
  * either value of `normalized`).  Returns 0 for sizes hla2_forward rejects.
+ * The size depends on the segment plan, which depends on the SM count of the
+ * CURRENT device: query it with the device that will run the forward current
+ * (without a visible device the plan assumes 152 SMs).
  */
 HLA2_API size_t hla2_forward_workspace(int B, int H, int T, int d, int dv, int dtype);
+
+/*
+ * The forward's segment plan [HLA §4: the sequence is cut into segments
+ * whose summaries are scanned]: each head's ceil(T/128) chunks of 128 tokens
+ * are cut into *nseg runs of *chunks_per_segment chunks (the last run may be
+ * shorter), one CTA per run.  sm_count > 0 plans for that many SMs (what-if
+ * queries, tests); sm_count <= 0 uses the current device's SM count, which is
+ * what hla2_forward does.  *sm_count_used (may be NULL) receives the count
+ * planned for.  Host only: reads the device attribute once per device, no
+ * GPU work.  Errors: HLA2_ERR_INVALID (B, H, T <= 0 or a NULL nseg /
+ * chunks_per_segment), HLA2_ERR_UNSUPPORTED (B*H > 65535).
+ */
+HLA2_API int hla2_forward_plan(int B, int H, int T, int sm_count, int* nseg, int* chunks_per_segment,
+                               int* sm_count_used);
 
 /*
  * Masked second-order HLA forward, chunk-parallel [HLA §4]: the sequence of

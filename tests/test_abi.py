@@ -95,21 +95,80 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         hla2.lib()
 
 
-@pytest.mark.parametrize("B,H,T,d", [(1, 16, 65536, 128), (4, 16, 4096, 64), (2, 8, 2048, 64), (1, 1, 65536, 128),
-                                     (3, 1, 5000, 64), (1, 40, 200, 32), (1, 128, 16384, 128)])
-def test_bench_plan_mirror_matches_library(B, H, T, d):
-    """bench.py reports the segment plan from a Python copy of the library's
-    plan search; the workspace size (summaries, prefixes, totals, decay
-    factors) pins the two to the same segment count."""
-    import bench
-    nseg, seglen = bench.segments_per_head(B * H, T)
+def _plan_restated(BH, T, sms):
+    """The plan search restated from its description in include/hla2.h and
+    hla2_api.cu: runs of `seglen` 128-token chunks (the last may be shorter),
+    full runs dispatched first, each CTA costing its chunks + 2 on the first
+    free of `sms` SMs; the run length minimises twice the makespan + nseg."""
+    import heapq
     nchunk = (T + 127) // 128
-    assert (nchunk + seglen - 1) // seglen == nseg
+    best = None
+    for ln in range(max(1, (nchunk + 4095) // 4096), nchunk + 1):
+        ns = (nchunk + ln - 1) // ln
+        tail = nchunk - (ns - 1) * ln
+        short = ns > 1 and tail < ln
+        full = BH * (ns - 1) if short else BH * ns
+        q, r = divmod(full, sms)
+        span = (q + 1 if r else q) * (ln + 2)
+        if short:
+            if BH > 20000:
+                span += -(-BH // sms) * (tail + 2)
+            else:
+                load = [(q + 1) * (ln + 2) if i < r else q * (ln + 2) for i in range(sms)]
+                heapq.heapify(load)
+                for _ in range(BH):
+                    t = heapq.heappop(load) + tail + 2
+                    heapq.heappush(load, t)
+                    span = max(span, t)
+        cost2 = 2 * span + ns
+        if best is None or cost2 < best[0]:
+            best = (cost2, ns, ln)
+    return best[1], best[2]
+
+
+PLAN_CASES = [(1, 16, 65536, 128), (4, 16, 4096, 64), (2, 8, 2048, 64), (1, 1, 65536, 128),
+              (3, 1, 5000, 64), (1, 40, 200, 32), (1, 128, 16384, 128)]
+
+
+@pytest.mark.parametrize("sms", [152, 148, 132, 76, 1])
+@pytest.mark.parametrize("B,H,T,d", PLAN_CASES)
+def test_plan_follows_the_sm_count(L, B, H, T, d, sms):
+    """hla2_forward_plan with a faked SM count gives the plan the search
+    describes for that count (the forward plans with the device's count)."""
+    nseg, seglen, used = hla2.hla2_forward_plan(B, H, T, sm_count=sms)
+    assert used == sms
+    assert (nseg, seglen) == _plan_restated(B * H, T, sms)
+    assert ((T + 127) // 128 + seglen - 1) // seglen == nseg
+
+
+@pytest.mark.parametrize("B,H,T,d", PLAN_CASES)
+def test_bench_plan_matches_workspace(L, B, H, T, d):
+    """bench.py reports the plan it reads from the library; the workspace size
+    (summaries, prefixes, totals, decay factors) pins that plan to the one the
+    forward uses on the same device (152 SMs when none is visible)."""
+    import bench
+    nseg, seglen = bench.segments_per_head(B, H, T)
+    assert (nseg, seglen) == hla2.hla2_forward_plan(B, H, T)[:2]
     R = d * d + 2 * d * d + 2 * d
     up = lambda n: (n + 63) // 64 * 64
     BH = B * H
     expect = 4 * (2 * up(BH * nseg * R) + up(BH * R) + up(2 * nseg))
     assert hla2.hla2_forward_workspace(B, H, T, d, d, hla2.HLA2_DTYPE_BF16) == expect
+
+
+def test_plan_without_device_assumes_gb300(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is visible: the plan uses its SM count")
+    assert hla2.hla2_forward_plan(1, 16, 65536)[2] == 152
+    assert hla2.hla2_forward_plan(1, 16, 65536) == hla2.hla2_forward_plan(1, 16, 65536, sm_count=152)
+
+
+def test_plan_rejects_bad_arguments(L):
+    n = ctypes.c_int(0)
+    assert L.hla2_forward_plan(0, 1, 64, 0, ctypes.byref(n), ctypes.byref(n), None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_forward_plan(1, 1, 64, 0, None, ctypes.byref(n), None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_forward_plan(300, 300, 64, 0, ctypes.byref(n), ctypes.byref(n), None) == hla2.HLA2_ERR_UNSUPPORTED
 
 
 def test_host_forward_workspace_and_checks(L):

@@ -82,3 +82,47 @@ def test_noalloc_rejects_problems_beyond_capacity():
     assert (o == 7.0).all()
     with pytest.raises(hla2.HLA2Error):
         hla2.hla2_forward_noalloc(q, q, q, o)
+
+
+def test_noalloc_wrapper_rejects_bad_arguments_before_launch():
+    """The Python wrapper checks what the C entry point cannot see (it only
+    gets pointers): an O of the wrong shape, and Q, K, V of mixed dtypes
+    (fp32 Q with bf16 K would make the kernels read K past its end).  Both
+    raise before anything is launched, so O keeps its contents."""
+    w = W.WORKLOADS[1]
+    q, k, v = (x.to(DEV) for x in W.make_inputs(w, B=1, H=2, T=300))
+    B, H, T, _ = q.shape
+    dv = v.shape[-1]
+    small = torch.full((B, H, T - 1, dv), 7.0, device=DEV)
+    with pytest.raises(ValueError, match="shape"):
+        hla2.hla2_forward_noalloc(q, k, v, O=small)
+    o = torch.full((B, H, T, dv), 7.0, device=DEV)
+    with pytest.raises(ValueError, match="share a dtype"):
+        hla2.hla2_forward_noalloc(q.float(), k, v, O=o)
+    torch.cuda.synchronize()
+    assert (small == 7.0).all() and (o == 7.0).all()
+
+
+def test_noalloc_writes_stay_inside_o():
+    """O is carved out of a larger allocation whose margins hold a byte
+    pattern; after two calls (T = 129 and a ragged 5000) every margin byte
+    still holds it, and the inputs are unchanged."""
+    margin = 64 * 1024
+    w = W.WORKLOADS[3]
+    for T in (129, 5000):
+        q, k, v = (x.to(DEV) for x in W.make_inputs(w, H=3, T=T))
+        B, H, _, d = q.shape
+        dv = v.shape[-1]
+        n = B * H * T * dv
+        buf = torch.empty(n + 2 * (margin // 4), device=DEV, dtype=torch.float32)
+        buf.view(torch.uint8).fill_(0xA5)
+        o = buf[margin // 4: margin // 4 + n].view(B, H, T, dv)
+        snap = [x.clone() for x in (q, k, v)]
+        rc = _noalloc_raw(q, k, v, o)
+        assert rc == hla2.HLA2_OK, hla2.hla2_last_error_detail()
+        torch.cuda.synchronize()
+        assert hla2.hla2_device_status() == 0
+        b = buf.view(torch.uint8)
+        assert (b[:margin] == 0xA5).all() and (b[margin + 4 * n:] == 0xA5).all()
+        assert all(torch.equal(x, y) for x, y in zip((q, k, v), snap))
+        assert torch.isfinite(o).all()
