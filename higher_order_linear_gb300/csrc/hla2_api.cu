@@ -362,9 +362,16 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, 1.0f, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
-    // exclusive scan of the summaries
-    rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
-    if (rc) return rc;
+    // exclusive scan of the summaries: one launch on the tensor-core path
+    if (use_tc) {
+        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, record_len(d, dv), summary_offsets(d, dv), nullptr, status,
+                          normalized != 0};
+        e = launch_tc_scan(kScanHLA, sa, BH, d, dv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "scan");
+    } else {
+        rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
+        if (rc) return rc;
+    }
     if (prof) cudaEventRecord(pe.ev[2], s);
     // outputs
     if (use_tc) e = launch_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, status, s);
@@ -606,8 +613,15 @@ int hla2_ahla_forward(const void* Q, const void* K, const void* V, float* O, int
                            : launch_ahla_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized,
                                               plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "ahla segment summaries");
-    rc = forward_scan_ahla(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
-    if (rc) return rc;
+    if (use_tc) {
+        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, record_len(d, dv), summary_offsets(d, dv), nullptr, status,
+                          false};
+        e = launch_tc_scan(kScanAHLA, sa, BH, d, dv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ahla scan");
+    } else {
+        rc = forward_scan_ahla(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
+        if (rc) return rc;
+    }
     e = use_tc ? launch_ahla_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, plan, status, s)
                : launch_ahla_walk(1, Q, K, V, dtype, O, ws.prefix, nullptr, BH, T, d, dv, normalized, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "ahla segment outputs");
@@ -733,35 +747,17 @@ int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, in
     int* status = nullptr;
     if (use_tc && !(status = device_status_word())) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
     if (use_tc) {
-        // tensor cores: segment summaries S|C|.|P|. from the walks, the decayed
-        // scan of S, the cross terms f_r S_<r C_r on tensor cores, the decayed
-        // scan of P with f_r^2, then the output walks
+        // tensor cores: segment summaries S|C|.|P|. from the walks, the segment
+        // factors, the decayed scan (one launch: S_<r and P_<r with the cross
+        // terms f_r S_<r C_r on tensor cores), then the output walks
         const RecOff ro = summary_offsets(d, dv);
         cudaError_t e = launch_decay_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, gamma, plan, status, s);
         if (e != cudaSuccess) return cuda_fail(e, "decay segment summaries");
         e = launch_decay_factors(ws.fac, T, gamma, plan, s);
-        if (e == cudaSuccess)
-            e = launch_decay_exscan(ws.summ, ws.prefix, BH, plan.nseg, ro.R, 0, (size_t)d * d, nullptr, ro.R, ws.fac, s);
-        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of S");
-        CrossArgs a{};
-        a.A = ws.prefix + ro.S; a.sA = (long long)ro.R;
-        a.B = ws.summ + ro.C;   a.sB = (long long)ro.R;
-        a.base = ws.summ + ro.X; a.sbase = (long long)ro.R;
-        a.out = ws.prefix + ro.X; a.sout = (long long)ro.R;
-        a.alpha = 1.f; a.d = d; a.dv = dv; a.status = status;
-        a.pscale = ws.fac; a.pscale_mod = plan.nseg;
-        for (long long b0 = 0; b0 < (long long)BH * plan.nseg; b0 += 65535) {
-            CrossArgs c = a;
-            const long long nb = (long long)BH * plan.nseg - b0;
-            c.nb = (int)(nb < 65535 ? nb : 65535);
-            c.pscale_off = b0;
-            c.A += b0 * ro.R; c.B += b0 * ro.R; c.base += b0 * ro.R; c.out += b0 * ro.R;
-            e = launch_tc_cross(c, s);
-            if (e != cudaSuccess) return cuda_fail(e, "decay scan: cross terms");
-        }
-        e = launch_decay_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, (size_t)d * dv, nullptr, ro.R,
-                                ws.fac + plan.nseg, s);
-        if (e != cudaSuccess) return cuda_fail(e, "decay scan: prefix sums of P");
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan: segment factors");
+        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, ws.fac, status, false};
+        e = launch_tc_scan(kScanDecay, sa, BH, d, dv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decay scan");
         e = launch_decay_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, gamma, plan, status, s);
         if (e != cudaSuccess) return cuda_fail(e, "decay segment outputs");
         return HLA2_OK;

@@ -203,4 +203,25 @@ cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const v
 // (d = dv in {64, 128}, no extra column).
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);
 
+// The forward's exclusive scan over segment summaries in one launch
+// (hla2_tc_scan.cu), d = dv in {64, 128}: CTA (r, head) folds records
+// 0..r-1 of summ [BH][nseg][R] into prefix record r, cross products on
+// tensor cores (split-bf16 operands).  It writes only the fields the output
+// walks read:
+//   kScanHLA:   S_<r (S), P_<r (X); with extra, also p_<r (x) from m and p
+//   kScanDecay: S_<r, P_<r with the decayed combine (fac = launch_decay_factors)
+//   kScanAHLA:  P_<r (C), E_<r (X) from M (S), P (C), E (X)
+enum ScanOpKind { kScanHLA = 0, kScanDecay = 1, kScanAHLA = 2 };
+struct ScanArgs {
+    const float* summ;
+    float* prefix;
+    int nseg;
+    size_t R;
+    RecOff ro;
+    const float* fac;  // decayed: fac[r] = gamma^{n_r}, fac[nseg + r] = gamma^{2 n_r}
+    int* status;
+    bool extra;
+};
+cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cudaStream_t s);
+
 }  // namespace hla2

@@ -697,20 +697,6 @@ struct CrossLayout {
     static constexpr uint32_t kBytes = 2 * kA + 2 * kB;
 };
 
-// Write the bf16 hi and lo parts of 4 fp32 values (columns c..c+3 of row r).
-__device__ __forceinline__ void put4_split(const Tile& hi, const Tile& lo, int r, int c, float4 x) {
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y), h1 = __floats2bfloat162_rn(x.z, x.w);
-    const uint32_t l0 = pack_bf16(x.x - __low2float(h0), x.y - __high2float(h0));
-    const uint32_t l1 = pack_bf16(x.z - __low2float(h1), x.w - __high2float(h1));
-    const uint32_t off = (uint32_t)((c & 7) >> 2) * 8u;  // which half of the 16-byte chunk
-    const uint32_t ah = hi.chunk(r, c >> 6, (c & 63) >> 3) + off;
-    const uint32_t al = lo.chunk(r, c >> 6, (c & 63) >> 3) + off;
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(ah), "r"(*reinterpret_cast<const uint32_t*>(&h0)),
-                 "r"(*reinterpret_cast<const uint32_t*>(&h1))
-                 : "memory");
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(al), "r"(l0), "r"(l1) : "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
     using CL = CrossLayout<D>;
