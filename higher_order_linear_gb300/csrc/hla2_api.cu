@@ -364,9 +364,12 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     if (prof) cudaEventRecord(pe.ev[1], s);
     // exclusive scan of the summaries: one launch on the tensor-core path
     if (use_tc) {
-        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, record_len(d, dv), summary_offsets(d, dv), nullptr, status,
-                          normalized != 0};
+        const RecOff ro = summary_offsets(d, dv);
+        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, nullptr, status, normalized != 0};
         e = launch_tc_scan(kScanHLA, sa, BH, d, dv, s);
+        if (e == cudaSuccess && plan.nseg > tc_scan_full_max_segments())  // exclusive sums of the terms X_r (and x_r)
+            e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X,
+                              (size_t)d * dv + (normalized ? (size_t)d : 0), nullptr, 0, s);
         if (e != cudaSuccess) return cuda_fail(e, "scan");
     } else {
         rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
@@ -614,9 +617,11 @@ int hla2_ahla_forward(const void* Q, const void* K, const void* V, float* O, int
                                               plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "ahla segment summaries");
     if (use_tc) {
-        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, record_len(d, dv), summary_offsets(d, dv), nullptr, status,
-                          false};
+        const RecOff ro = summary_offsets(d, dv);
+        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, nullptr, status, false};
         e = launch_tc_scan(kScanAHLA, sa, BH, d, dv, s);
+        if (e == cudaSuccess && plan.nseg > tc_scan_full_max_segments())  // exclusive sums of the terms Y_r
+            e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, (size_t)d * dv, nullptr, 0, s);
         if (e != cudaSuccess) return cuda_fail(e, "ahla scan");
     } else {
         rc = forward_scan_ahla(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
@@ -757,6 +762,9 @@ int hla2_decay_forward(const void* Q, const void* K, const void* V, float* O, in
         if (e != cudaSuccess) return cuda_fail(e, "decay scan: segment factors");
         const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, ws.fac, status, false};
         e = launch_tc_scan(kScanDecay, sa, BH, d, dv, s);
+        if (e == cudaSuccess && plan.nseg > tc_scan_full_max_segments())  // decayed sums of the terms X_r with f_r^2
+            e = launch_decay_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, (size_t)d * dv, nullptr, ro.R,
+                                    ws.fac + plan.nseg, s);
         if (e != cudaSuccess) return cuda_fail(e, "decay scan");
         e = launch_decay_tc_walk(1, Q, K, V, O, ws.prefix, nullptr, BH, T, d, dv, gamma, plan, status, s);
         if (e != cudaSuccess) return cuda_fail(e, "decay segment outputs");

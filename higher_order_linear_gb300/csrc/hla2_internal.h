@@ -203,14 +203,17 @@ cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const v
 // (d = dv in {64, 128}, no extra column).
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);
 
-// The forward's exclusive scan over segment summaries in one launch
-// (hla2_tc_scan.cu), d = dv in {64, 128}: CTA (r, head) folds records
-// 0..r-1 of summ [BH][nseg][R] into prefix record r, cross products on
-// tensor cores (split-bf16 operands).  It writes only the fields the output
-// walks read:
-//   kScanHLA:   S_<r (S), P_<r (X); with extra, also p_<r (x) from m and p
-//   kScanDecay: S_<r, P_<r with the decayed combine (fac = launch_decay_factors)
-//   kScanAHLA:  P_<r (C), E_<r (X) from M (S), P (C), E (X)
+// The forward's exclusive scan over segment summaries (hla2_tc_scan.cu),
+// d = dv in {64, 128}: CTA (head, r) folds the product factor of records
+// 0..r-1 (S_<r, or P_<r for AHLA, the prefix's final value) and takes the
+// cross products on tensor cores (split-bf16 operands).  Up to
+// tc_scan_full_max_segments() segments it writes complete prefixes; above,
+// it leaves record r's term X_r in prefix record r, and an exclusive running
+// sum of the X field (launch_exscan / launch_decay_exscan with fac + nseg)
+// completes them.  Fields written (terms, or their exclusive sums):
+//   kScanHLA:   S_<r (S), X_r = P_r + S_<r C_r (X); with extra, x_r = p_r + S_<r m_r (x)
+//   kScanDecay: S_<r (S, decayed fold), X_r = P_r + f_r S_<r C_r (X)
+//   kScanAHLA:  P_<r (C), X_r = E_r + M_r P_<r (X), from M (S), P (C), E (X)
 enum ScanOpKind { kScanHLA = 0, kScanDecay = 1, kScanAHLA = 2 };
 struct ScanArgs {
     const float* summ;
@@ -223,5 +226,8 @@ struct ScanArgs {
     bool extra;
 };
 cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cudaStream_t s);
+// Scans of at most this many segments complete every prefix inside
+// launch_tc_scan (no running-sum pass is needed afterwards).
+int tc_scan_full_max_segments();
 
 }  // namespace hla2

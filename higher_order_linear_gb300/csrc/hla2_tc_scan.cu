@@ -7,28 +7,33 @@
 // scan gives every segment the state of the serial recurrence at its start.
 //
 // The forward cuts each head into a few segments (about ten on the long
-// workloads), so the scan is short and latency-bound: the element-serial
-// sums and the batched products it used to run as three launches cost more in
-// launch and pass latency than in work.  Here one CTA computes one segment's
-// prefix by folding the records before it, in order:
-//   HLA (P-form):  S_<r = sum_{j<r} S_j,        P_<r = sum_{j<r} (P_j + S_<j C_j)
-//                  (normalised: p_<r = sum_{j<r} (p_j + S_<j m_j))
-//   decayed:       S_<j+1 = f_j S_<j + S_j,     P_<j+1 = f_j^2 P_<j + P_j + f_j S_<j C_j
-//                  (f_j = gamma^{tokens of segment j}, the decayed combine)
-//   AHLA:          P_<r = sum_{j<r} P_j,        E_<r = sum_{j<r} (E_j + M_j P_<j)
-// The running sums stay in fp32 registers; each product is taken on the
-// tensor cores with both operands split into bf16 hi + lo parts
+// workloads), so the scan is short and latency-bound.  It runs as one launch
+// of a CTA per (head, record r):
+//   1. fold the product factor over the earlier records: S_<r (HLA, with the
+//      decay factors for the decayed operator) or P_<r (AHLA), which is also
+//      the prefix's own final value;
+//   2. take record r's cross product on tensor cores: the term
+//      X_r = P_r + S_<r C_r (HLA), P_r + f_r S_<r C_r (decayed, f_r =
+//      gamma^{tokens of segment r}), E_r + M_r P_<r (AHLA); normalised HLA
+//      also x_r = p_r + S_<r m_r;
+//   3. a second launch (the element-parallel running sums of hla2_scan.cu)
+//      turns the terms into exclusive prefix sums in place:
+//      P_<n = sum_{r<n} X_r (decayed: P_<n+1 = f_n^2 P_<n + X_n).
+// Every product has both operands split into bf16 hi + lo parts
 // (hi*hi + hi*lo + lo*hi, fp32 accumulation in tensor memory), which keeps
-// about 16 significant bits of every operand, as the batched cross kernel did.
-// CTA r does r - 1 products (the first prefix factor is zero), so the last
-// segment's CTA bounds the launch; with about ten segments that is far below
-// the three launches it replaces.
+// about 16 significant bits of every operand.  Running sums are fp32, laid out
+// so that a warp reads and writes whole rows of a record.
 #include "hla2_tc_common.cuh"
 
 namespace hla2 {
 namespace {
 
 constexpr int kScanWarps = 16;  // four per 32-lane quarter of tensor memory
+// Scans of up to this many segments run in one launch (each CTA sums its
+// whole prefix); longer ones take one product per CTA and a running-sum pass.
+// On GB300 the single launch took 8.6 us at 3 segments (against 18.6 us for
+// the two launches) and 43 us at 10 (against 27 us).
+constexpr int kScanFullMaxSegments = 4;
 constexpr int kScanThreadsTC = kScanWarps * 32;
 
 template <int D>
@@ -36,7 +41,9 @@ struct ScanTileLayout {
     static constexpr uint32_t kA = 128u * D * 2u;  // A operand keeps 128 rows (MMA M = 128); rows >= D are zero
     static constexpr uint32_t kB = (uint32_t)D * D * 2u;
     static constexpr uint32_t Ahi = 0, Alo = kA, Bhi = 2 * kA, Blo = 2 * kA + kB;
-    static constexpr uint32_t kBytes = 2 * kA + 2 * kB;
+    static constexpr int kStageLd = D + 4;  // fp32 row stride of the product staging (padded against bank conflicts)
+    static constexpr uint32_t Stage = 2 * kA + 2 * kB;
+    static constexpr uint32_t kBytes = Stage + (uint32_t)D * kStageLd * 4u;
 };
 
 template <int NC>
@@ -57,58 +64,64 @@ __device__ __forceinline__ void tmem_ld_nc(uint32_t taddr, float (&v)[NC]) {
     for (int i = 0; i < NC; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Loads NC consecutive floats (16-byte aligned) into v.
-template <int NC>
-__device__ __forceinline__ void ld_row(const float* p, float (&v)[NC]) {
+// Element layout of the running sums: thread t holds the float4 pieces
+// f = t + kScanThreadsTC * i of a D x D matrix (row 4f / D, column 4f % D),
+// so that a warp reads and writes whole rows (coalesced).  Only the product
+// drain uses the tensor-memory layout (lane = row), through a staging buffer.
+template <int D>
+struct Piece {
+    static constexpr int N = D * D / 4 / kScanThreadsTC;  // float4 pieces per thread
+    __device__ static int row(int tid, int i) { return (4 * (tid + kScanThreadsTC * i)) / D; }
+    __device__ static int col(int tid, int i) { return (4 * (tid + kScanThreadsTC * i)) % D; }
+};
+
+template <int D>
+__device__ __forceinline__ void ld_mat(const float* m, int tid, float4 (&v)[Piece<D>::N]) {
 #pragma unroll
-    for (int i = 0; i < NC; i += 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(p + i));
-        v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
-    }
-}
-template <int NC>
-__device__ __forceinline__ void st_row(float* p, const float (&v)[NC]) {
-#pragma unroll
-    for (int i = 0; i < NC; i += 4) *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-}
-template <int NC>
-__device__ __forceinline__ void put_split_row(const Tile& hi, const Tile& lo, int r, int c0, const float (&v)[NC]) {
-#pragma unroll
-    for (int i = 0; i < NC; i += 4) put4_split(hi, lo, r, c0 + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+    for (int i = 0; i < Piece<D>::N; ++i) v[i] = __ldg(reinterpret_cast<const float4*>(m) + tid + kScanThreadsTC * i);
 }
 
-template <int D, int OP, bool EXTRA>
+// FULL: CTA r computes its whole prefix (every term X_j, j < r, summed in
+// registers): one launch, r - 1 products in a row; for short scans.
+// Otherwise CTA r computes only its own term X_r, and an exclusive running
+// sum over the records (a second, element-parallel launch) completes the
+// prefixes: one product per CTA; for longer scans.
+template <int D, int OP, bool EXTRA, bool FULL>
 __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) {
     using TL = ScanTileLayout<D>;
-    constexpr int NC = D / 4;  // columns per thread: four warps share a lane quarter
+    using PC = Piece<D>;
+    constexpr int NV = PC::N;
+    constexpr int NC = D / 4;  // drain: columns per warp (four warps share a lane quarter)
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     __shared__ __align__(8) unsigned long long bar_mma;
     __shared__ uint32_t tmem_slot;
-    __shared__ float px_part[4][128];  // normalised walk: partial S_<j m_j per column part
-    __shared__ int s_abort;
+    __shared__ int s_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, part = warp >> 2;
-    const int row = quarter * 32 + lane;
-    const int c0 = part * NC;
-    const bool state_row = row < D;
-    const int r = blockIdx.x, head = blockIdx.y;
+    const int drow = quarter * 32 + lane;  // tensor-memory lane this thread drains
+    const int dc0 = part * NC;
+    // grid (BH, nseg): the records with the longest folds (largest r) go first
+    const int head = blockIdx.x, r = (int)gridDim.y - 1 - (int)blockIdx.y;
     const size_t R = a.R;
     const float* rec0 = a.summ + (size_t)head * a.nseg * R;
     float* out = a.prefix + ((size_t)head * a.nseg + r) * R;
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tAh{dsm + TL::Ahi, 128}, tAl{dsm + TL::Alo, 128}, tBh{dsm + TL::Bhi, D}, tBl{dsm + TL::Blo, D};
+    float* stage = reinterpret_cast<float*>(dsm_raw + (dsm - smem_u32(dsm_raw)) + TL::Stage);
     constexpr uint32_t kCols = D < 32 ? 32 : D;
 
-    // field offsets: the running pair (acc1, acc2) and the record fields feeding them
-    //   HLA / decayed: acc1 = S (S), acc2 = P (X); product S_<j C_j, C at C
-    //   AHLA:          acc1 = P (C), acc2 = E (X); product M_j P_<j, M at S
+    // fields: F1 is folded over the earlier records into the prefix factor
+    // (S_<j, or P_<j for AHLA), which is also the prefix's own final value;
+    // record j's term is X_j = F2_j + f_j * (product), F2 and the product:
+    //   HLA / decayed: F1 = S, F2 = P (at X), product S_<j C_j  (C at C)
+    //   AHLA:          F1 = P (at C), F2 = E (at X), product M_j P_<j  (M at S)
     const size_t off1 = (OP == kScanAHLA) ? a.ro.C : a.ro.S;
     const size_t off2 = a.ro.X;
-    const size_t offR = (OP == kScanAHLA) ? a.ro.S : a.ro.C;  // the record's own product factor
+    const size_t offR = (OP == kScanAHLA) ? a.ro.S : a.ro.C;
 
     if (tid == 0) {
-        s_abort = 0;
+        s_flag = 0;
         mbar_init(smem_u32(&bar_mma), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -118,8 +131,7 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // A rows >= D never change: zero them once (both parts)
-    if (D < 128)
+    if (D < 128)  // A rows >= D stay zero
         for (int i = tid; i < (128 - D) * D / 4; i += kScanThreadsTC)
             put4_split(tAh, tAl, D + i / (D / 4), (i % (D / 4)) * 4, make_float4(0.f, 0.f, 0.f, 0.f));
     tc_fence_before();
@@ -128,108 +140,145 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
     const uint32_t tmem = tmem_slot;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
-
-    float acc1[NC], acc2[NC];
-#pragma unroll
-    for (int i = 0; i < NC; ++i) acc1[i] = acc2[i] = 0.f;
-    float px = 0.f, ax = 0.f;  // normalised: this part's sum of S_<j m_j, and sum of p_j (part 0)
-    bool ok = true;
     uint32_t phase = 0;
 
-    for (int j = 0; j < r; ++j) {
-        const float* rec = rec0 + (size_t)j * R;
-        // the product has a zero factor for j = 0 (S_<0 = 0, P_<0 = 0)
-        const bool prod = j > 0;
-        if (prod) {
-            // operands of this record's product: A (M = output rows, K-major),
-            // B (rows = contraction index, read MN-major)
-            if (state_row) {
-                float x[NC];
-                ld_row<NC>(rec + offR + (size_t)row * D + c0, x);
-                if (OP == kScanAHLA) {
-                    put_split_row<NC>(tAh, tAl, row, c0, x);      // A = M_j
-                    put_split_row<NC>(tBh, tBl, row, c0, acc1);   // B = P_<j
-                } else {
-                    put_split_row<NC>(tAh, tAl, row, c0, acc1);   // A = S_<j
-                    put_split_row<NC>(tBh, tBl, row, c0, x);      // B = C_j
-                }
-            }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (tid == 0) {
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBh.mnmaj(ks), idesc, ks > 0);
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBl.mnmaj(ks), idesc, 1);
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAl.kmaj(ks), tBh.mnmaj(ks), idesc, 1);
-                mma_commit(smem_u32(&bar_mma));
-            }
-            __syncwarp();
-        }
-        // while the products run: this record's summands (S_<j, P_<j, or
-        // P_<j, E_<j for AHLA, already fed the tiles and the p term above)
-        float f = 1.f, f2 = 1.f;
-        if (OP == kScanDecay) {
-            f = __ldg(a.fac + j);
-            f2 = __ldg(a.fac + a.nseg + j);
-        }
-        if (EXTRA && state_row) {
-            // p_<r gathers p_j + S_<j m_j: this thread's columns of S_<j times m_j
-            float m[NC];
-            ld_row<NC>(rec + a.ro.m + c0, m);
+    // acc += f * (the product of record j's factor xop with the running factor
+    // acc1), on tensor cores; false when a bounded wait ran out (block-uniform)
+    auto add_product = [&](const float4 (&acc1)[NV], const float4 (&xop)[NV], float f, float4 (&acc)[NV]) -> bool {
+        // A (output rows, K-major), B (rows = contraction index, MN-major)
 #pragma unroll
-            for (int i = 0; i < NC; ++i) px = fmaf(acc1[i], m[i], px);
-            if (part == 0) ax += __ldg(rec + a.ro.x + row);
-        }
-        if (state_row) {
-            float x[NC];
-            ld_row<NC>(rec + off1 + (size_t)row * D + c0, x);
-#pragma unroll
-            for (int i = 0; i < NC; ++i) acc1[i] = fmaf(f, acc1[i], x[i]);
-            ld_row<NC>(rec + off2 + (size_t)row * D + c0, x);
-#pragma unroll
-            for (int i = 0; i < NC; ++i) acc2[i] = fmaf(f2, acc2[i], x[i]);
-        }
-        if (prod) {
-            // bounded wait for the products, then this thread's lane and columns
-            bool done = mbar_try(smem_u32(&bar_mma), phase);
-            if (!done) {
-                const unsigned long long t0 = globaltimer();
-                while (!(done = mbar_try(smem_u32(&bar_mma), phase)))
-                    if (globaltimer() - t0 > kWaitNs) break;
-            }
-            phase ^= 1u;
-            tc_fence_after();
-            if (!done) {
-                if (lane == 0) atomicExch(a.status, (int)kDevWaitTimeout);
-                s_abort = 1;
-            }
-            __syncwarp();
-            // the load is warp-collective: a warp loads only once every lane saw
-            // the products complete; rows >= D are loaded and ignored
-            if (__all_sync(0xffffffffu, done)) {
-                float pr[NC];
-                tmem_ld_nc<NC>(tmem + lane_off + (uint32_t)c0, pr);
-#pragma unroll
-                for (int i = 0; i < NC; ++i) acc2[i] = fmaf(f, pr[i], acc2[i]);
-            }
-            tc_fence_before();
-            __syncthreads();  // tensor memory and the operand tiles are reused by the next product
-            if (s_abort) {  // block-uniform: read after the barrier
-                ok = false;
-                break;
+        for (int i = 0; i < NV; ++i) {
+            const int rr = PC::row(tid, i), cc = PC::col(tid, i);
+            if (OP == kScanAHLA) {
+                put4_split(tAh, tAl, rr, cc, xop[i]);   // A = M_j
+                put4_split(tBh, tBl, rr, cc, acc1[i]);  // B = P_<j
+            } else {
+                put4_split(tAh, tAl, rr, cc, acc1[i]);  // A = S_<j
+                put4_split(tBh, tBl, rr, cc, xop[i]);   // B = C_j
             }
         }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();  // tiles written; the previous staged product read
+        tc_fence_after();
+        if (tid == 0) {
+            for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBh.mnmaj(ks), idesc, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAh.kmaj(ks), tBl.mnmaj(ks), idesc, 1);
+            for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tmem, tAl.kmaj(ks), tBh.mnmaj(ks), idesc, 1);
+            mma_commit(smem_u32(&bar_mma));
+        }
+        __syncwarp();
+        bool done = mbar_try(smem_u32(&bar_mma), phase);
+        if (!done) {
+            const unsigned long long t0 = globaltimer();
+            while (!(done = mbar_try(smem_u32(&bar_mma), phase)))
+                if (globaltimer() - t0 > kWaitNs) break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+        if (!done) {
+            if (lane == 0) atomicExch(a.status, (int)kDevWaitTimeout);
+            s_flag = 1;
+        }
+        __syncwarp();
+        // drain (warp-collective, lane = row) into the staging buffer, only
+        // once every lane saw the products complete; rows >= D are dropped
+        if (__all_sync(0xffffffffu, done)) {
+            float pr[NC];
+            tmem_ld_nc<NC>(tmem + lane_off + (uint32_t)dc0, pr);
+            if (drow < D)
+#pragma unroll
+                for (int i = 0; i < NC; i += 4)
+                    *reinterpret_cast<float4*>(stage + drow * TL::kStageLd + dc0 + i) =
+                        make_float4(pr[i], pr[i + 1], pr[i + 2], pr[i + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();  // staged; tensor memory free for the next product
+        if (s_flag) return false;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float4 y = *reinterpret_cast<const float4*>(stage + PC::row(tid, i) * TL::kStageLd + PC::col(tid, i));
+            acc[i] = make_float4(fmaf(f, y.x, acc[i].x), fmaf(f, y.y, acc[i].y), fmaf(f, y.z, acc[i].z),
+                                 fmaf(f, y.w, acc[i].w));
+        }
+        return true;
+    };
+    auto fold = [&](float4 (&acc)[NV], const float* m, float f) {  // acc = f * acc + m
+        float4 x[NV];
+        ld_mat<D>(m, tid, x);
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            acc[i] = make_float4(fmaf(f, acc[i].x, x[i].x), fmaf(f, acc[i].y, x[i].y), fmaf(f, acc[i].z, x[i].z),
+                                 fmaf(f, acc[i].w, x[i].w));
+    };
+    // normalised: x_j = p_j + S_<j m_j, per row (threads sharing a row reduce over it)
+    constexpr int kLanesPerRow = D / 4;
+    auto add_pterm = [&](const float4 (&acc1)[NV], const float* rec, float (&px)[NV]) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float4 m = __ldg(reinterpret_cast<const float4*>(rec + a.ro.m + PC::col(tid, i)));
+            px[i] += acc1[i].x * m.x + acc1[i].y * m.y + acc1[i].z * m.z + acc1[i].w * m.w;
+        }
+    };
+
+    float4 acc1[NV], acc2[NV];  // F1 folded; the prefix's corrected part (FULL) or this record's term
+    float px[NV];
+    float ax = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        acc1[i] = acc2[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        px[i] = 0.f;
+    }
+    if (FULL) {
+        // the whole prefix: X_<j+1 = f_j^2 X_<j + F2_j + f_j (product of record j)
+        for (int j = 0; j < r; ++j) {
+            const float* rec = rec0 + (size_t)j * R;
+            const float f = (OP == kScanDecay) ? __ldg(a.fac + j) : 1.f;
+            const float f2 = (OP == kScanDecay) ? __ldg(a.fac + a.nseg + j) : 1.f;
+            fold(acc2, rec + off2, f2);
+            if (EXTRA) {
+                add_pterm(acc1, rec, px);
+                if (tid < D) ax += __ldg(rec + a.ro.x + tid);
+            }
+            if (j > 0) {
+                float4 xop[NV];
+                ld_mat<D>(rec + offR, tid, xop);
+                if (!add_product(acc1, xop, f, acc2)) break;
+            }
+            fold(acc1, rec + off1, f);
+        }
+    } else {
+        // this record's term X_r; the running sum over records follows in a second launch
+        for (int i0 = 0; i0 < r; ++i0) fold(acc1, rec0 + (size_t)i0 * R + off1, (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f);
+        const float* rec = rec0 + (size_t)r * R;
+        fold(acc2, rec + off2, 1.f);
+        if (EXTRA) {
+            add_pterm(acc1, rec, px);
+            if (tid < D) ax = __ldg(rec + a.ro.x + tid);
+        }
+        if (r > 0) {
+            float4 xop[NV];
+            ld_mat<D>(rec + offR, tid, xop);
+            add_product(acc1, xop, (OP == kScanDecay) ? __ldg(a.fac + r) : 1.f, acc2);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        reinterpret_cast<float4*>(out + off1)[tid + kScanThreadsTC * i] = acc1[i];
+        reinterpret_cast<float4*>(out + off2)[tid + kScanThreadsTC * i] = acc2[i];
     }
     if (EXTRA) {
-        px_part[part][row] = px;
+        float* rowdot = stage;
+        __syncthreads();  // every thread has read the staged products
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float v = px[i];
+#pragma unroll
+            for (int o = kLanesPerRow / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if ((tid % kLanesPerRow) == 0) rowdot[PC::row(tid, i)] = v;
+        }
         __syncthreads();
-    }
-    if (ok && state_row) {
-        st_row<NC>(out + off1 + (size_t)row * D + c0, acc1);
-        st_row<NC>(out + off2 + (size_t)row * D + c0, acc2);
-        if (EXTRA && part == 0) out[a.ro.x + row] = ax + px_part[0][row] + px_part[1][row] + px_part[2][row] +
-                                                    px_part[3][row];
+        if (tid < D) out[a.ro.x + tid] = ax + rowdot[tid];
     }
     tc_fence_before();
     __syncthreads();
@@ -238,33 +287,38 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
 }
 
-template <int D, int OP, bool EXTRA>
+template <int D, int OP, bool EXTRA, bool FULL>
 cudaError_t launch_scan_t(const ScanArgs& a, int BH, cudaStream_t s) {
     const size_t smem = ScanTileLayout<D>::kBytes + 1024;
-    auto kern = tc_scan_kernel<D, OP, EXTRA>;
+    auto kern = tc_scan_kernel<D, OP, EXTRA, FULL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.nseg, BH);
+    dim3 grid(BH, a.nseg);
     kern<<<grid, kScanThreadsTC, smem, s>>>(a);
     note_launches(1);
     return cudaGetLastError();
 }
 
+template <int D, bool FULL>
+cudaError_t launch_scan_d(int op, const ScanArgs& a, int BH, cudaStream_t s) {
+    if (op == kScanHLA)
+        return a.extra ? launch_scan_t<D, kScanHLA, true, FULL>(a, BH, s) : launch_scan_t<D, kScanHLA, false, FULL>(a, BH, s);
+    if (op == kScanDecay) return launch_scan_t<D, kScanDecay, false, FULL>(a, BH, s);
+    return launch_scan_t<D, kScanAHLA, false, FULL>(a, BH, s);
+}
+
 }  // namespace
+
+int tc_scan_full_max_segments() { return kScanFullMaxSegments; }
 
 cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cudaStream_t s) {
     if (BH == 0 || a.nseg == 0) return cudaSuccess;
     if (d != dv || (d != 64 && d != 128) || BH > 65535 || a.nseg > 65535) return cudaErrorInvalidValue;
-    if (a.extra && op != kScanHLA) return cudaErrorInvalidValue;
-    if (op == kScanHLA) {
-        if (a.extra) return d == 128 ? launch_scan_t<128, kScanHLA, true>(a, BH, s) : launch_scan_t<64, kScanHLA, true>(a, BH, s);
-        return d == 128 ? launch_scan_t<128, kScanHLA, false>(a, BH, s) : launch_scan_t<64, kScanHLA, false>(a, BH, s);
-    }
-    if (op == kScanDecay)
-        return d == 128 ? launch_scan_t<128, kScanDecay, false>(a, BH, s) : launch_scan_t<64, kScanDecay, false>(a, BH, s);
-    if (op == kScanAHLA)
-        return d == 128 ? launch_scan_t<128, kScanAHLA, false>(a, BH, s) : launch_scan_t<64, kScanAHLA, false>(a, BH, s);
-    return cudaErrorInvalidValue;
+    if ((a.extra && op != kScanHLA) || (op != kScanHLA && op != kScanDecay && op != kScanAHLA))
+        return cudaErrorInvalidValue;
+    const bool full = a.nseg <= kScanFullMaxSegments;
+    if (d == 128) return full ? launch_scan_d<128, true>(op, a, BH, s) : launch_scan_d<128, false>(op, a, BH, s);
+    return full ? launch_scan_d<64, true>(op, a, BH, s) : launch_scan_d<64, false>(op, a, BH, s);
 }
 
 }  // namespace hla2
