@@ -861,10 +861,10 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
         return mode == 0 ? launch_t<64, 0, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
                          : launch_t<64, 1, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     }
-    if (d == 128) return mode == 0 ? launch_t<128, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
-                                   : launch_t<128, 1, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
-    if (d == 64) return mode == 0 ? launch_t<64, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
-                                  : launch_t<64, 1, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    // unnormalised outputs: the walk pipelined across chunks (hla2_tc_out.cu)
+    if (mode == 1) return launch_tc_out(Q, K, V, O, prefix, BH, T, d, dv, plan, status, s);
+    if (d == 128) return launch_t<128, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    if (d == 64) return launch_t<64, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     return cudaErrorInvalidValue;
 }
 
