@@ -16,20 +16,21 @@
 // instead of two.
 //
 // Tensor memory holds two working regions besides the running S and P:
-//   alpha: A, then W            beta: X (= Q S0 + A K), then O
-// so that the next chunk's A = Q K^T can start in alpha as soon as W has been
-// drained, while O of the current chunk is still being formed and drained in
-// beta; Q is double-buffered for the same reason, and each chunk's V starts
-// loading as soon as the previous O has completed.  In shared memory the bf16
-// A and then W share one tile, X another (O leaves through both); the bf16
-// operand copies of S0 and P0 share a third: S0 is read by Q S0 early in a
-// chunk, P0 by Q P0 late in it.
+//   alpha: A, then W (each packed to bf16 in place, the A operand of A K and
+//          of W V)          beta: X (= Q S0 + A K), then O
+// so that X and O never wait for alpha, and nothing on the chain waits for
+// shared memory: the drains of A and W stay in tensor memory, X goes to its
+// own tile (the B operand of W and the A operand of X^T V), and O leaves
+// through staging boxes that the next drains do not touch.  Q is
+// double-buffered, and each chunk's V starts loading as soon as the previous
+// O has completed (loads come from their own warp).  The bf16 operand copies of S0 and P0 share one tile: S0
+// is read by Q S0 early in a chunk, P0 by Q P0 late in it.
 //
 // Precision: products take bf16 operands with fp32 accumulation; the running
 // S and P stay fp32 in tensor memory.  On a head's first chunk, where an
 // output can be a single product (t = 0 gives (q.k)^2 v) and roundings do not
 // average out, X and W are split into bf16 hi + lo parts (W = Q X_hi^T +
-// Q X_lo^T, O = W_hi V + W_lo V).
+// Q X_lo^T, O = W_hi V + W_lo V; W_lo packed next to W_hi in alpha).
 #include "hla2_tc_common.cuh"
 
 namespace hla2 {
@@ -44,17 +45,22 @@ struct OutParams {
 template <int D>
 struct OutLayout {
     static constexpr uint32_t kTok = kL * D * 2;  // Q, K, V tiles
-    static constexpr uint32_t kSq = kL * kL * 2;  // A / W tile; X tile (O staging)
+    static constexpr uint32_t kSq = kL * kL * 2;  // X tile (and, at D = 128, the first O staging box of each warp)
     static constexpr uint32_t kSt = D * D * 2;    // S0 / P0 tile
-    static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, A = 4 * kTok, X = A + kSq, SP = X + kSq;
+    // O staging (the other box of each warp at D = 128, the only one at
+    // D = 64; eight 4 KB boxes) and, on a head's first chunk, X_lo (kL x D)
+    static constexpr uint32_t kO = kSq;
+    static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, X = 4 * kTok, O = X + kSq, SP = O + kO;
     static constexpr uint32_t kBytes = SP + kSt;
 };
 
-// Warp roles as in the other walks: warps 0..7 drain tensor memory (warp w
-// owns lane quarter w % 4 and column half w / 4 of every region), warp 8
-// (lane 0) issues every TMA copy and MMA; they meet only on mbarriers.
+// Warp roles: warps 0..7 drain tensor memory (warp w owns lane quarter w % 4
+// and column half w / 4 of every region), warp 8 (lane 0) issues every MMA,
+// warp 9 (lane 0) every tile load, so that MMA issue never waits behind a
+// busy bulk-copy queue; the roles meet only on mbarriers.
+constexpr int kThreadsOut = (kDrainWarps + 2) * 32;
 template <int D>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsOut, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
               const __grid_constant__ CUtensorMap mR, OutParams p) {
@@ -70,6 +76,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    const bool producer = warp == kDrainWarps + 1;
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
@@ -79,12 +86,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
+    const bool drainer = warp < kDrainWarps;
+    const bool state_rows = drainer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
-    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL}, tSP{dsm + LY::SP, D};
+    const Tile tX{dsm + LY::X, kL}, tO{dsm + LY::O, kL}, tSP{dsm + LY::SP, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
@@ -107,7 +115,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tAl_ = tmem + 0;           // alpha: A, then W (and W_lo on a head's first chunk)
+    const uint32_t tAl_ = tmem + 0;           // alpha: A, then W (packed bf16 in place; W_lo too on a first chunk)
     const uint32_t tBe_ = tmem + 128;         // beta: Q S0 + A K = X, then O
     const uint32_t tS_ = tmem + 128 + D;      // running S
     const uint32_t tP_ = tmem + 128 + 2 * D;  // running P
@@ -143,27 +151,41 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
     };
-    auto drain128 = [&](uint32_t treg, const Tile& t, bool mask) {
-        uint32_t r[64];
-        tmem_ld_cols<64>(treg + lane_off + c128, r);
-        put_row32(t, row, c128, r, mask);
-        put_row32(t, row, c128 + 32, r + 32, mask);
-    };
     auto drainD = [&](uint32_t treg, const Tile& t) {
         uint32_t r[64];
         tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
         put_row32(t, row, cD, r, false);
         if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
     };
-    // packed W_lo: drain warp h stores the bf16 pairs of its W columns
-    // [64h, 64h+64) into the first 32 of those columns, which it has itself
-    // just read, so no other warp's pending read is overwritten.  K-step ks
-    // of W_lo V reads 8 packed columns.
-    auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * 64 + 8 * (ks & 3)); };
+    // Packed bf16 operands in alpha: drain warp h packs the pairs of its
+    // columns [64h, 64h+64) (A, or W and on a first chunk also W_lo) into
+    // columns [64h, 64h+32) (and W_lo into [64h+32, 64h+64)), which it has
+    // itself just read, so no other warp's pending read is overwritten.
+    // K-step ks (16 tokens) of the product reads 8 packed columns.
+    auto pk_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * 64 + 8 * (ks & 3)); };
+    // this lane's 64 columns of alpha -> bf16 pairs (masked to columns <= row),
+    // optionally with the lo parts, written back packed
+    auto pack_alpha = [&](bool split) {
+        uint32_t r[64];
+        tmem_ld_cols<64>(tAl_ + lane_off + c128, r);
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+            if (c128 + 2 * j > row) x0 = 0.f;
+            if (c128 + 2 * j + 1 > row) x1 = 0.f;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+            hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+            if (split) lo[j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
+        }
+        tmem_st32(tAl_ + lane_off + (uint32_t)c128, hi);
+        if (split) tmem_st32(tAl_ + lane_off + (uint32_t)c128 + 32u, lo);
+        tmem_st_wait();
+    };
 
     // ---- prologue: the first tiles start moving while the drain warps load
     // the segment prefix (S0, P0) into tensor memory and S0 into its tile ----
-    if (issuer && lane == 0 && nchunks > 0) {
+    if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ0, &mQ, tQ0, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -172,10 +194,10 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     if (state_rows && nchunks > 0) {
         // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
         // 32 x 32 fp32 boxes by bulk tensor loads (mR maps the records as
-        // (3D + 2) rows of D floats) into a private staging area in the A / X
+        // (3D + 2) rows of D floats) into a private staging area in the X / O
         // tiles, which nothing else touches before the first chunk
         const int rec = head * p.nseg + seg;
-        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+        const uint32_t stage = dsm + LY::X + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
@@ -206,7 +228,6 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     tc_fence_after();
 
     constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
-    constexpr uint32_t iSD = idesc_bf16(128, 128, false, false);  // W = Q X^T: N = 128 tokens
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);    // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
@@ -217,25 +238,17 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                const bool has_next = it + 1 < nchunks;
-                const bool first = c == 0;            // S0 = P0 = 0; X, W split
-                const bool prev_first = it > 0 && c == 1;
+                const bool first = c == 0;  // S0 = P0 = 0; X, W split
                 const Tile& tQ = (it & 1) ? tQ1 : tQ0;
                 if (!wait_bar((it & 1) ? LQ1 : LQ0, (uint32_t)((it >> 1) & 1)) || !wait_bar(LK, ph)) break;
-                // alpha is free once the previous W was drained (and, after a
-                // head's first chunk, once O has read W_lo from it)
-                if (it > 0 && !wait_bar(prev_first ? DO : DW, pph)) break;
+                // alpha is free once the previous O has read W from it
+                if (it > 0 && !wait_bar(CO, pph)) break;
                 tc_fence_after();
                 // A = Q K^T
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                 mma_commit(bar(CA));
                 if (it > 0) {
-                    // the previous O complete: the V tile and the other Q buffer
-                    // are no longer read, so this chunk's V and the next Q start
-                    // moving; then beta free (O read out) and S0 in its tile
-                    if (!wait_bar(CO, pph)) break;
-                    issue_load(LV, &mV, tV, c);
-                    if (has_next) issue_load((it + 1) & 1 ? LQ1 : LQ0, &mQ, (it + 1) & 1 ? tQ1 : tQ0, c + 1);
+                    // beta free (O read out) and S0 of this chunk in its tile
                     if (!wait_bar(DO, pph) || !wait_bar(DS, pph)) break;
                     tc_fence_after();
                 }
@@ -244,56 +257,70 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.kmaj(ks), iKK, ks > 0);
                 mma_commit(bar(CQS));
                 for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
-                if (!wait_bar(DA, ph)) break;  // sA = A
+                if (!wait_bar(DA, ph)) break;  // A packed in alpha
                 tc_fence_after();
-                // X += A K
+                // X += A K  (A from tensor memory)
                 for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tBe_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                    mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CX));
-                if (has_next) {
-                    if (!wait_bar(CX, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
-                }
-                if (!wait_bar(DX, ph)) break;  // sX = X (and X_lo in sA on a head's first chunk); beta free
+                if (!wait_bar(DX, ph)) break;  // sX = X (and sO = X_lo on a head's first chunk); beta free
                 tc_fence_after();
-                // W = Q X^T (+ Q X_lo^T)
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tX.kmaj(ks), iSD, ks > 0);
+                // W = Q X^T (+ Q X_lo^T) into alpha (A there was read by A K)
+                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tX.kmaj(ks), iSq, ks > 0);
                 if (first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tA.kmaj(ks), iSD, 1);
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tO.kmaj(ks), iSq, 1);
                 mma_commit(bar(CW));
                 // P += X^T V once P0 of this chunk has left TMEM P
                 if (!wait_bar(LV, ph) || !wait_bar(DP, ph)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                 mma_commit(bar(CP));
-                if (!wait_bar(DW, ph)) break;  // sA = W (hi; W_lo packed in alpha on a first chunk)
+                if (!wait_bar(DW, ph)) break;  // W packed in alpha (and W_lo on a head's first chunk)
                 tc_fence_after();
-                // O = Q P0 + W V (+ W_lo V)
+                // O = Q P0 + W V (+ W_lo V)  (W from tensor memory)
                 if (!first)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.mnmaj(ks), iKM, ks > 0);
                 for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tBe_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                    mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                 if (first)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tBe_, tAl_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 32u, tV.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CO));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+    } else if (producer) {
+        // =========================== producer ===========================
+        // each tile loads as soon as its buffer is free: the next K once A K
+        // (its last reader) completed, the next V and the Q after next once O
+        // (the last reader of this chunk's V and Q) completed
+        if (lane == 0) {
+            for (int it = 0; it + 1 < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1;
+                if (!wait_bar(CX, ph)) break;
+                issue_load(LK, &mK, tK, c + 1);
+                if (!wait_bar(CO, ph)) break;
+                issue_load(LV, &mV, tV, c + 1);
+                if (it + 2 < nchunks) issue_load((it & 1) ? LQ1 : LQ0, &mQ, (it & 1) ? tQ1 : tQ0, c + 2);
+            }
+        }
     } else {
         // ========================== drain warps ==========================
+        // this warp's O staging boxes (32 rows x 32 fp32 columns, 4 KB each):
+        // the first in sX at D = 128 (the same rows and column block as this
+        // warp's own share of X, so only its own stores must have left it
+        // before its X drain) and the other in sO; at D = 64 the only one in sO
+        const uint32_t wbox = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
         for (int it = 0; it < nchunks; ++it) {
             const uint32_t ph = it & 1;
             const int c = c_begin + it;
             const bool has_next = it + 1 < nchunks;
             const bool first = c == 0;
-            // A -> sA (masked).  sA last held W of the previous chunk (read by
-            // its O, complete) and then one of its O boxes: wait until the
-            // bulk stores have read both O pieces out of sA and sX.
+            // A packed in place (masked)
             if (!wait_bar(CA, ph)) break;
             tc_fence_after();
-            if (lane == 0) tma_store_wait_read();
-            __syncwarp();
-            drain128(tAl_, tA, true);
+            pack_alpha(false);
             drained(DA);
             // P0 of this chunk -> the S0 / P0 tile, once Q S0 has read S0 (a
             // head's first chunk has P0 = 0 and skips Q P0)
@@ -303,44 +330,37 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (!first) drainD(tP_, tSP);
                 drained(DP);
             }
-            // X -> sX (bf16; the previous O boxes left it before the A drain);
-            // on a head's first chunk split into hi (sX) and lo (sA: A has been
-            // read by A K, and W goes there only once W has read X_lo)
+            // X -> sX (bf16); on a head's first chunk split into hi (sX) and
+            // lo (sO).  At D = 128 this warp's first O box of the previous
+            // chunk must have left sX (the second, newer one may still be
+            // read out of sO).
             if (!wait_bar(CX, ph)) break;
             tc_fence_after();
+            if (D == 128) {
+                if (lane == 0) tma_store_wait_read_all_but_1();
+                __syncwarp();
+            }
             {
                 uint32_t x[64];
                 tmem_ld_cols<D / 2>(tBe_ + lane_off + cD, x);
                 if (first) {
-                    put_row32_split2(tX, tA, row, cD, x, false);
-                    if (D == 128) put_row32_split2(tX, tA, row, cD + 32, x + 32, false);
+                    put_row32_split2(tX, tO, row, cD, x, false);
+                    if (D == 128) put_row32_split2(tX, tO, row, cD + 32, x + 32, false);
                 } else {
                     put_row32(tX, row, cD, x, false);
                     if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
                 }
             }
             drained(DX);
-            // W -> sA (masked): A there was last read by A K, complete
+            // W packed in place (masked; hi and lo on a head's first chunk)
             if (!wait_bar(CW, ph)) break;
             tc_fence_after();
-            if (first) {
-                uint32_t lo[32];
-                {
-                    uint32_t r[64];
-                    tmem_ld_cols<64>(tAl_ + lane_off + c128, r);
-                    put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
-                    put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
-                }
-                tmem_st32(tAl_ + lane_off + (uint32_t)c128, lo);  // W_lo -> alpha (own columns, packed)
-                tmem_st_wait();
-            } else {
-                drain128(tAl_, tA, true);
-            }
+            pack_alpha(first);
             drained(DW);
             // O: out of beta into registers (beta then free), the next chunk's
             // S0 into its tile (Q P0 has read P0), then O leaves by bulk tensor
-            // stores, staged in sX (X was last read by X^T V) and, at D = 128,
-            // sA (W was last read by O), one 4 KB box per warp in each
+            // stores from the staging boxes (X was last read by X^T V and X_lo
+            // by W, both complete once O is)
             if (!wait_bar(CO, ph)) break;
             tc_fence_after();
             {
@@ -351,11 +371,20 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     drainD(tS_, tSP);
                     drained(DS);
                 }
-                const uint32_t wbox = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
                 const int t0 = c * kL + quarter * 32;  // first token of this warp's rows
 #pragma unroll
                 for (int g = 0; g < D / 64; ++g) {
-                    const uint32_t scratch = (g == 0 ? tX.base : tA.base) + wbox;
+                    const bool in_o = D == 64 || g == 1;
+                    // the previous box in the same buffer has left it (at D = 128
+                    // the box just sent to sX may still be pending)
+                    if (in_o) {
+                        if (lane == 0) {
+                            if (D == 128) tma_store_wait_read_all_but_1();
+                            else tma_store_wait_read();
+                        }
+                        __syncwarp();
+                    }
+                    const uint32_t scratch = (in_o ? tO.base : tX.base) + wbox;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
@@ -398,7 +427,7 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, kThreadsOut, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
