@@ -54,20 +54,42 @@ struct OutLayout {
     static constexpr uint32_t kBytes = SP + kSt;
 };
 
-// Warp roles: warps 0..7 drain tensor memory (warp w owns lane quarter w % 4
-// and column half w / 4 of every region), warp 8 (lane 0) issues every MMA,
-// warp 9 (lane 0) every tile load, so that MMA issue never waits behind a
-// busy bulk-copy queue; the roles meet only on mbarriers.
-constexpr int kThreadsOut = (kDrainWarps + 2) * 32;
+// Warp roles: the drain warps move results out of tensor memory (warp w
+// owns lane quarter w % 4 and, in every region, a share of the columns:
+// 32 of a D-wide region, 128 / (D / 32) of alpha), one warp (lane 0) issues
+// every MMA, another every tile load, so that MMA issue never waits behind a
+// busy bulk-copy queue; the roles meet only on mbarriers.  There are D / 8
+// drain warps (16 at D = 128), so that each drain is short.
 template <int D>
-__global__ void __launch_bounds__(kThreadsOut, 1)
+struct OutRoles {
+    static constexpr int kParts = D / 32;             // drain warps per lane quarter
+    static constexpr int kDrain = 4 * kParts;         // drain warps
+    static constexpr int kCA = 128 / kParts;          // alpha columns per drain warp
+    static constexpr int kState = (D / 32) * kParts;  // drain warps holding state rows (< D)
+    static constexpr int kThreads = (kDrain + 2) * 32;
+};
+
+// 16 fp32 TMEM columns of this thread's lane, stored / loaded with one call.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(OutRoles<D>::kThreads, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
               const __grid_constant__ CUtensorMap mR, OutParams p) {
     using LY = OutLayout<D>;
+    using RO = OutRoles<D>;
+    constexpr int NDW = RO::kDrain, CA = RO::kCA;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | final wait | drain warp w's prefix boxes
-    enum { LQ0, LQ1, LK, LV, CA, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, FIN, PB, NBAR = PB + kDrainWarps };
+    // (XB: every drain warp's O box has left sX, D = 128)
+    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, XB, FIN, PB, NBAR = PB + NDW };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -75,10 +97,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const bool issuer = warp == kDrainWarps;
-    const bool producer = warp == kDrainWarps + 1;
+    const bool drainer = warp < NDW;
+    const bool issuer = warp == NDW;
+    const bool producer = warp == NDW + 1;
     const int quarter = warp & 3;
-    const int half = (warp >> 2) & 1;
+    const int part = (warp >> 2) % RO::kParts;
     const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
     int head, seg;
     const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
@@ -86,9 +109,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool drainer = warp < kDrainWarps;
-    const bool state_rows = drainer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
-    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
+    const bool state_rows = drainer && quarter < D / 32;  // drain warp holding rows < D
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
@@ -99,8 +120,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DW || i == DO) cnt = kDrainWarps;
-            if (i == DS || i == DP) cnt = kStateWarps;
+            if (i == DA || i == DX || i == DW || i == DO || i == XB) cnt = NDW;
+            if (i == DS || i == DP) cnt = RO::kState;
             mbar_init(bar(i), cnt);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -120,8 +141,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const uint32_t tS_ = tmem + 128 + D;      // running S
     const uint32_t tP_ = tmem + 128 + 2 * D;  // running P
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int c128 = half * 64;     // this drain warp's columns in a 128-wide region
-    const int cD = half * (D / 2);  // ... and in a D-wide region
+    const int cD = part * 32;  // this drain warp's columns in a D-wide region
+    const int ca0 = part * CA;  // ... and in alpha
 
     constexpr uint32_t kTileBytes = kL * D * 2;
     auto wait_bar = [&](int b, uint32_t parity) -> bool {
@@ -151,35 +172,44 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
     };
+    // this warp's 32 columns of a D-wide fp32 region -> bf16 tile rows
     auto drainD = [&](uint32_t treg, const Tile& t) {
-        uint32_t r[64];
-        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
+        uint32_t r[32];
+        tmem_ld32(treg + lane_off + cD, r);
+        tmem_ld_wait();
         put_row32(t, row, cD, r, false);
-        if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
     };
-    // Packed bf16 operands in alpha: drain warp h packs the pairs of its
-    // columns [64h, 64h+64) (A, or W and on a first chunk also W_lo) into
-    // columns [64h, 64h+32) (and W_lo into [64h+32, 64h+64)), which it has
-    // itself just read, so no other warp's pending read is overwritten.
-    // K-step ks (16 tokens) of the product reads 8 packed columns.
-    auto pk_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * 64 + 8 * (ks & 3)); };
-    // this lane's 64 columns of alpha -> bf16 pairs (masked to columns <= row),
+    // Packed bf16 operands in alpha: drain warp (q, part) packs the pairs of
+    // its alpha columns [ca0, ca0 + CA) (A, or W and on a first chunk also
+    // W_lo) into [ca0, ca0 + CA/2) (W_lo into [ca0 + CA/2, ca0 + CA)), which
+    // it has itself just read, so no other warp's pending read is
+    // overwritten.  K-step ks (16 tokens) of the product reads 8 packed
+    // columns.
+    auto pk_col = [](int ks) -> uint32_t { return (uint32_t)(CA * ((16 * ks) / CA) + ((16 * ks) % CA) / 2); };
+    // this lane's alpha columns -> bf16 pairs (masked to columns <= row),
     // optionally with the lo parts, written back packed
     auto pack_alpha = [&](bool split) {
-        uint32_t r[64];
-        tmem_ld_cols<64>(tAl_ + lane_off + c128, r);
-        uint32_t hi[32], lo[32];
+        uint32_t r[CA];
+        tmem_ld32(tAl_ + lane_off + ca0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        if (CA == 64) tmem_ld32(tAl_ + lane_off + ca0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[CA == 64 ? 32 : 0]));
+        tmem_ld_wait();
+        uint32_t hi[CA / 2], lo[CA / 2];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < CA / 2; ++j) {
             float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
-            if (c128 + 2 * j > row) x0 = 0.f;
-            if (c128 + 2 * j + 1 > row) x1 = 0.f;
+            if (ca0 + 2 * j > row) x0 = 0.f;
+            if (ca0 + 2 * j + 1 > row) x1 = 0.f;
             const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
             hi[j] = *reinterpret_cast<const uint32_t*>(&h);
             if (split) lo[j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
         }
-        tmem_st32(tAl_ + lane_off + (uint32_t)c128, hi);
-        if (split) tmem_st32(tAl_ + lane_off + (uint32_t)c128 + 32u, lo);
+        if (CA == 64) {
+            tmem_st32(tAl_ + lane_off + (uint32_t)ca0, *reinterpret_cast<uint32_t(*)[32]>(&hi[0]));
+            if (split) tmem_st32(tAl_ + lane_off + (uint32_t)(ca0 + CA / 2), *reinterpret_cast<uint32_t(*)[32]>(&lo[0]));
+        } else {
+            tmem_st16(tAl_ + lane_off + (uint32_t)ca0, hi);
+            if (split) tmem_st16(tAl_ + lane_off + (uint32_t)(ca0 + CA / 2), lo);
+        }
         tmem_st_wait();
     };
 
@@ -193,32 +223,25 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     }
     if (state_rows && nchunks > 0) {
         // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
-        // 32 x 32 fp32 boxes by bulk tensor loads (mR maps the records as
+        // 32 x 32 fp32 box by bulk tensor loads (mR maps the records as
         // (3D + 2) rows of D floats) into a private staging area in the X / O
         // tiles, which nothing else touches before the first chunk
         const int rec = head * p.nseg + seg;
-        const uint32_t stage = dsm + LY::X + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+        const uint32_t stage = dsm + LY::X + (uint32_t)warp * 4096u;
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
                 fence_proxy_async();
-                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
-#pragma unroll
-                for (int g = 0; g < D / 64; ++g)
-                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? 0 : 2 * D + 1) + quarter * 32, rec,
-                                bar(PB + warp));
+                mbar_expect_tx(bar(PB + warp), 4096u);
+                tma_load_3d(stage, &mR, cD, (m == 0 ? 0 : 2 * D + 1) + quarter * 32, rec, bar(PB + warp));
             }
             __syncwarp();
             if (!wait_bar(PB + warp, (uint32_t)m)) break;
-#pragma unroll
-            for (int g = 0; g < D / 64; ++g) {
-                const int cb = cD + 32 * g;
-                uint32_t r[32];
-                box32_read(stage + (uint32_t)g * 4096u, lane, r);
-                tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cb, r);
-                if (m == 0) put_row32(tSP, row, cb, r, false);  // bf16 S0; P0 follows once Q S0 has read it
-            }
-            __syncwarp();  // every lane has read the boxes before the next load reuses them
+            uint32_t r[32];
+            box32_read(stage, lane, r);
+            tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cD, r);
+            if (m == 0) put_row32(tSP, row, cD, r, false);  // bf16 S0; P0 follows once Q S0 has read it
+            __syncwarp();  // every lane has read the box before the next load reuses it
         }
         tmem_st_wait();
     }
@@ -246,7 +269,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 tc_fence_after();
                 // A = Q K^T
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
-                mma_commit(bar(CA));
+                mma_commit(bar(CA_));
                 if (it > 0) {
                     // beta free (O read out) and S0 of this chunk in its tile
                     if (!wait_bar(DO, pph) || !wait_bar(DS, pph)) break;
@@ -284,7 +307,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 32u, tV.mnmaj(ks), iKM, 1);
+                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + (uint32_t)(CA / 2), tV.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CO));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
@@ -305,20 +328,23 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (it + 2 < nchunks) issue_load((it & 1) ? LQ1 : LQ0, &mQ, (it & 1) ? tQ1 : tQ0, c + 2);
             }
         }
-    } else {
+    } else if (drainer) {
         // ========================== drain warps ==========================
-        // this warp's O staging boxes (32 rows x 32 fp32 columns, 4 KB each):
-        // the first in sX at D = 128 (the same rows and column block as this
-        // warp's own share of X, so only its own stores must have left it
-        // before its X drain) and the other in sO; at D = 64 the only one in sO
-        const uint32_t wbox = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+        // This warp's O staging box (32 rows x 32 fp32 columns, 4 KB): at
+        // D = 128 the warps of column parts 0, 1 stage in sX (which the next
+        // X drain rewrites: it waits until every such box has been read out)
+        // and parts 2, 3 in sO; at D = 64 every box is in sO, where only this
+        // warp's own next box goes.
+        const bool box_in_x = D == 128 && part < 2;
+        const uint32_t wbox = (uint32_t)(part & 1) * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+        const uint32_t scratch = (box_in_x ? tX.base : tO.base) + wbox;
         for (int it = 0; it < nchunks; ++it) {
             const uint32_t ph = it & 1;
             const int c = c_begin + it;
             const bool has_next = it + 1 < nchunks;
             const bool first = c == 0;
             // A packed in place (masked)
-            if (!wait_bar(CA, ph)) break;
+            if (!wait_bar(CA_, ph)) break;
             tc_fence_after();
             pack_alpha(false);
             drained(DA);
@@ -331,25 +357,23 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 drained(DP);
             }
             // X -> sX (bf16); on a head's first chunk split into hi (sX) and
-            // lo (sO).  At D = 128 this warp's first O box of the previous
-            // chunk must have left sX (the second, newer one may still be
-            // read out of sO).
+            // lo (sO).  At D = 128 the O boxes staged in sX must have left it.
             if (!wait_bar(CX, ph)) break;
             tc_fence_after();
             if (D == 128) {
-                if (lane == 0) tma_store_wait_read_all_but_1();
-                __syncwarp();
+                // every drain warp's previous O box has left sX (an mbarrier
+                // with a bounded wait rather than a named barrier, so that a
+                // warp that gave up cannot strand the others)
+                if (box_in_x && lane == 0) tma_store_wait_read();
+                drained(XB);
+                if (!wait_bar(XB, ph)) break;
             }
             {
-                uint32_t x[64];
-                tmem_ld_cols<D / 2>(tBe_ + lane_off + cD, x);
-                if (first) {
-                    put_row32_split2(tX, tO, row, cD, x, false);
-                    if (D == 128) put_row32_split2(tX, tO, row, cD + 32, x + 32, false);
-                } else {
-                    put_row32(tX, row, cD, x, false);
-                    if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
-                }
+                uint32_t x[32];
+                tmem_ld32(tBe_ + lane_off + cD, x);
+                tmem_ld_wait();
+                if (first) put_row32_split2(tX, tO, row, cD, x, false);
+                else put_row32(tX, row, cD, x, false);
             }
             drained(DX);
             // W packed in place (masked; hi and lo on a head's first chunk)
@@ -358,44 +382,33 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             pack_alpha(first);
             drained(DW);
             // O: out of beta into registers (beta then free), the next chunk's
-            // S0 into its tile (Q P0 has read P0), then O leaves by bulk tensor
-            // stores from the staging boxes (X was last read by X^T V and X_lo
-            // by W, both complete once O is)
+            // S0 into its tile (Q P0 has read P0), then O leaves by a bulk
+            // tensor store from this warp's staging box (X was last read by
+            // X^T V and X_lo by W, both complete once O is)
             if (!wait_bar(CO, ph)) break;
             tc_fence_after();
             {
-                uint32_t r[64];
-                tmem_ld_cols<D / 2>(tBe_ + lane_off + cD, r);
+                uint32_t r[32];
+                tmem_ld32(tBe_ + lane_off + cD, r);
+                tmem_ld_wait();
                 drained(DO);
                 if (state_rows && has_next) {
                     drainD(tS_, tSP);
                     drained(DS);
                 }
-                const int t0 = c * kL + quarter * 32;  // first token of this warp's rows
-#pragma unroll
-                for (int g = 0; g < D / 64; ++g) {
-                    const bool in_o = D == 64 || g == 1;
-                    // the previous box in the same buffer has left it (at D = 128
-                    // the box just sent to sX may still be pending)
-                    if (in_o) {
-                        if (lane == 0) {
-                            if (D == 128) tma_store_wait_read_all_but_1();
-                            else tma_store_wait_read();
-                        }
-                        __syncwarp();
-                    }
-                    const uint32_t scratch = (in_o ? tO.base : tX.base) + wbox;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
-                                     r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
-                                     r[32 * g + 4 * q + 3]);
-                    fence_proxy_async();
+                if (!box_in_x) {  // the previous box in sO has left it
+                    if (lane == 0) tma_store_wait_read();
                     __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&mO, scratch, cD + 32 * g, t0, head);
-                        tma_store_commit();
-                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4), r[4 * q],
+                                 r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&mO, scratch, cD, c * kL + quarter * 32, head);
+                    tma_store_commit();
                 }
             }
         }
@@ -427,7 +440,7 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsOut, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, OutRoles<D>::kThreads, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
