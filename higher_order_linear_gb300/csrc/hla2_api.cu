@@ -481,8 +481,17 @@ int hla2_chunk_summaries(const void* Q, const void* K, const void* V, float* sum
     p.nseg = p.nchunk;  // one chunk per segment
     p.seglen = 1;
     if (p.nseg > 65535) return fail(HLA2_ERR_UNSUPPORTED, "%d chunks per head exceeds 65535", p.nseg);
-    cudaError_t e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, 1.0f, p,
-                                reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e;
+    if (tc_chunk_supported(d, dv, L, dtype, dev)) {
+        int* status = device_status_word();
+        if (!status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+        e = launch_tc_chunk(Q, K, V, summ, B * H, T, d, L, status, s);
+    } else {
+        e = launch_walk(2, Q, K, V, dtype, nullptr, nullptr, summ, B * H, T, d, dv, 0, 0, 1.0f, p, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "hla2_chunk_summaries");
     return HLA2_OK;
 }
@@ -532,6 +541,12 @@ int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_o
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     return (!with_state_out && tc_supported(d, dv, dtype, normalized, dev)) ? 1 : 0;
+}
+
+int hla2_chunk_summaries_path(int d, int dv, int L, int dtype) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return tc_chunk_supported(d, dv, L, dtype, dev) ? 1 : 0;
 }
 
 int hla2_profile_enable(int on) {

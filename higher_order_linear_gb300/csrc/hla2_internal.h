@@ -179,6 +179,11 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
                            float* O, const float* prefix, float* summ,
                            int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
                            cudaStream_t s);
+// Chunk summaries S|C|m|G|h on tensor cores (hla2_tc_chunk.cu): bf16 inputs,
+// d = dv in {64, 128}, chunk length L in {64, 128}.
+bool tc_chunk_supported(int d, int dv, int L, int dtype, int device);
+cudaError_t launch_tc_chunk(const void* Q, const void* K, const void* V, float* summ, int BH, int T, int d, int L,
+                            int* status, cudaStream_t s);
 // The unnormalised HLA output walk pipelined across chunks (hla2_tc_out.cu),
 // d = dv in {64, 128}, bf16: outputs of every segment from its prefix S|.|.|P|.
 cudaError_t launch_tc_out(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,

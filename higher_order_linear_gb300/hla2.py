@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.hla2_profile_read.restype = i
             L.hla2_forward_path.argtypes = [i, i, i, i, i]
             L.hla2_forward_path.restype = i
+            L.hla2_chunk_summaries_path.argtypes = [i, i, i, i]
+            L.hla2_chunk_summaries_path.restype = i
             L.hla2_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
             L.hla2_forward_noalloc.restype = i
             L.hla2_forward_host_workspace.argtypes = [i, i, i, i, i, i, i]

@@ -376,6 +376,14 @@ HLA2_API int hla2_profile_enable(int on);
 HLA2_API int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_out);
 
 /*
+ * 1 when hla2_chunk_summaries with these sizes runs on the tensor cores of
+ * the current device (bf16, d = dv in {64, 128}, L in {64, 128}; G and h
+ * from split-bf16 operands, about 16 significant bits), 0 when it runs on
+ * the fp32 CUDA-core walk.  Host only.
+ */
+HLA2_API int hla2_chunk_summaries_path(int d, int dv, int L, int dtype);
+
+/*
  * Waits for the events recorded since the previous read, writes the summed
  * phase durations in milliseconds to ms_out[0..min(n,3)-1], the number of
  * profiled forwards to *forwards (if not NULL) and the number of kernels the

@@ -77,3 +77,22 @@ def test_scan_long_context_chunk_level():
     ref_p = oracle.scan_fold(ref_s[0, 0], w.d, w.dv)
     errs = per_field_err(f64(p[0, 0, 1:]), ref_p[1:], w.d, w.dv)
     assert max(errs) < 1e-4, errs
+
+
+@pytest.mark.parametrize("d,L,T", [(64, 64, 1000), (64, 128, 1000), (128, 64, 777), (128, 128, 640),
+                                   (128, 64, 64), (64, 64, 65), (128, 128, 1)])
+def test_chunk_summaries_tensor_core(d, L, T):
+    """bf16 inputs with d = dv in {64, 128} and L in {64, 128} take the
+    tensor-core kernel (two chunks per 128-token tile at L = 64; odd chunk
+    counts and ragged tails leave the missing chunk unwritten); every field
+    stays within the fp32 walk's 1e-5 of the oracle."""
+    assert hla2.lib().hla2_chunk_summaries_path(d, d, L, hla2.HLA2_DTYPE_BF16) == 1
+    assert hla2.lib().hla2_chunk_summaries_path(d, d, 32, hla2.HLA2_DTYPE_BF16) == 0
+    assert hla2.lib().hla2_chunk_summaries_path(d, d, L, hla2.HLA2_DTYPE_F32) == 0
+    g = torch.Generator().manual_seed(d + L + T)
+    B, H = 1, 3
+    q, k, v = ((torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16) for _ in range(3))
+    got = hla2.hla2_chunk_summaries(q.to(DEV), k.to(DEV), v.to(DEV), L)
+    ref = oracle.chunk_summaries(f64(q), f64(k), f64(v), L=L)
+    errs = per_field_err(f64(got), ref, d, d)
+    assert max(errs) < 1e-5, errs
