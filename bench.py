@@ -378,6 +378,25 @@ def main():
                 "tensor_frac_of_bf16_burst": (alg_flops(w) * tokens / (ms_step / 1e3) / 1e12) / peaks["bf16_tflops"]
                 if fwd_steps else 0.0}
 
+    # ---- the same forward handing over each head's final state (prefill ->
+    # decode), timed like the headline ----
+    with_state = None
+    if fwd_steps:
+        st = torch.empty(w.B * w.H, hla2.record_len(w.d, w.dv), device=dev, dtype=torch.float32)
+        sfwd = lambda: hla2.hla2_forward(q, k, v, O, normalized=w.normalized, workspace=ws, state_out=st)
+        for _ in range(args.warmup):
+            sfwd()
+        barrier()
+        n_s = max(1, min(args.steps, 50))
+        ms_s = max_over_ranks(timed(sfwd, n_s, flush))
+        if hla2.hla2_device_status() != 0:
+            raise SystemExit(f"device status after the forward with state_out: {hla2.hla2_last_error_detail()}")
+        with_state = {"ms_per_step": ms_s, "steps": n_s, "value": replicas.job_throughput(tokens, world, ms_s),
+                      "unit": UNIT, "vs_headline_ms": ms_s / ms_step_max if ms_step_max > 0 else None,
+                      "path": "tcgen05" if L.hla2_forward_path(w.d, w.dv, dcode, int(w.normalized), 1) == 1
+                      else "cuda-core"}
+        del st
+
     # ---- the ratio-normalised workload (B4 H16 T4096 d=dv=64, q, k >= 0) ----
     normalized = None
     if not args.no_normalized and fwd_steps and args.workload == FWD_WORKLOAD and not (args.T or args.H):
@@ -704,7 +723,7 @@ def main():
                 "config": fwd_config(w, segments_per_head(w.B, w.H, w.T), l2_note), "path": path,
                 "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
                 "cpu_baseline": cpu, "decode": decode, "ahla": ahla, "variants": variants, "small": small,
-                "normalized": normalized, "chunk_level": chunk_level}
+                "normalized": normalized, "chunk_level": chunk_level, "with_state_out": with_state}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

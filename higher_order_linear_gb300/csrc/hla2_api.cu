@@ -349,7 +349,7 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     const bool want_extra = normalized || state_out;  // p (and m) needed
     int dev = 0;
     cudaGetDevice(&dev);
-    const bool use_tc = !state_out && tc_supported(d, dv, dtype, normalized, dev);
+    const bool use_tc = tc_supported(d, dv, dtype, normalized, dev);
     int* status = device_status_word();
     if (!status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
     cudaError_t e;
@@ -357,19 +357,32 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
     const bool prof = g_profile_on.load() && prof_begin(pe);
     if (prof) cudaEventRecord(pe.ev[0], s);
 
-    // segment summaries
-    if (use_tc) e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, status, s);
-    else e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, 1.0f, plan, s);
+    // segment summaries (with the final state wanted the tensor-core walk
+    // also forms m and p, which the normalised walk always does)
+    const RecOff ro = summary_offsets(d, dv);
+    if (use_tc) {
+        e = launch_tc_walk(0, Q, K, V, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, plan, status, s,
+                           state_out && !normalized);
+    } else {
+        e = launch_walk(0, Q, K, V, dtype, nullptr, nullptr, ws.summ, BH, T, d, dv, normalized, 0, 1.0f, plan, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "segment summaries");
     if (prof) cudaEventRecord(pe.ev[1], s);
     // exclusive scan of the summaries: one launch on the tensor-core path
+    // (plus the running sums of the terms for long scans or a final state)
     if (use_tc) {
-        const RecOff ro = summary_offsets(d, dv);
-        const ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, nullptr, status, normalized != 0};
+        const bool extra = normalized || state_out;
+        ScanArgs sa{ws.summ, ws.prefix, plan.nseg, ro.R, ro, nullptr, status, extra};
+        if (state_out) {
+            sa.terms_only = true;
+            sa.tot = ws.tot;  // plain totals of S | C | m
+            sa.tot_len = ro.X;
+        }
         e = launch_tc_scan(kScanHLA, sa, BH, d, dv, s);
-        if (e == cudaSuccess && plan.nseg > tc_scan_full_max_segments())  // exclusive sums of the terms X_r (and x_r)
-            e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X,
-                              (size_t)d * dv + (normalized ? (size_t)d : 0), nullptr, 0, s);
+        if (e == cudaSuccess && (state_out || plan.nseg > tc_scan_full_max_segments()))
+            // exclusive sums of the terms X_r (and x_r), with their totals
+            e = launch_exscan(ws.prefix, ws.prefix, BH, plan.nseg, ro.R, ro.X, (size_t)d * dv + (extra ? (size_t)d : 0),
+                              state_out ? ws.tot + ro.X : nullptr, ro.R, s);
         if (e != cudaSuccess) return cuda_fail(e, "scan");
     } else {
         rc = forward_scan(ws, BH, plan, d, dv, want_extra, state_out != nullptr, use_tc, status, s);
@@ -387,23 +400,8 @@ int hla2_forward(const void* Q, const void* K, const void* V, float* O, int B, i
 
     if (state_out) {
         // final state in decode order S|C|G|m|h: G = S C - P, h = S m - p
-        const RecOff so = summary_offsets(d, dv);
-        const RecOff dof = decode_offsets(d, dv);
-        const long long R = (long long)so.R;
-        e = launch_copy_strided(ws.tot + so.S, R, state_out + dof.S, R, (size_t)d * d + (size_t)d * dv, BH, s);
-        if (e == cudaSuccess) e = launch_copy_strided(ws.tot + so.m, R, state_out + dof.m, R, (size_t)d, BH, s);
-        if (e != cudaSuccess) return cuda_fail(e, "state_out copy");
-        CrossArgs a{};
-        a.A = ws.tot + so.S; a.sA = R;
-        a.B = ws.tot + so.C; a.sB = R;
-        a.bx = ws.tot + so.m; a.sbx = R;
-        a.base = ws.tot + so.X; a.sbase = R;
-        a.basex = ws.tot + so.x; a.sbasex = R;
-        a.out = state_out + dof.X; a.sout = R;
-        a.outx = state_out + dof.x; a.soutx = R;
-        a.alpha = -1.f; a.d = d; a.dv = dv; a.nb = BH;
-        e = launch_cross(a, s);
-        if (e != cudaSuccess) return cuda_fail(e, "state_out G");
+        e = launch_state_tail(ws.tot, state_out, BH, d, dv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "state_out");
     }
     return HLA2_OK;
 }
@@ -512,7 +510,13 @@ int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int 
     // 1. exclusive sums of S | C | m
     cudaError_t e = launch_exscan(summ, prefix, (int)BH, N, R, 0, ro.X, nullptr, 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "hla2_scan: prefix sums");
-    // 2. Y_r = G_r + S_r C_<r, y_r = h_r + S_r m_<r
+    // 2. Y_r = G_r + S_r C_<r, y_r = h_r + S_r m_<r (tensor cores with
+    //    split-bf16 operands where they apply, exact fp32 otherwise)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool use_tc = tc_supported(d, dv, HLA2_DTYPE_BF16, 0, dev);
+    int* status = use_tc ? device_status_word() : nullptr;
+    if (use_tc && !status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
     CrossArgs a{};
     a.A = summ + ro.S; a.sA = (long long)R;
     a.B = prefix + ro.C; a.sB = (long long)R;
@@ -521,14 +525,14 @@ int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int 
     a.basex = summ + ro.x; a.sbasex = (long long)R;
     a.out = prefix + ro.X; a.sout = (long long)R;
     a.outx = prefix + ro.x; a.soutx = (long long)R;
-    a.alpha = 1.f; a.d = d; a.dv = dv;
+    a.alpha = 1.f; a.d = d; a.dv = dv; a.status = status;
     for (long long b0 = 0; b0 < BH * N; b0 += 65535) {
         CrossArgs c = a;
         const long long nb = BH * N - b0;
         c.nb = (int)(nb < 65535 ? nb : 65535);
         c.A += b0 * R; c.B += b0 * R; c.bx += b0 * R;
         c.base += b0 * R; c.basex += b0 * R; c.out += b0 * R; c.outx += b0 * R;
-        e = launch_cross(c, s);
+        e = use_tc ? launch_tc_cross(c, s) : launch_cross(c, s);
         if (e != cudaSuccess) return cuda_fail(e, "hla2_scan: cross terms");
     }
     // 3. exclusive sums of G | h (in place)
@@ -540,7 +544,8 @@ int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int 
 int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    return (!with_state_out && tc_supported(d, dv, dtype, normalized, dev)) ? 1 : 0;
+    (void)with_state_out;  // the tensor-core forward also hands over the final state
+    return tc_supported(d, dv, dtype, normalized, dev) ? 1 : 0;
 }
 
 int hla2_chunk_summaries_path(int d, int dv, int L, int dtype) {

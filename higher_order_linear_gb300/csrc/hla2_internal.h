@@ -131,7 +131,8 @@ cudaError_t launch_decay_exscan(const float* in, float* out, int BH, int N, size
 // Exclusive running sum along the record axis for the element range
 // [off, off+len) of every record: out[b][n][i] = sum_{r<n} in[b][r][i].
 // in may equal out.  If total != nullptr, total[b*total_stride + i] receives
-// the inclusive sum (element i relative to off).
+// the inclusive sum (element i relative to off); with out == nullptr only
+// the totals are written.
 cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, size_t off, size_t len,
                           float* total, size_t total_stride, cudaStream_t s);
 
@@ -159,6 +160,10 @@ struct CrossArgs {
 cudaError_t launch_cross(const CrossArgs& a, cudaStream_t s);
 
 // Copy `len` floats from each of nb records (strided) to another layout.
+// The final decode state S|C|G|m|h of each of BH heads from its P-form
+// totals S|C|m|P|p (records of summary_offsets(d, dv)): G = S C - P,
+// h = S m - p in fp32.
+cudaError_t launch_state_tail(const float* tot, float* state, int BH, int d, int dv, cudaStream_t s);
 cudaError_t launch_copy_strided(const float* src, long long s_src, float* dst, long long s_dst,
                                 size_t len, int nb, cudaStream_t s);
 
@@ -174,11 +179,13 @@ cudaError_t launch_ahla_step(float* state, const float* q, const float* k, const
                              int n, int d, int dv, int normalized, cudaStream_t s);
 
 // ---- tensor-core segment walks (hla2_tc.cu) ----
+// mode 0 writes the segment summaries S|C|.|P|. (and m, p when normalised or
+// with_p), mode 1 the outputs from the prefixes S|.|.|P|(p).
 bool tc_supported(int d, int dv, int dtype, int normalized, int device);
 cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V,
                            float* O, const float* prefix, float* summ,
                            int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
-                           cudaStream_t s);
+                           cudaStream_t s, bool with_p = false);
 // Chunk summaries S|C|m|G|h on tensor cores (hla2_tc_chunk.cu): bf16 inputs,
 // d = dv in {64, 128}, chunk length L in {64, 128}.
 bool tc_chunk_supported(int d, int dv, int L, int dtype, int device);
@@ -209,7 +216,8 @@ cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const v
                                  int BH, int T, int d, int dv, float gamma, SegPlan plan, int* status,
                                  cudaStream_t s);
 // Batched out = alpha*base + A*B on tensor cores with split-bf16 operands
-// (d = dv in {64, 128}, no extra column).
+// (d = dv in {64, 128}); the optional column outx = alpha*basex + A*bx is
+// taken in fp32 on the CUDA cores.
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s);
 
 // The forward's exclusive scan over segment summaries (hla2_tc_scan.cu),
@@ -233,6 +241,12 @@ struct ScanArgs {
     const float* fac;  // decayed: fac[r] = gamma^{n_r}, fac[nseg + r] = gamma^{2 n_r}
     int* status;
     bool extra;
+    bool terms_only = false;  // always leave terms (no complete prefixes), whatever nseg
+    // optional: tot[head * R + i] = sum over the records of summ[..][i] for
+    // i < tot_len (the plain sums S | C | m of a final state), formed by
+    // extra CTAs of the same launch
+    float* tot = nullptr;
+    size_t tot_len = 0;
 };
 cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cudaStream_t s);
 // Scans of at most this many segments complete every prefix inside

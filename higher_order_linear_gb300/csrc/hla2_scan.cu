@@ -23,6 +23,7 @@ namespace {
 constexpr int kScanThreads = 256;
 constexpr int kScanUnroll = 8;
 
+template <bool WRITE>
 __global__ void __launch_bounds__(kScanThreads)
 exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
               size_t total_stride) {
@@ -39,13 +40,13 @@ exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t l
         for (int j = 0; j < kScanUnroll; ++j) x[j] = pin[(size_t)(r + j) * R];
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
-            pout[(size_t)(r + j) * R] = run;
+            if (WRITE) pout[(size_t)(r + j) * R] = run;
             run += x[j];
         }
     }
     for (; r < N; ++r) {
         const float x = pin[(size_t)r * R];
-        pout[(size_t)r * R] = run;
+        if (WRITE) pout[(size_t)r * R] = run;
         run += x;
     }
     if (total) total[(size_t)bh * total_stride + i] = run;
@@ -53,6 +54,7 @@ exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t l
 
 // Same scan, four consecutive elements per thread (16-byte accesses); used
 // when the element range, the record length and the pointers allow it.
+template <bool WRITE>
 __global__ void __launch_bounds__(kScanThreads)
 exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
                size_t total_stride) {
@@ -69,13 +71,13 @@ exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t 
         for (int j = 0; j < kScanUnroll; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
 #pragma unroll
         for (int j = 0; j < kScanUnroll; ++j) {
-            *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
+            if (WRITE) *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
             run.x += x[j].x; run.y += x[j].y; run.z += x[j].z; run.w += x[j].w;
         }
     }
     for (; r < N; ++r) {
         const float4 x = *reinterpret_cast<const float4*>(pin + (size_t)r * R);
-        *reinterpret_cast<float4*>(pout + (size_t)r * R) = run;
+        if (WRITE) *reinterpret_cast<float4*>(pout + (size_t)r * R) = run;
         run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
     }
     if (total) *reinterpret_cast<float4*>(total + (size_t)bh * total_stride + i) = run;
@@ -233,6 +235,88 @@ decay_exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, s
     if (total) *reinterpret_cast<float4*>(total + (size_t)bh * total_stride + i) = run;
 }
 
+// Final state in decode order from the P-form totals of a head (one record
+// S|C|m|P|p): S, C, m copied, G = S C - P (fp32, summed in k order) and
+// h = S m - p.  CTA (row block, column block, head) owns the 16 x 32 block of
+// G at rows 16 blk_r.., columns 32 blk_c..: it stages its S rows and C
+// columns in shared memory (every load issued before the first store), then
+// thread t forms row t / 8 of the block at the four columns 4 (t % 8) .. + 3.
+// Column block 0 also copies its S rows and forms h for them; every CTA
+// copies its part of C.
+constexpr int kTailRows = 16, kTailCols = 32, kTailThreads = 128;
+
+__global__ void __launch_bounds__(kTailThreads)
+state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecOff dof) {
+    __shared__ __align__(16) float sC[128][kTailCols];   // C[k][c0 + j]
+    __shared__ float sS[kTailRows][128 + 1];              // S[i0 + r][k], padded rows
+    __shared__ float sm[128];
+    const int head = blockIdx.z, i0 = blockIdx.x * kTailRows, c0 = blockIdx.y * kTailCols;
+    const int nr = d - i0 < kTailRows ? d - i0 : kTailRows;
+    const int nc = dv - c0 < kTailCols ? dv - c0 : kTailCols;
+    const float* t = tot + (size_t)head * so.R;
+    float* o = state + (size_t)head * dof.R;
+    const int tid = threadIdx.x;
+    {
+        constexpr int kNC = 128 * kTailCols / kTailThreads, kNS = kTailRows * 128 / kTailThreads;
+        float vc[kNC], vs[kNS];
+#pragma unroll
+        for (int q = 0; q < kNC; ++q) {
+            const int i = tid + q * kTailThreads, k = i / kTailCols, j = i % kTailCols;
+            vc[q] = (k < d && j < nc) ? t[so.C + (size_t)k * dv + c0 + j] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kNS; ++q) {
+            const int i = tid + q * kTailThreads, r = i / 128, k = i % 128;
+            vs[q] = (r < nr && k < d) ? t[so.S + (size_t)(i0 + r) * d + k] : 0.f;
+        }
+        const float vm = tid < d ? t[so.m + tid] : 0.f;
+#pragma unroll
+        for (int q = 0; q < kNC; ++q) {
+            const int i = tid + q * kTailThreads;
+            sC[i / kTailCols][i % kTailCols] = vc[q];
+        }
+#pragma unroll
+        for (int q = 0; q < kNS; ++q) {
+            const int i = tid + q * kTailThreads;
+            sS[i / 128][i % 128] = vs[q];
+        }
+        sm[tid] = vm;
+    }
+    __syncthreads();
+    for (int i = tid; i < nr * nc; i += kTailThreads) {
+        const int r = i / nc, j = i % nc;
+        o[dof.C + (size_t)(i0 + r) * dv + c0 + j] = sC[i0 + r][j];
+    }
+    if (blockIdx.y == 0) {
+        for (int i = tid; i < nr * d; i += kTailThreads) o[dof.S + (size_t)i0 * d + i] = sS[i / d][i % d];
+        if (blockIdx.x == 0)
+            for (int i = tid; i < d; i += kTailThreads) o[dof.m + i] = sm[i];
+        // h: warp w takes rows w, w + 4, ... (lanes split k, then a fixed-order reduction)
+        const int lane = tid & 31;
+        for (int r = tid >> 5; r < nr; r += kTailThreads / 32) {
+            float h = 0.f;
+            for (int k = lane; k < d; k += 32) h = fmaf(sS[r][k], sm[k], h);
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1) h += __shfl_xor_sync(0xffffffffu, h, w);
+            if (lane == 0) o[dof.x + i0 + r] = h - t[so.x + i0 + r];
+        }
+    }
+    const int r = tid >> 3, j0 = 4 * (tid & 7);
+    if (r >= nr || j0 >= nc) return;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < d; ++k) {
+        const float4 c = *reinterpret_cast<const float4*>(&sC[k][j0]);
+        const float x = sS[r][k];
+        a0 = fmaf(x, c.x, a0); a1 = fmaf(x, c.y, a1); a2 = fmaf(x, c.z, a2); a3 = fmaf(x, c.w, a3);
+    }
+    const float acc[4] = {a0, a1, a2, a3};
+    const size_t g = (size_t)(i0 + r) * dv + c0 + j0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (j0 + q < nc) o[dof.X + g + q] = acc[q] - t[so.X + g + q];
+}
+
 __global__ void copy_strided_kernel(const float* src, long long s_src, float* dst, long long s_dst, size_t len) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int b = blockIdx.y;
@@ -246,12 +330,15 @@ cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, 
     if (BH == 0 || len == 0) return cudaSuccess;
     const bool vec = ((off | len | R | total_stride) % 4 == 0) && ((reinterpret_cast<uintptr_t>(in) |
                      reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(total)) % 16 == 0);
+    if (!out && !total) return cudaErrorInvalidValue;
     if (vec) {
         dim3 grid((unsigned)((len / 4 + kScanThreads - 1) / kScanThreads), BH);
-        exscan4_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        if (out) exscan4_kernel<true><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        else exscan4_kernel<false><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
     } else {
         dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
-        exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        if (out) exscan_kernel<true><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        else exscan_kernel<false><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
     }
     note_launches(1);
     return cudaGetLastError();
@@ -285,6 +372,15 @@ cudaError_t launch_decay_exscan(const float* in, float* out, int BH, int N, size
         dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
         decay_exscan_kernel<<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride, fac);
     }
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_tail(const float* tot, float* state, int BH, int d, int dv, cudaStream_t s) {
+    if (BH == 0) return cudaSuccess;
+    if (d <= 0 || dv <= 0 || d > 128 || dv > 128 || BH > 65535) return cudaErrorInvalidValue;
+    dim3 grid((d + kTailRows - 1) / kTailRows, (dv + kTailCols - 1) / kTailCols, BH);
+    state_tail_kernel<<<grid, kTailThreads, 0, s>>>(tot, state, d, dv, summary_offsets(d, dv), decode_offsets(d, dv));
     note_launches(1);
     return cudaGetLastError();
 }

@@ -87,8 +87,19 @@ struct Layout {
 // ones (V -> [V | 1]) is a 16-column tile of ones: the denominator is
 // Q p0 + W 1 and p grows by X^T 1 (the summary walk also gathers m = Q^T 1),
 // all N = 16 products into their own tensor-memory columns.
-template <int D, int MODE, bool NORM>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+//
+// XP (unnormalised summary walk whose final state is wanted): the segment's
+// m = sum_t q_t and p = sum_t x_t are gathered on the CUDA cores.  For m, one
+// more warp reads each chunk's Q tile by columns (lane l keeps running sums of
+// the bf16 pairs l, l + 32, ... of every row, in row order) and the issuer
+// refills a Q buffer only after that warp has read it (barriers DQ and DQ2,
+// one per Q buffer like LQ and LQ2, so that a phase never completes twice
+// before its waiter looks).  For p,
+// each drain thread keeps a running sum of the X row it drains (fp32, before
+// rounding); one transposing butterfly at the end sums a warp's rows and the
+// four lane quarters are added in a fixed order.
+template <int D, int MODE, bool NORM, bool XP>
+__global__ void __launch_bounds__(XP ? kThreadsTC + 32 : kThreadsTC, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
                const __grid_constant__ CUtensorMap mR, TCParams p) {
@@ -96,7 +107,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
     // (PB + w: drain warp w's prefix boxes, output walk)
-    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, FIN, PB,
+    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, FIN, PX, DQ, DQ2, PB,
            NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
@@ -106,6 +117,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    const bool msum = XP && warp == kDrainWarps + 1;  // XP: the Q column-sum warp
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
@@ -131,7 +143,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DW || i == DX2 || i == DO) cnt = kDrainWarps;
+            if (i == DA || i == DX || i == DW || i == DX2 || i == DO || i == PX) cnt = kDrainWarps;
             if (i == DS || i == DP) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
@@ -488,14 +500,53 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     mma_commit(bar(CP));
                     if (it + 2 < nchunks) {
                         if (!wait_bar(CQ, ph)) break;
+                        if (XP && !wait_bar(qodd ? DQ2 : DQ, qph)) break;  // the column-sum warp has read this Q
                         issue_load(qodd ? LQ2 : LQ, &mQ, tQc, c + 2);  // this buffer's next chunk
                     }
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+    } else if (msum) {
+        // ================ Q column sums (XP summary walk) ================
+        // lane l: bf16 pairs l + 32 g of every row (columns 2l + 64g, + 1);
+        // a warp's loads cover 128 contiguous bytes of one row
+        float macc[D / 32] = {};
+        for (int it = 0; it < nchunks; ++it) {
+            const bool qodd = it & 1;
+            if (!wait_bar(qodd ? LQ2 : LQ, (uint32_t)((it >> 1) & 1))) break;
+            const Tile& tQc = qodd ? tQ2 : tQ;
+            const uint32_t boff = (uint32_t)(lane & 3) << 2;
+#pragma unroll
+            for (int g = 0; g < D / 64; ++g)
+#pragma unroll 1
+                for (int r0 = 0; r0 < kL; r0 += 16) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = ld_shared_u32(tQc.chunk(r0 + j, g, lane >> 2) + boff);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        macc[2 * g] += __uint_as_float(v[j] << 16);
+                        macc[2 * g + 1] += __uint_as_float(v[j] & 0xFFFF0000u);
+                    }
+                }
+            __syncwarp();
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(qodd ? DQ2 : DQ)) : "memory");
+        }
+        if (nchunks > 0 && !abort_flag) {
+            const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
+            float* out = p.summ + ((size_t)head * p.nseg + seg) * R + 2 * (size_t)D * D;
+#pragma unroll
+            for (int g = 0; g < D / 64; ++g) {
+                out[64 * g + 2 * lane] = macc[2 * g];
+                out[64 * g + 2 * lane + 1] = macc[2 * g + 1];
+            }
+        }
     } else {
         // ========================== drain warps ==========================
+        // XP: running sums of this thread's X row (columns cD .. cD + D/2)
+        float xacc[XP ? D / 2 : 1] = {};
         for (int it = 0; it < nchunks; ++it) {
             const uint32_t ph = it & 1;
             const bool has_next = it + 1 < nchunks;
@@ -630,9 +681,21 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 drained(DA);
                 if (!wait_bar(CX2, ph)) break;
                 tc_fence_after();
-                if (NORM) drainDs(tA_, tX, tXl);
-                else drainD(tA_, tX);  // X -> sX
-                drained(DX);
+                if constexpr (NORM) {
+                    drainDs(tA_, tX, tXl);
+                    drained(DX);
+                } else if constexpr (XP) {
+                    uint32_t xr[64];
+                    tmem_ld_cols<D / 2>(tA_ + lane_off + cD, xr);  // X -> sX, then into this row's sums
+                    put_row32(tX, row, cD, xr, false);
+                    if (D == 128) put_row32(tX, row, cD + 32, xr + 32, false);
+                    drained(DX);
+#pragma unroll
+                    for (int j = 0; j < D / 2; ++j) xacc[j] += __uint_as_float(xr[j]);
+                } else {
+                    drainD(tA_, tX);  // X -> sX
+                    drained(DX);
+                }
                 if (state_rows && has_next) {
                     if (NORM) drainDs(tS_, tS, tSl);
                     else drainD(tS_, tS);  // S_local of the next chunk -> sS
@@ -674,6 +737,34 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 out[3 * (size_t)D * D + D + row] = __uint_as_float(pv);
             }
         }
+        if (MODE == 0 && XP && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
+            // p of the segment: each warp leaves the column sums of its 32 rows
+            // in the (dead) S tile, and the quarter-0 warps add the four quarters
+            float pacc[2];
+            {
+                uint32_t xb[32];
+#pragma unroll
+                for (int g = 0; g < D / 64; ++g) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) xb[j] = __float_as_uint(xacc[32 * g + j]);
+                    pacc[g] = warp_colsum32(xb, lane);
+                }
+            }
+            float* px = reinterpret_cast<float*>(dsm_raw + (dsm + LY::S - smem_u32(dsm_raw)));
+            px[quarter * D + cD + lane] = pacc[0];
+            if (D == 128) px[quarter * D + cD + 32 + lane] = pacc[1];
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(PX)) : "memory");
+            if (quarter == 0 && wait_bar(PX, 0)) {
+                const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
+                float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
+#pragma unroll
+                for (int j = 0; j < D / 2; j += 32) {
+                    const int c = cD + j + lane;
+                    out[3 * (size_t)D * D + D + c] = ((px[c] + px[D + c]) + px[2 * D + c]) + px[3 * D + c];
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -684,11 +775,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 
 
 // ------------------------------------------------------- cross products ----
-// out[b] = base[b] + A[b] B[b] for a batch of fp32 D x D matrices (the
+// out[b] = alpha base[b] + A[b] B[b] for a batch of fp32 D x D matrices (the
 // scan's S_<r C_r terms).  Each fp32 operand x is split into bf16 parts
 // hi = bf16(x), lo = bf16(x - hi), and the product is taken as
 // A_hi B_hi + A_hi B_lo + A_lo B_hi on the tensor cores (fp32 accumulation),
-// which keeps about 16 significant bits of every operand.
+// which keeps about 16 significant bits of every operand.  The optional
+// column outx[b] = alpha basex[b] + A[b] bx[b] (the normaliser's matrix-vector
+// term) is formed in fp32 on the CUDA cores from the A rows as they arrive.
 template <int D>
 struct CrossLayout {
     static constexpr uint32_t kA = 128u * D * 2u;  // A tiles keep 128 rows (MMA M = 128)
@@ -734,6 +827,28 @@ __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
             const int i = tid + j * 256;
             xa[j] = __ldg(reinterpret_cast<const float4*>(A) + i);
             xb[j] = __ldg(reinterpret_cast<const float4*>(B) + i);
+        }
+        if (a.bx && a.outx) {
+            // D / 4 consecutive lanes hold one row of A (256 is a multiple of
+            // D / 4, so a lane keeps its column quad for every j)
+            const float4 m = __ldg(reinterpret_cast<const float4*>(a.bx + b * a.sbx) + (tid % (D / 4)));
+            const float* basex = a.basex ? a.basex + b * a.sbasex : nullptr;
+            float* outx = a.outx + b * a.soutx;
+            const float sc = a.pscale ? a.pscale[(a.pscale_off + b) % a.pscale_mod] : 1.f;
+            float part[kPer];
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                part[j] = fmaf(xa[j].x, m.x, fmaf(xa[j].y, m.y, fmaf(xa[j].z, m.z, xa[j].w * m.w)));
+#pragma unroll
+            for (int o = D / 8; o > 0; o >>= 1)
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
+            if (tid % (D / 4) == 0)
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int r = (tid + j * 256) / (D / 4);
+                    outx[r] = fmaf(a.alpha, basex ? basex[r] : 0.f, sc * part[j]);
+                }
         }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
@@ -804,7 +919,7 @@ cudaError_t launch_cross_t(const CrossArgs& a, cudaStream_t s) {
 }
 
 
-template <int D, int MODE, bool NORM>
+template <int D, int MODE, bool NORM, bool XP = false>
 cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
                      int T, SegPlan plan, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mo;
@@ -826,11 +941,11 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     }
     TCParams prm{T, plan.nseg, plan.nchunk, plan.seglen, summ, prefix, O, status};
     const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;
-    auto kern = tc_walk_kernel<D, MODE, NORM>;
+    auto kern = tc_walk_kernel<D, MODE, NORM, XP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, XP ? kThreadsTC + 32 : kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -853,7 +968,7 @@ bool tc_supported(int d, int dv, int dtype, int normalized, int device) {
 
 cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
                            float* summ, int BH, int T, int d, int dv, int normalized, SegPlan plan, int* status,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool with_p) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
     if (normalized) {
@@ -863,6 +978,11 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
     }
     // unnormalised outputs: the walk pipelined across chunks (hla2_tc_out.cu)
     if (mode == 1) return launch_tc_out(Q, K, V, O, prefix, BH, T, d, dv, plan, status, s);
+    if (with_p) {
+        if (d == 128) return launch_t<128, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+        if (d == 64) return launch_t<64, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+        return cudaErrorInvalidValue;
+    }
     if (d == 128) return launch_t<128, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     if (d == 64) return launch_t<64, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     return cudaErrorInvalidValue;
@@ -870,7 +990,7 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
 
 cudaError_t launch_tc_cross(const CrossArgs& a, cudaStream_t s) {
     if (a.nb == 0) return cudaSuccess;
-    if (a.d != a.dv || a.bx || a.outx) return cudaErrorInvalidValue;
+    if (a.d != a.dv) return cudaErrorInvalidValue;
     if (a.d == 128) return launch_cross_t<128>(a, s);
     if (a.d == 64) return launch_cross_t<64>(a, s);
     return cudaErrorInvalidValue;

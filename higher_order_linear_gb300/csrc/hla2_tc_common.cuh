@@ -220,6 +220,28 @@ __device__ __forceinline__ void put_row32_split2(const Tile& hi, const Tile& lo,
     for (int q = 0; q < 4; ++q) st_shared_v4(lo.chunk(r, b, c0 + q), l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
 }
 
+// Column sums over a warp: lane i holds row i's 32 fp32 values (as bits) in
+// r[0..31]; lane j gets the sum over all lanes of column j.  A transposing
+// butterfly: at step w the lanes with bit w set keep the upper w of their
+// remaining columns and trade the lower w with lane ^ w, so each step halves
+// the columns a lane holds (31 shuffles for the 32 columns).
+__device__ __forceinline__ float warp_colsum32(const uint32_t* r, int lane) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float send = up ? v[k] : v[k + w];
+            const float keep = up ? v[k + w] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
 // Write the bf16 hi and lo parts of 4 fp32 values (columns c..c+3 of row r).
 __device__ __forceinline__ void put4_split(const Tile& hi, const Tile& lo, int r, int c, float4 x) {
     const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y), h1 = __floats2bfloat162_rn(x.z, x.w);
@@ -271,6 +293,12 @@ __device__ __forceinline__ void box32_store(const CUtensorMap* map, uint32_t scr
         tma_store_3d(map, scratch, x, y, z);
         tma_store_commit();
     }
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {

@@ -35,6 +35,7 @@ constexpr int kScanWarps = 16;  // four per 32-lane quarter of tensor memory
 // the two launches) and 43 us at 10 (against 27 us).
 constexpr int kScanFullMaxSegments = 4;
 constexpr int kScanThreadsTC = kScanWarps * 32;
+constexpr int kTotParts = 8;  // CTAs per head that form the plain totals (ScanArgs::tot)
 
 template <int D>
 struct ScanTileLayout {
@@ -101,9 +102,39 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
     const int quarter = warp & 3, part = warp >> 2;
     const int drow = quarter * 32 + lane;  // tensor-memory lane this thread drains
     const int dc0 = part * NC;
-    // grid (BH, nseg): the records with the longest folds (largest r) go first
-    const int head = blockIdx.x, r = (int)gridDim.y - 1 - (int)blockIdx.y;
+    // grid (BH, nseg [+ kTotParts]): the records with the longest folds
+    // (largest r) go first, the plain totals last
+    const int head = blockIdx.x, r = a.nseg - 1 - (int)blockIdx.y;
     const size_t R = a.R;
+    if ((int)blockIdx.y >= a.nseg) {
+        // plain totals over the records, part z of the float4 range, records
+        // added in order
+        const int z = (int)blockIdx.y - a.nseg;
+        const size_t n4 = a.tot_len / 4, per = (n4 + kTotParts - 1) / kTotParts;
+        const size_t i_end = n4 < (z + 1) * per ? n4 : (z + 1) * per;
+        const float4* src = reinterpret_cast<const float4*>(a.summ + (size_t)head * a.nseg * R);
+        float4* dst = reinterpret_cast<float4*>(a.tot + (size_t)head * R);
+        const size_t R4 = R / 4;
+        for (size_t i = z * per + tid; i < i_end; i += kScanThreadsTC) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int j = 0;
+            for (; j + 4 <= a.nseg; j += 4) {
+                float4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x[u] = __ldg(src + (size_t)(j + u) * R4 + i);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x += x[u].x; acc.y += x[u].y; acc.z += x[u].z; acc.w += x[u].w;
+                }
+            }
+            for (; j < a.nseg; ++j) {
+                const float4 x = __ldg(src + (size_t)j * R4 + i);
+                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            }
+            dst[i] = acc;
+        }
+        return;
+    }
     const float* rec0 = a.summ + (size_t)head * a.nseg * R;
     float* out = a.prefix + ((size_t)head * a.nseg + r) * R;
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
@@ -293,7 +324,7 @@ cudaError_t launch_scan_t(const ScanArgs& a, int BH, cudaStream_t s) {
     auto kern = tc_scan_kernel<D, OP, EXTRA, FULL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(BH, a.nseg);
+    dim3 grid(BH, a.nseg + (a.tot ? kTotParts : 0));
     kern<<<grid, kScanThreadsTC, smem, s>>>(a);
     note_launches(1);
     return cudaGetLastError();
@@ -316,7 +347,9 @@ cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cud
     if (d != dv || (d != 64 && d != 128) || BH > 65535 || a.nseg > 65535) return cudaErrorInvalidValue;
     if ((a.extra && op != kScanHLA) || (op != kScanHLA && op != kScanDecay && op != kScanAHLA))
         return cudaErrorInvalidValue;
-    const bool full = a.nseg <= kScanFullMaxSegments;
+    if (a.tot && (a.tot_len % 4 != 0 || a.tot_len > a.R || a.R % 4 != 0 || a.nseg + kTotParts > 65535))
+        return cudaErrorInvalidValue;
+    const bool full = !a.terms_only && a.nseg <= kScanFullMaxSegments;
     if (d == 128) return full ? launch_scan_d<128, true>(op, a, BH, s) : launch_scan_d<128, false>(op, a, BH, s);
     return full ? launch_scan_d<64, true>(op, a, BH, s) : launch_scan_d<64, false>(op, a, BH, s);
 }

@@ -104,7 +104,9 @@ HLA2_API int hla2_forward_plan(int B, int H, int T, int sm_count, int* nseg, int
  *             garbage afterwards.
  *   state_out optional (NULL to skip): receives each head's final state after
  *             token T-1 in the hla2_step layout, [B*H][d*d + 2*d*dv + 2*d]
- *             fp32, so that decoding can continue with hla2_step.
+ *             fp32, so that decoding can continue with hla2_step.  On the
+ *             tensor-core path (hla2_forward_path == 1) its G part carries the
+ *             outputs' bf16-operand rounding; S, C and m are fp32 sums.
  * Errors: HLA2_ERR_INVALID (nulls, sizes <= 0, misalignment),
  *         HLA2_ERR_UNSUPPORTED (d or dv > 128, unknown dtype),
  *         HLA2_ERR_WORKSPACE, HLA2_ERR_LAUNCH.
@@ -225,7 +227,10 @@ HLA2_API int hla2_chunk_summaries(const void* Q, const void* K, const void* V, f
  * Because S, C and m combine by plain addition, the scan is evaluated as an
  * exclusive sum of (S, C, m), one product S_r C_<r (and S_r m_<r) per record,
  * and an exclusive sum of G_r + S_r C_<r: the same value as any bracketing of
- * the combine, up to fp32 rounding.
+ * the combine, up to fp32 rounding.  With d = dv in {64, 128} on sm_103 the
+ * products S_r C_<r run on the tensor cores with each fp32 operand split into
+ * bf16 hi + lo parts (about 16 significant bits per operand, fp32
+ * accumulation); S_r m_<r and every sum stay fp32 on the CUDA cores.
  * Errors: HLA2_ERR_INVALID, HLA2_ERR_UNSUPPORTED, HLA2_ERR_LAUNCH.
  */
 HLA2_API int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int dv,

@@ -40,7 +40,10 @@ def test_tensor_core_path_selected():
     assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 0) == 1   # normalised: split operands
     assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 1, 0) == 0
     assert L.hla2_forward_path(16, 16, hla2.HLA2_DTYPE_F32, 0, 0) == 0
-    assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 1) == 0
+    # the final state is handed over from the tensor-core forward too
+    assert L.hla2_forward_path(128, 128, hla2.HLA2_DTYPE_BF16, 0, 1) == 1
+    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 0, 1) == 1
+    assert L.hla2_forward_path(64, 64, hla2.HLA2_DTYPE_BF16, 1, 1) == 1
 
 
 @pytest.mark.parametrize("T", [1, 127, 128, 129, 383, 2000, 5000])
@@ -211,6 +214,88 @@ def test_state_out_then_step_continues(dtype, norm):
         outs.append(hla2.hla2_step(state, qt, kt, vt, normalized=norm))
     got = torch.stack(outs, dim=1).reshape(B, H, extra, dv)
     assert relerr(f64(got), ref[..., T:, :]) < 1e-4
+
+
+@pytest.mark.parametrize("d,T,norm", [(128, 129, False), (128, 1000, False), (128, 3000, False),
+                                      (64, 129, False), (64, 1000, False), (64, 3000, False),
+                                      (64, 1000, True), (64, 3000, True)])
+def test_state_out_tensor_core(d, T, norm):
+    """bf16 d = dv in {64, 128} with state_out on the tcgen05 walks (one-chunk
+    segments with a one-token tail at T = 129, a scan short enough for one
+    launch at T = 1000, a longer one at T = 3000): S, C and m of the handed-over
+    state are fp32 sums (1e-5 per field); G and h carry the walks' rounding
+    (the forward's bound over the whole state); decoding then continues."""
+    assert hla2.lib().hla2_forward_path(d, d, hla2.HLA2_DTYPE_BF16, int(norm), 1) == 1
+    B, H, extra, dv = 1, 3, 12, d
+    g = torch.Generator().manual_seed(d * 1000 + T + int(norm))
+    if norm:
+        q = torch.rand(B, H, T + extra, d, generator=g) / d ** 0.5
+        k = torch.rand(B, H, T + extra, d, generator=g) / d ** 0.5
+    else:
+        q = torch.randn(B, H, T + extra, d, generator=g) / d ** 0.5
+        k = torch.randn(B, H, T + extra, d, generator=g) / d ** 0.5
+    v = torch.randn(B, H, T + extra, dv, generator=g) / d ** 0.5
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    tol = TOL_NORMALIZED if norm else TOL_TC_BF16
+    ref = oracle_forward(q, k, v, normalized=norm)
+    state = torch.empty(B * H, hla2.record_len(d, dv), device=DEV)
+    out = run_gpu(q[..., :T, :], k[..., :T, :], v[..., :T, :], normalized=norm, state_out=state)
+    assert relerr(f64(out), ref[..., :T, :]) < tol
+    summ = oracle.chunk_summaries(f64(q[..., :T, :]), f64(k[..., :T, :]), f64(v[..., :T, :]), L=T)[:, :, 0]
+    expect = oracle.summary_to_decode_state(summ, d, dv).reshape(B * H, -1)
+    got = f64(state)
+    nS, nC = d * d, d * dv
+    cut = {"S": (0, nS), "C": (nS, nS + nC), "m": (nS + 2 * nC, nS + 2 * nC + d)}
+    for name, (a, b) in cut.items():
+        assert relerr(got[:, a:b], expect[:, a:b]) < 1e-5, name
+    assert relerr(got, expect) < tol
+    outs = []
+    for t in range(T, T + extra):
+        qt = q[..., t, :].reshape(B * H, d).float().to(DEV)
+        kt = k[..., t, :].reshape(B * H, d).float().to(DEV)
+        vt = v[..., t, :].reshape(B * H, dv).float().to(DEV)
+        outs.append(hla2.hla2_step(state, qt, kt, vt, normalized=norm))
+    got_o = torch.stack(outs, dim=1).reshape(B, H, extra, dv)
+    assert relerr(f64(got_o), ref[..., T:, :]) < tol
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_state_out_graph_capture(dtype):
+    """The forward with state_out issues only stream-ordered work too: captured
+    in a CUDA graph and replayed on new inputs it gives the eager O and final
+    state bit for bit."""
+    B, H, T, d = 1, 4, 2000, 64 if dtype == torch.bfloat16 else 32
+    g0 = torch.Generator().manual_seed(5)
+    mk = lambda: [(torch.randn(B, H, T, d, generator=g0) / d ** 0.5).to(dtype).to(DEV) for _ in range(3)]
+    (q, k, v), (q2, k2, v2) = mk(), mk()
+    ws = torch.empty(hla2.hla2_forward_workspace(B, H, T, d, d, hla2.HLA2_DTYPE_BF16 if dtype == torch.bfloat16
+                                                 else hla2.HLA2_DTYPE_F32), device=DEV, dtype=torch.uint8)
+    O = torch.empty(B, H, T, d, device=DEV)
+    st = torch.empty(B * H, hla2.record_len(d, d), device=DEV)
+    call = lambda a, b, c: hla2.hla2_forward(a, b, c, O, workspace=ws, state_out=st)
+    refs = []
+    for x in ((q2, k2, v2), (q, k, v)):
+        call(*x)
+        torch.cuda.synchronize()
+        refs.append((O.clone(), st.clone()))
+    sq, sk, sv = q.clone(), k.clone(), v.clone()
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        call(sq, sk, sv)
+        cs.synchronize()
+        with torch.cuda.graph(graph, stream=cs):
+            call(sq, sk, sv)
+    torch.cuda.synchronize()
+    for (a, b, c), (o_ref, s_ref) in (((q, k, v), refs[1]), ((q2, k2, v2), refs[0])):
+        sq.copy_(a); sk.copy_(b); sv.copy_(c)
+        O.zero_(); st.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(O, o_ref)
+        assert torch.equal(st, s_ref)
+    assert hla2.hla2_device_status() == 0
 
 
 @pytest.mark.parametrize("op", ["hla", "ahla", "unmasked", "decay"])
