@@ -53,8 +53,9 @@ exscan_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t l
 }
 
 // Same scan, four consecutive elements per thread (16-byte accesses); used
-// when the element range, the record length and the pointers allow it.
-template <bool WRITE>
+// when the element range, the record length and the pointers allow it.  U
+// records are loaded at a time (more in flight for long record axes).
+template <bool WRITE, int U>
 __global__ void __launch_bounds__(kScanThreads)
 exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t len, float* total,
                size_t total_stride) {
@@ -65,12 +66,12 @@ exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t 
     float* pout = out + (size_t)bh * N * R + off + i;
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
     int r = 0;
-    for (; r + kScanUnroll <= N; r += kScanUnroll) {
-        float4 x[kScanUnroll];
+    for (; r + U <= N; r += U) {
+        float4 x[U];
 #pragma unroll
-        for (int j = 0; j < kScanUnroll; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
+        for (int j = 0; j < U; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
 #pragma unroll
-        for (int j = 0; j < kScanUnroll; ++j) {
+        for (int j = 0; j < U; ++j) {
             if (WRITE) *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
             run.x += x[j].x; run.y += x[j].y; run.z += x[j].z; run.w += x[j].w;
         }
@@ -333,8 +334,17 @@ cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, 
     if (!out && !total) return cudaErrorInvalidValue;
     if (vec) {
         dim3 grid((unsigned)((len / 4 + kScanThreads - 1) / kScanThreads), BH);
-        if (out) exscan4_kernel<true><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
-        else exscan4_kernel<false><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        // long record axes keep 16 records per thread in flight (the element
+        // range alone gives too few threads to cover the latency)
+        if (N >= 64) {
+            if (out) exscan4_kernel<true, 16><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+            else exscan4_kernel<false, 16><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
+        } else {
+            if (out) exscan4_kernel<true, kScanUnroll><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total,
+                                                                                       total_stride);
+            else exscan4_kernel<false, kScanUnroll><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total,
+                                                                                    total_stride);
+        }
     } else {
         dim3 grid((unsigned)((len + kScanThreads - 1) / kScanThreads), BH);
         if (out) exscan_kernel<true><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);

@@ -874,6 +874,16 @@ __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
         mma_commit(smem_u32(&bar_mma));
     }
     __syncwarp();
+    // this thread's part of base (row `row`, columns cD .. cD + D/2), loaded
+    // while the products run
+    const bool out_rows = (D == 128) || quarter < D / 32;
+    const int cD = half * (D / 2);
+    float4 bv[D / 8];
+    if (out_rows) {
+        const float* base = a.base + b * a.sbase;
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) bv[j] = __ldg(reinterpret_cast<const float4*>(base + (size_t)row * D + cD) + j);
+    }
     // bounded wait for the products
     bool ok = mbar_try(smem_u32(&bar_mma), 0);
     if (!ok) {
@@ -883,16 +893,14 @@ __global__ void __launch_bounds__(256, 1) tc_cross_kernel(CrossArgs a) {
         if (!ok && lane == 0) atomicExch(a.status, (int)kDevWaitTimeout);
     }
     tc_fence_after();
-    if (ok && ((D == 128) || quarter < D / 32)) {
+    if (ok && out_rows) {
         uint32_t r[64];
-        const int cD = half * (D / 2);
         tmem_ld_cols<D / 2>(tmem + ((uint32_t)(quarter * 32) << 16) + cD, r);
-        const float* base = a.base + b * a.sbase;
         float* out = a.out + b * a.sout;
         const float sc = a.pscale ? a.pscale[(a.pscale_off + b) % a.pscale_mod] : 1.f;
 #pragma unroll
         for (int j = 0; j < D / 2; j += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(base + (size_t)row * D + cD + j);
+            const float4 x = bv[j / 4];
             *reinterpret_cast<float4*>(out + (size_t)row * D + cD + j) =
                 make_float4(fmaf(a.alpha, x.x, sc * __uint_as_float(r[j])),
                             fmaf(a.alpha, x.y, sc * __uint_as_float(r[j + 1])),
