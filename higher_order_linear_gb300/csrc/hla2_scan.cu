@@ -251,13 +251,17 @@ state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecO
     __shared__ __align__(16) float sC[128][kTailCols];   // C[k][c0 + j]
     __shared__ float sS[kTailRows][128 + 1];              // S[i0 + r][k], padded rows
     __shared__ float sm[128];
+    __shared__ float sp[kTailRows];                       // p[i0 + r]
     const int head = blockIdx.z, i0 = blockIdx.x * kTailRows, c0 = blockIdx.y * kTailCols;
     const int nr = d - i0 < kTailRows ? d - i0 : kTailRows;
     const int nc = dv - c0 < kTailCols ? dv - c0 : kTailCols;
     const float* t = tot + (size_t)head * so.R;
     float* o = state + (size_t)head * dof.R;
     const int tid = threadIdx.x;
+    float vp[4];  // P at this thread's G entries (row tid / 8, columns 4 (tid % 8) .. + 3 of the block)
     {
+        // every load is issued before the first shared-memory store, so that
+        // they overlap (fixed trip counts, predicated on the sizes)
         constexpr int kNC = 128 * kTailCols / kTailThreads, kNS = kTailRows * 128 / kTailThreads;
         float vc[kNC], vs[kNS];
 #pragma unroll
@@ -271,6 +275,13 @@ state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecO
             vs[q] = (r < nr && k < d) ? t[so.S + (size_t)(i0 + r) * d + k] : 0.f;
         }
         const float vm = tid < d ? t[so.m + tid] : 0.f;
+        const float vps = (blockIdx.y == 0 && tid < nr) ? t[so.x + i0 + tid] : 0.f;
+        {
+            const int r = tid >> 3, j0 = 4 * (tid & 7);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                vp[q] = (r < nr && j0 + q < nc) ? t[so.X + (size_t)(i0 + r) * dv + c0 + j0 + q] : 0.f;
+        }
 #pragma unroll
         for (int q = 0; q < kNC; ++q) {
             const int i = tid + q * kTailThreads;
@@ -282,6 +293,7 @@ state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecO
             sS[i / 128][i % 128] = vs[q];
         }
         sm[tid] = vm;
+        if (tid < kTailRows) sp[tid] = vps;
     }
     __syncthreads();
     for (int i = tid; i < nr * nc; i += kTailThreads) {
@@ -299,7 +311,7 @@ state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecO
             for (int k = lane; k < d; k += 32) h = fmaf(sS[r][k], sm[k], h);
 #pragma unroll
             for (int w = 16; w >= 1; w >>= 1) h += __shfl_xor_sync(0xffffffffu, h, w);
-            if (lane == 0) o[dof.x + i0 + r] = h - t[so.x + i0 + r];
+            if (lane == 0) o[dof.x + i0 + r] = h - sp[r];
         }
     }
     const int r = tid >> 3, j0 = 4 * (tid & 7);
@@ -315,7 +327,7 @@ state_tail_kernel(const float* tot, float* state, int d, int dv, RecOff so, RecO
     const size_t g = (size_t)(i0 + r) * dv + c0 + j0;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        if (j0 + q < nc) o[dof.X + g + q] = acc[q] - t[so.X + g + q];
+        if (j0 + q < nc) o[dof.X + g + q] = acc[q] - vp[q];
 }
 
 __global__ void copy_strided_kernel(const float* src, long long s_src, float* dst, long long s_dst, size_t len) {
