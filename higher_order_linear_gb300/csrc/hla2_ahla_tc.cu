@@ -145,7 +145,11 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         }
         return true;
     };
+    // every tile load is issued by the issuer's lane 0, which settles them
+    // (waits for the last of each barrier) before the CTA exits
+    LoadLedger<3> loads(bar(0));  // LQ, LK, LV
     auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        loads.note(b);
         mbar_expect_tx(bar(b), kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
@@ -211,9 +215,11 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         (void)pre;
         const int rec = head * p.nseg + seg;
         const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+        LoadLedger<1> boxes(bar(PB + warp));
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
+                boxes.note(0);
                 fence_proxy_async();
                 mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
 #pragma unroll
@@ -233,6 +239,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             }
             __syncwarp();  // every lane has read the boxes before the next load reuses them
         }
+        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         tmem_st_wait();
     }
     fence_proxy_async();
@@ -347,6 +354,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
     } else {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {

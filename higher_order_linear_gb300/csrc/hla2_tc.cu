@@ -107,7 +107,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains
     // (PB + w: drain warp w's prefix boxes, output walk)
-    enum { LQ, LK, LV, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, LQ2, FIN, PX, DQ, DQ2, PB,
+    enum { LQ, LK, LV, LQ2, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, FIN, PX, DQ, DQ2, PB,
            NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
@@ -195,7 +195,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         }
         return true;
     };
+    // every tile load is issued by the issuer's lane 0, which settles them
+    // (waits for the last of each barrier) before the CTA exits
+    LoadLedger<4> loads(bar(0));  // LQ, LK, LV, LQ2
     auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        loads.note(b);
         mbar_expect_tx(bar(b), kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
@@ -277,9 +281,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         // tiles, which nothing else touches before the first chunk
         const int rec = head * p.nseg + seg;
         const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+        LoadLedger<1> boxes(bar(PB + warp));
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
+                boxes.note(0);
                 fence_proxy_async();
                 mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
 #pragma unroll
@@ -300,6 +306,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             }
             __syncwarp();  // every lane has read the boxes before the next load reuses them
         }
+        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         if (NORM && half == 0) {
             // p0 = S0 m0 - h0 of the prefix (record slot after P)
             const float p0 = pre[3 * (size_t)D * D + D + row];
@@ -507,6 +514,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
     } else if (msum) {
         // ================ Q column sums (XP summary walk) ================
         // lane l: bf16 pairs l + 32 g of every row (columns 2l + 64g, + 1);

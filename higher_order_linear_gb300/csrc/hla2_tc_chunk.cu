@@ -126,7 +126,10 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ 
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // B V
 
     if (issuer) {
+        // lane 0 issues the tile loads and settles them before the CTA exits
+        LoadLedger<1> loads(bar(LD));
         if (lane == 0) {
+            loads.note(0);
             mbar_expect_tx(bar(LD), 3u * kL * D * 2u);
 #pragma unroll
             for (int k = 0; k < D / 64; ++k) {
@@ -169,6 +172,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ 
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         }
     } else {
         // ========================== drain warps ==========================

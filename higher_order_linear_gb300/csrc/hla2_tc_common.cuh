@@ -268,6 +268,36 @@ __device__ __forceinline__ bool mma_wait_all(uint32_t mbar) {
     return true;
 }
 
+// Bulk tensor loads that one thread issued on its load barriers (one phase
+// per load, nobody else arrives there).  Before the CTA exits, that thread
+// calls settle(): it waits, at most kWaitNs in all and whatever the abort
+// state, until the last phase it armed on each barrier has completed, so that
+// no copy is still writing this CTA's shared memory when a wait elsewhere ran
+// out and the CTA unwinds early.  In a normal run every load has long landed.
+template <int N>
+struct LoadLedger {
+    static_assert(N <= 16, "two bits per barrier in one word");
+    uint32_t bar0;   // shared address of barrier index 0
+    uint32_t state;  // per barrier i: bit 2i = armed at least once, bit 2i + 1 = parity of its last phase
+    __device__ explicit LoadLedger(uint32_t b0) : bar0(b0), state(0u) {}
+    __device__ void note(int b) {
+        const uint32_t armed = 1u << (2 * b);
+        if (state & armed) state ^= armed << 1;
+        else state |= armed;
+    }
+    __device__ bool settle() const {
+        const unsigned long long t0 = globaltimer();
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (!((state >> (2 * i)) & 1u)) continue;
+            const uint32_t a = bar0 + 8u * (uint32_t)i, parity = (state >> (2 * i + 1)) & 1u;
+            while (!mbar_try(a, parity))
+                if (globaltimer() - t0 > kWaitNs) return false;
+        }
+        return true;
+    }
+};
+
 // Load NC (32 or 64) consecutive TMEM columns of this thread's lane, one wait.
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) {

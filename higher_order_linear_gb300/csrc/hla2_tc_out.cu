@@ -160,7 +160,12 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         }
         return true;
     };
+    // every tile load is issued by the producer's lane 0, which settles them
+    // (waits for the last of each barrier) before the CTA exits
+    LoadLedger<4> loads(bar(0));  // LQ0, LQ1, LK, LV
+    static_assert(LQ0 == 0 && LQ1 == 1 && LK == 2 && LV == 3, "load barriers first");
     auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        loads.note(b);
         mbar_expect_tx(bar(b), kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
@@ -228,9 +233,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         // tiles, which nothing else touches before the first chunk
         const int rec = head * p.nseg + seg;
         const uint32_t stage = dsm + LY::X + (uint32_t)warp * 4096u;
+        LoadLedger<1> boxes(bar(PB + warp));
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
+                boxes.note(0);
                 fence_proxy_async();
                 mbar_expect_tx(bar(PB + warp), 4096u);
                 tma_load_3d(stage, &mR, cD, (m == 0 ? 0 : 2 * D + 1) + quarter * 32, rec, bar(PB + warp));
@@ -243,6 +250,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             if (m == 0) put_row32(tSP, row, cD, r, false);  // bf16 S0; P0 follows once Q S0 has read it
             __syncwarp();  // every lane has read the box before the next load reuses it
         }
+        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         tmem_st_wait();
     }
     fence_proxy_async();
@@ -327,6 +335,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 issue_load(LV, &mV, tV, c + 1);
                 if (it + 2 < nchunks) issue_load((it & 1) ? LQ1 : LQ0, &mQ, (it & 1) ? tQ1 : tQ0, c + 2);
             }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         }
     } else if (drainer) {
         // ========================== drain warps ==========================

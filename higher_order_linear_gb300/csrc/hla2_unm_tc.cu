@@ -103,7 +103,12 @@ unm_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     auto tileQ = [&](int b) { return Tile{dsm + (uint32_t)b * LY::kBuf, kL}; };
     auto tileK = [&](int b) { return Tile{dsm + (uint32_t)b * LY::kBuf + LY::kTok, kL}; };
     auto tileV = [&](int b) { return Tile{dsm + (uint32_t)b * LY::kBuf + 2 * LY::kTok, kL}; };
+    // the issuer's lane 0 issues every tile load and settles them before the
+    // CTA exits (waits for the last of each barrier)
+    LoadLedger<2> loads(bar(L0));
+    static_assert(L0 == 0 && L1 == 1, "load barriers first");
     auto load = [&](int b, int chunk) {
+        loads.note(b);
         mbar_expect_tx(bar(L0 + b), 3u * LY::kTok);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) {
@@ -138,6 +143,7 @@ unm_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             // FIN completes once every product has: the records can be read out
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
     } else if (state_rows && nchunks > 0) {
         // records S (row 0) and C (row D) leave as 32 x 32 boxes through the
         // dead tile area once the last chunk's products are done
@@ -258,7 +264,11 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         }
         return true;
     };
+    // every tile load is issued by the issuer's lane 0, which settles them
+    // (waits for the last of each barrier) before the CTA exits
+    LoadLedger<3> loads(bar(0));  // LQ, LK, LV
     auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
+        loads.note(b);
         mbar_expect_tx(bar(b), kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
@@ -305,9 +315,11 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     if (state_rows) {
         const int rec = head * p.nseg + seg;
         const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
+        LoadLedger<1> boxes(bar(PB + warp));
 #pragma unroll 1
         for (int m = 0; m < 2; ++m) {
             if (lane == 0) {
+                boxes.note(0);
                 fence_proxy_async();
                 mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
 #pragma unroll
@@ -326,6 +338,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             __syncwarp();
         }
+        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
         tmem_st_wait();
     }
     fence_proxy_async();
@@ -406,6 +419,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
+        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
     } else {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {
