@@ -541,6 +541,22 @@ int hla2_scan(const float* summ, float* prefix, int B, int H, int N, int d, int 
     return HLA2_OK;
 }
 
+int hla2_selftest_wait_runout(int* flag, int wait_us, hla2_stream_t stream) {
+    if (!flag) return fail(HLA2_ERR_INVALID, "null flag pointer");
+    if (reinterpret_cast<uintptr_t>(flag) % 4 != 0) return fail(HLA2_ERR_INVALID, "flag pointer not 4-byte aligned");
+    if (wait_us < 1 || wait_us > 2000000) return fail(HLA2_ERR_INVALID, "wait_us must be in [1, 2000000] (got %d)", wait_us);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(HLA2_ERR_LAUNCH, "no current device");
+    if (!tc_supported(64, 64, HLA2_DTYPE_BF16, 0, dev))
+        return fail(HLA2_ERR_UNSUPPORTED, "the self-test needs tensor memory (sm_103)");
+    int* status = device_status_word();
+    if (!status) return fail(HLA2_ERR_LAUNCH, "cannot resolve the device status word");
+    cudaError_t e = launch_selftest_runout(status, 1000ull * (unsigned long long)wait_us, flag,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test");
+    return HLA2_OK;
+}
+
 int hla2_forward_path(int d, int dv, int dtype, int normalized, int with_state_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;

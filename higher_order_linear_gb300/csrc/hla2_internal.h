@@ -253,4 +253,9 @@ cudaError_t launch_tc_scan(int op, const ScanArgs& a, int BH, int d, int dv, cud
 // launch_tc_scan (no running-sum pass is needed afterwards).
 int tc_scan_full_max_segments();
 
+// A bounded device wait that runs out on purpose (hla2_selftest.cu): one CTA
+// waits wait_ns on an mbarrier nothing arrives on, sets *status, writes 0 to
+// *out (1 had the wait completed) and releases its tensor memory.
+cudaError_t launch_selftest_runout(int* status, unsigned long long wait_ns, int* out, cudaStream_t s);
+
 }  // namespace hla2

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.hla2_last_error_detail.restype = i
             L.hla2_device_status.argtypes = [vp]
             L.hla2_device_status.restype = i
+            L.hla2_selftest_wait_runout.argtypes = [vp, i, vp]
+            L.hla2_selftest_wait_runout.restype = i
             L.hla2_profile_enable.argtypes = [i]
             L.hla2_profile_enable.restype = i
             L.hla2_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), i, ctypes.POINTER(i),
@@ -415,6 +417,17 @@ def hla2_scan(summ: torch.Tensor, d: int, dv: int, prefix: torch.Tensor | None =
 
 def hla2_device_status(stream=None) -> int:
     return int(lib().hla2_device_status(_stream(stream)))
+
+
+def hla2_selftest_wait_runout(flag: torch.Tensor, wait_us: int, stream=None) -> None:
+    """Runs the library's wait run-out on purpose (see include/hla2.h); flag
+    is a CUDA int32 tensor of one element that receives 0 when the wait gave
+    up.  Read the status afterwards with hla2_device_status."""
+    if not (isinstance(flag, torch.Tensor) and flag.is_cuda and flag.dtype == torch.int32 and flag.numel() >= 1):
+        raise ValueError("flag must be a CUDA int32 tensor with at least one element")
+    with torch.cuda.device(flag.device):
+        _check(lib().hla2_selftest_wait_runout(ctypes.c_void_p(flag.data_ptr()), int(wait_us), _stream(stream)),
+               "hla2_selftest_wait_runout")
 
 
 def hla2_profile_enable(on: bool = True) -> None:

@@ -365,6 +365,22 @@ HLA2_API int hla2_last_error_detail(char* buf, size_t n);
 HLA2_API int hla2_device_status(hla2_stream_t stream);
 
 /*
+ * Exercises the device error path on purpose, without any fault (no
+ * counterpart on the pages).  Launches one CTA that takes tensor memory,
+ * waits on a barrier that nothing arrives on, gives up after wait_us
+ * microseconds the way every bounded wait of the library does (it sets the
+ * device status word), releases its tensor memory and returns.
+ *   flag     device int (caller-owned, 4-byte aligned): receives 0 when the
+ *            wait gave up (1 would mean it completed, which cannot happen).
+ *   wait_us  1 .. 2,000,000.
+ * A following hla2_device_status returns HLA2_ERR_DEVICE (and clears the
+ * word); the context stays usable.  Errors: HLA2_ERR_INVALID (null or
+ * misaligned flag, wait_us out of range), HLA2_ERR_UNSUPPORTED (a device
+ * without tensor memory), HLA2_ERR_LAUNCH.
+ */
+HLA2_API int hla2_selftest_wait_runout(int* flag, int wait_us, hla2_stream_t stream);
+
+/*
  * Instrumentation (no counterpart on the pages).  While enabled, every
  * hla2_forward records CUDA events on its stream around its three phases:
  * [0] segment summaries, [1] exclusive scan, [2] segment outputs.

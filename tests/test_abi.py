@@ -196,3 +196,12 @@ def test_host_forward_workspace_and_checks(L):
         hla2.HLA2_ERR_INVALID
     assert "aligned" in hla2.hla2_last_error_detail()
     assert L.hla2_forward_host(p, p, p, p, B, H, T, 200, dv, 0, bf, G, dev, need, None) == hla2.HLA2_ERR_UNSUPPORTED
+
+
+def test_selftest_runout_rejects_bad_arguments(L):
+    """The wait run-out self-test checks its arguments before any CUDA call."""
+    assert L.hla2_selftest_wait_runout(None, 1000, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_selftest_wait_runout(_fake(4098), 1000, None) == hla2.HLA2_ERR_INVALID  # misaligned
+    assert L.hla2_selftest_wait_runout(_fake(), 0, None) == hla2.HLA2_ERR_INVALID
+    assert L.hla2_selftest_wait_runout(_fake(), 2000001, None) == hla2.HLA2_ERR_INVALID
+    assert "wait_us" in hla2.hla2_last_error_detail()
