@@ -59,13 +59,23 @@ struct OutLayout {
 // 32 of a D-wide region, 128 / (D / 32) of alpha), one warp (lane 0) issues
 // every MMA, another every tile load, so that MMA issue never waits behind a
 // busy bulk-copy queue; the roles meet only on mbarriers.  There are D / 8
-// drain warps (16 at D = 128), so that each drain is short.
+// drain warps (16 at D = 128), so that each drain is short.  At D = 128 they
+// form two groups of eight (two warps per lane quarter): the alpha warps
+// pack A and W, the beta warps drain X, O and the state, so that packing the
+// next chunk's A never waits behind the previous chunk's O stores.  At D = 64
+// every drain warp does both.  Columns go in groups of 32: an alpha warp
+// takes kAG groups of alpha, a beta warp kBG groups of each D-wide region.
 template <int D>
 struct OutRoles {
-    static constexpr int kParts = D / 32;             // drain warps per lane quarter
-    static constexpr int kDrain = 4 * kParts;         // drain warps
-    static constexpr int kCA = 128 / kParts;          // alpha columns per drain warp
-    static constexpr int kState = (D / 32) * kParts;  // drain warps holding state rows (< D)
+    static constexpr int kParts = D / 32;              // drain warps per lane quarter
+    static constexpr int kDrain = 4 * kParts;          // drain warps
+    static constexpr bool kSplit = D == 128;           // alpha and beta warps apart
+    static constexpr int kAPer = kSplit ? kParts / 2 : kParts;  // alpha warps per quarter
+    static constexpr int kBPer = kSplit ? kParts / 2 : kParts;  // beta warps per quarter
+    static constexpr int kAG = 4 / kAPer;              // alpha groups per alpha warp
+    static constexpr int kBG = (D / 32) / kBPer;       // D-wide groups per beta warp
+    static constexpr int kAlpha = 4 * kAPer, kBeta = 4 * kBPer;
+    static constexpr int kState = (D / 32) * kBPer;    // beta warps holding state rows (< D)
     static constexpr int kThreads = (kDrain + 2) * 32;
 };
 
@@ -85,11 +95,10 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap mR, OutParams p) {
     using LY = OutLayout<D>;
     using RO = OutRoles<D>;
-    constexpr int NDW = RO::kDrain, CA = RO::kCA;
+    constexpr int NDW = RO::kDrain, AG = RO::kAG, BG = RO::kBG;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | final wait | drain warp w's prefix boxes
-    // (XB: every drain warp's O box has left sX, D = 128)
-    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, XB, FIN, PB, NBAR = PB + NDW };
+    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, FIN, PB, NBAR = PB + NDW };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -109,7 +118,10 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool state_rows = drainer && quarter < D / 32;  // drain warp holding rows < D
+    const bool alpha_w = drainer && (!RO::kSplit || part < RO::kAPer);  // packs A and W
+    const bool beta_w = drainer && (!RO::kSplit || part >= RO::kAPer);  // drains X, O and the state
+    const int aw = part, bw = RO::kSplit ? part - RO::kAPer : part;     // index among its kind in a quarter
+    const bool state_rows = beta_w && quarter < D / 32;  // beta warp holding rows < D
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
@@ -120,7 +132,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DW || i == DO || i == XB) cnt = NDW;
+            if (i == DA || i == DW) cnt = RO::kAlpha;
+            if (i == DX || i == DO) cnt = RO::kBeta;
             if (i == DS || i == DP) cnt = RO::kState;
             mbar_init(bar(i), cnt);
         }
@@ -141,8 +154,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const uint32_t tS_ = tmem + 128 + D;      // running S
     const uint32_t tP_ = tmem + 128 + 2 * D;  // running P
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int cD = part * 32;  // this drain warp's columns in a D-wide region
-    const int ca0 = part * CA;  // ... and in alpha
+    const int cD = part * 32;  // this drain warp's columns of the segment prefix (prologue)
+    auto acol = [&](int g) { return (aw * AG + g) * 32; };  // alpha group g of this alpha warp
+    auto bcol = [&](int g) { return (bw * BG + g) * 32; };  // D-wide group g of this beta warp
 
     constexpr uint32_t kTileBytes = kL * D * 2;
     auto wait_bar = [&](int b, uint32_t parity) -> bool {
@@ -177,43 +191,44 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
     };
-    // this warp's 32 columns of a D-wide fp32 region -> bf16 tile rows
+    // this beta warp's groups of a D-wide fp32 region -> bf16 tile rows
     auto drainD = [&](uint32_t treg, const Tile& t) {
-        uint32_t r[32];
-        tmem_ld32(treg + lane_off + cD, r);
-        tmem_ld_wait();
-        put_row32(t, row, cD, r, false);
+#pragma unroll
+        for (int g = 0; g < BG; ++g) {
+            uint32_t r[32];
+            tmem_ld32(treg + lane_off + bcol(g), r);
+            tmem_ld_wait();
+            put_row32(t, row, bcol(g), r, false);
+        }
     };
-    // Packed bf16 operands in alpha: drain warp (q, part) packs the pairs of
-    // its alpha columns [ca0, ca0 + CA) (A, or W and on a first chunk also
-    // W_lo) into [ca0, ca0 + CA/2) (W_lo into [ca0 + CA/2, ca0 + CA)), which
-    // it has itself just read, so no other warp's pending read is
-    // overwritten.  K-step ks (16 tokens) of the product reads 8 packed
-    // columns.
-    auto pk_col = [](int ks) -> uint32_t { return (uint32_t)(CA * ((16 * ks) / CA) + ((16 * ks) % CA) / 2); };
-    // this lane's alpha columns -> bf16 pairs (masked to columns <= row),
+    // Packed bf16 operands in alpha: each 32-column group [c0, c0 + 32) of
+    // alpha (A, or W and on a first chunk also W_lo) is packed in place, its
+    // pairs into [c0, c0 + 16) and the lo parts into [c0 + 16, c0 + 32), by the
+    // alpha warp that has itself just read the group, so no other warp's
+    // pending read is overwritten.  K-step ks (16 tokens) of the product
+    // reads 8 packed columns.
+    auto pk_col = [](int ks) -> uint32_t { return (uint32_t)(32 * ((16 * ks) / 32) + ((16 * ks) % 32) / 2); };
+    // this alpha warp's groups -> bf16 pairs (masked to columns <= row),
     // optionally with the lo parts, written back packed
     auto pack_alpha = [&](bool split) {
-        uint32_t r[CA];
-        tmem_ld32(tAl_ + lane_off + ca0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        if (CA == 64) tmem_ld32(tAl_ + lane_off + ca0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[CA == 64 ? 32 : 0]));
-        tmem_ld_wait();
-        uint32_t hi[CA / 2], lo[CA / 2];
 #pragma unroll
-        for (int j = 0; j < CA / 2; ++j) {
-            float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
-            if (ca0 + 2 * j > row) x0 = 0.f;
-            if (ca0 + 2 * j + 1 > row) x1 = 0.f;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-            hi[j] = *reinterpret_cast<const uint32_t*>(&h);
-            if (split) lo[j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
-        }
-        if (CA == 64) {
-            tmem_st32(tAl_ + lane_off + (uint32_t)ca0, *reinterpret_cast<uint32_t(*)[32]>(&hi[0]));
-            if (split) tmem_st32(tAl_ + lane_off + (uint32_t)(ca0 + CA / 2), *reinterpret_cast<uint32_t(*)[32]>(&lo[0]));
-        } else {
-            tmem_st16(tAl_ + lane_off + (uint32_t)ca0, hi);
-            if (split) tmem_st16(tAl_ + lane_off + (uint32_t)(ca0 + CA / 2), lo);
+        for (int g = 0; g < AG; ++g) {
+            const int c0 = acol(g);
+            uint32_t r[32];
+            tmem_ld32(tAl_ + lane_off + c0, r);
+            tmem_ld_wait();
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+                if (c0 + 2 * j > row) x0 = 0.f;
+                if (c0 + 2 * j + 1 > row) x1 = 0.f;
+                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+                if (split) lo[j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
+            }
+            tmem_st16(tAl_ + lane_off + (uint32_t)c0, hi);
+            if (split) tmem_st16(tAl_ + lane_off + (uint32_t)(c0 + 16), lo);
         }
         tmem_st_wait();
     };
@@ -226,7 +241,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         issue_load(LV, &mV, tV, c_begin);
         if (nchunks > 1) issue_load(LQ1, &mQ, tQ1, c_begin + 1);
     }
-    if (state_rows && nchunks > 0) {
+    if (drainer && quarter < D / 32 && nchunks > 0) {  // every drain warp holding rows < D
         // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
         // 32 x 32 fp32 box by bulk tensor loads (mR maps the records as
         // (3D + 2) rows of D floats) into a private staging area in the X / O
@@ -315,7 +330,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + (uint32_t)(CA / 2), tV.mnmaj(ks), iKM, 1);
+                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tV.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CO));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
@@ -339,86 +354,94 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         }
     } else if (drainer) {
         // ========================== drain warps ==========================
-        // This warp's O staging box (32 rows x 32 fp32 columns, 4 KB): at
-        // D = 128 the warps of column parts 0, 1 stage in sX (which the next
-        // X drain rewrites: it waits until every such box has been read out)
-        // and parts 2, 3 in sO; at D = 64 every box is in sO, where only this
-        // warp's own next box goes.
-        const bool box_in_x = D == 128 && part < 2;
-        const uint32_t wbox = (uint32_t)(part & 1) * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
-        const uint32_t scratch = (box_in_x ? tX.base : tO.base) + wbox;
+        // A beta warp's O staging box (32 rows x 32 fp32 columns, 4 KB) is its
+        // own region of sO (rows 32 quarter.., block bw); its O groups pass
+        // through it one after the other, each once the previous one has
+        // been read out by its bulk store.  (On a head's first chunk the X
+        // drain puts this warp's X_lo rows in the same region, before any O.)
+        const uint32_t box = tO.base + (uint32_t)(bw & 1) * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
+        int o_row0 = 0;  // first token of this warp's O rows in the current chunk
+        auto stage_o = [&](const uint32_t (&r)[32], int g) {
+            if (lane == 0) tma_store_wait_read();  // the box's previous content has left
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(box + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1],
+                             r[4 * q + 2], r[4 * q + 3]);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&mO, box, bcol(g), o_row0, head);
+                tma_store_commit();
+            }
+        };
         for (int it = 0; it < nchunks; ++it) {
             const uint32_t ph = it & 1;
             const int c = c_begin + it;
             const bool has_next = it + 1 < nchunks;
             const bool first = c == 0;
-            // A packed in place (masked)
-            if (!wait_bar(CA_, ph)) break;
-            tc_fence_after();
-            pack_alpha(false);
-            drained(DA);
-            // P0 of this chunk -> the S0 / P0 tile, once Q S0 has read S0 (a
-            // head's first chunk has P0 = 0 and skips Q P0)
-            if (!wait_bar(CQS, ph)) break;
-            tc_fence_after();
-            if (state_rows) {
-                if (!first) drainD(tP_, tSP);
-                drained(DP);
+            static_assert(BG <= 2, "a beta warp holds at most one O group while it drains S");
+            if (alpha_w) {
+                // A packed in place (masked)
+                if (!wait_bar(CA_, ph)) break;
+                tc_fence_after();
+                pack_alpha(false);
+                drained(DA);
             }
-            // X -> sX (bf16); on a head's first chunk split into hi (sX) and
-            // lo (sO).  At D = 128 the O boxes staged in sX must have left it.
-            if (!wait_bar(CX, ph)) break;
-            tc_fence_after();
-            if (D == 128) {
-                // every drain warp's previous O box has left sX (an mbarrier
-                // with a bounded wait rather than a named barrier, so that a
-                // warp that gave up cannot strand the others)
-                if (box_in_x && lane == 0) tma_store_wait_read();
-                drained(XB);
-                if (!wait_bar(XB, ph)) break;
+            if (beta_w) {
+                // P0 of this chunk -> the S0 / P0 tile, once Q S0 has read S0 (a
+                // head's first chunk has P0 = 0 and skips Q P0)
+                if (!wait_bar(CQS, ph)) break;
+                tc_fence_after();
+                if (state_rows) {
+                    if (!first) drainD(tP_, tSP);
+                    drained(DP);
+                }
+                // X -> sX (bf16); on a head's first chunk split into hi (sX) and
+                // lo (sO)
+                if (!wait_bar(CX, ph)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int g = 0; g < BG; ++g) {
+                    uint32_t x[32];
+                    tmem_ld32(tBe_ + lane_off + bcol(g), x);
+                    tmem_ld_wait();
+                    if (first) put_row32_split2(tX, tO, row, bcol(g), x, false);
+                    else put_row32(tX, row, bcol(g), x, false);
+                }
+                drained(DX);
             }
-            {
-                uint32_t x[32];
-                tmem_ld32(tBe_ + lane_off + cD, x);
-                tmem_ld_wait();
-                if (first) put_row32_split2(tX, tO, row, cD, x, false);
-                else put_row32(tX, row, cD, x, false);
+            if (alpha_w) {
+                // W packed in place (masked; hi and lo on a head's first chunk)
+                if (!wait_bar(CW, ph)) break;
+                tc_fence_after();
+                pack_alpha(first);
+                drained(DW);
             }
-            drained(DX);
-            // W packed in place (masked; hi and lo on a head's first chunk)
-            if (!wait_bar(CW, ph)) break;
-            tc_fence_after();
-            pack_alpha(first);
-            drained(DW);
-            // O: out of beta into registers (beta then free), the next chunk's
-            // S0 into its tile (Q P0 has read P0), then O leaves by a bulk
-            // tensor store from this warp's staging box (X was last read by
-            // X^T V and X_lo by W, both complete once O is)
-            if (!wait_bar(CO, ph)) break;
-            tc_fence_after();
-            {
+            if (beta_w) {
+                // O: the first group through the staging box, the last one into
+                // registers, then beta is free; the next chunk's S0 into its
+                // tile (Q P0 has read P0); then the last group through the box
+                // (X_lo, in the box region on a head's first chunk, was last
+                // read by W, complete once O is)
+                if (!wait_bar(CO, ph)) break;
+                tc_fence_after();
+                o_row0 = c * kL + quarter * 32;
                 uint32_t r[32];
-                tmem_ld32(tBe_ + lane_off + cD, r);
+                tmem_ld32(tBe_ + lane_off + bcol(0), r);
                 tmem_ld_wait();
+                stage_o(r, 0);
+#pragma unroll
+                for (int g = 1; g < BG; ++g) {
+                    tmem_ld32(tBe_ + lane_off + bcol(g), r);  // BG <= 2: the last group
+                    tmem_ld_wait();
+                }
                 drained(DO);
                 if (state_rows && has_next) {
                     drainD(tS_, tSP);
                     drained(DS);
                 }
-                if (!box_in_x) {  // the previous box in sO has left it
-                    if (lane == 0) tma_store_wait_read();
-                    __syncwarp();
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4), r[4 * q],
-                                 r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&mO, scratch, cD, c * kL + quarter * 32, head);
-                    tma_store_commit();
-                }
+                if (BG > 1) stage_o(r, BG - 1);
             }
         }
         if (lane == 0) tma_store_wait_all();
