@@ -184,9 +184,16 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
     };
-    // a drain warp announces that its share of a region is done
+    // a drain warp announces that its share of a region is done (after
+    // shared-memory writes the async proxy will read: with a proxy fence)
     auto drained = [&](int b) {
         fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
+    };
+    // ... after tensor-memory writes only (the packs of alpha)
+    auto packed = [&](int b) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
@@ -386,7 +393,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (!wait_bar(CA_, ph)) break;
                 tc_fence_after();
                 pack_alpha(false);
-                drained(DA);
+                packed(DA);
             }
             if (beta_w) {
                 // P0 of this chunk -> the S0 / P0 tile, once Q S0 has read S0 (a
@@ -416,7 +423,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (!wait_bar(CW, ph)) break;
                 tc_fence_after();
                 pack_alpha(first);
-                drained(DW);
+                packed(DW);
             }
             if (beta_w) {
                 // O: the first group through the staging box, the last one into
