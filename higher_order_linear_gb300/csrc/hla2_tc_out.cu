@@ -218,6 +218,29 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     // this alpha warp's groups -> bf16 pairs (masked to columns <= row),
     // optionally with the lo parts, written back packed
     auto pack_alpha = [&](bool split) {
+        if (!split && AG == 2) {
+            // both groups' loads in flight before the one wait (the common case)
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tAl_ + lane_off + acol(0), r0);
+            tmem_ld32(tAl_ + lane_off + acol(1), r1);
+            tmem_ld_wait();
+            auto pack16 = [&](const uint32_t (&r)[32], int c0) {
+                uint32_t hi[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+                    if (c0 + 2 * j > row) x0 = 0.f;
+                    if (c0 + 2 * j + 1 > row) x1 = 0.f;
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                    hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                tmem_st16(tAl_ + lane_off + (uint32_t)c0, hi);
+            };
+            pack16(r0, acol(0));
+            pack16(r1, acol(1));
+            tmem_st_wait();
+            return;
+        }
 #pragma unroll
         for (int g = 0; g < AG; ++g) {
             const int c0 = acol(g);
