@@ -98,8 +98,13 @@ struct Layout {
 // each drain thread keeps a running sum of the X row it drains (fp32, before
 // rounding); one transposing butterfly at the end sums a warp's rows and the
 // four lane quarters are added in a fixed order.
+// Threads: the drain warps, the issuer and, in the summary walk, a load warp
+// (and with XP the column-sum warp).
+template <int MODE, bool XP>
+constexpr int walk_threads() { return kThreadsTC + (MODE == 0 ? 32 : 0) + (XP ? 32 : 0); }
+
 template <int D, int MODE, bool NORM, bool XP>
-__global__ void __launch_bounds__(XP ? kThreadsTC + 32 : kThreadsTC, 1)
+__global__ void __launch_bounds__(walk_threads<MODE, XP>(), 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
                const __grid_constant__ CUtensorMap mR, TCParams p) {
@@ -117,7 +122,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
-    const bool msum = XP && warp == kDrainWarps + 1;  // XP: the Q column-sum warp
+    // summary walk: a load warp issues every tile load as soon as its buffer
+    // is free, so that a load never waits behind the issuer's MMA waits
+    const bool producer = MODE == 0 && warp == kDrainWarps + 1;
+    const bool msum = XP && warp == kDrainWarps + 2;  // XP: the Q column-sum warp
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;  // TMEM lane / tile row owned by a drain thread
@@ -126,7 +134,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
+    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);  // drain warp holding rows < D
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
@@ -263,7 +271,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     // The first chunk's tiles start moving now, while the drain warps load the
     // segment prefix below (the barriers were initialised before the first
     // __syncthreads, so the issuer may use them).
-    if (issuer && lane == 0 && nchunks > 0) {
+    if ((MODE == 0 ? producer : issuer) && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -336,7 +344,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
                 // the tiles ahead<MODE>() chunks ahead start moving into L2 now
-                if (ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
+                if (MODE == 1 && ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
                 // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
                 const bool qodd = MODE == 0 && (it & 1);
                 const Tile& tQc = qodd ? tQ2 : tQ;
@@ -454,11 +462,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                     mma_commit(bar(CA));
                     if (it > 0) {
-                        // this chunk's V: the previous chunk's X^T V was V's last read
-                        if (!wait_bar(CP, pph)) break;
-                        issue_load(LV, &mV, tV, c);
-                    }
-                    if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
                         tc_fence_after();
                     }
@@ -488,10 +491,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         for (int ks = 0; ks < kL / 16; ++ks)
                             mma_bf16(tDen_, tQc.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CQ));
-                    if (has_next) {
-                        if (!wait_bar(CX2, ph)) break;
-                        issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
-                    }
                     if (!wait_bar(DX, ph)) break;  // sX = X
                     tc_fence_after();
                     // P += X^T V
@@ -505,16 +504,39 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
                     }
                     mma_commit(bar(CP));
-                    if (it + 2 < nchunks) {
-                        if (!wait_bar(CQ, ph)) break;
-                        if (XP && !wait_bar(qodd ? DQ2 : DQ, qph)) break;  // the column-sum warp has read this Q
-                        issue_load(qodd ? LQ2 : LQ, &mQ, tQc, c + 2);  // this buffer's next chunk
-                    }
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        if (MODE == 1 && lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+    } else if (producer) {
+        // ====================== loads (summary walk) ======================
+        // V of chunk c once the previous chunk's X^T V (V's last reader)
+        // completed, K of chunk c + 1 once A K completed, Q of chunk c + 2
+        // into its buffer once Q^T V completed (and, with XP, the column-sum
+        // warp has read it); the tiles one chunk ahead move into L2 early
+        if (lane == 0) {
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1, pph = (it + 1) & 1;
+                if (ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
+                if (it > 0) {
+                    if (!wait_bar(CP, pph)) break;
+                    issue_load(LV, &mV, tV, c);
+                }
+                if (it + 1 < nchunks) {
+                    if (!wait_bar(CX2, ph)) break;
+                    issue_load(LK, &mK, tK, c + 1);
+                }
+                if (it + 2 < nchunks) {
+                    const bool qodd = it & 1;
+                    if (!wait_bar(CQ, ph)) break;
+                    if (XP && !wait_bar(qodd ? DQ2 : DQ, (uint32_t)((it >> 1) & 1))) break;
+                    issue_load(qodd ? LQ2 : LQ, &mQ, qodd ? tQ2 : tQ, c + 2);
+                }
+            }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
     } else if (msum) {
         // ================ Q column sums (XP summary walk) ================
         // lane l: bf16 pairs l + 32 g of every row (columns 2l + 64g, + 1);
@@ -961,7 +983,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, XP ? kThreadsTC + 32 : kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, walk_threads<MODE, XP>(), smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
