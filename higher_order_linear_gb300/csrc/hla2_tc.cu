@@ -98,10 +98,10 @@ struct Layout {
 // each drain thread keeps a running sum of the X row it drains (fp32, before
 // rounding); one transposing butterfly at the end sums a warp's rows and the
 // four lane quarters are added in a fixed order.
-// Threads: the drain warps, the issuer and, in the summary walk, a load warp
-// (and with XP the column-sum warp).
+// Threads: the drain warps, the issuer, a load warp and, with XP, the
+// column-sum warp.
 template <int MODE, bool XP>
-constexpr int walk_threads() { return kThreadsTC + (MODE == 0 ? 32 : 0) + (XP ? 32 : 0); }
+constexpr int walk_threads() { return kThreadsTC + 32 + (XP ? 32 : 0); }
 
 template <int D, int MODE, bool NORM, bool XP>
 __global__ void __launch_bounds__(walk_threads<MODE, XP>(), 1)
@@ -122,9 +122,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
-    // summary walk: a load warp issues every tile load as soon as its buffer
-    // is free, so that a load never waits behind the issuer's MMA waits
-    const bool producer = MODE == 0 && warp == kDrainWarps + 1;
+    // a load warp issues every tile load as soon as its buffer is free, so
+    // that neither a load nor an MMA waits behind the other's waits
+    const bool producer = warp == kDrainWarps + 1;
     const bool msum = XP && warp == kDrainWarps + 2;  // XP: the Q column-sum warp
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
@@ -271,7 +271,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     // The first chunk's tiles start moving now, while the drain warps load the
     // segment prefix below (the barriers were initialised before the first
     // __syncthreads, so the issuer may use them).
-    if ((MODE == 0 ? producer : issuer) && lane == 0 && nchunks > 0) {
+    if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -343,8 +343,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                // the tiles ahead<MODE>() chunks ahead start moving into L2 now
-                if (MODE == 1 && ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
                 // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
                 const bool qodd = MODE == 0 && (it & 1);
                 const Tile& tQc = qodd ? tQ2 : tQ;
@@ -356,13 +354,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     // A = Q K^T
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                     mma_commit(bar(CA));
-                    if (it > 0) {
-                        // this chunk's V: the previous chunk's X^T V was V's last read (the
-                        // load waits here, behind A, rather than holding up A at the end of
-                        // the previous chunk)
-                        if (!wait_bar(CP, pph)) break;
-                        issue_load(LV, &mV, tV, c);
-                    }
                     if (it > 0) {
                         if (!wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
                         tc_fence_after();
@@ -404,10 +395,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                         mma_commit(bar(CX2));
                     }
-                    if (has_next) {
-                        if (!wait_bar(CX2, ph)) break;
-                        issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
-                    }
                     if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
                     tc_fence_after();
                     if (it > 0) {
@@ -424,12 +411,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     }
                     mma_commit(bar(CQ));
                     if (!wait_bar(LV, ph)) break;
-                    if (has_next) {
-                        // Q was last read by Q P0: the next chunk's Q starts moving now
-                        // (its first product waits on this load)
-                        if (!wait_bar(CQ, ph)) break;
-                        issue_load(LQ, &mQ, tQ, c + 1);
-                    }
                     tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
                     if (NORM || c == 0)  // W_lo V: every chunk when normalised, else the head's first
@@ -508,13 +489,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (MODE == 1 && lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
     } else if (producer) {
-        // ====================== loads (summary walk) ======================
+        // ============================ loads ============================
         // V of chunk c once the previous chunk's X^T V (V's last reader)
-        // completed, K of chunk c + 1 once A K completed, Q of chunk c + 2
-        // into its buffer once Q^T V completed (and, with XP, the column-sum
-        // warp has read it); the tiles one chunk ahead move into L2 early
+        // completed, K of chunk c + 1 once A K completed; in the summary walk
+        // Q of chunk c + 2 into its buffer once Q^T V completed (and, with XP,
+        // the column-sum warp has read it), in the output walk Q of chunk
+        // c + 1 once Q P0 completed; tiles ahead<MODE>() chunks ahead move
+        // into L2 early
         if (lane == 0) {
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
@@ -528,7 +510,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (!wait_bar(CX2, ph)) break;
                     issue_load(LK, &mK, tK, c + 1);
                 }
-                if (it + 2 < nchunks) {
+                if (MODE == 1 && it + 1 < nchunks) {
+                    if (!wait_bar(CQ, ph)) break;
+                    issue_load(LQ, &mQ, tQ, c + 1);
+                }
+                if (MODE == 0 && it + 2 < nchunks) {
                     const bool qodd = it & 1;
                     if (!wait_bar(CQ, ph)) break;
                     if (XP && !wait_bar(qodd ? DQ2 : DQ, (uint32_t)((it >> 1) & 1))) break;
