@@ -63,7 +63,7 @@ struct ALayout {
 };
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC + 32, 1)
 ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
                     const __grid_constant__ CUtensorMap mR, AParams p) {
@@ -80,6 +80,9 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    // a load warp issues every tile load as soon as its buffer is free, so
+    // that the MMA issuer never blocks on a reload
+    const bool producer = warp == kDrainWarps + 1;
     const int quarter = warp & 3;
     const int half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
@@ -88,7 +91,7 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
@@ -196,8 +199,8 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     const int nchunks = c_end - c_begin;
     // The first chunk's tiles start moving now, while the drain warps load the
     // segment prefix below (the barriers were initialised before the first
-    // __syncthreads, so the issuer may use them).
-    if (issuer && lane == 0 && nchunks > 0) {
+    // __syncthreads, so the load warp may use them).
+    if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -258,7 +261,6 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
                 const bool has_next = it + 1 < nchunks;
-                if (kAhead > 0 && it + kAhead < nchunks) prefetch(c + kAhead);
                 if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
                 if (MODE == 1) {
                     const bool first = c == 0;  // P0 = E0 = 0; A and Y split into hi + lo
@@ -290,13 +292,8 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     if (!first)
                         for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tE.mnmaj(ks), iKM, ks > 0);
                     mma_commit(bar(CQ));
-                    if (has_next) {
-                        if (!wait_bar(CQ, ph)) break;
-                        issue_load(LQ, &mQ, tQ, c + 1);
-                    }
                     if (!wait_bar(DY, ph)) break;  // sY = Y (and Y_lo on the first chunk); TMEM Y read
                     tc_fence_after();
-                    if (has_next) issue_load(LV, &mV, tV, c + 1);  // V was last read by A V (CY)
                     // E += K^T Y first (K's last read), then O += A Y
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, 1);
                     if (first)
@@ -309,10 +306,6 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                         for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tYl.mnmaj(ks), iKM, 1);
                     }
                     mma_commit(bar(CO));
-                    if (has_next) {
-                        if (!wait_bar(CE, ph)) break;
-                        issue_load(LK, &mK, tK, c + 1);  // K was last read by K^T Y
-                    }
                 } else {
                     const uint32_t acc0 = it > 0 ? 1u : 0u;  // segment-local sums start at zero
                     tc_fence_after();
@@ -338,23 +331,36 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     mma_commit(bar(CY));
                     if (!wait_bar(DY, ph)) break;  // sY = Y; TMEM A read (Q and V no longer read)
                     tc_fence_after();
-                    if (has_next) {
-                        issue_load(LQ, &mQ, tQ, c + 1);
-                        issue_load(LV, &mV, tV, c + 1);
-                    }
                     // E += K^T Y
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16(tE_, tK.mnmaj(ks), tY.mnmaj(ks), iMM, (acc0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(CE));
-                    if (has_next) {
-                        if (!wait_bar(CE, ph)) break;
-                        issue_load(LK, &mK, tK, c + 1);  // K was last read by K^T Y
-                    }
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+    } else if (producer) {
+        // ============================ loads ============================
+        // the next chunk's tiles once their last reader completed: V after
+        // A V (CY; in the summary walk also Q, whose last readers M and Y
+        // precede it), Q after Q E0 (CQ, output walk), K after K^T Y (CE)
+        if (lane == 0) {
+            for (int it = 0; it + 1 < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1;
+                if (kAhead > 0 && it + kAhead < nchunks) prefetch(c + kAhead);
+                if (!wait_bar(CY, ph)) break;
+                issue_load(LV, &mV, tV, c + 1);
+                if (MODE == 0) issue_load(LQ, &mQ, tQ, c + 1);
+                if (MODE == 1) {
+                    if (!wait_bar(CQ, ph)) break;
+                    issue_load(LQ, &mQ, tQ, c + 1);
+                }
+                if (!wait_bar(CE, ph)) break;
+                issue_load(LK, &mK, tK, c + 1);
+            }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
     } else {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {
@@ -485,7 +491,7 @@ cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
