@@ -105,7 +105,7 @@ struct DOutLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC + 32, 1)
 decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
                     const __grid_constant__ CUtensorMap mR, DParams p) {
@@ -119,6 +119,7 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    const bool producer = warp == kDrainWarps + 1;  // issues every tile load
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
     int head, seg;
@@ -126,7 +127,7 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
     const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
     const float lg = p.lg;
 
@@ -212,7 +213,7 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
         tmem_st_wait();
     };
 
-    if (issuer && lane == 0 && nchunks > 0) {
+    if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -302,8 +303,6 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     tc_fence_after();
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                     mma_commit(bar(CS));
-                    if (!wait_bar(CS, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);  // K was last read by the S update
                 }
                 if (!wait_bar(DW, ph)) break;              // sA = W~_hi, TMEM X' columns = W~_lo; TMEM A read
                 if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P0; TMEM P decayed
@@ -321,15 +320,26 @@ decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                     // P += sX^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                     mma_commit(bar(CP));
-                    if (!wait_bar(CO, ph)) break;
-                    issue_load(LQ, &mQ, tQ, c + 1);  // Q was last read by Q P0
-                    if (!wait_bar(CP, ph)) break;
-                    issue_load(LV, &mV, tV, c + 1);  // V was last read by the P update
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+    } else if (producer) {
+        // the next chunk's tiles once their last reader completed: K after the
+        // S update, Q after O (Q P0), V after the P update
+        if (lane == 0) {
+            for (int it = 0; it + 1 < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1;
+                if (!wait_bar(CS, ph)) break;
+                issue_load(LK, &mK, tK, c + 1);
+                if (!wait_bar(CO, ph)) break;
+                issue_load(LQ, &mQ, tQ, c + 1);
+                if (!wait_bar(CP, ph)) break;
+                issue_load(LV, &mV, tV, c + 1);
+            }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
     } else {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {
@@ -450,7 +460,7 @@ struct DSumLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC + 32, 1)
 decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mR, DParams p) {
     using LY = DSumLayout<D>;
@@ -463,6 +473,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    const bool producer = warp == kDrainWarps + 1;  // issues every tile load
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
     int head, seg;
@@ -470,7 +481,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
     const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
     const float lg = p.lg;
     const int seg_end_tok = min(p.T, c_end * kL);
@@ -544,12 +555,14 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);
 
+    if (producer && lane == 0 && nchunks > 0) {
+        issue_load(LQ, &mQ, tQa, c_begin);
+        issue_load(LK, &mK, tK, c_begin);
+        issue_load(LV, &mV, tV, c_begin);
+        if (nchunks > 1) issue_load(LQ2, &mQ, tQb, c_begin + 1);
+    }
     if (issuer) {
         if (lane == 0 && nchunks > 0) {
-            issue_load(LQ, &mQ, tQa, c_begin);
-            issue_load(LK, &mK, tK, c_begin);
-            issue_load(LV, &mV, tV, c_begin);
-            if (nchunks > 1) issue_load(LQ2, &mQ, tQb, c_begin + 1);
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
@@ -577,10 +590,6 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CS));
-                if (has_next) {
-                    if (!wait_bar(CS, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);  // K was last read by the S update
-                }
                 // C += Q'^T V (Q' = diag(F b) Q, scaled in place by the drains)
                 if (!wait_bar(DQ, ph) || !wait_bar(LV, ph)) break;
                 tc_fence_after();
@@ -593,19 +602,29 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CP));
-                if (it + 2 < nchunks) {
-                    if (!wait_bar(CC, ph)) break;
-                    issue_load(qodd ? LQ2 : LQ, &mQ, tQ, c + 2);  // this buffer's next chunk
-                }
-                if (has_next) {
-                    if (!wait_bar(CP, ph)) break;
-                    issue_load(LV, &mV, tV, c + 1);
-                }
             }
             // FIN completes once every product has: the records can be read out
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+    } else if (producer) {
+        // the next tiles once their last reader completed: K after the S
+        // update, the Q after next into this chunk's buffer after C (Q' read),
+        // V after the P update
+        if (lane == 0) {
+            for (int it = 0; it + 1 < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1;
+                if (!wait_bar(CS, ph)) break;
+                issue_load(LK, &mK, tK, c + 1);
+                if (it + 2 < nchunks) {
+                    if (!wait_bar(CC, ph)) break;
+                    issue_load((it & 1) ? LQ2 : LQ, &mQ, (it & 1) ? tQb : tQa, c + 2);
+                }
+                if (!wait_bar(CP, ph)) break;
+                issue_load(LV, &mV, tV, c + 1);
+            }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
     } else if (nchunks > 0) {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {
@@ -706,14 +725,14 @@ cudaError_t launch_d(int mode, const void* Q, const void* K, const void* V, floa
         auto kern = decay_tc_sum_kernel<D>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mr, prm);
+        kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mr, prm);
     } else {
         if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
         const size_t smem = DOutLayout<D>::kBytes + 1024;
         auto kern = decay_tc_out_kernel<D>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+        kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mo, mr, prm);
     }
     note_launches(1);
     return cudaGetLastError();
