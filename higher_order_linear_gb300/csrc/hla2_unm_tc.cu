@@ -191,7 +191,7 @@ struct UOutLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC + 32, 1)
 unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
                   const __grid_constant__ CUtensorMap mR, UParams p) {
@@ -205,6 +205,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issuer = warp == kDrainWarps;
+    const bool producer = warp == kDrainWarps + 1;  // issues every tile load
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;
     int head, seg;
@@ -212,7 +213,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
     const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool state_rows = !issuer && ((D == 128) || quarter < D / 32);
+    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
@@ -305,7 +306,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     };
 
     // the first chunk's tiles start moving while the drain warps load the prefix
-    if (issuer && lane == 0 && nchunks > 0) {
+    if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
@@ -381,10 +382,6 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CX2));
-                if (has_next) {
-                    if (!wait_bar(CX2, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);  // K was last read by A K
-                }
                 if (!wait_bar(DX, ph)) break;  // sX = X (and X_lo); TMEM X read
                 tc_fence_after();
                 // W = X Q^T
@@ -412,14 +409,25 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     // C += Q^T V
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tC_, tQ.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
                     mma_commit(bar(CC));
-                    if (!wait_bar(CC, ph)) break;
-                    issue_load(LQ, &mQ, tQ, c + 1);  // Q and V were last read by Q^T V
-                    issue_load(LV, &mV, tV, c + 1);
                 }
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
-        if (lane == 0 && !loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+    } else if (producer) {
+        // the next chunk's tiles once their last reader completed: K after
+        // A K, Q and V after Q^T V
+        if (lane == 0) {
+            for (int it = 0; it + 1 < nchunks; ++it) {
+                const int c = c_begin + it;
+                const uint32_t ph = it & 1;
+                if (!wait_bar(CX2, ph)) break;
+                issue_load(LK, &mK, tK, c + 1);
+                if (!wait_bar(CC, ph)) break;
+                issue_load(LQ, &mQ, tQ, c + 1);
+                issue_load(LV, &mV, tV, c + 1);
+            }
+            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        }
     } else {
         // ========================== drain warps ==========================
         for (int it = 0; it < nchunks; ++it) {
@@ -529,7 +537,7 @@ cudaError_t launch_u(int mode, const void* Q, const void* K, const void* V, floa
         auto kern = unm_tc_out_kernel<D>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kThreadsTC, smem, s>>>(mq, mk, mv, mo, mr, prm);
+        kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mo, mr, prm);
     }
     note_launches(1);
     return cudaGetLastError();
