@@ -191,10 +191,11 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
 bool tc_chunk_supported(int d, int dv, int L, int dtype, int device);
 cudaError_t launch_tc_chunk(const void* Q, const void* K, const void* V, float* summ, int BH, int T, int d, int L,
                             int* status, cudaStream_t s);
-// The unnormalised HLA output walk pipelined across chunks (hla2_tc_out.cu),
-// d = dv in {64, 128}, bf16: outputs of every segment from its prefix S|.|.|P|.
+// The HLA output walk pipelined across chunks (hla2_tc_out.cu), d = dv in
+// {64, 128} (normalised: d = 64), bf16: outputs of every segment from its
+// prefix S|.|.|P|.|p.
 cudaError_t launch_tc_out(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,
-                          int d, int dv, SegPlan plan, int* status, cudaStream_t s);
+                          int d, int dv, bool normalized, SegPlan plan, int* status, cudaStream_t s);
 // AHLA on tensor cores (hla2_ahla_tc.cu), d = dv in {64, 128}, bf16, unnormalised:
 // mode 0 writes the M|P|.|E|. parts of the segment summaries, mode 1 outputs.
 cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const void* V,

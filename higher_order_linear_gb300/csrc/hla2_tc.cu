@@ -995,13 +995,12 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
                            cudaStream_t s, bool with_p) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
+    // outputs: the walk pipelined across chunks (hla2_tc_out.cu)
+    if (mode == 1) return launch_tc_out(Q, K, V, O, prefix, BH, T, d, dv, normalized != 0, plan, status, s);
     if (normalized) {
         if (d != 64) return cudaErrorInvalidValue;
-        return mode == 0 ? launch_t<64, 0, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s)
-                         : launch_t<64, 1, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+        return launch_t<64, 0, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
     }
-    // unnormalised outputs: the walk pipelined across chunks (hla2_tc_out.cu)
-    if (mode == 1) return launch_tc_out(Q, K, V, O, prefix, BH, T, d, dv, plan, status, s);
     if (with_p) {
         if (d == 128) return launch_t<128, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
         if (d == 64) return launch_t<64, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);

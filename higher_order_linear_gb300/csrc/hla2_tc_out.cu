@@ -31,6 +31,14 @@
 // output can be a single product (t = 0 gives (q.k)^2 v) and roundings do not
 // average out, X and W are split into bf16 hi + lo parts (W = Q X_hi^T +
 // Q X_lo^T, O = W_hi V + W_lo V; W_lo packed next to W_hi in alpha).
+//
+// NORM (ratio-normalised variant, D = 64): o_t = q_t^T P_t / q_t^T p_t with
+// p = S m - h.  Every fp32 value that feeds a product is split into bf16 hi +
+// lo and both parts enter it (A, X, W, S0, P0, p0), which keeps about 16
+// significant bits of every operand; the denominator is Q p0 + W 1 and p
+// grows by X^T 1, N = 16 products against a tile of ones (the extra value
+// column) into their own tensor-memory columns.  X_lo sits in the X tile's
+// second 64-column block.
 #include "hla2_tc_common.cuh"
 
 namespace hla2 {
@@ -42,7 +50,7 @@ struct OutParams {
     int* status;
 };
 
-template <int D>
+template <int D, bool NORM>
 struct OutLayout {
     static constexpr uint32_t kTok = kL * D * 2;  // Q, K, V tiles
     static constexpr uint32_t kSq = kL * kL * 2;  // X tile (and, at D = 128, the first O staging box of each warp)
@@ -51,7 +59,12 @@ struct OutLayout {
     // D = 64; eight 4 KB boxes) and, on a head's first chunk, X_lo (kL x D)
     static constexpr uint32_t kO = kSq;
     static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, X = 4 * kTok, O = X + kSq, SP = O + kO;
-    static constexpr uint32_t kBytes = SP + kSt;
+    // NORM: X_lo in the X tile's second block; lo parts of S0 / P0; the ones
+    // (16 x 128 bf16); p0 hi and lo as row 0 of 16 x D tiles
+    static constexpr uint32_t XL = X + kL * 128u;
+    static constexpr uint32_t SPL = SP + kSt, ONES = SPL + kSt, P0H = ONES + 4096, P0L = P0H + 2048;
+    static constexpr uint32_t kBytes = NORM ? P0L + 2048 : SP + kSt;
+    static_assert(!NORM || D == 64, "the normalised walk's split tiles fit at D = 64");
 };
 
 // Warp roles: the drain warps move results out of tensor memory (warp w
@@ -88,12 +101,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(OutRoles<D>::kThreads, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
               const __grid_constant__ CUtensorMap mR, OutParams p) {
-    using LY = OutLayout<D>;
+    using LY = OutLayout<D, NORM>;
     using RO = OutRoles<D>;
     constexpr int NDW = RO::kDrain, AG = RO::kAG, BG = RO::kBG;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
@@ -126,6 +139,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tX{dsm + LY::X, kL}, tO{dsm + LY::O, kL}, tSP{dsm + LY::SP, D};
+    // NORM tiles (X_lo, S0 / P0 lo parts, ones, p0 hi / lo)
+    const Tile tXL{dsm + LY::XL, kL}, tSPL{dsm + LY::SPL, D}, tOnes{dsm + LY::ONES, 16};
+    const Tile tP0h{dsm + LY::P0H, 16}, tP0l{dsm + LY::P0L, 16};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
@@ -145,6 +161,12 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (NORM && tid < 256) {
+        // the ones (4 KB of bf16 1.0) and zeroed p0 tiles (P0H, P0L)
+        const uint32_t one2 = 0x3F803F80u;
+        st_shared_v4(tOnes.base + (uint32_t)tid * 16u, one2, one2, one2, one2);
+        st_shared_v4(tP0h.base + (uint32_t)tid * 16u, 0u, 0u, 0u, 0u);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -153,6 +175,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const uint32_t tBe_ = tmem + 128;         // beta: Q S0 + A K = X, then O
     const uint32_t tS_ = tmem + 128 + D;      // running S
     const uint32_t tP_ = tmem + 128 + 2 * D;  // running P
+    const uint32_t tPn_ = tmem + 128 + 3 * D;  // NORM: running p (16 columns, column 0 used)
+    const uint32_t tDen_ = tPn_ + 16;          // NORM: the chunk's denominators
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int cD = part * 32;  // this drain warp's columns of the segment prefix (prologue)
     auto acol = [&](int g) { return (aw * AG + g) * 32; };  // alpha group g of this alpha warp
@@ -205,8 +229,19 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             uint32_t r[32];
             tmem_ld32(treg + lane_off + bcol(g), r);
             tmem_ld_wait();
-            put_row32(t, row, bcol(g), r, false);
+            if (NORM) put_row32_split2(t, tSPL, row, bcol(g), r, false);  // t is the S0 / P0 tile
+            else put_row32(t, row, bcol(g), r, false);
         }
+    };
+    // NORM: p0 (one fp32 per state row) as row 0 of the 16 x D operand tiles
+    auto put_p0 = [&](float x) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+        const uint32_t off = (uint32_t)(row & 7) * 2u;
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0h.chunk(0, row >> 6, (row & 63) >> 3) + off),
+                     "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0l.chunk(0, row >> 6, (row & 63) >> 3) + off),
+                     "h"(*reinterpret_cast<const unsigned short*>(&l)) : "memory");
     };
     // Packed bf16 operands in alpha: each 32-column group [c0, c0 + 32) of
     // alpha (A, or W and on a first chunk also W_lo) is packed in place, its
@@ -292,10 +327,19 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             uint32_t r[32];
             box32_read(stage, lane, r);
             tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cD, r);
-            if (m == 0) put_row32(tSP, row, cD, r, false);  // bf16 S0; P0 follows once Q S0 has read it
+            if (m == 0) {  // bf16 S0; P0 follows once Q S0 has read it
+                if (NORM) put_row32_split2(tSP, tSPL, row, cD, r, false);
+                else put_row32(tSP, row, cD, r, false);
+            }
             __syncwarp();  // every lane has read the box before the next load reuses it
         }
         if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
+        if (NORM && part == 0 && quarter < D / 32) {
+            // p0 of the prefix (record slot after P), one value per state row
+            const size_t R = 3 * (size_t)D * D + 2 * (size_t)D;
+            const float p0 = p.prefix[((size_t)head * p.nseg + seg) * R + 3 * (size_t)D * D + D + row];
+            tmem_st1(tPn_ + lane_off, __float_as_uint(p0));
+        }
         tmem_st_wait();
     }
     fence_proxy_async();
@@ -307,6 +351,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);    // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
+    constexpr uint32_t iKK16 = idesc_bf16(128, 16, false, false);  // N = 16 (ones / p0), both K-major
+    constexpr uint32_t iMK16 = idesc_bf16(128, 16, true, false);   // N = 16, A MN-major
 
     if (issuer) {
         // ============================ issuer ============================
@@ -329,8 +375,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     tc_fence_after();
                 }
                 // X = Q S0 (S0 symmetric: its tile read K-major), then S += K^T K
-                if (!first)
+                if (!first) {
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.kmaj(ks), iKK, ks > 0);
+                    if (NORM)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSPL.kmaj(ks), iKK, 1);
+                }
                 mma_commit(bar(CQS));
                 for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                 if (!wait_bar(DA, ph)) break;  // A packed in alpha
@@ -338,29 +387,52 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // X += A K  (A from tensor memory)
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                if (NORM)  // + A_lo K
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tK.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CX));
                 if (!wait_bar(DX, ph)) break;  // sX = X (and sO = X_lo on a head's first chunk); beta free
                 tc_fence_after();
                 // W = Q X^T (+ Q X_lo^T) into alpha (A there was read by A K)
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tX.kmaj(ks), iSq, ks > 0);
-                if (first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), tO.kmaj(ks), iSq, 1);
+                if (first || NORM)
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), (NORM ? tXL : tO).kmaj(ks), iSq, 1);
                 mma_commit(bar(CW));
                 // P += X^T V once P0 of this chunk has left TMEM P
                 if (!wait_bar(LV, ph) || !wait_bar(DP, ph)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                if (NORM) {
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXL.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
+                    // p += X^T 1
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXL.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
+                }
                 mma_commit(bar(CP));
                 if (!wait_bar(DW, ph)) break;  // W packed in alpha (and W_lo on a head's first chunk)
                 tc_fence_after();
                 // O = Q P0 + W V (+ W_lo V)  (W from tensor memory)
-                if (!first)
+                if (!first) {
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.mnmaj(ks), iKM, ks > 0);
+                    if (NORM) {
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSPL.mnmaj(ks), iKM, 1);
+                        // denominator: Q p0 (+ W 1 below)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0h.kmaj(ks), iKK16, ks > 0);
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0l.kmaj(ks), iKK16, 1);
+                    }
+                }
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
-                if (first)
+                if (first || NORM)
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tV.mnmaj(ks), iKM, 1);
+                if (NORM) {
+                    // denominator += W_hi 1 + W_lo 1
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16_tmem_a(tDen_, tAl_ + pk_col(ks), tOnes.kmaj(ks), iKK16, (!first || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < kL / 16; ++ks)
+                        mma_bf16_tmem_a(tDen_, tAl_ + pk_col(ks) + 16u, tOnes.kmaj(ks), iKK16, 1);
+                }
                 mma_commit(bar(CO));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
@@ -415,7 +487,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // A packed in place (masked)
                 if (!wait_bar(CA_, ph)) break;
                 tc_fence_after();
-                pack_alpha(false);
+                pack_alpha(NORM);
                 packed(DA);
             }
             if (beta_w) {
@@ -424,7 +496,14 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (!wait_bar(CQS, ph)) break;
                 tc_fence_after();
                 if (state_rows) {
-                    if (!first) drainD(tP_, tSP);
+                    if (!first) {
+                        drainD(tP_, tSP);
+                        if (NORM && bw == 0) {  // p0 of this chunk -> its operand tiles
+                            const uint32_t pv = tmem_ld1(tPn_ + lane_off);
+                            tmem_ld_wait();
+                            put_p0(__uint_as_float(pv));
+                        }
+                    }
                     drained(DP);
                 }
                 // X -> sX (bf16); on a head's first chunk split into hi (sX) and
@@ -436,7 +515,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     uint32_t x[32];
                     tmem_ld32(tBe_ + lane_off + bcol(g), x);
                     tmem_ld_wait();
-                    if (first) put_row32_split2(tX, tO, row, bcol(g), x, false);
+                    if (NORM) put_row32_split2(tX, tXL, row, bcol(g), x, false);
+                    else if (first) put_row32_split2(tX, tO, row, bcol(g), x, false);
                     else put_row32(tX, row, bcol(g), x, false);
                 }
                 drained(DX);
@@ -445,7 +525,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // W packed in place (masked; hi and lo on a head's first chunk)
                 if (!wait_bar(CW, ph)) break;
                 tc_fence_after();
-                pack_alpha(first);
+                pack_alpha(first || NORM);
                 packed(DW);
             }
             if (beta_w) {
@@ -459,7 +539,16 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 o_row0 = c * kL + quarter * 32;
                 uint32_t r[32];
                 tmem_ld32(tBe_ + lane_off + bcol(0), r);
-                tmem_ld_wait();
+                if (NORM) {
+                    // ratio normalisation: o = num / den (plain IEEE division)
+                    static_assert(!NORM || BG == 1, "one O group per beta warp");
+                    const float den = __uint_as_float(tmem_ld1(tDen_ + lane_off));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) / den);
+                } else {
+                    tmem_ld_wait();
+                }
                 stage_o(r, 0);
 #pragma unroll
                 for (int g = 1; g < BG; ++g) {
@@ -483,7 +572,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-template <int D>
+template <int D, bool NORM>
 cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,
                          SegPlan plan, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mo, mr;
@@ -497,8 +586,8 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
     // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
     if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
     OutParams prm{T, plan.nseg, plan.nchunk, plan.seglen, prefix, status};
-    const size_t smem = OutLayout<D>::kBytes + 1024;
-    auto kern = tc_out_kernel<D>;
+    const size_t smem = OutLayout<D, NORM>::kBytes + 1024;
+    auto kern = tc_out_kernel<D, NORM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
@@ -510,11 +599,13 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
 }  // namespace
 
 cudaError_t launch_tc_out(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,
-                          int d, int dv, SegPlan plan, int* status, cudaStream_t s) {
+                          int d, int dv, bool normalized, SegPlan plan, int* status, cudaStream_t s) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
-    if (d == 128) return launch_out_t<128>(Q, K, V, O, prefix, BH, T, plan, status, s);
-    if (d == 64) return launch_out_t<64>(Q, K, V, O, prefix, BH, T, plan, status, s);
+    if (normalized) return d == 64 ? launch_out_t<64, true>(Q, K, V, O, prefix, BH, T, plan, status, s)
+                                   : cudaErrorInvalidValue;
+    if (d == 128) return launch_out_t<128, false>(Q, K, V, O, prefix, BH, T, plan, status, s);
+    if (d == 64) return launch_out_t<64, false>(Q, K, V, O, prefix, BH, T, plan, status, s);
     return cudaErrorInvalidValue;
 }
 
