@@ -35,10 +35,12 @@
 // NORM (ratio-normalised variant, D = 64): o_t = q_t^T P_t / q_t^T p_t with
 // p = S m - h.  Every fp32 value that feeds a product is split into bf16 hi +
 // lo and both parts enter it (A, X, W, S0, P0, p0), which keeps about 16
-// significant bits of every operand; the denominator is Q p0 + W 1 and p
-// grows by X^T 1, N = 16 products against a tile of ones (the extra value
-// column) into their own tensor-memory columns.  X_lo sits in the X tile's
-// second 64-column block.
+// significant bits of every operand.  p and the denominators ride along as
+// one more value column: V is read as [V | 1] and P0 as [P0 | p0] (N = 80
+// products, the extra 64-column block of each operand holding the ones or
+// p0), so P += X^T [V | 1] grows p in P's column D and O = Q [P0 | p0] +
+// W [V | 1] leaves the denominators in O's column D.  X_lo sits in the X
+// tile's second 64-column block.
 #include "hla2_tc_common.cuh"
 
 namespace hla2 {
@@ -58,13 +60,14 @@ struct OutLayout {
     // O staging (the other box of each warp at D = 128, the only one at
     // D = 64; eight 4 KB boxes) and, on a head's first chunk, X_lo (kL x D)
     static constexpr uint32_t kO = kSq;
-    static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, X = 4 * kTok, O = X + kSq, SP = O + kO;
-    // NORM: X_lo in the X tile's second block; lo parts of S0 / P0; the ones
-    // (16 x 128 bf16); p0 hi and lo as row 0 of 16 x D tiles
-    static constexpr uint32_t XL = X + kL * 128u;
-    static constexpr uint32_t SPL = SP + kSt, ONES = SPL + kSt, P0H = ONES + 4096, P0L = P0H + 2048;
-    static constexpr uint32_t kBytes = NORM ? P0L + 2048 : SP + kSt;
-    static_assert(!NORM || D == 64, "the normalised walk's split tiles fit at D = 64");
+    // NORM: the V tile's second block holds the ones ([V | 1]), the S0 / P0
+    // tile's second block p0 ([P0 | p0], column 0), then the same pair for
+    // the lo parts; X_lo in the X tile's second block
+    static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, X = (NORM ? 5 : 4) * kTok;
+    static constexpr uint32_t O = X + kSq, SP = O + kO, XL = X + kL * 128u;
+    static constexpr uint32_t SPL = SP + 2 * kSt;
+    static constexpr uint32_t kBytes = NORM ? SPL + 2 * kSt : SP + kSt;
+    static_assert(!NORM || D == 64, "the normalised walk's extended tiles fit at D = 64");
 };
 
 // Warp roles: the drain warps move results out of tensor memory (warp w
@@ -76,15 +79,18 @@ struct OutLayout {
 // form two groups of eight (two warps per lane quarter): the alpha warps
 // pack A and W, the beta warps drain X, O and the state, so that packing the
 // next chunk's A never waits behind the previous chunk's O stores.  At D = 64
-// every drain warp does both.  Columns go in groups of 32: an alpha warp
-// takes kAG groups of alpha, a beta warp kBG groups of each D-wide region.
-template <int D>
+// every drain warp does both, except in the normalised walk (D = 64, bf16
+// hi + lo packs twice as long), which has four warps per quarter split as at
+// D = 128.  Columns go in groups of 32: an alpha warp takes kAG groups of
+// alpha, a beta warp kBG groups of each D-wide region.
+template <int D, bool NORM>
 struct OutRoles {
-    static constexpr int kParts = D / 32;              // drain warps per lane quarter
+    static constexpr int kParts = NORM ? 4 : D / 32;   // drain warps per lane quarter
     static constexpr int kDrain = 4 * kParts;          // drain warps
-    static constexpr bool kSplit = D == 128;           // alpha and beta warps apart
+    static constexpr bool kSplit = kParts == 4;        // alpha and beta warps apart
     static constexpr int kAPer = kSplit ? kParts / 2 : kParts;  // alpha warps per quarter
     static constexpr int kBPer = kSplit ? kParts / 2 : kParts;  // beta warps per quarter
+    static constexpr int kBeta0 = kParts - kBPer;               // first beta part
     static constexpr int kAG = 4 / kAPer;              // alpha groups per alpha warp
     static constexpr int kBG = (D / 32) / kBPer;       // D-wide groups per beta warp
     static constexpr int kAlpha = 4 * kAPer, kBeta = 4 * kBPer;
@@ -102,12 +108,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 
 template <int D, bool NORM>
-__global__ void __launch_bounds__(OutRoles<D>::kThreads, 1)
+__global__ void __launch_bounds__(OutRoles<D, NORM>::kThreads, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
               const __grid_constant__ CUtensorMap mR, OutParams p) {
     using LY = OutLayout<D, NORM>;
-    using RO = OutRoles<D>;
+    using RO = OutRoles<D, NORM>;
     constexpr int NDW = RO::kDrain, AG = RO::kAG, BG = RO::kBG;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | final wait | drain warp w's prefix boxes
@@ -131,24 +137,24 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int c_begin = seg_chunk_begin(plan, seg);
     const int c_end = seg_chunk_begin(plan, seg + 1);
     const int nchunks = c_end - c_begin;
-    const bool alpha_w = drainer && (!RO::kSplit || part < RO::kAPer);  // packs A and W
-    const bool beta_w = drainer && (!RO::kSplit || part >= RO::kAPer);  // drains X, O and the state
-    const int aw = part, bw = RO::kSplit ? part - RO::kAPer : part;     // index among its kind in a quarter
+    const bool alpha_w = drainer && part < RO::kAPer;      // packs A and W
+    const bool beta_w = drainer && part >= RO::kBeta0;     // drains X, O and the state
+    const int aw = part, bw = part - RO::kBeta0;           // index among its kind in a quarter
     const bool state_rows = beta_w && quarter < D / 32;  // beta warp holding rows < D
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tX{dsm + LY::X, kL}, tO{dsm + LY::O, kL}, tSP{dsm + LY::SP, D};
-    // NORM tiles (X_lo, S0 / P0 lo parts, ones, p0 hi / lo)
-    const Tile tXL{dsm + LY::XL, kL}, tSPL{dsm + LY::SPL, D}, tOnes{dsm + LY::ONES, 16};
-    const Tile tP0h{dsm + LY::P0H, 16}, tP0l{dsm + LY::P0L, 16};
+    // NORM tiles (X_lo, S0 / P0 lo parts)
+    const Tile tXL{dsm + LY::XL, kL}, tSPL{dsm + LY::SPL, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DW) cnt = RO::kAlpha;
+            if (i == DA) cnt = RO::kAlpha;
+            if (i == DW) cnt = NORM ? RO::kDrain : RO::kAlpha;  // NORM: every drain warp packs W
             if (i == DX || i == DO) cnt = RO::kBeta;
             if (i == DS || i == DP) cnt = RO::kState;
             mbar_init(bar(i), cnt);
@@ -161,22 +167,30 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (NORM && tid < 256) {
-        // the ones (4 KB of bf16 1.0) and zeroed p0 tiles (P0H, P0L)
+    if (NORM) {
+        // the ones block of [V | 1] (bf16 1.0) and the zeroed p0 blocks of
+        // [P0 | p0] (hi and lo), 16 bytes per thread and step
         const uint32_t one2 = 0x3F803F80u;
-        st_shared_v4(tOnes.base + (uint32_t)tid * 16u, one2, one2, one2, one2);
-        st_shared_v4(tP0h.base + (uint32_t)tid * 16u, 0u, 0u, 0u, 0u);
+        for (uint32_t i = (uint32_t)tid; i < kL * 8u; i += blockDim.x)
+            st_shared_v4(tV.base + tV.block_bytes() + i * 16u, one2, one2, one2, one2);
+        for (uint32_t i = (uint32_t)tid; i < D * 8u; i += blockDim.x) {
+            st_shared_v4(tSP.base + tSP.block_bytes() + i * 16u, 0u, 0u, 0u, 0u);
+            st_shared_v4(tSPL.base + tSPL.block_bytes() + i * 16u, 0u, 0u, 0u, 0u);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tAl_ = tmem + 0;           // alpha: A, then W (packed bf16 in place; W_lo too on a first chunk)
-    const uint32_t tBe_ = tmem + 128;         // beta: Q S0 + A K = X, then O
-    const uint32_t tS_ = tmem + 128 + D;      // running S
-    const uint32_t tP_ = tmem + 128 + 2 * D;  // running P
-    const uint32_t tPn_ = tmem + 128 + 3 * D;  // NORM: running p (16 columns, column 0 used)
-    const uint32_t tDen_ = tPn_ + 16;          // NORM: the chunk's denominators
+    // NORM: beta and P are D + 16 columns wide (O and P with the extra column)
+    constexpr uint32_t kWide = NORM ? 32u * ((D + 16 + 31) / 32) : D;
+    const uint32_t tAl_ = tmem + 0;                 // alpha: A, then W (packed bf16 in place; W_lo too on a first chunk)
+    const uint32_t tBe_ = tmem + 128;               // beta: Q S0 + A K = X, then O
+    const uint32_t tS_ = tmem + 128 + kWide;        // running S
+    const uint32_t tP_ = tmem + 128 + kWide + D;    // running P
+    const uint32_t tPn_ = tP_ + D;                  // NORM: running p (P's extra column)
+    const uint32_t tDen_ = tBe_ + D;                // NORM: the chunk's denominators (O's extra column)
+    static_assert(128 + 2 * kWide + D <= kTmemCols, "tensor-memory columns");
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int cD = part * 32;  // this drain warp's columns of the segment prefix (prologue)
     auto acol = [&](int g) { return (aw * AG + g) * 32; };  // alpha group g of this alpha warp
@@ -233,14 +247,14 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             else put_row32(t, row, bcol(g), r, false);
         }
     };
-    // NORM: p0 (one fp32 per state row) as row 0 of the 16 x D operand tiles
+    // NORM: p0 (one fp32 per state row d) into column D of [P0 | p0], hi and
+    // lo (row d, first element of the second block)
     auto put_p0 = [&](float x) {
         const __nv_bfloat16 h = __float2bfloat16_rn(x);
         const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
-        const uint32_t off = (uint32_t)(row & 7) * 2u;
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0h.chunk(0, row >> 6, (row & 63) >> 3) + off),
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tSP.chunk(row, 1, 0)),
                      "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0l.chunk(0, row >> 6, (row & 63) >> 3) + off),
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tSPL.chunk(row, 1, 0)),
                      "h"(*reinterpret_cast<const unsigned short*>(&l)) : "memory");
     };
     // Packed bf16 operands in alpha: each 32-column group [c0, c0 + 32) of
@@ -251,8 +265,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     // reads 8 packed columns.
     auto pk_col = [](int ks) -> uint32_t { return (uint32_t)(32 * ((16 * ks) / 32) + ((16 * ks) % 32) / 2); };
     // this alpha warp's groups -> bf16 pairs (masked to columns <= row),
-    // optionally with the lo parts, written back packed
-    auto pack_alpha = [&](bool split) {
+    // optionally with the lo parts, written back packed; `one` packs the
+    // single group `part` instead (NORM's W, which every drain warp packs)
+    auto pack_alpha = [&](bool split, bool one = false) {
         if (!split && AG == 2) {
             // both groups' loads in flight before the one wait (the common case)
             uint32_t r0[32], r1[32];
@@ -278,22 +293,23 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         }
 #pragma unroll
         for (int g = 0; g < AG; ++g) {
-            const int c0 = acol(g);
+            if (one && g > 0) break;
+            const int c0 = one ? part * 32 : acol(g);
             uint32_t r[32];
             tmem_ld32(tAl_ + lane_off + c0, r);
             tmem_ld_wait();
-            uint32_t hi[16], lo[16];
+            uint32_t hl[32];  // the pairs, then (split) the lo parts
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
                 if (c0 + 2 * j > row) x0 = 0.f;
                 if (c0 + 2 * j + 1 > row) x1 = 0.f;
                 const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                hi[j] = *reinterpret_cast<const uint32_t*>(&h);
-                if (split) lo[j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
+                hl[j] = *reinterpret_cast<const uint32_t*>(&h);
+                hl[16 + j] = pack_bf16(x0 - __low2float(h), x1 - __high2float(h));
             }
-            tmem_st16(tAl_ + lane_off + (uint32_t)c0, hi);
-            if (split) tmem_st16(tAl_ + lane_off + (uint32_t)(c0 + 16), lo);
+            if (split) tmem_st32(tAl_ + lane_off + (uint32_t)c0, hl);
+            else tmem_st16(tAl_ + lane_off + (uint32_t)c0, hl);
         }
         tmem_st_wait();
     };
@@ -306,7 +322,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         issue_load(LV, &mV, tV, c_begin);
         if (nchunks > 1) issue_load(LQ1, &mQ, tQ1, c_begin + 1);
     }
-    if (drainer && quarter < D / 32 && nchunks > 0) {  // every drain warp holding rows < D
+    if (drainer && quarter < D / 32 && part < D / 32 && nchunks > 0) {  // rows < D, one box of columns each
         // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
         // 32 x 32 fp32 box by bulk tensor loads (mR maps the records as
         // (3D + 2) rows of D floats) into a private staging area in the X / O
@@ -351,8 +367,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);    // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
-    constexpr uint32_t iKK16 = idesc_bf16(128, 16, false, false);  // N = 16 (ones / p0), both K-major
-    constexpr uint32_t iMK16 = idesc_bf16(128, 16, true, false);   // N = 16, A MN-major
+    constexpr int NE = NORM ? D + 16 : D;                           // NORM: [V | 1], [P0 | p0]
+    constexpr uint32_t iKME = idesc_bf16(128, NE, false, true);     // N = NE, A K-major, B MN-major
+    constexpr uint32_t iMME = idesc_bf16(128, NE, true, true);      // N = NE, both MN-major
 
     if (issuer) {
         // ============================ issuer ============================
@@ -401,38 +418,24 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // P += X^T V once P0 of this chunk has left TMEM P
                 if (!wait_bar(LV, ph) || !wait_bar(DP, ph)) break;
                 tc_fence_after();
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                if (NORM) {
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXL.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                    // p += X^T 1
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXL.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
-                }
+                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMME, 1);
+                if (NORM)  // [P | p] += X_lo^T [V | 1]
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXL.mnmaj(ks), tV.mnmaj(ks), iMME, 1);
                 mma_commit(bar(CP));
                 if (!wait_bar(DW, ph)) break;  // W packed in alpha (and W_lo on a head's first chunk)
                 tc_fence_after();
                 // O = Q P0 + W V (+ W_lo V)  (W from tensor memory)
+                // (NORM: [O | den] = Q [P0 | p0] (hi, lo) + W [V | 1] (hi, lo))
                 if (!first) {
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.mnmaj(ks), iKM, ks > 0);
-                    if (NORM) {
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSPL.mnmaj(ks), iKM, 1);
-                        // denominator: Q p0 (+ W 1 below)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0h.kmaj(ks), iKK16, ks > 0);
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0l.kmaj(ks), iKK16, 1);
-                    }
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.mnmaj(ks), iKME, ks > 0);
+                    if (NORM)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSPL.mnmaj(ks), iKME, 1);
                 }
                 for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
+                    mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKME, (!first || ks > 0) ? 1u : 0u);
                 if (first || NORM)
                     for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tV.mnmaj(ks), iKM, 1);
-                if (NORM) {
-                    // denominator += W_hi 1 + W_lo 1
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16_tmem_a(tDen_, tAl_ + pk_col(ks), tOnes.kmaj(ks), iKK16, (!first || ks > 0) ? 1u : 0u);
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16_tmem_a(tDen_, tAl_ + pk_col(ks) + 16u, tOnes.kmaj(ks), iKK16, 1);
-                }
+                        mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tV.mnmaj(ks), iKME, 1);
                 mma_commit(bar(CO));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
@@ -521,11 +524,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 }
                 drained(DX);
             }
-            if (alpha_w) {
-                // W packed in place (masked; hi and lo on a head's first chunk)
+            if (alpha_w || NORM) {
+                // W packed in place (masked; hi and lo on a head's first chunk
+                // and in the normalised walk, where every drain warp packs one
+                // group)
                 if (!wait_bar(CW, ph)) break;
                 tc_fence_after();
-                pack_alpha(first || NORM);
+                pack_alpha(first || NORM, NORM);
                 packed(DW);
             }
             if (beta_w) {
@@ -539,28 +544,38 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 o_row0 = c * kL + quarter * 32;
                 uint32_t r[32];
                 tmem_ld32(tBe_ + lane_off + bcol(0), r);
-                if (NORM) {
-                    // ratio normalisation: o = num / den (plain IEEE division)
-                    static_assert(!NORM || BG == 1, "one O group per beta warp");
-                    const float den = __uint_as_float(tmem_ld1(tDen_ + lane_off));
+                if constexpr (BG == 1) {
+                    // one group: beta is free once it sits in registers, and the
+                    // next S0 goes out before the group is staged
+                    float den = 1.f;
+                    if (NORM) den = __uint_as_float(tmem_ld1(tDen_ + lane_off));
                     tmem_ld_wait();
+                    drained(DO);
+                    if (state_rows && has_next) {
+                        drainD(tS_, tSP);
+                        drained(DS);
+                    }
+                    if (NORM) {
+                        // ratio normalisation: o = num * (1 / den), the reciprocal
+                        // correctly rounded (within one more rounding of num / den)
+                        const float inv = __frcp_rn(den);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) / den);
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * inv);
+                    }
+                    stage_o(r, 0);
                 } else {
+                    static_assert(NORM == false, "the normalised walk has one O group per beta warp");
                     tmem_ld_wait();
-                }
-                stage_o(r, 0);
-#pragma unroll
-                for (int g = 1; g < BG; ++g) {
-                    tmem_ld32(tBe_ + lane_off + bcol(g), r);  // BG <= 2: the last group
+                    stage_o(r, 0);
+                    tmem_ld32(tBe_ + lane_off + bcol(1), r);  // BG == 2: the last group
                     tmem_ld_wait();
+                    drained(DO);
+                    if (state_rows && has_next) {
+                        drainD(tS_, tSP);
+                        drained(DS);
+                    }
+                    stage_o(r, 1);
                 }
-                drained(DO);
-                if (state_rows && has_next) {
-                    drainD(tS_, tSP);
-                    drained(DS);
-                }
-                if (BG > 1) stage_o(r, BG - 1);
             }
         }
         if (lane == 0) tma_store_wait_all();
@@ -591,7 +606,7 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, OutRoles<D>::kThreads, smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, OutRoles<D, NORM>::kThreads, smem, s>>>(mq, mk, mv, mo, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
