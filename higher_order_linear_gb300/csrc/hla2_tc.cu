@@ -1,25 +1,25 @@
-// hla2_tc.cu -- tensor-core segment walks of masked second-order HLA on
-// GB300 (sm_103a): tcgen05.mma with TMEM accumulators, TMA-staged tiles.
+// hla2_tc.cu -- tensor-core segment summary walk of masked second-order HLA
+// on GB300 (sm_103a): tcgen05.mma with TMEM accumulators, TMA-staged tiles.
+// (The output walk, which restarts every segment from its prefix, is
+// hla2_tc_out.cu.)
 //
 // HLA summary (arXiv 2510.27258): section 1 "Second-order HLA" (o_t =
 // q_t^T (S_t C_t - G_t), the causal A A^T V structure of section 2) and
 // section 4 "Parallel training via associative scans" (chunk-parallel form:
 // segment summaries, exclusive scan, restart from the prefix).
 //
-// One CTA walks one segment of one head in chunks of L = 128 tokens.  With
-// P = S C - G ("P-form"), the state entering a chunk is (S0, P0) and, for the
-// chunk's Q, K, V (128 x d, 128 x d, 128 x dv):
+// One CTA walks one segment of one head in chunks of L = 128 tokens, from a
+// zero state.  With P = S C - G ("P-form"), the state entering a chunk is
+// (S0, P0) and, for the chunk's Q, K, V (128 x d, 128 x d, 128 x dv):
 //   A = tril(Q K^T)                     (i <= t, diagonal kept)
 //   X = Q S0 + A K                      (so that P grows by X^T V)
-//   W = tril(A A^T + (Q S0) Q^T)        (j <= t)
-//   O = Q P0 + W V                      (the chunk's outputs)
-//   P0 += X^T V,   S0 += K^T K
-// Summary mode (from a zero state) also accumulates C = Q^T V and emits the
-// segment's S, C, P.  Every product is a dense 128-row contraction issued as
-// tcgen05.mma kind::f16 (bf16 operands from shared memory, fp32 accumulators
-// in tensor memory).  fp32 results that feed a later product (A, X, W, S0,
-// P0) are rounded to bf16 when written back to shared memory; the running S
-// and P stay fp32 in tensor memory for the whole segment.
+//   P0 += X^T V,   S0 += K^T K,   C += Q^T V
+// and the segment's S, C, P (with m and p when wanted) are its summary.
+// Every product is a dense 128-row contraction issued as tcgen05.mma
+// kind::f16 (bf16 operands from shared memory, fp32 accumulators in tensor
+// memory).  fp32 results that feed a later product (A, X, S0) are rounded to
+// bf16 when written back to shared memory; the running S, C and P stay fp32
+// in tensor memory for the whole segment.
 //
 // Operand layout: every tile lives in shared memory as rows of 128 bytes
 // (64 bf16) in the 128-byte-swizzled pattern TMA writes, split into 64-column
@@ -31,45 +31,36 @@
 namespace hla2 {
 namespace {
 
-// Chunks ahead whose tiles a walk pulls into L2 before their TMA loads, per
-// walk.  On the headline (B1 H16 T65536 d128): the output walk is fastest
-// with none (one, two or four chunks ahead made it 4-8% slower; its loads are
-// issued as early as the single-buffered tiles allow and HBM is busy with the
-// O stores); the summary walk gains 3% with one (two: 0.5%, four: 12% slower).
-template <int MODE>
-constexpr int ahead() { return MODE == 0 ? 1 : 0; }
+// Chunks ahead whose tiles the walk pulls into L2 before their TMA loads: on
+// B1 H16 T65536 d128 one gains 3% (two: 0.5%, four: 12% slower).
+constexpr int kAhead = 1;
 
 // ------------------------------------------------------------- kernel ----
 struct TCParams {
     int T, nseg, nchunk, seglen;
-    float* summ;          // mode 0 output records
-    const float* prefix;  // mode 1 input records
-    float* O;             // mode 1 outputs [BH][T][D]
+    float* summ;  // output records
     int* status;
 };
 
-template <int D, int MODE, bool NORM = false>
+template <int D, bool NORM = false>
 struct Layout {
     // byte offsets of the tiles inside the 1024-aligned dynamic shared memory
     static constexpr uint32_t kTok = kL * D * 2;      // Q, K, V, X tiles
-    static constexpr uint32_t kSq = kL * kL * 2;      // A / W tile
-    static constexpr uint32_t kSt = D * D * 2;        // S0 / P0 tiles
-    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq;
-    static constexpr uint32_t P = X + kTok;                       // mode 1 only
-    static constexpr uint32_t Q2 = X + kTok;                      // mode 0: second Q buffer
-    static constexpr uint32_t S = (MODE == 1) ? P + kSt : Q2 + kTok;
+    static constexpr uint32_t kSq = kL * kL * 2;      // A tile
+    static constexpr uint32_t kSt = D * D * 2;        // S tile
+    // NORM: the V tile's second 64-column block holds ones ([V | 1])
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + (NORM ? 2 : 1) * kTok, X = A + kSq;
+    static constexpr uint32_t Q2 = X + kTok;  // second Q buffer
+    static constexpr uint32_t S = Q2 + kTok;
     static constexpr uint32_t kEnd = S + kSt;
-    // ratio-normalised walks: bf16 lo halves of the split operands, a tile of
-    // ones (16 x 128, the extra value column) and p0 as an operand (16 x D)
+    // ratio-normalised walk: bf16 lo halves of the split operands
     static constexpr uint32_t Alo = kEnd, Xlo = Alo + kSq, Slo = Xlo + kTok;
-    static constexpr uint32_t Plo = Slo + kSt;                    // mode 1 only
-    static constexpr uint32_t Ones = (MODE == 1) ? Plo + kSt : Slo + kSt;
-    static constexpr uint32_t P0h = Ones + 4096, P0l = P0h + 2048;  // mode 1 only
-    static constexpr uint32_t kNormEnd = (MODE == 1) ? P0l + 2048 : Ones + 4096;
+    static constexpr uint32_t kNormEnd = Slo + kSt;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
     static constexpr uint32_t kBytes = (NORM ? kNormEnd : kEnd) + kPad;
+    static_assert(!NORM || D == 64, "the normalised walk's split tiles fit at D = 64");
 };
 
 // Warp roles.  Warps 0..7 drain tensor memory: warp w owns TMEM lane quarter
@@ -81,12 +72,12 @@ struct Layout {
 // drain wrote.  Drains thus overlap the MMAs that do not depend on them.
 //
 // NORM (ratio-normalised variant, D = 64): every fp32 intermediate that
-// feeds a product (A, Q S0, X, W, S0, P0, p0) is split into bf16 hi + lo
-// parts and the product is taken on both parts (hi*hi + hi*lo + lo*hi for
-// A A^T), which keeps about 16 significant bits.  The extra value column of
-// ones (V -> [V | 1]) is a 16-column tile of ones: the denominator is
-// Q p0 + W 1 and p grows by X^T 1 (the summary walk also gathers m = Q^T 1),
-// all N = 16 products into their own tensor-memory columns.
+// feeds a product (A, X, S0) is split into bf16 hi + lo parts and the
+// product is taken on both parts, which keeps about 16 significant bits.
+// The extra value column of ones rides along: V is read as [V | 1] (the V
+// tile's second 64-column block holds ones), so the N = D + 16 products
+// C += Q^T [V | 1] and P += X^T [V | 1] also gather m = sum_t q_t and
+// p = sum_t x_t in column D of C and P.
 //
 // XP (unnormalised summary walk whose final state is wanted): the segment's
 // m = sum_t q_t and p = sum_t x_t are gathered on the CUDA cores.  For m, one
@@ -100,20 +91,17 @@ struct Layout {
 // four lane quarters are added in a fixed order.
 // Threads: the drain warps, the issuer, a load warp and, with XP, the
 // column-sum warp.
-template <int MODE, bool XP>
+template <bool XP>
 constexpr int walk_threads() { return kThreadsTC + 32 + (XP ? 32 : 0); }
 
-template <int D, int MODE, bool NORM, bool XP>
-__global__ void __launch_bounds__(walk_threads<MODE, XP>(), 1)
+template <int D, bool NORM, bool XP>
+__global__ void __launch_bounds__(walk_threads<XP>(), 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
-               const __grid_constant__ CUtensorMap mR, TCParams p) {
-    using LY = Layout<D, MODE, NORM>;
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mR, TCParams p) {
+    using LY = Layout<D, NORM>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    // loads | MMA commits | drains
-    // (PB + w: drain warp w's prefix boxes, output walk)
-    enum { LQ, LK, LV, LQ2, CA, CXS, CW, CX2, CQ, CO, CP, DA, DX, DS, DW, DX2, DO, DP, FIN, PX, DQ, DQ2, PB,
-           NBAR = PB + kDrainWarps };
+    // loads | MMA commits | drains | final wait | XP: p exchange, Q column sums
+    enum { LQ, LK, LV, LQ2, CA, CXS, CX2, CQ, CP, DA, DX, DS, FIN, PX, DQ, DQ2, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -140,19 +128,18 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
-    const Tile tQ2{dsm + LY::Q2, kL};  // summary walk: Q of odd chunks (two Q buffers)
-    const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
-    // normalised walks only
-    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL}, tSl{dsm + LY::Slo, D}, tPl{dsm + LY::Plo, D};
-    const Tile tOnes{dsm + LY::Ones, 16}, tP0h{dsm + LY::P0h, 16}, tP0l{dsm + LY::P0l, 16};
+    const Tile tQ2{dsm + LY::Q2, kL};  // Q of odd chunks (two Q buffers)
+    const Tile tS{dsm + LY::S, D};
+    // normalised walk only
+    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL}, tSl{dsm + LY::Slo, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DW || i == DX2 || i == DO || i == PX) cnt = kDrainWarps;
-            if (i == DS || i == DP) cnt = kStateWarps;
+            if (i == DA || i == DX || i == PX) cnt = kDrainWarps;
+            if (i == DS) cnt = kStateWarps;
             mbar_init(bar(i), cnt);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -163,26 +150,27 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (NORM && tid < 256) {
-        // the ones tile (4 KB of bf16 1.0) and, in the output walk, zeroed p0 tiles
+    if (NORM) {
+        // the ones block of [V | 1] (bf16 1.0), 16 bytes per thread and step
         const uint32_t one2 = 0x3F803F80u;
-        st_shared_v4(tOnes.base + (uint32_t)tid * 16u, one2, one2, one2, one2);
-        if (MODE == 1) st_shared_v4(tP0h.base + (uint32_t)tid * 16u, 0u, 0u, 0u, 0u);  // P0h and P0l
+        for (uint32_t i = (uint32_t)tid; i < kL * 8u; i += blockDim.x)
+            st_shared_v4(tV.base + tV.block_bytes() + i * 16u, one2, one2, one2, one2);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    // tensor-memory regions (column offsets)
-    const uint32_t tA_ = tmem + 0;    // mode 1: A, then W, then O;  mode 0: A, then X
-    const uint32_t tX_ = tmem + 128;  // mode 1: Q S0, then X, then packed bf16 W_lo
-    const uint32_t tS_ = tmem + (MODE == 1 ? 256 : 128);
-    const uint32_t tP_ = tmem + (MODE == 1 ? 256 + D : 128 + D);
-    const uint32_t tC_ = tmem + 128 + 2 * D;  // mode 0 only
-    // normalised walks: p (16 columns, column 0 used) and the denominator
-    // (mode 1) or m (mode 0), after the regions above
-    const uint32_t tPn_ = tmem + (MODE == 1 ? 256 + 2 * D : 128 + 3 * D);
-    const uint32_t tDen_ = tPn_ + 16;  // mode 1: denominator;  mode 0: m
+    // tensor-memory regions (column offsets); NORM: P and C are D + 16
+    // columns wide, P += X^T [V | 1] and C += Q^T [V | 1] leaving p and m in
+    // their column D
+    constexpr uint32_t kWide = NORM ? 32u * ((D + 16 + 31) / 32) : D;
+    const uint32_t tA_ = tmem + 0;  // A, then X
+    const uint32_t tS_ = tmem + 128;
+    const uint32_t tP_ = tS_ + D;
+    const uint32_t tC_ = tP_ + kWide;
+    const uint32_t tPn_ = tP_ + D;  // NORM: p
+    const uint32_t tM_ = tC_ + D;   // NORM: m
+    static_assert(128 + D + 2 * kWide <= kTmemCols, "tensor-memory columns");
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int c128 = half * 64;      // this drain warp's columns in a 128-wide region
     const int cD = half * (D / 2);   // ... and in a D-wide region
@@ -252,77 +240,18 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         put_row32_split2(hi, lo, row, cD, r, false);
         if (D == 128) put_row32_split2(hi, lo, row, cD + 32, r + 32, false);
     };
-    // p0 (one fp32 per state row) as row 0 of the 16 x D operand tiles
-    auto put_p0 = [&](float x) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(x);
-        const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
-        const uint32_t off = (uint32_t)(row & 7) * 2u;
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0h.chunk(0, row >> 6, (row & 63) >> 3) + off),
-                     "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tP0l.chunk(0, row >> 6, (row & 63) >> 3) + off),
-                     "h"(*reinterpret_cast<const unsigned short*>(&l)) : "memory");
-    };
-    // packed W_lo: drain warp h stores the pairs of its W columns [64h, 64h+64)
-    // over the X columns it has itself just drained, so no other warp's
-    // pending read is overwritten.  K-step ks reads 8 packed columns.
-    auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * (D / 2) + 8 * (ks & 3)); };
 
     const int nchunks = c_end - c_begin;
-    // The first chunk's tiles start moving now, while the drain warps load the
-    // segment prefix below (the barriers were initialised before the first
-    // __syncthreads, so the issuer may use them).
+    // The first chunk's tiles start moving now (the barriers were initialised
+    // before the first __syncthreads, so the load warp may use them).
     if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
         issue_load(LK, &mK, tK, c_begin);
         issue_load(LV, &mV, tV, c_begin);
-        if (MODE == 0 && nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
-        for (int a = 1; a < ahead<MODE>() && a < nchunks; ++a) prefetch(c_begin + a);
+        if (nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
+        for (int a = 1; a < kAhead && a < nchunks; ++a) prefetch(c_begin + a);
     }
 
-    // ---- initial state (mode 1): S0, P0 fp32 into TMEM, bf16 into smem ----
-    if (MODE == 1 && state_rows) {
-        const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
-        const float* pre = p.prefix + ((size_t)head * p.nseg + seg) * R;
-        // S0 (record row 0) and P0 (record row 2D + 1) arrive as this warp's
-        // 32 x 32 fp32 boxes by bulk tensor loads (mR maps the records as
-        // (3D + 2) rows of D floats) into a private staging area in the A / X
-        // tiles, which nothing else touches before the first chunk
-        const int rec = head * p.nseg + seg;
-        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
-        LoadLedger<1> boxes(bar(PB + warp));
-#pragma unroll 1
-        for (int m = 0; m < 2; ++m) {
-            if (lane == 0) {
-                boxes.note(0);
-                fence_proxy_async();
-                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
-#pragma unroll
-                for (int g = 0; g < D / 64; ++g)
-                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? 0 : 2 * D + 1) + quarter * 32, rec,
-                                bar(PB + warp));
-            }
-            __syncwarp();
-            if (!wait_bar(PB + warp, (uint32_t)m)) break;
-#pragma unroll
-            for (int g = 0; g < D / 64; ++g) {
-                const int cb = cD + 32 * g;
-                uint32_t r[32];
-                box32_read(stage + (uint32_t)g * 4096u, lane, r);
-                tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cb, r);
-                if (NORM) put_row32_split2(m == 0 ? tS : tP, m == 0 ? tSl : tPl, row, cb, r, false);
-                else put_row32(m == 0 ? tS : tP, row, cb, r, false);
-            }
-            __syncwarp();  // every lane has read the boxes before the next load reuses them
-        }
-        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
-        if (NORM && half == 0) {
-            // p0 = S0 m0 - h0 of the prefix (record slot after P)
-            const float p0 = pre[3 * (size_t)D * D + D + row];
-            tmem_st1(tPn_ + lane_off, __float_as_uint(p0));
-            put_p0(p0);
-        }
-        tmem_st_wait();
-    }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -332,176 +261,75 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     constexpr uint32_t iKK = idesc_bf16(128, D, false, false);     // N = D, both K-major
     constexpr uint32_t iKM = idesc_bf16(128, D, false, true);      // A K-major, B MN-major
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);       // both MN-major
-    constexpr uint32_t iKK16 = idesc_bf16(128, 16, false, false);  // N = 16 (ones / p0), both K-major
-    constexpr uint32_t iMK16 = idesc_bf16(128, 16, true, false);   // N = 16, A MN-major
+    constexpr uint32_t iMME = idesc_bf16(128, NORM ? D + 16 : D, true, true);  // NORM: N = D + 16, [V | 1]
 
     if (issuer) {
         // ============================ issuer ============================
         if (lane == 0 && nchunks > 0) {
             int it = 0;
             for (; it < nchunks; ++it) {
-                const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                const bool has_next = it + 1 < nchunks;
-                // the summary walk alternates two Q buffers: chunk it uses buffer it & 1
-                const bool qodd = MODE == 0 && (it & 1);
+                // two Q buffers: chunk it uses buffer it & 1
+                const bool qodd = it & 1;
                 const Tile& tQc = qodd ? tQ2 : tQ;
-                const uint32_t qph = MODE == 0 ? (uint32_t)((it >> 1) & 1) : ph;
+                const uint32_t qph = (uint32_t)((it >> 1) & 1);
                 if (!wait_bar(qodd ? LQ2 : LQ, qph) || !wait_bar(LK, ph)) break;
-                if (MODE == 1) {
-                    if (it > 0 && !wait_bar(DO, pph)) break;  // O of the previous chunk read out of TMEM A
+                if (it > 0) {
+                    if (!wait_bar(DX, pph)) break;  // TMEM A (X of the previous chunk) read
                     tc_fence_after();
-                    // A = Q K^T
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
-                    mma_commit(bar(CA));
-                    if (it > 0) {
-                        if (!wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
-                        tc_fence_after();
-                    }
-                    // X = Q S0 ; S += K^T K
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                    if (NORM)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tSl.kmaj(ks), iKK, 1);
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
-                    mma_commit(bar(CXS));
-                    if (!wait_bar(DA, ph)) break;  // sA = A
-                    tc_fence_after();
-                    // W = A A^T
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tA.kmaj(ks), iSq, ks > 0);
-                    if (NORM) {
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tAl.kmaj(ks), iSq, 1);
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tA.kmaj(ks), iSq, 1);
-                    }
-                    if (!wait_bar(DX, ph)) break;  // sX = bf16(Q S0); TMEM X read
-                    tc_fence_after();
-                    // On a head's first chunk and in the normalised walk the W drain
-                    // writes W_lo over X's TMEM columns, so it reads X first: there
-                    // X = Q S0 + A K goes before the last W term (W then completes
-                    // last).  Otherwise W completes first and X after it, so that
-                    // W's drain, on the chain to O, does not wait for A K.
-                    const bool x_first = NORM || c == 0;
-                    if (x_first) {
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                        if (NORM)
-                            for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                        mma_commit(bar(CX2));
-                    }
-                    // W += (Q S0) Q^T
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tX.kmaj(ks), tQ.kmaj(ks), iSq, 1);
-                    if (NORM)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tXl.kmaj(ks), tQ.kmaj(ks), iSq, 1);
-                    mma_commit(bar(CW));
-                    if (!x_first) {
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                        mma_commit(bar(CX2));
-                    }
-                    if (!wait_bar(DW, ph)) break;  // sA = W_hi, TMEM W_lo; TMEM A read
-                    tc_fence_after();
-                    if (it > 0) {
-                        if (!wait_bar(DP, pph)) break;  // sP = P0 of this chunk; TMEM P read
-                        tc_fence_after();
-                    }
-                    // O = Q P0 + W_hi V + W_lo V
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
-                    if (NORM) {
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tPl.mnmaj(ks), iKM, 1);
-                        // denominator: Q p0 (+ W 1 below)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0h.kmaj(ks), iKK16, ks > 0);
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tDen_, tQ.kmaj(ks), tP0l.kmaj(ks), iKK16, 1);
-                    }
-                    mma_commit(bar(CQ));
-                    if (!wait_bar(LV, ph)) break;
-                    tc_fence_after();
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, 1);
-                    if (NORM || c == 0)  // W_lo V: every chunk when normalised, else the head's first
-                        for (int ks = 0; ks < kL / 16; ++ks)
-                            mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
-                    if (NORM) {
-                        // denominator += W_hi 1 + W_lo 1
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tDen_, tA.kmaj(ks), tOnes.kmaj(ks), iKK16, 1);
-                        for (int ks = 0; ks < kL / 16; ++ks)
-                            mma_bf16_tmem_a(tDen_, tX_ + wlo_col(ks), tOnes.kmaj(ks), iKK16, 1);
-                    }
-                    mma_commit(bar(CO));
-                    if (!wait_bar(DX2, ph)) break;  // sX = X
-                    tc_fence_after();
-                    // P += X^T V
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                    if (NORM) {
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                        // p += X^T 1
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
-                    }
-                    mma_commit(bar(CP));
-                } else {
-                    if (it > 0) {
-                        if (!wait_bar(DX, pph)) break;  // TMEM A (X of the previous chunk) read
-                        tc_fence_after();
-                    }
-                    // A = Q K^T
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
-                    mma_commit(bar(CA));
-                    if (it > 0) {
-                        if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
-                        tc_fence_after();
-                    }
-                    // S += K^T K
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(bar(CXS));
-                    if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
-                    tc_fence_after();
-                    // X = Q S_local + A K   (no S_local term on the segment's first chunk)
-                    if (it > 0) {
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                        if (NORM)
-                            for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tSl.kmaj(ks), iKK, 1);
-                    }
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
-                    if (NORM)
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                    mma_commit(bar(CX2));
-                    if (!wait_bar(LV, ph)) break;
-                    tc_fence_after();
-                    // C += Q^T V
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tC_, tQc.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
-                    if (NORM)  // m += Q^T 1
-                        for (int ks = 0; ks < kL / 16; ++ks)
-                            mma_bf16(tDen_, tQc.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(bar(CQ));
-                    if (!wait_bar(DX, ph)) break;  // sX = X
-                    tc_fence_after();
-                    // P += X^T V
-                    for (int ks = 0; ks < kL / 16; ++ks)
-                        mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
-                    if (NORM) {
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                        // p += X^T 1
-                        for (int ks = 0; ks < kL / 16; ++ks)
-                            mma_bf16(tPn_, tX.mnmaj(ks), tOnes.kmaj(ks), iMK16, (it > 0 || ks > 0) ? 1u : 0u);
-                        for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tPn_, tXl.mnmaj(ks), tOnes.kmaj(ks), iMK16, 1);
-                    }
-                    mma_commit(bar(CP));
                 }
+                // A = Q K^T
+                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
+                mma_commit(bar(CA));
+                if (it > 0) {
+                    if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
+                    tc_fence_after();
+                }
+                // S += K^T K
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CXS));
+                if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
+                tc_fence_after();
+                // X = Q S_local + A K   (no S_local term on the segment's first chunk)
+                if (it > 0) {
+                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
+                    if (NORM)
+                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tSl.kmaj(ks), iKK, 1);
+                }
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
+                if (NORM)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tA_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
+                mma_commit(bar(CX2));
+                if (!wait_bar(LV, ph)) break;
+                tc_fence_after();
+                // C += Q^T V  (NORM: [C | m] += Q^T [V | 1])
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tC_, tQc.mnmaj(ks), tV.mnmaj(ks), iMME, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar(CQ));
+                if (!wait_bar(DX, ph)) break;  // sX = X
+                tc_fence_after();
+                // P += X^T V  (NORM: [P | p] += X_hi^T [V | 1] + X_lo^T [V | 1])
+                for (int ks = 0; ks < kL / 16; ++ks)
+                    mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMME, (it > 0 || ks > 0) ? 1u : 0u);
+                if (NORM)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMME, 1);
+                mma_commit(bar(CP));
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
     } else if (producer) {
         // ============================ loads ============================
         // V of chunk c once the previous chunk's X^T V (V's last reader)
-        // completed, K of chunk c + 1 once A K completed; in the summary walk
-        // Q of chunk c + 2 into its buffer once Q^T V completed (and, with XP,
-        // the column-sum warp has read it), in the output walk Q of chunk
-        // c + 1 once Q P0 completed; tiles ahead<MODE>() chunks ahead move
-        // into L2 early
+        // completed, K of chunk c + 1 once A K completed, Q of chunk c + 2
+        // into its buffer once Q^T V completed (and, with XP, the column-sum
+        // warp has read it); tiles kAhead chunks ahead move into L2 early
         if (lane == 0) {
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                if (ahead<MODE>() > 0 && it + ahead<MODE>() < nchunks) prefetch(c + ahead<MODE>());
+                if (kAhead > 0 && it + kAhead < nchunks) prefetch(c + kAhead);
                 if (it > 0) {
                     if (!wait_bar(CP, pph)) break;
                     issue_load(LV, &mV, tV, c);
@@ -510,11 +338,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (!wait_bar(CX2, ph)) break;
                     issue_load(LK, &mK, tK, c + 1);
                 }
-                if (MODE == 1 && it + 1 < nchunks) {
-                    if (!wait_bar(CQ, ph)) break;
-                    issue_load(LQ, &mQ, tQ, c + 1);
-                }
-                if (MODE == 0 && it + 2 < nchunks) {
+                if (it + 2 < nchunks) {
                     const bool qodd = it & 1;
                     if (!wait_bar(CQ, ph)) break;
                     if (XP && !wait_bar(qodd ? DQ2 : DQ, (uint32_t)((it >> 1) & 1))) break;
@@ -566,166 +390,40 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         for (int it = 0; it < nchunks; ++it) {
             const uint32_t ph = it & 1;
             const bool has_next = it + 1 < nchunks;
-            if (MODE == 1) {
-                if (!wait_bar(CA, ph)) break;
-                tc_fence_after();
-                if (lane == 0) tma_store_wait_read();  // this warp's O piece has left its sA rows
-                __syncwarp();
-                if (NORM) drain128s(tA_, tA, tAl, true);
-                else drain128(tA_, tA, true);  // A -> sA (masked)
-                drained(DA);
-                if (!wait_bar(CXS, ph)) break;
-                tc_fence_after();
-                if (NORM) drainDs(tX_, tX, tXl);
-                else drainD(tX_, tX);  // bf16(Q S0) -> sX
+            if (!wait_bar(CA, ph)) break;
+            tc_fence_after();
+            if (NORM) drain128s(tA_, tA, tAl, true);
+            else drain128(tA_, tA, true);  // A -> sA (masked)
+            drained(DA);
+            if (!wait_bar(CX2, ph)) break;
+            tc_fence_after();
+            if constexpr (NORM) {
+                drainDs(tA_, tX, tXl);
                 drained(DX);
-                if (state_rows && has_next) {
-                    if (NORM) drainDs(tS_, tS, tSl);
-                    else drainD(tS_, tS);  // S0 of the next chunk -> sS
-                    drained(DS);
-                }
-                const bool x_first = NORM || c_begin + it == 0;  // as in the issuer
-                if (!wait_bar(CW, ph) || (x_first && !wait_bar(CX2, ph))) break;
-                tc_fence_after();
-                {
-                    // W is announced before X because the output products need it
-                    // first.  On the head's first chunk W is split into bf16 hi + lo:
-                    // there an output can be a single product (t = 0 gives (q.k)^2 v),
-                    // so the rounding of W is not averaged over many terms; W_lo lands
-                    // on this warp's X columns, so X is read out before it.  Later
-                    // chunks add the prefix term and many products, and plain bf16 W
-                    // suffices; there X completes after W and is read out after it.
-                    // X -> sX (hi, and lo in the normalised walk)
-                    auto put_x = [&](const uint32_t* x) {
-                        if (NORM) {
-                            put_row32_split2(tX, tXl, row, cD, x, false);
-                            if (D == 128) put_row32_split2(tX, tXl, row, cD + 32, x + 32, false);
-                        } else {
-                            put_row32(tX, row, cD, x, false);
-                            if (D == 128) put_row32(tX, row, cD + 32, x + 32, false);
-                        }
-                    };
-                    if (x_first) {
-                        uint32_t x[64];
-                        tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
-                        // at D = 128 X goes to shared memory before W is read out, which
-                        // keeps the live registers within the 168 this launch allows
-                        if (!NORM) put_x(x);
-                        uint32_t lo[32];
-                        {
-                            uint32_t r[64];
-                            tmem_ld_cols<64>(tA_ + lane_off + c128, r);
-                            put_row32_split(tA, row, c128, r, true, lo);  // W_hi -> sA (masked)
-                            put_row32_split(tA, row, c128 + 32, r + 32, true, lo + 16);
-                        }
-                        tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);  // W_lo -> TMEM
-                        tmem_st_wait();
-                        drained(DW);
-                        if (NORM) put_x(x);
-                    } else {
-                        drain128(tA_, tA, true);  // W -> sA (masked)
-                        drained(DW);
-                        if (!wait_bar(CX2, ph)) break;
-                        tc_fence_after();
-                        uint32_t x[64];
-                        tmem_ld_cols<D / 2>(tX_ + lane_off + cD, x);
-                        put_x(x);
-                    }
-                    drained(DX2);
-                }
-                if (!wait_bar(CO, ph)) break;
-                tc_fence_after();
-                {
-                    // O (fp32) leaves through the 4 KB of sA that hold this warp's
-                    // own rows and column half (W_hi there is dead once the output
-                    // products completed): 32 rows x 32 columns at a time, written
-                    // in the 128-byte-swizzled box layout and sent by a bulk tensor
-                    // store issued by this warp's lane 0.
-                    uint32_t r[64];
-                    tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
-                    if (NORM) {
-                        // ratio normalisation: o = num / den (plain IEEE division)
-                        const float den = __uint_as_float(tmem_ld1(tDen_ + lane_off));
-                        tmem_ld_wait();
+            } else if constexpr (XP) {
+                uint32_t xr[64];
+                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, xr);  // X -> sX, then into this row's sums
+                put_row32(tX, row, cD, xr, false);
+                if (D == 128) put_row32(tX, row, cD + 32, xr + 32, false);
+                drained(DX);
 #pragma unroll
-                        for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) / den);
-                    }
-                    // TMEM A is free once O sits in registers: the next chunk's
-                    // A = Q K^T need not wait for the stores below
-                    drained(DO);
-                    const uint32_t scratch = tA.base + (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
-                    const int t0 = (c_begin + it) * kL + quarter * 32;  // first token of this warp's rows
-#pragma unroll
-                    for (int g = 0; g < D / 64; ++g) {
-                        if (g > 0) {
-                            if (lane == 0) tma_store_wait_read();  // previous piece has left the scratch
-                            __syncwarp();
-                        }
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_shared_v4(scratch + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
-                                         r[32 * g + 4 * q], r[32 * g + 4 * q + 1], r[32 * g + 4 * q + 2],
-                                         r[32 * g + 4 * q + 3]);
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_3d(&mO, scratch, cD + 32 * g, t0, head);
-                            tma_store_commit();
-                        }
-                    }
-                }
-                if (state_rows && has_next) {
-                    if (!wait_bar(CP, ph)) break;
-                    tc_fence_after();
-                    if (NORM) {
-                        drainDs(tP_, tP, tPl);  // P0 of the next chunk -> sP (hi, lo)
-                        if (half == 0) {
-                            const uint32_t pv = tmem_ld1(tPn_ + lane_off);  // p0 of the next chunk
-                            tmem_ld_wait();
-                            put_p0(__uint_as_float(pv));
-                        }
-                    } else {
-                        drainD(tP_, tP);  // P0 of the next chunk -> sP
-                    }
-                    drained(DP);
-                }
+                for (int j = 0; j < D / 2; ++j) xacc[j] += __uint_as_float(xr[j]);
             } else {
-                if (!wait_bar(CA, ph)) break;
-                tc_fence_after();
-                if (NORM) drain128s(tA_, tA, tAl, true);
-                else drain128(tA_, tA, true);  // A -> sA (masked)
-                drained(DA);
-                if (!wait_bar(CX2, ph)) break;
-                tc_fence_after();
-                if constexpr (NORM) {
-                    drainDs(tA_, tX, tXl);
-                    drained(DX);
-                } else if constexpr (XP) {
-                    uint32_t xr[64];
-                    tmem_ld_cols<D / 2>(tA_ + lane_off + cD, xr);  // X -> sX, then into this row's sums
-                    put_row32(tX, row, cD, xr, false);
-                    if (D == 128) put_row32(tX, row, cD + 32, xr + 32, false);
-                    drained(DX);
-#pragma unroll
-                    for (int j = 0; j < D / 2; ++j) xacc[j] += __uint_as_float(xr[j]);
-                } else {
-                    drainD(tA_, tX);  // X -> sX
-                    drained(DX);
-                }
-                if (state_rows && has_next) {
-                    if (NORM) drainDs(tS_, tS, tSl);
-                    else drainD(tS_, tS);  // S_local of the next chunk -> sS
-                    drained(DS);
-                }
+                drainD(tA_, tX);  // X -> sX
+                drained(DX);
+            }
+            if (state_rows && has_next) {
+                if (NORM) drainDs(tS_, tS, tSl);
+                else drainD(tS_, tS);  // S_local of the next chunk -> sS
+                drained(DS);
             }
         }
-        if (MODE == 1 && lane == 0) tma_store_wait_all();
-        // ---- segment summary out (mode 0): S | C | m | P | p records, fp32 ----
-        if (MODE == 0 && state_rows && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
+        // ---- segment summary out: S | C | m | P | p records, fp32 ----
+        if (state_rows && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
             tc_fence_after();
             const size_t R = (size_t)D * D + 2 * (size_t)D * D + 2 * (size_t)D;
             float* out = p.summ + ((size_t)head * p.nseg + seg) * R;
-            // S, C, P leave through 32 x 32 boxes and bulk tensor stores (mO maps
+            // S, C, P leave through 32 x 32 boxes and bulk tensor stores (mR maps
             // the records as (3D + 2) rows of D floats: S at row 0, C at row D,
             // P at row 2D + 1).  Every tile is dead now: the last MMAs completed
             // and no load is in flight, so each warp stages its boxes in its own
@@ -746,14 +444,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             if (lane == 0) tma_store_wait_all();
             if (NORM && half == 0) {
                 // m (after C) and p (after P), one value per state row
-                const uint32_t mv = tmem_ld1(tDen_ + lane_off);
+                const uint32_t mv = tmem_ld1(tM_ + lane_off);
                 const uint32_t pv = tmem_ld1(tPn_ + lane_off);
                 tmem_ld_wait();
                 out[2 * (size_t)D * D + row] = __uint_as_float(mv);
                 out[3 * (size_t)D * D + D + row] = __uint_as_float(pv);
             }
         }
-        if (MODE == 0 && XP && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
+        if (XP && nchunks > 0 && wait_bar(CP, (nchunks - 1) & 1)) {
             // p of the segment: each warp leaves the column sums of its 32 rows
             // in the (dead) S tile, and the quarter-0 warps add the four quarters
             float pacc[2];
@@ -943,33 +641,25 @@ cudaError_t launch_cross_t(const CrossArgs& a, cudaStream_t s) {
 }
 
 
-template <int D, int MODE, bool NORM, bool XP = false>
-cudaError_t launch_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, float* summ, int BH,
-                     int T, SegPlan plan, int* status, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mo;
+template <int D, bool NORM, bool XP = false>
+cudaError_t launch_t(const void* Q, const void* K, const void* V, float* summ, int BH, int T, SegPlan plan, int* status,
+                     cudaStream_t s) {
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
-    // mR: the segment records (prefixes read by the output walk, summaries
-    // written by the summary walk) as (3D + 2) rows of D floats, 32 x 32 boxes
+    // mR: the segment summary records as (3D + 2) rows of D floats, 32 x 32 boxes
     CUtensorMap mr;
-    if (!make_map(&mr, MODE == 1 ? static_cast<const void*>(prefix) : static_cast<const void*>(summ),
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+    if (!make_map(&mr, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
         return cudaErrorInvalidValue;
-    if (MODE == 1) {
-        // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
-        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
-    } else {
-        mo = mr;  // unused
-    }
-    TCParams prm{T, plan.nseg, plan.nchunk, plan.seglen, summ, prefix, O, status};
-    const size_t smem = Layout<D, MODE, NORM>::kBytes + 1024;
-    auto kern = tc_walk_kernel<D, MODE, NORM, XP>;
+    TCParams prm{T, plan.nseg, plan.nchunk, plan.seglen, summ, status};
+    const size_t smem = Layout<D, NORM>::kBytes + 1024;
+    auto kern = tc_walk_kernel<D, NORM, XP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
-    kern<<<grid, walk_threads<MODE, XP>(), smem, s>>>(mq, mk, mv, mo, mr, prm);
+    kern<<<grid, walk_threads<XP>(), smem, s>>>(mq, mk, mv, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -999,15 +689,15 @@ cudaError_t launch_tc_walk(int mode, const void* Q, const void* K, const void* V
     if (mode == 1) return launch_tc_out(Q, K, V, O, prefix, BH, T, d, dv, normalized != 0, plan, status, s);
     if (normalized) {
         if (d != 64) return cudaErrorInvalidValue;
-        return launch_t<64, 0, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+        return launch_t<64, true>(Q, K, V, summ, BH, T, plan, status, s);
     }
     if (with_p) {
-        if (d == 128) return launch_t<128, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
-        if (d == 64) return launch_t<64, 0, false, true>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+        if (d == 128) return launch_t<128, false, true>(Q, K, V, summ, BH, T, plan, status, s);
+        if (d == 64) return launch_t<64, false, true>(Q, K, V, summ, BH, T, plan, status, s);
         return cudaErrorInvalidValue;
     }
-    if (d == 128) return launch_t<128, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
-    if (d == 64) return launch_t<64, 0, false>(Q, K, V, O, prefix, summ, BH, T, plan, status, s);
+    if (d == 128) return launch_t<128, false>(Q, K, V, summ, BH, T, plan, status, s);
+    if (d == 64) return launch_t<64, false>(Q, K, V, summ, BH, T, plan, status, s);
     return cudaErrorInvalidValue;
 }
 
