@@ -45,16 +45,19 @@ struct TCParams {
 template <int D, bool NORM = false>
 struct Layout {
     // byte offsets of the tiles inside the 1024-aligned dynamic shared memory
-    static constexpr uint32_t kTok = kL * D * 2;      // Q, K, V, X tiles
-    static constexpr uint32_t kSq = kL * kL * 2;      // A tile
+    static constexpr uint32_t kTok = kL * D * 2;      // Q, K, V tiles
+    static constexpr uint32_t kSq = kL * kL * 2;      // A tile, then X
     static constexpr uint32_t kSt = D * D * 2;        // S tile
-    // NORM: the V tile's second 64-column block holds ones ([V | 1])
-    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + (NORM ? 2 : 1) * kTok, X = A + kSq;
-    static constexpr uint32_t Q2 = X + kTok;  // second Q buffer
-    static constexpr uint32_t S = Q2 + kTok;
+    // NORM: the V tile's second 64-column block holds ones ([V | 1]).  X goes
+    // into the A tile: A K, A's only reader, has completed when X is drained,
+    // and the next A is drained only after X^T V (issued before it) completed.
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + (NORM ? 2 : 1) * kTok, X = A;
+    static constexpr uint32_t Q2 = A + kSq;  // second Q buffer
+    static constexpr uint32_t K2 = Q2 + kTok;  // second K buffer
+    static constexpr uint32_t S = K2 + kTok;
     static constexpr uint32_t kEnd = S + kSt;
-    // ratio-normalised walk: bf16 lo halves of the split operands
-    static constexpr uint32_t Alo = kEnd, Xlo = Alo + kSq, Slo = Xlo + kTok;
+    // ratio-normalised walk: bf16 lo halves of the split operands (X_lo over A_lo)
+    static constexpr uint32_t Alo = kEnd, Xlo = Alo, Slo = Alo + kSq;
     static constexpr uint32_t kNormEnd = Slo + kSt;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
@@ -101,7 +104,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     using LY = Layout<D, NORM>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | final wait | XP: p exchange, Q column sums
-    enum { LQ, LK, LV, LQ2, CA, CXS, CX2, CQ, CP, DA, DX, DS, FIN, PX, DQ, DQ2, NBAR };
+    enum { LQ, LK, LV, LQ2, LK2, CA, CXS, CX2, CQ, CP, DA, DX, DS, FIN, PX, DQ, DQ2, NBAR };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -126,9 +129,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
 
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
-    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
+    const Tile tQ{dsm + LY::Q, kL}, tK0{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
-    const Tile tQ2{dsm + LY::Q2, kL};  // Q of odd chunks (two Q buffers)
+    const Tile tQ2{dsm + LY::Q2, kL}, tK2{dsm + LY::K2, kL};  // Q and K of odd chunks (two buffers each)
     const Tile tS{dsm + LY::S, D};
     // normalised walk only
     const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL}, tSl{dsm + LY::Slo, D};
@@ -193,7 +196,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     };
     // every tile load is issued by the issuer's lane 0, which settles them
     // (waits for the last of each barrier) before the CTA exits
-    LoadLedger<4> loads(bar(0));  // LQ, LK, LV, LQ2
+    LoadLedger<5> loads(bar(0));  // LQ, LK, LV, LQ2, LK2
     auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
         loads.note(b);
         mbar_expect_tx(bar(b), kTileBytes);
@@ -246,9 +249,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     // before the first __syncthreads, so the load warp may use them).
     if (producer && lane == 0 && nchunks > 0) {
         issue_load(LQ, &mQ, tQ, c_begin);
-        issue_load(LK, &mK, tK, c_begin);
+        issue_load(LK, &mK, tK0, c_begin);
         issue_load(LV, &mV, tV, c_begin);
-        if (nchunks > 1) issue_load(LQ2, &mQ, tQ2, c_begin + 1);
+        if (nchunks > 1) {
+            issue_load(LQ2, &mQ, tQ2, c_begin + 1);
+            issue_load(LK2, &mK, tK2, c_begin + 1);
+        }
         for (int a = 1; a < kAhead && a < nchunks; ++a) prefetch(c_begin + a);
     }
 
@@ -269,11 +275,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             int it = 0;
             for (; it < nchunks; ++it) {
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                // two Q buffers: chunk it uses buffer it & 1
+                // two Q and two K buffers: chunk it uses buffer it & 1
                 const bool qodd = it & 1;
                 const Tile& tQc = qodd ? tQ2 : tQ;
+                const Tile& tK = qodd ? tK2 : tK0;
                 const uint32_t qph = (uint32_t)((it >> 1) & 1);
-                if (!wait_bar(qodd ? LQ2 : LQ, qph) || !wait_bar(LK, ph)) break;
+                if (!wait_bar(qodd ? LQ2 : LQ, qph) || !wait_bar(qodd ? LK2 : LK, qph)) break;
                 if (it > 0) {
                     if (!wait_bar(DX, pph)) break;  // TMEM A (X of the previous chunk) read
                     tc_fence_after();
@@ -322,9 +329,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     } else if (producer) {
         // ============================ loads ============================
         // V of chunk c once the previous chunk's X^T V (V's last reader)
-        // completed, K of chunk c + 1 once A K completed, Q of chunk c + 2
-        // into its buffer once Q^T V completed (and, with XP, the column-sum
-        // warp has read it); tiles kAhead chunks ahead move into L2 early
+        // completed; K of chunk c + 2 into its buffer once A K (of chunk c,
+        // the buffer's last reader) completed, Q of chunk c + 2 once Q^T V
+        // completed (and, with XP, the column-sum warp has read it); tiles
+        // kAhead chunks ahead move into L2 early
         if (lane == 0) {
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
@@ -334,12 +342,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                     if (!wait_bar(CP, pph)) break;
                     issue_load(LV, &mV, tV, c);
                 }
-                if (it + 1 < nchunks) {
-                    if (!wait_bar(CX2, ph)) break;
-                    issue_load(LK, &mK, tK, c + 1);
-                }
                 if (it + 2 < nchunks) {
                     const bool qodd = it & 1;
+                    if (!wait_bar(CX2, ph)) break;
+                    issue_load(qodd ? LK2 : LK, &mK, qodd ? tK2 : tK0, c + 2);
                     if (!wait_bar(CQ, ph)) break;
                     if (XP && !wait_bar(qodd ? DQ2 : DQ, (uint32_t)((it >> 1) & 1))) break;
                     issue_load(qodd ? LQ2 : LQ, &mQ, qodd ? tQ2 : tQ, c + 2);
