@@ -57,8 +57,8 @@ struct Layout {
     static constexpr uint32_t S = K2 + kTok;
     static constexpr uint32_t kEnd = S + kSt;
     // ratio-normalised walk: bf16 lo halves of the split operands (X_lo over A_lo)
-    static constexpr uint32_t Alo = kEnd, Xlo = Alo, Slo = Alo + kSq;
-    static constexpr uint32_t kNormEnd = Slo + kSt;
+    static constexpr uint32_t Alo = kEnd, Xlo = Alo;
+    static constexpr uint32_t kNormEnd = Alo + kSq;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
@@ -74,9 +74,11 @@ struct Layout {
 // the issuer waits on before it overwrites the region or reads what the
 // drain wrote.  Drains thus overlap the MMAs that do not depend on them.
 //
-// NORM (ratio-normalised variant, D = 64): every fp32 intermediate that
-// feeds a product (A, X, S0) is split into bf16 hi + lo parts and the
-// product is taken on both parts, which keeps about 16 significant bits.
+// NORM (ratio-normalised variant, D = 64): A and X, which feed products,
+// are split into bf16 hi + lo parts and the product is taken on both parts,
+// which keeps about 16 significant bits.  S0 is rounded to bf16 as in the
+// unnormalised walk (its rounding stays two orders below the 1e-4 bound on
+// the normalised outputs, where A's or X's would exceed it).
 // The extra value column of ones rides along: V is read as [V | 1] (the V
 // tile's second 64-column block holds ones), so the N = D + 16 products
 // C += Q^T [V | 1] and P += X^T [V | 1] also gather m = sum_t q_t and
@@ -134,7 +136,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     const Tile tQ2{dsm + LY::Q2, kL}, tK2{dsm + LY::K2, kL};  // Q and K of odd chunks (two buffers each)
     const Tile tS{dsm + LY::S, D};
     // normalised walk only
-    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL}, tSl{dsm + LY::Slo, D};
+    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
@@ -299,11 +301,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 if (!wait_bar(DA, ph)) break;  // sA = A; TMEM A read
                 tc_fence_after();
                 // X = Q S_local + A K   (no S_local term on the segment's first chunk)
-                if (it > 0) {
+                if (it > 0)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                    if (NORM)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tSl.kmaj(ks), iKK, 1);
-                }
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tA_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (it > 0 || ks > 0) ? 1u : 0u);
                 if (NORM)
@@ -419,8 +418,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 drained(DX);
             }
             if (state_rows && has_next) {
-                if (NORM) drainDs(tS_, tS, tSl);
-                else drainD(tS_, tS);  // S_local of the next chunk -> sS
+                drainD(tS_, tS);  // S_local of the next chunk -> sS
                 drained(DS);
             }
         }

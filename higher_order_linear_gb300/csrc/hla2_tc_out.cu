@@ -33,9 +33,11 @@
 // Q X_lo^T, O = W_hi V + W_lo V; W_lo packed next to W_hi in alpha).
 //
 // NORM (ratio-normalised variant, D = 64): o_t = q_t^T P_t / q_t^T p_t with
-// p = S m - h.  Every fp32 value that feeds a product is split into bf16 hi +
-// lo and both parts enter it (A, X, W, S0, P0, p0), which keeps about 16
-// significant bits of every operand.  p and the denominators ride along as
+// p = S m - h.  The fp32 values that feed a product are split into bf16 hi +
+// lo and both parts enter it (A, X, W, P0, p0), which keeps about 16
+// significant bits of those operands; S0 is rounded to bf16 alone (its
+// rounding stays two orders below the 1e-4 bound on the outputs, where any
+// of the others would come within a factor of three of it or exceed it).  p and the denominators ride along as
 // one more value column: V is read as [V | 1] and P0 as [P0 | p0] (N = 80
 // products, the extra 64-column block of each operand holding the ones or
 // p0), so P += X^T [V | 1] grows p in P's column D and O = Q [P0 | p0] +
@@ -62,7 +64,7 @@ struct OutLayout {
     static constexpr uint32_t kO = kSq;
     // NORM: the V tile's second block holds the ones ([V | 1]), the S0 / P0
     // tile's second block p0 ([P0 | p0], column 0), then the same pair for
-    // the lo parts; X_lo in the X tile's second block
+    // the lo parts of P0 and p0; X_lo in the X tile's second block
     static constexpr uint32_t Q0 = 0, Q1 = kTok, K = 2 * kTok, V = 3 * kTok, X = (NORM ? 5 : 4) * kTok;
     static constexpr uint32_t O = X + kSq, SP = O + kO, XL = X + kL * 128u;
     static constexpr uint32_t SPL = SP + 2 * kSt;
@@ -145,7 +147,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
     const Tile tQ0{dsm + LY::Q0, kL}, tQ1{dsm + LY::Q1, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
     const Tile tX{dsm + LY::X, kL}, tO{dsm + LY::O, kL}, tSP{dsm + LY::SP, D};
-    // NORM tiles (X_lo, S0 / P0 lo parts)
+    // NORM tiles (X_lo, the lo part of P0)
     const Tile tXL{dsm + LY::XL, kL}, tSPL{dsm + LY::SPL, D};
     auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
@@ -237,13 +239,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
     };
     // this beta warp's groups of a D-wide fp32 region -> bf16 tile rows
-    auto drainD = [&](uint32_t treg, const Tile& t) {
+    auto drainD = [&](uint32_t treg, const Tile& t, bool split) {
 #pragma unroll
         for (int g = 0; g < BG; ++g) {
             uint32_t r[32];
             tmem_ld32(treg + lane_off + bcol(g), r);
             tmem_ld_wait();
-            if (NORM) put_row32_split2(t, tSPL, row, bcol(g), r, false);  // t is the S0 / P0 tile
+            if (NORM && split) put_row32_split2(t, tSPL, row, bcol(g), r, false);  // t is the S0 / P0 tile
             else put_row32(t, row, bcol(g), r, false);
         }
     };
@@ -344,8 +346,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             box32_read(stage, lane, r);
             tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cD, r);
             if (m == 0) {  // bf16 S0; P0 follows once Q S0 has read it
-                if (NORM) put_row32_split2(tSP, tSPL, row, cD, r, false);
-                else put_row32(tSP, row, cD, r, false);
+                put_row32(tSP, row, cD, r, false);
             }
             __syncwarp();  // every lane has read the box before the next load reuses it
         }
@@ -394,8 +395,6 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // X = Q S0 (S0 symmetric: its tile read K-major), then S += K^T K
                 if (!first) {
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.kmaj(ks), iKK, ks > 0);
-                    if (NORM)
-                        for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSPL.kmaj(ks), iKK, 1);
                 }
                 mma_commit(bar(CQS));
                 for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
@@ -500,7 +499,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 tc_fence_after();
                 if (state_rows) {
                     if (!first) {
-                        drainD(tP_, tSP);
+                        drainD(tP_, tSP, true);
                         if (NORM && bw == 0) {  // p0 of this chunk -> its operand tiles
                             const uint32_t pv = tmem_ld1(tPn_ + lane_off);
                             tmem_ld_wait();
@@ -552,7 +551,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     tmem_ld_wait();
                     drained(DO);
                     if (state_rows && has_next) {
-                        drainD(tS_, tSP);
+                        drainD(tS_, tSP, false);
                         drained(DS);
                     }
                     if (NORM) {
@@ -571,7 +570,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     tmem_ld_wait();
                     drained(DO);
                     if (state_rows && has_next) {
-                        drainD(tS_, tSP);
+                        drainD(tS_, tSP, false);
                         drained(DS);
                     }
                     stage_o(r, 1);
