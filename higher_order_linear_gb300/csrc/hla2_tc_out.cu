@@ -118,8 +118,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     using RO = OutRoles<D, NORM>;
     constexpr int NDW = RO::kDrain, AG = RO::kAG, BG = RO::kBG;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    // loads | MMA commits | drains | final wait | drain warp w's prefix boxes
-    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, FIN, PB, NBAR = PB + NDW };
+    // loads | MMA commits | drains | the S += K^T K commit | final wait |
+    // drain warp w's prefix boxes
+    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, CK, FIN, PB, NBAR = PB + NDW };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -155,7 +156,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         abort_flag = 0;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == DA) cnt = RO::kAlpha;
+            if (i == DA) cnt = NORM ? RO::kDrain : RO::kAlpha;  // NORM: every drain warp packs A
             if (i == DW) cnt = NORM ? RO::kDrain : RO::kAlpha;  // NORM: every drain warp packs W
             if (i == DX || i == DO) cnt = RO::kBeta;
             if (i == DS || i == DP) cnt = RO::kState;
@@ -392,12 +393,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     if (!wait_bar(DO, pph) || !wait_bar(DS, pph)) break;
                     tc_fence_after();
                 }
-                // X = Q S0 (S0 symmetric: its tile read K-major), then S += K^T K
+                // X = Q S0 (S0 symmetric: its tile read K-major)
                 if (!first) {
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tBe_, tQ.kmaj(ks), tSP.kmaj(ks), iKK, ks > 0);
                 }
                 mma_commit(bar(CQS));
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                 if (!wait_bar(DA, ph)) break;  // A packed in alpha
                 tc_fence_after();
                 // X += A K  (A from tensor memory)
@@ -407,6 +407,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tK.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CX));
+                // S += K^T K after A K: it then runs beside the X drain, not
+                // beside the pack of A, whose tensor-memory traffic it slowed
+                // (K's last reader now, so the next K waits for CK)
+                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                mma_commit(bar(CK));
                 if (!wait_bar(DX, ph)) break;  // sX = X (and sO = X_lo on a head's first chunk); beta free
                 tc_fence_after();
                 // W = Q X^T (+ Q X_lo^T) into alpha (A there was read by A K)
@@ -441,14 +446,14 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         }
     } else if (producer) {
         // =========================== producer ===========================
-        // each tile loads as soon as its buffer is free: the next K once A K
-        // (its last reader) completed, the next V and the Q after next once O
-        // (the last reader of this chunk's V and Q) completed
+        // each tile loads as soon as its buffer is free: the next K once
+        // S += K^T K (its last reader) completed, the next V and the Q after
+        // next once O (the last reader of this chunk's V and Q) completed
         if (lane == 0) {
             for (int it = 0; it + 1 < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1;
-                if (!wait_bar(CX, ph)) break;
+                if (!wait_bar(CK, ph)) break;
                 issue_load(LK, &mK, tK, c + 1);
                 if (!wait_bar(CO, ph)) break;
                 issue_load(LV, &mV, tV, c + 1);
@@ -485,11 +490,12 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             const bool has_next = it + 1 < nchunks;
             const bool first = c == 0;
             static_assert(BG <= 2, "a beta warp holds at most one O group while it drains S");
-            if (alpha_w) {
-                // A packed in place (masked)
+            if (alpha_w || NORM) {
+                // A packed in place (masked; hi and lo in the normalised walk,
+                // where every drain warp packs one group)
                 if (!wait_bar(CA_, ph)) break;
                 tc_fence_after();
-                pack_alpha(NORM);
+                pack_alpha(NORM, NORM);
                 packed(DA);
             }
             if (beta_w) {
