@@ -65,21 +65,19 @@ exscan4_kernel(const float* in, float* out, int N, size_t R, size_t off, size_t 
     const float* pin = in + (size_t)bh * N * R + off + i;
     float* pout = out + (size_t)bh * N * R + off + i;
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    int r = 0;
-    for (; r + U <= N; r += U) {
+    // U records per round, every load of a round issued before its sums (the
+    // last round predicated, so that a short axis is one round of loads)
+    for (int r = 0; r < N; r += U) {
         float4 x[U];
 #pragma unroll
-        for (int j = 0; j < U; ++j) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
+        for (int j = 0; j < U; ++j)
+            if (r + j < N) x[j] = *reinterpret_cast<const float4*>(pin + (size_t)(r + j) * R);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
+            if (r + j >= N) break;
             if (WRITE) *reinterpret_cast<float4*>(pout + (size_t)(r + j) * R) = run;
             run.x += x[j].x; run.y += x[j].y; run.z += x[j].z; run.w += x[j].w;
         }
-    }
-    for (; r < N; ++r) {
-        const float4 x = *reinterpret_cast<const float4*>(pin + (size_t)r * R);
-        if (WRITE) *reinterpret_cast<float4*>(pout + (size_t)r * R) = run;
-        run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
     }
     if (total) *reinterpret_cast<float4*>(total + (size_t)bh * total_stride + i) = run;
 }
@@ -346,9 +344,9 @@ cudaError_t launch_exscan(const float* in, float* out, int BH, int N, size_t R, 
     if (!out && !total) return cudaErrorInvalidValue;
     if (vec) {
         dim3 grid((unsigned)((len / 4 + kScanThreads - 1) / kScanThreads), BH);
-        // long record axes keep 16 records per thread in flight (the element
-        // range alone gives too few threads to cover the latency)
-        if (N >= 64) {
+        // axes longer than 8 records keep 16 records per thread in flight (the
+        // element range alone gives too few threads to cover the latency)
+        if (N > kScanUnroll) {
             if (out) exscan4_kernel<true, 16><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
             else exscan4_kernel<false, 16><<<grid, kScanThreads, 0, s>>>(in, out, N, R, off, len, total, total_stride);
         } else {

@@ -279,8 +279,24 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
             fold(acc1, rec + off1, f);
         }
     } else {
-        // this record's term X_r; the running sum over records follows in a second launch
-        for (int i0 = 0; i0 < r; ++i0) fold(acc1, rec0 + (size_t)i0 * R + off1, (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f);
+        // this record's term X_r; the running sum over records follows in a second launch.
+        // Two records' loads are in flight before their (in-order) folds.
+        int i0 = 0;
+        for (; i0 + 1 < r; i0 += 2) {
+            float4 x0[NV], x1[NV];
+            ld_mat<D>(rec0 + (size_t)i0 * R + off1, tid, x0);
+            ld_mat<D>(rec0 + (size_t)(i0 + 1) * R + off1, tid, x1);
+            const float f0 = (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f;
+            const float f1 = (OP == kScanDecay) ? __ldg(a.fac + i0 + 1) : 1.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const float4 t = make_float4(fmaf(f0, acc1[i].x, x0[i].x), fmaf(f0, acc1[i].y, x0[i].y),
+                                             fmaf(f0, acc1[i].z, x0[i].z), fmaf(f0, acc1[i].w, x0[i].w));
+                acc1[i] = make_float4(fmaf(f1, t.x, x1[i].x), fmaf(f1, t.y, x1[i].y), fmaf(f1, t.z, x1[i].z),
+                                      fmaf(f1, t.w, x1[i].w));
+            }
+        }
+        if (i0 < r) fold(acc1, rec0 + (size_t)i0 * R + off1, (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f);
         const float* rec = rec0 + (size_t)r * R;
         fold(acc2, rec + off2, 1.f);
         if (EXTRA) {
