@@ -48,17 +48,22 @@ struct Layout {
     static constexpr uint32_t kTok = kL * D * 2;      // Q, K, V tiles
     static constexpr uint32_t kSq = kL * kL * 2;      // A tile, then X
     static constexpr uint32_t kSt = D * D * 2;        // S tile
-    // NORM: the V tile's second 64-column block holds ones ([V | 1]).  X goes
-    // into the A tile: A K, A's only reader, has completed when X is drained,
-    // and the next A is drained only after X^T V (issued before it) completed.
-    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + (NORM ? 2 : 1) * kTok, X = A;
-    static constexpr uint32_t Q2 = A + kSq;  // second Q buffer
-    static constexpr uint32_t K2 = Q2 + kTok;  // second K buffer
+    // NORM: the V tile's second 64-column block holds ones ([V | 1]).
+    // At D = 128 X goes into the A tile (shared memory is full): A K, A's only
+    // reader, has completed when X is drained, and the next A is drained only
+    // after X^T V (issued before it) completed.  At D = 64 X has a tile of its
+    // own, and X^T V of a chunk is issued after the next chunk's A = Q K^T
+    // (kDeferP), off the chain A -> drain -> A K -> drain -> next A.
+    static constexpr bool kSepX = D < 128;
+    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + (NORM ? 2 : 1) * kTok;
+    static constexpr uint32_t X = kSepX ? A + kSq : A;
+    static constexpr uint32_t Q2 = kSepX ? X + kTok : A + kSq;  // second Q buffer
+    static constexpr uint32_t K2 = Q2 + kTok;                  // second K buffer
     static constexpr uint32_t S = K2 + kTok;
     static constexpr uint32_t kEnd = S + kSt;
-    // ratio-normalised walk: bf16 lo halves of the split operands (X_lo over A_lo)
-    static constexpr uint32_t Alo = kEnd, Xlo = Alo;
-    static constexpr uint32_t kNormEnd = Alo + kSq;
+    // ratio-normalised walk: bf16 lo halves of the split operands
+    static constexpr uint32_t Alo = kEnd, Xlo = kSepX ? Alo + kSq : Alo;
+    static constexpr uint32_t kNormEnd = kSepX ? Xlo + kTok : Alo + kSq;
     // MN-major operands read with M = 128 > D see a second 64-column block
     // one block past the tile: keep valid memory there when D = 64.
     static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
@@ -271,6 +276,16 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     constexpr uint32_t iMM = idesc_bf16(128, D, true, true);       // both MN-major
     constexpr uint32_t iMME = idesc_bf16(128, NORM ? D + 16 : D, true, true);  // NORM: N = D + 16, [V | 1]
 
+    constexpr bool kDeferP = LY::kSepX;
+    // P += X^T V of chunk j (NORM: [P | p] += X_hi^T [V | 1] + X_lo^T [V | 1])
+    auto issue_p = [&](int j) {
+        for (int ks = 0; ks < kL / 16; ++ks)
+            mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMME, (j > 0 || ks > 0) ? 1u : 0u);
+        if (NORM)
+            for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMME, 1);
+        mma_commit(bar(CP));
+    };
+
     if (issuer) {
         // ============================ issuer ============================
         if (lane == 0 && nchunks > 0) {
@@ -290,6 +305,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 // A = Q K^T
                 for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQc.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
                 mma_commit(bar(CA));
+                if (kDeferP && it > 0) issue_p(it - 1);  // X and V of the previous chunk are in place
                 if (it > 0) {
                     if (!wait_bar(DS, pph)) break;  // sS = S_local of this chunk; TMEM S read
                     tc_fence_after();
@@ -314,14 +330,15 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16(tC_, tQc.mnmaj(ks), tV.mnmaj(ks), iMME, (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(bar(CQ));
-                if (!wait_bar(DX, ph)) break;  // sX = X
+                if (!kDeferP) {
+                    if (!wait_bar(DX, ph)) break;  // sX = X
+                    tc_fence_after();
+                    issue_p(it);
+                }
+            }
+            if (kDeferP && it == nchunks && wait_bar(DX, (uint32_t)((nchunks - 1) & 1))) {
                 tc_fence_after();
-                // P += X^T V  (NORM: [P | p] += X_hi^T [V | 1] + X_lo^T [V | 1])
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMME, (it > 0 || ks > 0) ? 1u : 0u);
-                if (NORM)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tXl.mnmaj(ks), tV.mnmaj(ks), iMME, 1);
-                mma_commit(bar(CP));
+                issue_p(nchunks - 1);
             }
             if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
         }
