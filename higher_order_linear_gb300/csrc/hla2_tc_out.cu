@@ -82,9 +82,11 @@ struct OutLayout {
 // pack A and W, the beta warps drain X, O and the state, so that packing the
 // next chunk's A never waits behind the previous chunk's O stores.  At D = 64
 // every drain warp does both, except in the normalised walk (D = 64, bf16
-// hi + lo packs twice as long), which has four warps per quarter split as at
-// D = 128.  Columns go in groups of 32: an alpha warp takes kAG groups of
-// alpha, a beta warp kBG groups of each D-wide region.
+// hi + lo packs twice as long), which has four warps per quarter: two of them
+// also drain X, O and the state, and all four pack A and W, one 32-column
+// group each (the split packs are the longest steps of its chunk).  Columns
+// go in groups of 32: an alpha warp takes kAG groups of alpha, a beta warp
+// kBG groups of each D-wide region.
 template <int D, bool NORM>
 struct OutRoles {
     static constexpr int kParts = NORM ? 4 : D / 32;   // drain warps per lane quarter
