@@ -747,6 +747,9 @@ cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const v
                                  cudaStream_t s) {
     if (BH == 0 || plan.nseg == 0) return cudaSuccess;
     if (plan.granule != kL || d != dv || !decay_tc_gamma_ok(gamma)) return cudaErrorInvalidValue;
+    // outputs: the walk pipelined across chunks (hla2_tc_out.cu)
+    if (mode == 1)
+        return launch_tc_out_decay(Q, K, V, O, prefix, BH, T, d, dv, (float)std::log2((double)gamma), plan, status, s);
     if (d == 128) return launch_d<128>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
     if (d == 64) return launch_d<64>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
     return cudaErrorInvalidValue;

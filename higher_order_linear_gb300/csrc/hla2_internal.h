@@ -196,6 +196,10 @@ cudaError_t launch_tc_chunk(const void* Q, const void* K, const void* V, float* 
 // prefix S|.|.|P|.|p.
 cudaError_t launch_tc_out(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,
                           int d, int dv, bool normalized, SegPlan plan, int* status, cudaStream_t s);
+// The same walk for the decayed operator (lg = log2(gamma), gamma in the
+// tensor-core range): outputs from the decayed prefix S|.|.|P|.
+cudaError_t launch_tc_out_decay(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH,
+                                int T, int d, int dv, float lg, SegPlan plan, int* status, cudaStream_t s);
 // AHLA on tensor cores (hla2_ahla_tc.cu), d = dv in {64, 128}, bf16, unnormalised:
 // mode 0 writes the M|P|.|E|. parts of the segment summaries, mode 1 outputs.
 cudaError_t launch_ahla_tc_walk(int mode, const void* Q, const void* K, const void* V,

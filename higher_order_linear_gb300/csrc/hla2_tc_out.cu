@@ -52,6 +52,7 @@ struct OutParams {
     int T, nseg, nchunk, seglen;
     const float* prefix;  // segment prefix records (S and P read)
     int* status;
+    float lg;  // DECAY: log2(gamma)
 };
 
 template <int D, bool NORM>
@@ -111,7 +112,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-template <int D, bool NORM>
+template <int D, bool NORM, bool DECAY>
 __global__ void __launch_bounds__(OutRoles<D, NORM>::kThreads, 1)
 tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
@@ -122,7 +123,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | the S += K^T K commit | final wait |
     // drain warp w's prefix boxes
-    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, CK, FIN, PB, NBAR = PB + NDW };
+    // (DK: DECAY, K scaled in place by the beta warps)
+    enum { LQ0, LQ1, LK, LV, CA_, CQS, CX, CW, CP, CO, DA, DP, DX, DW, DO, DS, CK, DK, FIN, PB, NBAR = PB + NDW };
+    static_assert(!(NORM && DECAY), "one operator per walk");
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -159,8 +162,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
             if (i == DA) cnt = NORM ? RO::kDrain : RO::kAlpha;  // NORM: every drain warp packs A
-            if (i == DW) cnt = NORM ? RO::kDrain : RO::kAlpha;  // NORM: every drain warp packs W
-            if (i == DX || i == DO) cnt = RO::kBeta;
+            // NORM, and DECAY at D = 128: every drain warp packs (split) W
+            if (i == DW) cnt = (NORM || (DECAY && D == 128)) ? RO::kDrain : RO::kAlpha;
+            if (i == DX || i == DO || i == DK) cnt = RO::kBeta;
             if (i == DS || i == DP) cnt = RO::kState;
             mbar_init(bar(i), cnt);
         }
@@ -200,6 +204,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     const int cD = part * 32;  // this drain warp's columns of the segment prefix (prologue)
     auto acol = [&](int g) { return (aw * AG + g) * 32; };  // alpha group g of this alpha warp
     auto bcol = [&](int g) { return (bw * BG + g) * 32; };  // D-wide group g of this beta warp
+    // DECAY: g^n, and the real length of chunk c (the last one may be short)
+    auto gp = [&](float n) { return exp2f(n * p.lg); };
+    auto clen = [&](int c) { return (float)min(kL, p.T - c * kL); };
 
     constexpr uint32_t kTileBytes = kL * D * 2;
     auto wait_bar = [&](int b, uint32_t parity) -> bool {
@@ -242,7 +249,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
     };
     // this beta warp's groups of a D-wide fp32 region -> bf16 tile rows
-    auto drainD = [&](uint32_t treg, const Tile& t, bool split) {
+    // (DECAY, wb: the tensor-memory copy is then multiplied by `decay` for
+    // the next update)
+    auto drainD = [&](uint32_t treg, const Tile& t, bool split, float decay = 1.f, bool wb = false) {
 #pragma unroll
         for (int g = 0; g < BG; ++g) {
             uint32_t r[32];
@@ -250,7 +259,26 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             tmem_ld_wait();
             if (NORM && split) put_row32_split2(t, tSPL, row, bcol(g), r, false);  // t is the S0 / P0 tile
             else put_row32(t, row, bcol(g), r, false);
+            if (DECAY && wb) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+                tmem_st32(treg + lane_off + bcol(g), r);
+            }
         }
+        if (DECAY && wb) tmem_st_wait();
+    };
+    // DECAY: this beta warp's groups of a D-wide region multiplied by `decay` in place
+    auto rescale = [&](uint32_t treg, float decay) {
+#pragma unroll
+        for (int g = 0; g < BG; ++g) {
+            uint32_t r[32];
+            tmem_ld32(treg + lane_off + bcol(g), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+            tmem_st32(treg + lane_off + bcol(g), r);
+        }
+        tmem_st_wait();
     };
     // NORM: p0 (one fp32 per state row d) into column D of [P0 | p0], hi and
     // lo (row d, first element of the second block)
@@ -272,7 +300,11 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
     // this alpha warp's groups -> bf16 pairs (masked to columns <= row),
     // optionally with the lo parts, written back packed; `one` packs the
     // single group `part` instead (NORM's W, which every drain warp packs)
-    auto pack_alpha = [&](bool split, bool one = false) {
+    // (DECAY: each value times s and, when colfac is set, its column factor
+    // g^{-(col+1)}, stepped from the group's first column by 1 / g, before
+    // the mask and the rounding)
+    const float ginv = DECAY ? exp2f(-p.lg) : 1.f;
+    auto pack_alpha = [&](bool split, bool one = false, bool colfac = false, float s = 1.f) {
         if (!split && AG == 2) {
             // both groups' loads in flight before the one wait (the common case)
             uint32_t r0[32], r1[32];
@@ -281,9 +313,16 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             tmem_ld_wait();
             auto pack16 = [&](const uint32_t (&r)[32], int c0) {
                 uint32_t hi[16];
+                float cf = (DECAY && colfac) ? exp2f(-(float)(c0 + 1) * p.lg) * s : s;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+                    if constexpr (DECAY) {
+                        x0 *= cf;
+                        if (colfac) cf *= ginv;
+                        x1 *= cf;
+                        if (colfac) cf *= ginv;
+                    }
                     if (c0 + 2 * j > row) x0 = 0.f;
                     if (c0 + 2 * j + 1 > row) x1 = 0.f;
                     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -304,9 +343,16 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             tmem_ld32(tAl_ + lane_off + c0, r);
             tmem_ld_wait();
             uint32_t hl[32];  // the pairs, then (split) the lo parts
+            float cf = (DECAY && colfac) ? exp2f(-(float)(c0 + 1) * p.lg) * s : s;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
+                if constexpr (DECAY) {
+                    x0 *= cf;
+                    if (colfac) cf *= ginv;
+                    x1 *= cf;
+                    if (colfac) cf *= ginv;
+                }
                 if (c0 + 2 * j > row) x0 = 0.f;
                 if (c0 + 2 * j + 1 > row) x1 = 0.f;
                 const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -347,10 +393,15 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
             if (!wait_bar(PB + warp, (uint32_t)m)) break;
             uint32_t r[32];
             box32_read(stage, lane, r);
-            tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cD, r);
             if (m == 0) {  // bf16 S0; P0 follows once Q S0 has read it
                 put_row32(tSP, row, cD, r, false);
+                if constexpr (DECAY) {  // TMEM S decayed over the first chunk (the P0 drain decays P)
+                    const float f = gp(clen(c_begin));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                }
             }
+            tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cD, r);
             __syncwarp();  // every lane has read the box before the next load reuses it
         }
         if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
@@ -405,15 +456,18 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // X += A K  (A from tensor memory)
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
-                if (NORM)  // + A_lo K
+                if (NORM || (DECAY && first))  // + A_lo K
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tK.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CX));
                 // S += K^T K after A K: it then runs beside the X drain, not
                 // beside the pack of A, whose tensor-memory traffic it slowed
-                // (K's last reader now, so the next K waits for CK)
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
-                mma_commit(bar(CK));
+                // (K's last reader now, so the next K waits for CK).  DECAY:
+                // S += K'^T K' once the beta warps have scaled K, after W
+                if (!DECAY) {
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CK));
+                }
                 if (!wait_bar(DX, ph)) break;  // sX = X (and sO = X_lo on a head's first chunk); beta free
                 tc_fence_after();
                 // W = Q X^T (+ Q X_lo^T) into alpha (A there was read by A K)
@@ -421,6 +475,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 if (first || NORM)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tAl_, tQ.kmaj(ks), (NORM ? tXL : tO).kmaj(ks), iSq, 1);
                 mma_commit(bar(CW));
+                if (DECAY) {
+                    // S += K'^T K', K' = diag(sqrt(b)) K scaled in place by the beta warps
+                    if (!wait_bar(DK, ph)) break;
+                    tc_fence_after();
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CK));
+                }
                 // P += X^T V once P0 of this chunk has left TMEM P
                 if (!wait_bar(LV, ph) || !wait_bar(DP, ph)) break;
                 tc_fence_after();
@@ -439,7 +500,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 }
                 for (int ks = 0; ks < kL / 16; ++ks)
                     mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks), tV.mnmaj(ks), iKME, (!first || ks > 0) ? 1u : 0u);
-                if (first || NORM)
+                if (first || NORM || DECAY)
                     for (int ks = 0; ks < kL / 16; ++ks)
                         mma_bf16_tmem_a(tBe_, tAl_ + pk_col(ks) + 16u, tV.mnmaj(ks), iKME, 1);
                 mma_commit(bar(CO));
@@ -472,6 +533,12 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         // drain puts this warp's X_lo rows in the same region, before any O.)
         const uint32_t box = tO.base + (uint32_t)(bw & 1) * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
         int o_row0 = 0;  // first token of this warp's O rows in the current chunk
+        // DECAY: o_t = g^{2(t+1)} O'_t
+        auto scale_o = [&](uint32_t (&r)[32]) {
+            const float os = gp(2.f * (float)(row + 1));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * os);
+        };
         auto stage_o = [&](const uint32_t (&r)[32], int g) {
             if (lane == 0) tma_store_wait_read();  // the box's previous content has left
             __syncwarp();
@@ -497,7 +564,8 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 // where every drain warp packs one group)
                 if (!wait_bar(CA_, ph)) break;
                 tc_fence_after();
-                pack_alpha(NORM, NORM);
+                // (DECAY: A~ = A g^{-(i+1)} by columns, split on a head's first chunk)
+                pack_alpha(NORM || (DECAY && first), NORM, DECAY, 1.f);
                 packed(DA);
             }
             if (beta_w) {
@@ -507,7 +575,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                 tc_fence_after();
                 if (state_rows) {
                     if (!first) {
-                        drainD(tP_, tSP, true);
+                        drainD(tP_, tSP, true, DECAY ? gp(2.f * clen(c)) : 1.f, DECAY);  // DECAY: TMEM P decayed
                         if (NORM && bw == 0) {  // p0 of this chunk -> its operand tiles
                             const uint32_t pv = tmem_ld1(tPn_ + lane_off);
                             tmem_ld_wait();
@@ -525,19 +593,47 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
                     uint32_t x[32];
                     tmem_ld32(tBe_ + lane_off + bcol(g), x);
                     tmem_ld_wait();
+                    if constexpr (DECAY) {  // sX = g^{2L-1-t} X'
+                        const float xs = gp(2.f * clen(c) - 1.f - (float)row);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * xs);
+                    }
                     if (NORM) put_row32_split2(tX, tXL, row, bcol(g), x, false);
                     else if (first) put_row32_split2(tX, tO, row, bcol(g), x, false);
                     else put_row32(tX, row, bcol(g), x, false);
                 }
                 drained(DX);
+                if constexpr (DECAY) {
+                    // K' = diag(sqrt(b)) K in place (row = token, b = g^{L-1-t}):
+                    // A and A~ K, its other readers, have completed
+                    const float kf = gp(0.5f * (clen(c) - 1.f - (float)row));
+#pragma unroll
+                    for (int g = 0; g < BG; ++g)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int col = bcol(g) + 8 * q;
+                            const uint32_t a = tK.chunk(row, col >> 6, (col & 63) >> 3);
+                            uint32_t w[4];
+                            ld_shared_v4(a, w[0], w[1], w[2], w[3]);
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+                                w[h] = pack_bf16(__low2float(v2) * kf, __high2float(v2) * kf);
+                            }
+                            st_shared_v4(a, w[0], w[1], w[2], w[3]);
+                        }
+                    drained(DK);
+                }
             }
-            if (alpha_w || NORM) {
+            if (alpha_w || NORM || DECAY) {
                 // W packed in place (masked; hi and lo on a head's first chunk
                 // and in the normalised walk, where every drain warp packs one
-                // group)
+                // group; DECAY: W~ = g^{-2L} tril(W'), split on every chunk, by
+                // every drain warp at D = 128)
                 if (!wait_bar(CW, ph)) break;
                 tc_fence_after();
-                pack_alpha(first || NORM, NORM);
+                pack_alpha(first || NORM || DECAY, NORM || (DECAY && D == 128), false,
+                           DECAY ? gp(-2.f * clen(c)) : 1.f);
                 packed(DW);
             }
             if (beta_w) {
@@ -569,19 +665,26 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * inv);
                     }
+                    if (DECAY) scale_o(r);
                     stage_o(r, 0);
+                    // DECAY: TMEM S decayed for the next update (S += K'^T K'
+                    // waits for K', which this warp scales after it)
+                    if (DECAY && state_rows && has_next) rescale(tS_, gp(clen(c + 1)));
                 } else {
                     static_assert(NORM == false, "the normalised walk has one O group per beta warp");
                     tmem_ld_wait();
+                    if (DECAY) scale_o(r);
                     stage_o(r, 0);
                     tmem_ld32(tBe_ + lane_off + bcol(1), r);  // BG == 2: the last group
                     tmem_ld_wait();
+                    if (DECAY) scale_o(r);
                     drained(DO);
                     if (state_rows && has_next) {
                         drainD(tS_, tSP, false);
                         drained(DS);
                     }
                     stage_o(r, 1);
+                    if (DECAY && state_rows && has_next) rescale(tS_, gp(clen(c + 1)));  // as above
                 }
             }
         }
@@ -594,9 +697,9 @@ tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CU
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-template <int D, bool NORM>
+template <int D, bool NORM, bool DECAY = false>
 cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH, int T,
-                         SegPlan plan, int* status, cudaStream_t s) {
+                         SegPlan plan, int* status, cudaStream_t s, float lg = 0.f) {
     CUtensorMap mq, mk, mv, mo, mr;
     if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
@@ -607,9 +710,9 @@ cudaError_t launch_out_t(const void* Q, const void* K, const void* V, float* O, 
         return cudaErrorInvalidValue;
     // O: fp32 boxes of 32 rows x 32 columns (one drain warp's piece)
     if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
-    OutParams prm{T, plan.nseg, plan.nchunk, plan.seglen, prefix, status};
+    OutParams prm{T, plan.nseg, plan.nchunk, plan.seglen, prefix, status, lg};
     const size_t smem = OutLayout<D, NORM>::kBytes + 1024;
-    auto kern = tc_out_kernel<D, NORM>;
+    auto kern = tc_out_kernel<D, NORM, DECAY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.nseg, BH);
@@ -628,6 +731,15 @@ cudaError_t launch_tc_out(const void* Q, const void* K, const void* V, float* O,
                                    : cudaErrorInvalidValue;
     if (d == 128) return launch_out_t<128, false>(Q, K, V, O, prefix, BH, T, plan, status, s);
     if (d == 64) return launch_out_t<64, false>(Q, K, V, O, prefix, BH, T, plan, status, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc_out_decay(const void* Q, const void* K, const void* V, float* O, const float* prefix, int BH,
+                                int T, int d, int dv, float lg, SegPlan plan, int* status, cudaStream_t s) {
+    if (BH == 0 || plan.nseg == 0) return cudaSuccess;
+    if (plan.granule != kL || d != dv) return cudaErrorInvalidValue;
+    if (d == 128) return launch_out_t<128, false, true>(Q, K, V, O, prefix, BH, T, plan, status, s, lg);
+    if (d == 64) return launch_out_t<64, false, true>(Q, K, V, O, prefix, BH, T, plan, status, s, lg);
     return cudaErrorInvalidValue;
 }
 
