@@ -1,6 +1,7 @@
-// hla2_decay_tc.cu -- tensor-core segment walks of the exponentially decayed
-// masked operator on GB300 (sm_103a): tcgen05.mma with TMEM accumulators,
-// TMA tiles.
+// hla2_decay_tc.cu -- tensor-core segment summary walk of the exponentially
+// decayed masked operator on GB300 (sm_103a): tcgen05.mma with TMEM
+// accumulators, TMA tiles.  The outputs run on the pipelined output walk
+// (hla2_tc_out.cu) with the chunk form below.
 //
 // Operator (HLA summary, arXiv 2510.27258, section 4 names decayed operators
 // among those the scan covers): every prefix moment decays by gamma per token,
@@ -84,361 +85,6 @@ __device__ __forceinline__ void scale_row(const Tile& src, const Tile& dst, int 
         }
         st_shared_v4(dst.chunk(r, col >> 6, (col & 63) >> 3), w[0], w[1], w[2], w[3]);
     }
-}
-
-// ------------------------------------------------------------- outputs ----
-template <int D>
-struct DOutLayout {
-    static constexpr uint32_t kTok = kL * D * 2;  // Q, K, V, X tiles
-    static constexpr uint32_t kSq = kL * kL * 2;  // A~ / W~ tile
-    static constexpr uint32_t kSt = D * D * 2;    // S0 / P0 tiles
-    static constexpr uint32_t Q = 0, K = Q + kTok, V = K + kTok, A = V + kTok, X = A + kSq;
-    static constexpr uint32_t S = X + kTok, P = S + kSt;
-    static constexpr uint32_t kEnd = P + kSt;
-    // a head's first chunk: A~_lo in the S0 tile and sX_lo in the P0 tile at
-    // D = 128 (the state is zero there); own tiles at D = 64
-    static constexpr uint32_t Alo = (D == 128) ? S : kEnd;
-    static constexpr uint32_t Xlo = (D == 128) ? P : kEnd + kSq;
-    static constexpr uint32_t kEnd2 = (D == 128) ? kEnd : kEnd + kSq + kTok;
-    static constexpr uint32_t kPad = (D < 128) ? 16384u : 0u;
-    static constexpr uint32_t kBytes = kEnd2 + kPad;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreadsTC + 32, 1)
-decay_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO,
-                    const __grid_constant__ CUtensorMap mR, DParams p) {
-    using LY = DOutLayout<D>;
-    extern __shared__ __align__(1024) unsigned char dsm_raw[];
-    enum { LQ, LK, LV, CA, CX, CS, CW, CO, CP, DA, DX, DK, DW, DO, DS, DP, FIN, PB, NBAR = PB + kDrainWarps };
-    __shared__ __align__(8) unsigned long long bars[NBAR];
-    __shared__ float colf[kL];  // g^{-(i+1)}
-    __shared__ uint32_t tmem_slot;
-    __shared__ volatile int abort_flag;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issuer = warp == kDrainWarps;
-    const bool producer = warp == kDrainWarps + 1;  // issues every tile load
-    const int quarter = warp & 3, half = (warp >> 2) & 1;
-    const int row = quarter * 32 + lane;
-    int head, seg;
-    const SegPlan plan{kL, p.nchunk, p.nseg, p.seglen};
-    block_segment(plan, gridDim.y, (long long)blockIdx.y * gridDim.x + blockIdx.x, head, seg);
-    const int c_begin = seg_chunk_begin(plan, seg), c_end = seg_chunk_begin(plan, seg + 1);
-    const int nchunks = c_end - c_begin;
-    const bool state_rows = warp < kDrainWarps && ((D == 128) || quarter < D / 32);
-    constexpr int kStateWarps = (D == 128) ? kDrainWarps : 2 * (D / 32);
-    const float lg = p.lg;
-
-    const uint32_t dsm = (smem_u32(dsm_raw) + 1023u) & ~1023u;
-    const Tile tQ{dsm + LY::Q, kL}, tK{dsm + LY::K, kL}, tV{dsm + LY::V, kL};
-    const Tile tA{dsm + LY::A, kL}, tX{dsm + LY::X, kL};
-    const Tile tS{dsm + LY::S, D}, tP{dsm + LY::P, D};
-    const Tile tAl{dsm + LY::Alo, kL}, tXl{dsm + LY::Xlo, kL};
-    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
-
-    if (tid < kL) colf[tid] = gpow(lg, -(float)(tid + 1));
-    if (tid == 0) {
-        abort_flag = 0;
-        for (int i = 0; i < NBAR; ++i) {
-            uint32_t cnt = 1;
-            if (i == DA || i == DX || i == DK || i == DW || i == DO) cnt = kDrainWarps;
-            if (i == DS || i == DP) cnt = kStateWarps;
-            mbar_init(bar(i), cnt);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    // tensor memory: A~, then W', then O' | X', then packed W~_lo | S | P
-    const uint32_t tA_ = tmem + 0, tX_ = tmem + 128, tS_ = tmem + 256, tP_ = tmem + 256 + D;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int c128 = half * 64;
-    const int cD = half * (D / 2);
-    // packed W~_lo: warp half h holds W columns [64h, 64h + 64) as 32 packed
-    // columns at X' column h * D/2 (a K-step ks reads 8 of them)
-    auto wlo_col = [](int ks) -> uint32_t { return (uint32_t)((ks >> 2) * (D / 2) + 8 * (ks & 3)); };
-
-    constexpr uint32_t kTileBytes = kL * D * 2;
-    auto wait_bar = [&](int b, uint32_t parity) -> bool {
-        const uint32_t a = bar(b);
-        if (abort_flag) return false;
-        if (mbar_try(a, parity)) return true;
-        const unsigned long long t0 = globaltimer();
-        while (!mbar_try(a, parity)) {
-            if (abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) {
-                abort_flag = 1;
-                atomicExch(p.status, (int)kDevWaitTimeout);
-                return false;
-            }
-        }
-        return true;
-    };
-    // every tile load is issued by the issuer's lane 0, which settles them
-    // (waits for the last of each barrier) before the CTA exits
-    LoadLedger<3> loads(bar(0));  // LQ, LK, LV
-    auto issue_load = [&](int b, const CUtensorMap* map, const Tile& t, int chunk) {
-        loads.note(b);
-        mbar_expect_tx(bar(b), kTileBytes);
-#pragma unroll
-        for (int k = 0; k < D / 64; ++k) tma_load_3d(t.base + k * t.block_bytes(), map, k * 64, chunk * kL, head, bar(b));
-    };
-    auto drained = [&](int b) {
-        fence_proxy_async();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(b)) : "memory");
-    };
-    // TMEM state rows (D columns of this warp's half) -> bf16 tile; the TMEM
-    // copy is multiplied by `decay` for the next chunk's update
-    auto drain_state = [&](uint32_t treg, const Tile& t, float decay) {
-        uint32_t r[64];
-        tmem_ld_cols<D / 2>(treg + lane_off + cD, r);
-        put_row32(t, row, cD, r, false);
-        if (D == 128) put_row32(t, row, cD + 32, r + 32, false);
-#pragma unroll
-        for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
-        tmem_st32(treg + lane_off + cD, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        if (D == 128) tmem_st32(treg + lane_off + cD + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_st_wait();
-    };
-
-    if (producer && lane == 0 && nchunks > 0) {
-        issue_load(LQ, &mQ, tQ, c_begin);
-        issue_load(LK, &mK, tK, c_begin);
-        issue_load(LV, &mV, tV, c_begin);
-    }
-    // ---- initial state: S0 (record row 0), P0 (record row 2D+1) by bulk
-    // tensor loads into per-warp staging in the A / X tiles; bf16 copies as
-    // they are, TMEM copies decayed over the first chunk (g^L, g^{2L})
-    if (state_rows && nchunks > 0) {
-        const int rec = head * p.nseg + seg;
-        const float L0 = (float)chunk_len(p.T, c_begin);
-        const uint32_t stage = dsm + LY::A + (uint32_t)warp * (uint32_t)(D / 64) * 4096u;
-        LoadLedger<1> boxes(bar(PB + warp));
-#pragma unroll 1
-        for (int m = 0; m < 2; ++m) {
-            if (lane == 0) {
-                boxes.note(0);
-                fence_proxy_async();
-                mbar_expect_tx(bar(PB + warp), (uint32_t)(D / 64) * 4096u);
-#pragma unroll
-                for (int g = 0; g < D / 64; ++g)
-                    tma_load_3d(stage + (uint32_t)g * 4096u, &mR, cD + 32 * g, (m == 0 ? 0 : 2 * D + 1) + quarter * 32,
-                                rec, bar(PB + warp));
-            }
-            __syncwarp();
-            if (!wait_bar(PB + warp, (uint32_t)m)) break;
-            const float decay = gpow(lg, (m == 0 ? 1.f : 2.f) * L0);
-#pragma unroll
-            for (int g = 0; g < D / 64; ++g) {
-                const int cb = cD + 32 * g;
-                uint32_t r[32];
-                box32_read(stage + (uint32_t)g * 4096u, lane, r);
-                put_row32(m == 0 ? tS : tP, row, cb, r, false);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
-                tmem_st32((m == 0 ? tS_ : tP_) + lane_off + cb, r);
-            }
-            __syncwarp();
-        }
-        if (lane == 0 && !boxes.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
-        tmem_st_wait();
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    constexpr uint32_t iSq = idesc_bf16(128, 128, false, false);  // 128 x 128, both K-major
-    constexpr uint32_t iKK = idesc_bf16(128, D, false, false);    // N = D, both K-major
-    constexpr uint32_t iKM = idesc_bf16(128, D, false, true);     // A K-major, B MN-major
-    constexpr uint32_t iMM = idesc_bf16(128, D, true, true);      // both MN-major
-
-    if (issuer) {
-        // ============================ issuer ============================
-        if (lane == 0 && nchunks > 0) {
-            for (int it = 0; it < nchunks; ++it) {
-                const int c = c_begin + it;
-                const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                const bool has_next = it + 1 < nchunks;
-                const bool first = c == 0;  // S0 = P0 = 0; A~ and sX split into hi + lo
-                if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
-                if (it > 0 && !wait_bar(DO, pph)) break;  // O' of the previous chunk read out of TMEM A
-                tc_fence_after();
-                // A = Q K^T
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tK.kmaj(ks), iSq, ks > 0);
-                mma_commit(bar(CA));
-                if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0; TMEM S decayed
-                if (!wait_bar(DA, ph)) break;              // sA = A~ (A~_lo)
-                tc_fence_after();
-                // X' = Q S0 + A~ K
-                if (!first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tX_, tA.kmaj(ks), tK.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
-                if (first)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
-                mma_commit(bar(CX));
-                if (!wait_bar(DX, ph)) break;  // sX = g^{2L-1-t} X' (and its lo part); TMEM X' read
-                tc_fence_after();
-                // W' = Q sX^T
-                for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tX.kmaj(ks), iSq, ks > 0);
-                if (first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tXl.kmaj(ks), iSq, 1);
-                mma_commit(bar(CW));
-                if (has_next) {
-                    // S += K'^T K' (K' = diag(sqrt(b)) K, scaled in place by the drains)
-                    if (!wait_bar(DK, ph)) break;
-                    tc_fence_after();
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
-                    mma_commit(bar(CS));
-                }
-                if (!wait_bar(DW, ph)) break;              // sA = W~_hi, TMEM X' columns = W~_lo; TMEM A read
-                if (it > 0 && !wait_bar(DP, pph)) break;  // sP = P0; TMEM P decayed
-                tc_fence_after();
-                // O' = Q P0 + W~_hi V + W~_lo V
-                if (!first)
-                    for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tA_, tQ.kmaj(ks), tP.mnmaj(ks), iKM, ks > 0);
-                if (!wait_bar(LV, ph)) break;
-                tc_fence_after();
-                for (int ks = 0; ks < kL / 16; ++ks)
-                    mma_bf16(tA_, tA.kmaj(ks), tV.mnmaj(ks), iKM, (!first || ks > 0) ? 1u : 0u);
-                for (int ks = 0; ks < kL / 16; ++ks) mma_bf16_tmem_a(tA_, tX_ + wlo_col(ks), tV.mnmaj(ks), iKM, 1);
-                mma_commit(bar(CO));
-                if (has_next) {
-                    // P += sX^T V
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tP_, tX.mnmaj(ks), tV.mnmaj(ks), iMM, 1);
-                    mma_commit(bar(CP));
-                }
-            }
-            if (!mma_wait_all(bar(FIN))) atomicExch(p.status, (int)kDevWaitTimeout);
-        }
-    } else if (producer) {
-        // the next chunk's tiles once their last reader completed: K after the
-        // S update, Q after O (Q P0), V after the P update
-        if (lane == 0) {
-            for (int it = 0; it + 1 < nchunks; ++it) {
-                const int c = c_begin + it;
-                const uint32_t ph = it & 1;
-                if (!wait_bar(CS, ph)) break;
-                issue_load(LK, &mK, tK, c + 1);
-                if (!wait_bar(CO, ph)) break;
-                issue_load(LQ, &mQ, tQ, c + 1);
-                if (!wait_bar(CP, ph)) break;
-                issue_load(LV, &mV, tV, c + 1);
-            }
-            if (!loads.settle()) atomicExch(p.status, (int)kDevWaitTimeout);
-        }
-    } else {
-        // ========================== drain warps ==========================
-        for (int it = 0; it < nchunks; ++it) {
-            const int c = c_begin + it;
-            const uint32_t ph = it & 1, pph = (it + 1) & 1;
-            const bool has_next = it + 1 < nchunks;
-            const bool first = c == 0;
-            const float L = (float)chunk_len(p.T, c);
-            if (!wait_bar(CA, ph)) break;
-            tc_fence_after();
-            // this warp's O pieces have left sA and sX
-            if (lane == 0) tma_store_wait_read();
-            __syncwarp();
-            {
-                // A~ = tril(A) g^{-(i+1)} -> sA (A~_lo -> its tile on the first chunk)
-                uint32_t r[64];
-                tmem_ld_cols<64>(tA_ + lane_off + c128, r);
-                put_row32_cf(tA, tAl, first, row, c128, r, colf, 1.f, true);
-                put_row32_cf(tA, tAl, first, row, c128 + 32, r + 32, colf, 1.f, true);
-            }
-            drained(DA);
-            if (!wait_bar(CX, ph)) break;
-            if (it > 0 && !wait_bar(CP, pph)) break;  // the previous P update has read sX
-            tc_fence_after();
-            {
-                // sX = g^{2L-1-t} X'  (hi, and lo on the first chunk)
-                uint32_t r[64];
-                tmem_ld_cols<D / 2>(tX_ + lane_off + cD, r);
-                const float xs = gpow(lg, 2.f * L - 1.f - (float)row);
-                put_row32_cf(tX, tXl, first, row, cD, r, nullptr, xs, false);
-                if (D == 128) put_row32_cf(tX, tXl, first, row, cD + 32, r + 32, nullptr, xs, false);
-            }
-            drained(DX);
-            if (has_next) {
-                // K' = diag(sqrt(b)) K in place (row = token; b = g^{L-1-t}): its
-                // other products (A, A~ K) have completed
-                scale_row<D / 16>(tK, tK, row, cD, gpow(lg, 0.5f * (L - 1.f - (float)row)));
-                drained(DK);
-            }
-            if (!wait_bar(CW, ph)) break;
-            tc_fence_after();
-            {
-                // W~ = g^{-2L} tril(W'): hi -> sA, lo packed -> TMEM over this warp's X' columns
-                // (32 columns at a time to bound the live registers)
-                uint32_t lo[32];
-                const float ws = gpow(lg, -2.f * L);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[32];
-                    tmem_ld32(tA_ + lane_off + c128 + 32 * hh, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * ws);
-                    put_row32_split(tA, row, c128 + 32 * hh, r, true, lo + 16 * hh);
-                }
-                tmem_st32(tX_ + lane_off + (uint32_t)(half * (D / 2)), lo);
-                tmem_st_wait();
-            }
-            drained(DW);
-            if (state_rows && has_next) {
-                if (!wait_bar(CS, ph)) break;
-                tc_fence_after();
-                drain_state(tS_, tS, gpow(lg, (float)chunk_len(p.T, c + 1)));  // S0 of the next chunk
-                drained(DS);
-            }
-            if (!wait_bar(CO, ph)) break;
-            tc_fence_after();
-            {
-                // o_t = g^{2(t+1)} O'_t: piece 0 through this warp's 4 KB of sA,
-                // piece 1 (D = 128) through the same rows of sX once the P update has read it
-                uint32_t r[64];
-                tmem_ld_cols<D / 2>(tA_ + lane_off + cD, r);
-                drained(DO);
-                const float os = gpow(lg, 2.f * (float)(row + 1));
-#pragma unroll
-                for (int j = 0; j < D / 2; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * os);
-                const uint32_t wofs = (uint32_t)half * (kL * 128u) + (uint32_t)(quarter * 32) * 128u;
-                const int t0 = c * kL + quarter * 32;
-                box32_store(&mO, tA.base + wofs, r, lane, cD, t0, head);
-                if (D == 128) {
-                    if (has_next && !wait_bar(CP, ph)) break;
-                    tc_fence_after();
-                    box32_store(&mO, tX.base + wofs, r + 32, lane, cD + 32, t0, head);
-                }
-            }
-            if (state_rows && has_next) {
-                if (!wait_bar(CP, ph)) break;
-                tc_fence_after();
-                drain_state(tP_, tP, gpow(lg, 2.f * (float)chunk_len(p.T, c + 1)));  // P0 of the next chunk
-                drained(DP);
-            }
-        }
-        if (lane == 0) tma_store_wait_all();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 // ----------------------------------------------------------- summaries ----
@@ -564,9 +210,7 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     if (issuer) {
         if (lane == 0 && nchunks > 0) {
             for (int it = 0; it < nchunks; ++it) {
-                const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                const bool has_next = it + 1 < nchunks;
                 const bool qodd = it & 1;  // Q buffer of this chunk
                 const Tile& tQ = qodd ? tQb : tQa;
                 if (!wait_bar(qodd ? LQ2 : LQ, (uint32_t)((it >> 1) & 1)) || !wait_bar(LK, ph)) break;
@@ -707,33 +351,22 @@ decay_tc_sum_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 }
 
 template <int D>
-cudaError_t launch_d(int mode, const void* Q, const void* K, const void* V, float* O, const float* prefix,
-                     float* summ, int BH, int T, float gamma, SegPlan plan, int* status, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mo, mr;
+cudaError_t launch_d(const void* Q, const void* K, const void* V, float* summ, int BH, int T, float gamma,
+                     SegPlan plan, int* status, cudaStream_t s) {
+    CUtensorMap mq, mk, mv, mr;
     if (!make_map(&mq, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64) ||
         !make_map(&mv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, T, BH, 64))
         return cudaErrorInvalidValue;
-    if (!make_map(&mr, mode == 1 ? static_cast<const void*>(prefix) : static_cast<const void*>(summ),
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
+    if (!make_map(&mr, summ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, 3 * D + 2, BH * plan.nseg, 32, 32))
         return cudaErrorInvalidValue;
     DParams prm{T, plan.nseg, plan.nchunk, plan.seglen, (float)std::log2((double)gamma), status};
     dim3 grid(plan.nseg, BH);
-    cudaError_t e;
-    if (mode == 0) {
-        const size_t smem = DSumLayout<D>::kBytes + 1024;
-        auto kern = decay_tc_sum_kernel<D>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mr, prm);
-    } else {
-        if (!make_map(&mo, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, BH, 32, 32)) return cudaErrorInvalidValue;
-        const size_t smem = DOutLayout<D>::kBytes + 1024;
-        auto kern = decay_tc_out_kernel<D>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mo, mr, prm);
-    }
+    const size_t smem = DSumLayout<D>::kBytes + 1024;
+    auto kern = decay_tc_sum_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreadsTC + 32, smem, s>>>(mq, mk, mv, mr, prm);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -750,8 +383,9 @@ cudaError_t launch_decay_tc_walk(int mode, const void* Q, const void* K, const v
     // outputs: the walk pipelined across chunks (hla2_tc_out.cu)
     if (mode == 1)
         return launch_tc_out_decay(Q, K, V, O, prefix, BH, T, d, dv, (float)std::log2((double)gamma), plan, status, s);
-    if (d == 128) return launch_d<128>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
-    if (d == 64) return launch_d<64>(mode, Q, K, V, O, prefix, summ, BH, T, gamma, plan, status, s);
+    if (mode != 0) return cudaErrorInvalidValue;
+    if (d == 128) return launch_d<128>(Q, K, V, summ, BH, T, gamma, plan, status, s);
+    if (d == 64) return launch_d<64>(Q, K, V, summ, BH, T, gamma, plan, status, s);
     return cudaErrorInvalidValue;
 }
 

@@ -37,12 +37,22 @@
 // lo and both parts enter it (A, X, W, P0, p0), which keeps about 16
 // significant bits of those operands; S0 is rounded to bf16 alone (its
 // rounding stays two orders below the 1e-4 bound on the outputs, where any
-// of the others would come within a factor of three of it or exceed it).  p and the denominators ride along as
-// one more value column: V is read as [V | 1] and P0 as [P0 | p0] (N = 80
-// products, the extra 64-column block of each operand holding the ones or
-// p0), so P += X^T [V | 1] grows p in P's column D and O = Q [P0 | p0] +
-// W [V | 1] leaves the denominators in O's column D.  X_lo sits in the X
-// tile's second 64-column block.
+// of the others would come within a factor of three of it or exceed it).
+// p and the denominators ride along as one more value column: V is read as
+// [V | 1] and P0 as [P0 | p0] (N = 80 products, the extra 64-column block of
+// each operand holding the ones or p0), so P += X^T [V | 1] grows p in P's
+// column D and O = Q [P0 | p0] + W [V | 1] leaves the denominators in O's
+// column D.  X_lo sits in the X tile's second 64-column block.
+//
+// DECAY (exponentially decayed operator, gamma in the tensor-core range):
+// the same pipeline on the decayed chunk form of hla2_decay_tc.cu.  A~ =
+// tril(Q K^T) g^{-(i+1)} (column factors in the pack of A, split on a head's
+// first chunk), X' = Q S0 + A~ K drained as sX = g^{2L-1-t} X', W~ =
+// g^{-2L} tril(Q sX^T) split into hi + lo on every chunk (packed by every
+// drain warp at D = 128), o_t = g^{2(t+1)} O'_t in the O drain; the beta
+// warps scale K in place to K' = diag(sqrt(b)) K once A and A~ K have read it
+// (S += K'^T K' then waits for them), and multiply tensor-memory P by
+// g^{2L} when they hand P0 over and S by g^{L} after they hand S0 over.
 #include "hla2_tc_common.cuh"
 
 namespace hla2 {
