@@ -198,7 +198,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     using LY = UOutLayout<D>;
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     // loads | MMA commits | drains | (PB + w: drain warp w's prefix boxes)
-    enum { LQ, LK, LV, CA, CXS, CX2, CW, CO, CC, DA, DX, DW, DO, DS, DC, FIN, PB, NBAR = PB + kDrainWarps };
+    enum { LQ, LK, LV, CA, CXS, CX2, CW, CO, CC, CSU, DA, DX, DW, DO, DS, DC, FIN, PB, NBAR = PB + kDrainWarps };
     __shared__ __align__(8) unsigned long long bars[NBAR];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -368,11 +368,9 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 mma_commit(bar(CA));
                 if (it > 0 && !wait_bar(DS, pph)) break;  // sS = S0 of this chunk; TMEM S read
                 tc_fence_after();
-                // X = Q S0 ; S += K^T K (the state after the segment's last chunk is not needed)
+                // X = Q S0
                 if (!first)
                     for (int ks = 0; ks < D / 16; ++ks) mma_bf16(tX_, tQ.kmaj(ks), tS.kmaj(ks), iKK, ks > 0);
-                if (has_next)
-                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
                 mma_commit(bar(CXS));
                 if (!wait_bar(DA, ph)) break;  // sA = A (and A_lo on the first chunk)
                 tc_fence_after();
@@ -382,6 +380,12 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 if (first)
                     for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tX_, tAl.kmaj(ks), tK.mnmaj(ks), iKM, 1);
                 mma_commit(bar(CX2));
+                if (has_next) {
+                    // S += K^T K after A K, beside the X drain rather than the A
+                    // drain (the state after the segment's last chunk is not needed)
+                    for (int ks = 0; ks < kL / 16; ++ks) mma_bf16(tS_, tK.mnmaj(ks), tK.mnmaj(ks), iMM, 1);
+                    mma_commit(bar(CSU));
+                }
                 if (!wait_bar(DX, ph)) break;  // sX = X (and X_lo); TMEM X read
                 tc_fence_after();
                 // W = X Q^T
@@ -420,7 +424,7 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             for (int it = 0; it + 1 < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1;
-                if (!wait_bar(CX2, ph)) break;
+                if (!wait_bar(CSU, ph)) break;  // S += K^T K, K's last reader
                 issue_load(LK, &mK, tK, c + 1);
                 if (!wait_bar(CC, ph)) break;
                 issue_load(LQ, &mQ, tQ, c + 1);
@@ -445,12 +449,6 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (first) drain128s(tA_, tA, tAl, true);  // A -> sA (hi), A_lo (masked)
             else drain128(tA_, tA, true);              // A -> sA (masked)
             drained(DA);
-            if (!wait_bar(CXS, ph)) break;
-            tc_fence_after();
-            if (state_rows && has_next && !first) {
-                drainD(tS_, tS);  // S0 of the next chunk -> sS
-                drained(DS);
-            }
             if (!wait_bar(CX2, ph)) break;
             tc_fence_after();
             if (D == 128) {
@@ -460,6 +458,12 @@ unm_tc_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             if (first) drainDs(tX_, tX, tXl);  // X -> sX (hi), X_lo
             else drainD(tX_, tX);              // X -> sX
             drained(DX);
+            if (state_rows && has_next && !first) {
+                if (!wait_bar(CSU, ph)) break;
+                tc_fence_after();
+                drainD(tS_, tS);  // S0 of the next chunk -> sS
+                drained(DS);
+            }
             if (!wait_bar(CW, ph)) break;
             tc_fence_after();
             if (first) drain128s(tA_, tA, tWl, true);  // W -> sA (hi), W_lo (masked)
