@@ -260,7 +260,6 @@ ahla_tc_walk_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
             for (int it = 0; it < nchunks; ++it) {
                 const int c = c_begin + it;
                 const uint32_t ph = it & 1, pph = (it + 1) & 1;
-                const bool has_next = it + 1 < nchunks;
                 if (!wait_bar(LQ, ph) || !wait_bar(LK, ph)) break;
                 if (MODE == 1) {
                     const bool first = c == 0;  // P0 = E0 = 0; A and Y split into hi + lo
