@@ -43,12 +43,12 @@ BYTES_PER_TOKEN_FWD = None  # set from the workload: 2*(2d+dv) + 4*dv
 # valid only for the kernel source it was taken on, keyed by (kernel, workload).
 # Both were captured at full size with one-pass metrics (profiles/*.md give
 # the commands and the raw figures):
-#  - tc_out_kernel<128> (the output walk), B1 H16 T65536: 826.4 + 489.0 MB;
+#  - tc_out_kernel<128> (the output walk), B1 H16 T65536: 826.4 + 489.2 MB;
 #  - decode step_kernel, 4096 heads: 815.9 + 752.5 MB.
 # Writes still in L2 when a kernel ends are not counted, so the write side
 # sits a little below the algorithmic bytes.
 NCU_TRAFFIC = {
-    ("tcgen05", "hla2-fwd-B1H16T65536-d128-bf16"): 826412128 + 489001056,  # tc_out_kernel<128>
+    ("tcgen05", "hla2-fwd-B1H16T65536-d128-bf16"): 826415968 + 489178976,  # tc_out_kernel<128>
     ("step", "hla2-step-n4096-d128-fp32-prefill1024-steps512"): 815852544 + 752451328,
 }
 
