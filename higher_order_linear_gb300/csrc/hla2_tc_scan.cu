@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
     constexpr int NC = D / 4;  // drain: columns per warp (four warps share a lane quarter)
     extern __shared__ __align__(1024) unsigned char dsm_raw[];
     __shared__ __align__(8) unsigned long long bar_mma;
+    __shared__ __align__(8) unsigned long long ring_bar[3];  // the fold's record ring (one barrier per buffer)
     __shared__ uint32_t tmem_slot;
     __shared__ int s_flag;
 
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
     if (tid == 0) {
         s_flag = 0;
         mbar_init(smem_u32(&bar_mma), 1);
+        for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&ring_bar[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -280,23 +282,53 @@ __global__ void __launch_bounds__(kScanThreadsTC, 1) tc_scan_kernel(ScanArgs a) 
         }
     } else {
         // this record's term X_r; the running sum over records follows in a second launch.
-        // Two records' loads are in flight before their (in-order) folds.
-        int i0 = 0;
-        for (; i0 + 1 < r; i0 += 2) {
-            float4 x0[NV], x1[NV];
-            ld_mat<D>(rec0 + (size_t)i0 * R + off1, tid, x0);
-            ld_mat<D>(rec0 + (size_t)(i0 + 1) * R + off1, tid, x1);
-            const float f0 = (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f;
-            const float f1 = (OP == kScanDecay) ? __ldg(a.fac + i0 + 1) : 1.f;
+        // The fold's records arrive by bulk copies into a ring of kRing
+        // shared-memory buffers (the operand tiles and the staging are free
+        // until the product; at D < 128 the ring starts past A, whose rows
+        // >= D hold zeros), kRing records in flight, folded in order.
+        constexpr int kRing = (D == 128) ? 3 : 2;
+        constexpr uint32_t kRecBytes = (uint32_t)D * D * 4u, kRingOff = (D < 128) ? TL::Bhi : 0u;
+        static_assert(kRingOff + kRing * kRecBytes <= TL::kBytes, "the ring fits the kernel's shared memory");
+        LoadLedger<kRing> ring(smem_u32(&ring_bar[0]));
+        auto issue_rec = [&](int j) {  // thread 0
+            const int b = j % kRing;
+            ring.note(b);
+            mbar_expect_tx(smem_u32(&ring_bar[b]), kRecBytes);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(dsm + kRingOff + (uint32_t)b * kRecBytes), "l"(rec0 + (size_t)j * R + off1),
+                         "r"(kRecBytes), "r"(smem_u32(&ring_bar[b]))
+                         : "memory");
+        };
+        if (tid == 0)
+            for (int j = 0; j < kRing && j < r; ++j) issue_rec(j);
+        for (int i0 = 0; i0 < r; ++i0) {
+            const uint32_t rb = smem_u32(&ring_bar[i0 % kRing]), par = (uint32_t)((i0 / kRing) & 1);
+            bool ok = mbar_try(rb, par);
+            if (!ok) {
+                const unsigned long long t0 = globaltimer();
+                while (!(ok = mbar_try(rb, par)))
+                    if (globaltimer() - t0 > kWaitNs) break;
+            }
+            if (!ok) {
+                atomicExch(a.status, (int)kDevWaitTimeout);
+                s_flag = 1;
+            }
+            const float* buf = reinterpret_cast<const float*>(dsm_raw + (dsm - smem_u32(dsm_raw)) + kRingOff +
+                                                              (uint32_t)(i0 % kRing) * kRecBytes);
+            const float f = (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f;
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
-                const float4 t = make_float4(fmaf(f0, acc1[i].x, x0[i].x), fmaf(f0, acc1[i].y, x0[i].y),
-                                             fmaf(f0, acc1[i].z, x0[i].z), fmaf(f0, acc1[i].w, x0[i].w));
-                acc1[i] = make_float4(fmaf(f1, t.x, x1[i].x), fmaf(f1, t.y, x1[i].y), fmaf(f1, t.z, x1[i].z),
-                                      fmaf(f1, t.w, x1[i].w));
+                const float4 x = reinterpret_cast<const float4*>(buf)[tid + kScanThreadsTC * i];
+                acc1[i] = make_float4(fmaf(f, acc1[i].x, x.x), fmaf(f, acc1[i].y, x.y), fmaf(f, acc1[i].z, x.z),
+                                      fmaf(f, acc1[i].w, x.w));
             }
+            __syncthreads();  // every thread has read the buffer (and seen any timeout)
+            if (s_flag) break;
+            if (tid == 0 && i0 + kRing < r) issue_rec(i0 + kRing);
         }
-        if (i0 < r) fold(acc1, rec0 + (size_t)i0 * R + off1, (OP == kScanDecay) ? __ldg(a.fac + i0) : 1.f);
+        // no copy may still be landing when the buffers become operand tiles
+        if (tid == 0 && !ring.settle()) atomicExch(a.status, (int)kDevWaitTimeout);
+        __syncthreads();
         const float* rec = rec0 + (size_t)r * R;
         fold(acc2, rec + off2, 1.f);
         if (EXTRA) {
